@@ -1,0 +1,179 @@
+/*
+ * mamba3.h -- C ABI of the B300 (sm_103a) Mamba-3 layer-recurrence library.
+ *
+ * The library computes the Mamba-3 selective state-space recurrence for every
+ * (batch, head) sequence:
+ *
+ *   h_t = alpha_t h_{t-1} + beta_t B_{t-1} x_{t-1}^T + gamma_t B_t x_t^T,
+ *   alpha_t = exp(dt_t (A_t + i theta_t)),  beta_t = (1 - lambda_t) dt_t alpha_t,
+ *   gamma_t = lambda_t dt_t,                y_t = C_t^T h_t,
+ *
+ * with a complex state realised as a real one whose (2k, 2k+1) entries are
+ * rotated by the data-dependent angle dt_t theta_{t,k}, and MIMO rank R
+ * (B_t is N x R, x_t is P x R).  Sources (Mamba-3 pages):
+ *   - exponential-trapezoidal update: linkstar.cloud/article/869, section
+ *     "第一刀：指数梯形离散化 / Mamba-3的升级";
+ *   - complex state as 2x2 block rotations and its RoPE form: same page,
+ *     sections "第二刀：复值状态空间" and "RoPE技巧";
+ *   - MIMO: same page, section "第三刀：多输入多输出";
+ *   - chunked prefill, recurrent decode: same page, sections "第一刀"
+ *     (parallel form) and "训练怎么办" (chunked algorithm).
+ *
+ * Conventions shared by every call
+ *   - All tensor pointers are caller-owned DEVICE memory on the current CUDA
+ *     device, row-major and contiguous, base address 16-byte aligned.  The
+ *     library allocates no device memory; the prefill workspace is supplied by
+ *     the caller after a size query.
+ *   - Element type of the per-token inputs and of y is dims->dtype (fp32 or
+ *     bf16).  The state h is always fp32.  The carry (B_prev, x_prev) has the
+ *     input dtype.
+ *   - dt, A, lambda are already activated (dt >= 0, A <= 0, 0 <= lambda <= 1
+ *     for a stable recurrence; other values are computed as given); theta is
+ *     in radians.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t, NULL = legacy
+ *     default stream).  The return value reports argument validation and
+ *     launch status; on an argument error nothing is launched or written.
+ *     Device-side wait limits report through mamba3_device_status().
+ *   - Inputs must not overlap outputs, except that a state may be updated in
+ *     place where a call says so.
+ *   - Supported shapes: N even with 2 <= N <= 256, 1 <= P <= 128, P a
+ *     multiple of 4, 1 <= R <= 8, nheads >= 1, batch >= 0, seqlen >= 0.
+ *     Anything else returns M3_ERR_UNSUPPORTED.
+ */
+#ifndef MAMBA3_H
+#define MAMBA3_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    M3_OK = 0,
+    M3_ERR_INVALID_ARG = 1,   /* NULL / misaligned pointer, negative size, NULL dims */
+    M3_ERR_UNSUPPORTED = 2,   /* shape or dtype outside the supported set */
+    M3_ERR_WORKSPACE = 3,     /* workspace missing or smaller than the queried size */
+    M3_ERR_CUDA = 4,          /* a CUDA runtime call or kernel launch failed */
+    M3_ERR_TIMEOUT = 5        /* a device-side wait gave up (see mamba3_device_status) */
+} m3_status;
+
+typedef enum { M3_F32 = 0, M3_BF16 = 1 } m3_dtype;
+
+/* Problem sizes.  P = head dim, N = real state size (N/2 complex pairs),
+ * R = MIMO rank.  chunk = tokens per chunk of the prefill kernels, 0 = the
+ * library's choice; the result does not depend on it beyond rounding. */
+typedef struct {
+    int batch;
+    int seqlen;      /* L; ignored by mamba3_decode_step */
+    int nheads;      /* H */
+    int headdim;     /* P */
+    int dstate;      /* N */
+    int rank;        /* R */
+    int chunk;
+    int dtype;       /* m3_dtype */
+} m3_dims;
+
+/* Recurrent state of every (batch, head): the checkpoint between calls.
+ *   h      [batch][H][N][P] fp32, the true (unrotated) state after the last token;
+ *   B_prev [batch][H][R][N] dtype, that token's B (unrotated);
+ *   x_prev [batch][H][R][P] dtype, that token's x.
+ * (B_prev, x_prev) feed the next call's beta (left-endpoint) term. */
+typedef struct {
+    float *h;
+    void *B_prev;
+    void *x_prev;
+} m3_state;
+
+/*
+ * Workspace bytes mamba3_scan_fwd needs for `dims` on the current device
+ * (0 is a valid answer).  Returns M3_ERR_INVALID_ARG for NULL arguments and
+ * M3_ERR_UNSUPPORTED for unsupported shapes.
+ */
+m3_status mamba3_scan_fwd_workspace(const m3_dims *dims, size_t *bytes);
+
+/*
+ * Chunked prefill over L = dims->seqlen tokens of every (b, h) sequence.
+ *
+ * Inputs (dtype unless stated):
+ *   x      [batch][L][H][R][P]      B, C [batch][L][H][R][N]
+ *   dt, A, lambda [batch][L][H]     theta [batch][L][H][N/2]
+ *   state_in: initial state and carry, or NULL for h0 = 0 and no carry.
+ * Outputs:
+ *   y      [batch][L][H][R][P] dtype, y_t = C_t^T h_t (rounded once to dtype);
+ *   state_out: final state h_L (fp32) and carry (B_{L-1}, x_{L-1}); NULL = not
+ *     written.  state_out may equal state_in (in-place update); otherwise the
+ *     two must not overlap.
+ *   workspace: device buffer of at least the queried size (may be NULL when the
+ *     query returned 0).  It holds per-segment fp32 states between kernels.
+ * L = 0 copies state_in (or zeros) to state_out.
+ */
+m3_status mamba3_scan_fwd(const m3_dims *dims, const void *x, const void *B, const void *C,
+                          const void *dt, const void *A, const void *lambda, const void *theta,
+                          const m3_state *state_in, void *y, const m3_state *state_out,
+                          void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * One-token recurrent step for every (b, h), updating `state` in place
+ * (linkstar.cloud article, section "第一刀": the recursion used at inference).
+ *
+ * Inputs (dtype): x [batch][H][R][P]; B, C [batch][H][R][N];
+ *   dt, A, lambda [batch][H]; theta [batch][H][N/2].
+ * state: h (fp32) and carry; on return h is the state after this token and
+ *   the carry is (B, x) of this token.  All three pointers are required.
+ * Output: y [batch][H][R][P] dtype.
+ * dims->seqlen and dims->chunk are ignored.
+ */
+m3_status mamba3_decode_step(const m3_dims *dims, const void *x, const void *B, const void *C,
+                             const void *dt, const void *A, const void *lambda, const void *theta,
+                             const m3_state *state, void *y, void *stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the library's device status
+ * word on the current device.  Returns M3_OK, or M3_ERR_TIMEOUT when a kernel
+ * gave up a bounded wait since the last call (its outputs are then invalid),
+ * or M3_ERR_CUDA when the synchronisation itself failed.
+ */
+m3_status mamba3_device_status(void *stream);
+
+/* Human-readable name of a status code (static string). */
+const char *mamba3_status_string(int status);
+
+/* Number of kernels this library has launched since it was loaded (all
+ * devices, all streams); lets a caller count launches in a timed region. */
+uint64_t mamba3_launch_count(void);
+
+/* Kernels of the library, for tracing. */
+typedef enum {
+    M3_KERNEL_PREFILL_STATE = 0,    /* prefill pass 1: per-segment end states */
+    M3_KERNEL_SEGMENT_PASS = 1,     /* prefill pass 2: state passing across segments */
+    M3_KERNEL_PREFILL_OUTPUT = 2,   /* prefill pass 3: outputs, final state, carry */
+    M3_KERNEL_DECODE = 3,           /* decode step */
+    M3_KERNEL_COUNT = 4
+} m3_kernel;
+
+/*
+ * Starts tracing: each of the next `max_launches` launches of `kernel` (an
+ * m3_kernel) is bracketed by two CUDA events recorded on the stream it is
+ * launched on.  Events are created here on the current device (no device
+ * memory is allocated).  A trace already running is discarded.  Returns
+ * M3_ERR_INVALID_ARG for a bad kernel id or max_launches < 1.
+ */
+m3_status mamba3_trace_begin(int kernel, int max_launches);
+
+/*
+ * Ends tracing: waits for the traced launches, returns how many there were
+ * and their summed device time in milliseconds, and releases the events.
+ * Returns M3_ERR_INVALID_ARG when no trace is running.
+ */
+m3_status mamba3_trace_end(int *launches, double *total_ms);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int mamba3_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MAMBA3_H */

@@ -1,0 +1,276 @@
+// Host side of the C ABI declared in include/mamba3.h: argument validation,
+// planning of the prefill segments, kernel dispatch, status reporting.
+#include <atomic>
+#include <mutex>
+#include <vector>
+
+#include "m3_internal.cuh"
+
+namespace m3 {
+
+static std::atomic<uint64_t> g_launches{0};
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+// ---- tracing: event pairs around the launches of one kernel
+static std::mutex g_trace_mu;
+static int g_trace_kernel = -1;
+static int g_trace_max = 0;
+static std::vector<cudaEvent_t> g_trace_ev;   // [2 * max]: start, stop
+static int g_trace_n = 0;
+
+void trace_mark(int kernel, cudaStream_t s, int phase) {
+    std::lock_guard<std::mutex> lock(g_trace_mu);
+    if (kernel != g_trace_kernel || g_trace_n >= g_trace_max) return;
+    cudaEventRecord(g_trace_ev[2 * g_trace_n + phase], s);
+    if (phase == 1) ++g_trace_n;
+}
+
+static void trace_release_locked() {
+    for (cudaEvent_t e : g_trace_ev) cudaEventDestroy(e);
+    g_trace_ev.clear();
+    g_trace_kernel = -1;
+    g_trace_max = 0;
+    g_trace_n = 0;
+}
+
+// One status word per device (a module-scope __device__ variable exists once
+// per device context); kernels set bits, mamba3_device_status reads + clears.
+__device__ unsigned g_status_word;
+
+static constexpr int kMaxDevices = 64;
+static std::mutex g_mu;
+static unsigned *g_status_ptr[kMaxDevices];
+static int g_sms[kMaxDevices];
+
+unsigned *device_status_word() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_status_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+        g_status_ptr[dev] = static_cast<unsigned *>(p);
+    }
+    return g_status_ptr[dev];
+}
+
+int sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_sms[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            return 148;
+        g_sms[dev] = n;
+    }
+    return g_sms[dev];
+}
+
+}  // namespace m3
+
+using namespace m3;
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shape / dtype check shared by both entry points.
+m3_status check_dims(const m3_dims *d, bool prefill) {
+    if (!d) return M3_ERR_INVALID_ARG;
+    if (d->batch < 0 || d->nheads < 1 || (prefill && d->seqlen < 0) || d->chunk < 0)
+        return M3_ERR_INVALID_ARG;
+    if (d->dtype != M3_F32 && d->dtype != M3_BF16) return M3_ERR_UNSUPPORTED;
+    if (d->headdim < 1 || d->headdim > 128 || (d->headdim % 4) != 0) return M3_ERR_UNSUPPORTED;
+    if (d->dstate < 2 || d->dstate > 256 || (d->dstate % 2) != 0) return M3_ERR_UNSUPPORTED;
+    if (d->rank < 1 || d->rank > 8) return M3_ERR_UNSUPPORTED;
+    return M3_OK;
+}
+
+bool ptr_ok(const void *p) { return p && aligned16(p); }
+
+m3_status plan_scan(const m3_dims &d, ScanPlan *pl) {
+    if (!simt_plan(d, sm_count(), pl)) return M3_ERR_UNSUPPORTED;
+    return M3_OK;
+}
+
+size_t elem_size(int dtype) { return dtype == M3_F32 ? 4 : 2; }
+
+}  // namespace
+
+extern "C" {
+
+m3_status mamba3_scan_fwd_workspace(const m3_dims *dims, size_t *bytes) {
+    if (!bytes) return M3_ERR_INVALID_ARG;
+    m3_status st = check_dims(dims, true);
+    if (st != M3_OK) return st;
+    ScanPlan pl;
+    if ((st = plan_scan(*dims, &pl)) != M3_OK) return st;
+    *bytes = pl.ws_bytes;
+    return M3_OK;
+}
+
+m3_status mamba3_scan_fwd(const m3_dims *dims, const void *x, const void *B, const void *C,
+                          const void *dt, const void *A, const void *lambda, const void *theta,
+                          const m3_state *state_in, void *y, const m3_state *state_out,
+                          void *workspace, size_t workspace_bytes, void *stream) {
+    m3_status st = check_dims(dims, true);
+    if (st != M3_OK) return st;
+    const m3_dims &d = *dims;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool work = d.batch > 0 && d.seqlen > 0;
+    if (work) {
+        for (const void *p : {x, B, C, dt, A, lambda, theta, (const void *)y})
+            if (!ptr_ok(p)) return M3_ERR_INVALID_ARG;
+    }
+    if (state_in) {
+        if (!ptr_ok(state_in->h)) return M3_ERR_INVALID_ARG;
+        if ((state_in->B_prev == nullptr) != (state_in->x_prev == nullptr)) return M3_ERR_INVALID_ARG;
+        if (state_in->B_prev && (!aligned16(state_in->B_prev) || !aligned16(state_in->x_prev)))
+            return M3_ERR_INVALID_ARG;
+    }
+    if (state_out) {
+        if (!ptr_ok(state_out->h)) return M3_ERR_INVALID_ARG;
+        if ((state_out->B_prev == nullptr) != (state_out->x_prev == nullptr)) return M3_ERR_INVALID_ARG;
+        if (state_out->B_prev && (!aligned16(state_out->B_prev) || !aligned16(state_out->x_prev)))
+            return M3_ERR_INVALID_ARG;
+    }
+    ScanPlan pl;
+    if ((st = plan_scan(d, &pl)) != M3_OK) return st;
+    if (d.batch == 0) return M3_OK;
+
+    const size_t bh = (size_t)d.batch * d.nheads;
+    const size_t hbytes = bh * d.dstate * d.headdim * sizeof(float);
+    const size_t es = elem_size(d.dtype);
+    const size_t bbytes = bh * d.rank * d.dstate * es, xbytes = bh * d.rank * d.headdim * es;
+    if (!work) {
+        // L = 0: the state and carry pass through unchanged (zeros without state_in)
+        if (!state_out) return M3_OK;
+        cudaError_t e = cudaSuccess;
+        if (state_in && state_in->h != state_out->h)
+            e = cudaMemcpyAsync(state_out->h, state_in->h, hbytes, cudaMemcpyDeviceToDevice, s);
+        else if (!state_in)
+            e = cudaMemsetAsync(state_out->h, 0, hbytes, s);
+        if (e == cudaSuccess && state_out->B_prev) {
+            if (state_in && state_in->B_prev) {
+                if (state_in->B_prev != state_out->B_prev)
+                    e = cudaMemcpyAsync(state_out->B_prev, state_in->B_prev, bbytes, cudaMemcpyDeviceToDevice, s);
+                if (e == cudaSuccess && state_in->x_prev != state_out->x_prev)
+                    e = cudaMemcpyAsync(state_out->x_prev, state_in->x_prev, xbytes, cudaMemcpyDeviceToDevice, s);
+            } else {
+                e = cudaMemsetAsync(state_out->B_prev, 0, bbytes, s);
+                if (e == cudaSuccess) e = cudaMemsetAsync(state_out->x_prev, 0, xbytes, s);
+            }
+        }
+        return e == cudaSuccess ? M3_OK : M3_ERR_CUDA;
+    }
+    if (pl.ws_bytes > 0 && (!workspace || workspace_bytes < pl.ws_bytes || !aligned16(workspace)))
+        return M3_ERR_WORKSPACE;
+
+    ScanArgs a{};
+    a.dtype = d.dtype; a.batch = d.batch; a.L = d.seqlen; a.H = d.nheads;
+    a.P = d.headdim; a.N = d.dstate; a.R = d.rank;
+    a.x = x; a.B = B; a.C = C; a.dt = dt; a.A = A; a.lam = lambda; a.theta = theta;
+    a.h0 = state_in ? state_in->h : nullptr;
+    a.Bprev = state_in ? state_in->B_prev : nullptr;
+    a.xprev = state_in ? state_in->x_prev : nullptr;
+    a.y = y;
+    a.h_out = state_out ? state_out->h : nullptr;
+    a.Bprev_out = state_out ? state_out->B_prev : nullptr;
+    a.xprev_out = state_out ? state_out->x_prev : nullptr;
+    if (pl.ws_bytes > 0) {
+        const size_t state_b = bh * pl.nseg * d.dstate * d.headdim * sizeof(float);
+        a.ws_state = static_cast<float *>(workspace);
+        a.ws_tot = reinterpret_cast<float *>(static_cast<char *>(workspace) + ((state_b + 255) / 256) * 256);
+    }
+    cudaError_t e = simt_scan(a, pl, s);
+    return e == cudaSuccess ? M3_OK : M3_ERR_CUDA;
+}
+
+m3_status mamba3_decode_step(const m3_dims *dims, const void *x, const void *B, const void *C,
+                             const void *dt, const void *A, const void *lambda, const void *theta,
+                             const m3_state *state, void *y, void *stream) {
+    m3_status st = check_dims(dims, false);
+    if (st != M3_OK) return st;
+    if (!state) return M3_ERR_INVALID_ARG;
+    for (const void *p : {x, B, C, dt, A, lambda, theta, (const void *)y, (const void *)state->h,
+                          (const void *)state->B_prev, (const void *)state->x_prev})
+        if (!ptr_ok(p)) return M3_ERR_INVALID_ARG;
+    const m3_dims &d = *dims;
+    if (d.batch == 0) return M3_OK;
+    cudaError_t e = decode_step(d.dtype, d.batch, d.nheads, d.headdim, d.dstate, d.rank, x, B, C, dt,
+                                A, lambda, theta, state->h, state->B_prev, state->x_prev, y,
+                                static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? M3_OK : M3_ERR_CUDA;
+}
+
+m3_status mamba3_device_status(void *stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return M3_ERR_CUDA;
+    unsigned *w = device_status_word();
+    if (!w) return M3_ERR_CUDA;
+    unsigned v = 0;
+    if (cudaMemcpy(&v, w, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return M3_ERR_CUDA;
+    if (v != 0) {
+        const unsigned zero = 0;
+        if (cudaMemcpy(w, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return M3_ERR_CUDA;
+    }
+    return (v & kStatusTimeout) ? M3_ERR_TIMEOUT : M3_OK;
+}
+
+const char *mamba3_status_string(int status) {
+    switch (status) {
+        case M3_OK: return "ok";
+        case M3_ERR_INVALID_ARG: return "invalid argument";
+        case M3_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+        case M3_ERR_WORKSPACE: return "workspace missing or too small";
+        case M3_ERR_CUDA: return "CUDA error";
+        case M3_ERR_TIMEOUT: return "device-side wait timed out";
+        default: return "unknown status";
+    }
+}
+
+m3_status mamba3_trace_begin(int kernel, int max_launches) {
+    if (kernel < 0 || kernel >= M3_KERNEL_COUNT || max_launches < 1) return M3_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(g_trace_mu);
+    trace_release_locked();
+    g_trace_ev.resize(2 * (size_t)max_launches, nullptr);
+    for (auto &e : g_trace_ev) {
+        if (cudaEventCreate(&e) != cudaSuccess) {
+            e = nullptr;
+            for (auto &f : g_trace_ev)
+                if (f) cudaEventDestroy(f);
+            g_trace_ev.clear();
+            return M3_ERR_CUDA;
+        }
+    }
+    g_trace_kernel = kernel;
+    g_trace_max = max_launches;
+    g_trace_n = 0;
+    return M3_OK;
+}
+
+m3_status mamba3_trace_end(int *launches, double *total_ms) {
+    std::lock_guard<std::mutex> lock(g_trace_mu);
+    if (g_trace_kernel < 0) return M3_ERR_INVALID_ARG;
+    double total = 0.0;
+    m3_status st = M3_OK;
+    for (int i = 0; i < g_trace_n; ++i) {
+        float ms = 0.f;
+        if (cudaEventSynchronize(g_trace_ev[2 * i + 1]) != cudaSuccess ||
+            cudaEventElapsedTime(&ms, g_trace_ev[2 * i], g_trace_ev[2 * i + 1]) != cudaSuccess) {
+            st = M3_ERR_CUDA;
+            break;
+        }
+        total += ms;
+    }
+    if (launches) *launches = g_trace_n;
+    if (total_ms) *total_ms = total;
+    trace_release_locked();
+    return st;
+}
+
+uint64_t mamba3_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int mamba3_version(void) { return 100; }
+
+}  // extern "C"

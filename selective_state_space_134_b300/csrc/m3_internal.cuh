@@ -1,0 +1,78 @@
+// Internal declarations of the Mamba-3 recurrence library (not part of the C ABI).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/mamba3.h"
+
+namespace m3 {
+
+// ---------------------------------------------------------------- element types
+__device__ __forceinline__ float to_f(float v) { return v; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+template <typename T> __device__ __forceinline__ T from_f(float v);
+template <> __device__ __forceinline__ float from_f<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) {
+    return __float2bfloat16_rn(v);
+}
+
+// Device status word bits (read and cleared by mamba3_device_status).
+enum : unsigned { kStatusTimeout = 1u };
+
+// ---------------------------------------------------------------- launch plumbing
+void count_launch();                 // +1 to the library's launch counter
+// Tracing marks around a launch of `kernel` (m3_kernel) on stream s:
+// phase 0 just before the launch, phase 1 just after it.
+void trace_mark(int kernel, cudaStream_t s, int phase);
+unsigned *device_status_word();      // address of this device's status word (nullptr on error)
+int sm_count();                      // SMs of the current device (cached)
+
+// ---------------------------------------------------------------- prefill plan
+// Prefill runs over segments of `seglen` tokens (a multiple of the chunk Q).
+// Segment g of every (b, h) sequence starts from state H'_g:
+//   - pass 1 (segment_state, g < nseg-1): state at the segment end from a zero
+//     start, plus the segment's total log-decay and angles;
+//   - pass 2 (segment_pass): H'_0 = h0 + carry term, H'_{g+1} = T_g H'_g + S_g;
+//   - pass 3 (segment_output): y for every token of the segment and, for the
+//     last segment, the final state and carry.
+// With nseg == 1 only pass 3 runs and it reads h0 and the carry itself.
+struct ScanPlan {
+    int Q;        // tokens per chunk
+    int nseg;     // segments per sequence
+    int seglen;   // tokens per segment (multiple of Q), last one may be shorter
+    int path;     // kPathSimt or kPathTc
+    size_t ws_bytes;
+};
+enum { kPathSimt = 0, kPathTc = 1 };
+
+struct ScanArgs {
+    int dtype, batch, L, H, P, N, R;
+    const void *x, *B, *C, *dt, *A, *lam, *theta;
+    const float *h0;            // may be null (zero state)
+    const void *Bprev, *xprev;  // may be null (no carry)
+    void *y;
+    float *h_out;               // may be null
+    void *Bprev_out, *xprev_out;  // may be null
+    float *ws_state;            // [b*H][nseg][N][P]  (nseg > 1)
+    float *ws_tot;              // [b*H][nseg-1][1 + N/2]
+};
+
+// Workspace layout sizes (bytes) for a plan.
+size_t scan_workspace_bytes(int batch, int H, int N, int P, int nseg);
+
+// SIMT path (any supported shape and dtype).
+bool simt_plan(const m3_dims &d, int sms, ScanPlan *plan);   // false = unsupported
+cudaError_t simt_scan(const ScanArgs &a, const ScanPlan &plan, cudaStream_t s);
+
+// Segment state passing (shared by both paths).
+cudaError_t segment_pass(const ScanArgs &a, const ScanPlan &plan, cudaStream_t s);
+
+// Decode step.
+cudaError_t decode_step(int dtype, int batch, int H, int P, int N, int R, const void *x,
+                        const void *B, const void *C, const void *dt, const void *A,
+                        const void *lam, const void *theta, float *h, void *Bprev, void *xprev,
+                        void *y, cudaStream_t s);
+
+}  // namespace m3

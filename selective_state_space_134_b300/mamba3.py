@@ -1,0 +1,192 @@
+"""Python binding of libmamba3.so (the C ABI in include/mamba3.h).
+
+Argument marshalling only: tensors are passed as raw device pointers and every
+step of the recurrence runs in the library's CUDA kernels.  PyTorch provides
+device memory and the current stream.  There is no fallback: if the library is
+missing or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmamba3.so")
+
+M3_OK, M3_ERR_INVALID_ARG, M3_ERR_UNSUPPORTED, M3_ERR_WORKSPACE, M3_ERR_CUDA, M3_ERR_TIMEOUT = range(6)
+M3_F32, M3_BF16 = 0, 1
+_DTYPE_CODE = {torch.float32: M3_F32, torch.bfloat16: M3_BF16}
+
+
+class m3_dims(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int), ("seqlen", ctypes.c_int), ("nheads", ctypes.c_int),
+                ("headdim", ctypes.c_int), ("dstate", ctypes.c_int), ("rank", ctypes.c_int),
+                ("chunk", ctypes.c_int), ("dtype", ctypes.c_int)]
+
+
+class m3_state(ctypes.Structure):
+    _fields_ = [("h", ctypes.c_void_p), ("B_prev", ctypes.c_void_p), ("x_prev", ctypes.c_void_p)]
+
+
+class Mamba3Error(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Loads libmamba3.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m selective_state_space_134_b300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, dp, sp = ctypes.c_void_p, ctypes.POINTER(m3_dims), ctypes.POINTER(m3_state)
+        L.mamba3_scan_fwd_workspace.argtypes = [dp, ctypes.POINTER(ctypes.c_size_t)]
+        L.mamba3_scan_fwd_workspace.restype = ctypes.c_int
+        L.mamba3_scan_fwd.argtypes = [dp] + [vp] * 7 + [sp, vp, sp, vp, ctypes.c_size_t, vp]
+        L.mamba3_scan_fwd.restype = ctypes.c_int
+        L.mamba3_decode_step.argtypes = [dp] + [vp] * 7 + [sp, vp, vp]
+        L.mamba3_decode_step.restype = ctypes.c_int
+        L.mamba3_device_status.argtypes = [vp]
+        L.mamba3_device_status.restype = ctypes.c_int
+        L.mamba3_status_string.argtypes = [ctypes.c_int]
+        L.mamba3_status_string.restype = ctypes.c_char_p
+        L.mamba3_launch_count.argtypes = []
+        L.mamba3_launch_count.restype = ctypes.c_uint64
+        L.mamba3_trace_begin.argtypes = [ctypes.c_int, ctypes.c_int]
+        L.mamba3_trace_begin.restype = ctypes.c_int
+        L.mamba3_trace_end.argtypes = [ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_double)]
+        L.mamba3_trace_end.restype = ctypes.c_int
+        L.mamba3_version.argtypes = []
+        L.mamba3_version.restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().mamba3_status_string(int(status)).decode()
+
+
+def launch_count() -> int:
+    return int(lib().mamba3_launch_count())
+
+
+def _check(status: int, what: str):
+    if status != M3_OK:
+        raise Mamba3Error(status, what)
+
+
+def _stream_ptr(stream) -> Optional[int]:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return t.data_ptr()
+
+
+@dataclass
+class State:
+    """Recurrent state: h [b,H,N,P] fp32; carry B_prev [b,H,R,N], x_prev [b,H,R,P] (input dtype)."""
+    h: torch.Tensor
+    B_prev: Optional[torch.Tensor] = None
+    x_prev: Optional[torch.Tensor] = None
+
+    def c(self) -> m3_state:
+        return m3_state(_ptr(self.h), _ptr(self.B_prev), _ptr(self.x_prev))
+
+    @staticmethod
+    def zeros(batch, nheads, P, N, R, dtype, device="cuda") -> "State":
+        return State(torch.zeros(batch, nheads, N, P, dtype=torch.float32, device=device),
+                     torch.zeros(batch, nheads, R, N, dtype=dtype, device=device),
+                     torch.zeros(batch, nheads, R, P, dtype=dtype, device=device))
+
+
+def dims(batch, seqlen, nheads, P, N, R, dtype, chunk=0) -> m3_dims:
+    code = _DTYPE_CODE.get(dtype, dtype) if isinstance(dtype, torch.dtype) else int(dtype)
+    return m3_dims(batch, seqlen, nheads, P, N, R, chunk, code)
+
+
+def scan_fwd_workspace(d: m3_dims) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().mamba3_scan_fwd_workspace(ctypes.byref(d), ctypes.byref(n)), "mamba3_scan_fwd_workspace")
+    return int(n.value)
+
+
+def scan_fwd(x, B, C, dt, A, lam, theta, state_in: Optional[State] = None,
+             state_out: Optional[State] = None, chunk: int = 0, y: Optional[torch.Tensor] = None,
+             workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Chunked prefill.  x [b,L,H,R,P]; B, C [b,L,H,R,N]; dt, A, lam [b,L,H]; theta [b,L,H,N/2].
+
+    Returns y [b,L,H,R,P] (input dtype).  ``state_out`` (may be ``state_in``) receives the final
+    state and carry.  The workspace is allocated here through torch unless given.
+    """
+    b, L, H, R, P = x.shape
+    N = B.shape[-1]
+    d = dims(b, L, H, P, N, R, x.dtype, chunk)
+    if y is None:
+        y = torch.empty_like(x)
+    ws_bytes = scan_fwd_workspace(d)
+    if workspace is None and ws_bytes > 0:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=x.device)
+    st_in = state_in.c() if state_in is not None else None
+    st_out = state_out.c() if state_out is not None else None
+    rc = lib().mamba3_scan_fwd(ctypes.byref(d), _ptr(x), _ptr(B), _ptr(C), _ptr(dt), _ptr(A), _ptr(lam),
+                               _ptr(theta), ctypes.byref(st_in) if st_in is not None else None, _ptr(y),
+                               ctypes.byref(st_out) if st_out is not None else None,
+                               _ptr(workspace), workspace.numel() if workspace is not None else 0,
+                               _stream_ptr(stream))
+    _check(rc, "mamba3_scan_fwd")
+    return y
+
+
+def decode_step(x, B, C, dt, A, lam, theta, state: State, y: Optional[torch.Tensor] = None,
+                stream=None) -> torch.Tensor:
+    """One token for every (b, h).  x [b,H,R,P]; B, C [b,H,R,N]; dt, A, lam [b,H]; theta [b,H,N/2].
+
+    Updates ``state`` in place and returns y [b,H,R,P].
+    """
+    b, H, R, P = x.shape
+    N = B.shape[-1]
+    d = dims(b, 1, H, P, N, R, x.dtype)
+    if y is None:
+        y = torch.empty_like(x)
+    st = state.c()
+    rc = lib().mamba3_decode_step(ctypes.byref(d), _ptr(x), _ptr(B), _ptr(C), _ptr(dt), _ptr(A),
+                                  _ptr(lam), _ptr(theta), ctypes.byref(st), _ptr(y), _stream_ptr(stream))
+    _check(rc, "mamba3_decode_step")
+    return y
+
+
+KERNEL_PREFILL_STATE, KERNEL_SEGMENT_PASS, KERNEL_PREFILL_OUTPUT, KERNEL_DECODE = range(4)
+
+
+def trace_begin(kernel: int, max_launches: int):
+    """Brackets the next ``max_launches`` launches of ``kernel`` with CUDA events (library-side)."""
+    _check(lib().mamba3_trace_begin(int(kernel), int(max_launches)), "mamba3_trace_begin")
+
+
+def trace_end():
+    """Returns (launches, total_ms) of the traced kernel and stops tracing."""
+    n, ms = ctypes.c_int(0), ctypes.c_double(0.0)
+    _check(lib().mamba3_trace_end(ctypes.byref(n), ctypes.byref(ms)), "mamba3_trace_end")
+    return int(n.value), float(ms.value)
+
+
+def device_status(stream=None) -> int:
+    """Synchronises the stream and returns (and clears) the device status (M3_OK or M3_ERR_TIMEOUT)."""
+    return int(lib().mamba3_device_status(_stream_ptr(stream)))

@@ -1,0 +1,136 @@
+"""The C-ABI library: it loads, exports every symbol include/mamba3.h declares,
+and rejects bad arguments with a status code before launching anything.
+
+These run without a GPU.  On a machine with a GPU, the pointers handed to the
+library are real (tiny) device allocations, so a validation bug could never
+send a kernel to a bogus address.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import selective_state_space_134_b300 as m3
+from selective_state_space_134_b300 import mamba3 as api
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "mamba3.h")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(mamba3_\w+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol():
+    names = declared_functions()
+    assert {"mamba3_scan_fwd", "mamba3_decode_step", "mamba3_scan_fwd_workspace"} <= set(names)
+    lib = m3.lib()
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings_and_version():
+    assert m3.status_string(0) == "ok"
+    for code in range(1, 6):
+        assert m3.status_string(code) not in ("ok", "unknown status")
+    assert m3.status_string(99) == "unknown status"
+    assert m3.lib().mamba3_version() >= 100
+
+
+class Ptrs:
+    """16-byte aligned pointers: real device buffers when a GPU exists, else fake addresses."""
+
+    def __init__(self):
+        self.keep = []
+        self.gpu = torch.cuda.is_available()
+        self.fake = 0x100000
+
+    def get(self, nbytes=4096):
+        if self.gpu:
+            t = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+            self.keep.append(t)
+            return t.data_ptr()
+        self.fake += 1 << 20
+        return self.fake
+
+
+def call_scan(d, ptrs, overrides=None, state_in=None, state_out=None, ws=None, ws_bytes=0):
+    args = {k: ptrs.get() for k in ("x", "B", "C", "dt", "A", "lam", "theta", "y")}
+    args.update(overrides or {})
+    lib = m3.lib()
+    return lib.mamba3_scan_fwd(ctypes.byref(d) if d is not None else None, args["x"], args["B"], args["C"], args["dt"], args["A"],
+                               args["lam"], args["theta"], state_in, args["y"], state_out, ws, ws_bytes, None)
+
+
+def test_workspace_query_validates():
+    lib = m3.lib()
+    n = ctypes.c_size_t(0)
+    assert lib.mamba3_scan_fwd_workspace(None, ctypes.byref(n)) == api.M3_ERR_INVALID_ARG
+    d = m3.dims(4, 4096, 32, 64, 64, 1, torch.bfloat16)
+    assert lib.mamba3_scan_fwd_workspace(ctypes.byref(d), None) == api.M3_ERR_INVALID_ARG
+    assert lib.mamba3_scan_fwd_workspace(ctypes.byref(d), ctypes.byref(n)) == 0
+    for bad, code in [(dict(dstate=63), api.M3_ERR_UNSUPPORTED), (dict(dstate=258), api.M3_ERR_UNSUPPORTED),
+                      (dict(headdim=6), api.M3_ERR_UNSUPPORTED), (dict(headdim=132), api.M3_ERR_UNSUPPORTED),
+                      (dict(rank=9), api.M3_ERR_UNSUPPORTED), (dict(rank=0), api.M3_ERR_UNSUPPORTED),
+                      (dict(dtype=7), api.M3_ERR_UNSUPPORTED), (dict(batch=-1), api.M3_ERR_INVALID_ARG),
+                      (dict(seqlen=-5), api.M3_ERR_INVALID_ARG), (dict(nheads=0), api.M3_ERR_INVALID_ARG),
+                      (dict(chunk=-1), api.M3_ERR_INVALID_ARG)]:
+        dd = m3.dims(4, 4096, 32, 64, 64, 1, torch.bfloat16)
+        for k, v in bad.items():
+            setattr(dd, k, v)
+        assert lib.mamba3_scan_fwd_workspace(ctypes.byref(dd), ctypes.byref(n)) == code, bad
+
+
+def test_scan_rejects_bad_pointers_before_launch():
+    ptrs = Ptrs()
+    before = m3.launch_count()
+    d = m3.dims(1, 16, 2, 16, 16, 1, torch.float32)
+    assert call_scan(None, ptrs) == api.M3_ERR_INVALID_ARG
+    for k in ("x", "B", "C", "dt", "A", "lam", "theta", "y"):
+        assert call_scan(d, ptrs, {k: None}) == api.M3_ERR_INVALID_ARG, k
+        assert call_scan(d, ptrs, {k: ptrs.get() + 4}) == api.M3_ERR_INVALID_ARG, k   # misaligned
+    # state with a carry half missing
+    st = api.m3_state(ptrs.get(), ptrs.get(), None)
+    assert call_scan(d, ptrs, state_in=ctypes.byref(st)) == api.M3_ERR_INVALID_ARG
+    assert call_scan(d, ptrs, state_out=ctypes.byref(st)) == api.M3_ERR_INVALID_ARG
+    st = api.m3_state(None, None, None)
+    assert call_scan(d, ptrs, state_in=ctypes.byref(st)) == api.M3_ERR_INVALID_ARG
+    assert m3.launch_count() == before
+
+
+def test_scan_requires_workspace_when_queried_nonzero():
+    ptrs = Ptrs()
+    d = m3.dims(1, 1 << 16, 1, 16, 16, 1, torch.float32)   # one long sequence: segmented, needs workspace
+    need = m3.scan_fwd_workspace(d)
+    assert need > 0
+    before = m3.launch_count()
+    assert call_scan(d, ptrs) == api.M3_ERR_WORKSPACE
+    assert call_scan(d, ptrs, ws=ptrs.get(), ws_bytes=need - 1) == api.M3_ERR_WORKSPACE
+    assert m3.launch_count() == before
+
+
+def test_decode_rejects_bad_arguments_before_launch():
+    ptrs = Ptrs()
+    lib = m3.lib()
+    before = m3.launch_count()
+    d = m3.dims(2, 1, 2, 16, 16, 1, torch.bfloat16)
+    good = {k: ptrs.get() for k in ("x", "B", "C", "dt", "A", "lam", "theta", "y")}
+
+    def call(over=None, state="good"):
+        a = dict(good)
+        a.update(over or {})
+        st = api.m3_state(ptrs.get(), ptrs.get(), ptrs.get()) if state == "good" else state
+        return lib.mamba3_decode_step(ctypes.byref(d), a["x"], a["B"], a["C"], a["dt"], a["A"], a["lam"],
+                                      a["theta"], ctypes.byref(st) if st is not None else None, a["y"], None)
+
+    assert call(state=None) == api.M3_ERR_INVALID_ARG
+    assert call(state=api.m3_state(ptrs.get(), None, ptrs.get())) == api.M3_ERR_INVALID_ARG
+    for k in good:
+        assert call({k: None}) == api.M3_ERR_INVALID_ARG, k
+    dd = m3.dims(2, 1, 2, 16, 15, 1, torch.bfloat16)
+    assert lib.mamba3_decode_step(ctypes.byref(dd), *[good[k] for k in ("x", "B", "C", "dt", "A", "lam", "theta")],
+                                  None, good["y"], None) == api.M3_ERR_UNSUPPORTED
+    assert m3.launch_count() == before

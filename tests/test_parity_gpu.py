@@ -1,0 +1,212 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 CPU oracle.
+
+Metric: max|y - y_ref| / rms(y_ref) (and the same for the final state), with
+the tolerances of the Mamba-3 recurrence study: 1e-4 for fp32 inputs, 2e-2 for
+bf16 inputs (fp32 state on the GPU in both cases).  Small cases compare every
+element; full-size workloads compare sampled (b, h) sequences, which the
+oracle computes one by one on the same inputs.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import selective_state_space_134_b300 as m3
+from selective_state_space_134_b300.synth import WORKLOADS, decode_pool, decode_state, prefill_inputs, to_f64
+from helpers import KEYS, TOL, norm_err, oracle_full, oracle_slices
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from selective_state_space_134_b300 import build
+    build.build()
+    torch.cuda.init()
+
+
+def gpu_scan(inp, state_in=None, chunk=0, carry_out=True, inplace=False):
+    x = inp["x"]
+    b, L, H, R, P = x.shape
+    N = inp["B"].shape[-1]
+    if inplace:
+        st_out = state_in
+    else:
+        st_out = m3.State.zeros(b, H, P, N, R, x.dtype) if carry_out else \
+            m3.State(torch.zeros(b, H, N, P, device="cuda"))
+    y = m3.scan_fwd(*(inp[k] for k in KEYS), state_in=state_in, state_out=st_out, chunk=chunk)
+    assert m3.device_status() == m3.M3_OK
+    torch.cuda.synchronize()
+    return y, st_out
+
+
+def random_state(b, H, P, N, R, dtype, seed=0):
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    return m3.State(torch.randn(b, H, N, P, device="cuda", generator=g),
+                    torch.randn(b, H, R, N, device="cuda", generator=g).to(dtype),
+                    torch.randn(b, H, R, P, device="cuda", generator=g).to(dtype))
+
+
+SMALL = {
+    # name: (workload, overrides)
+    "tiny_f32": ("tiny_f32", {}),
+    "siso_n64_small": ("siso_n64", dict(batch=2, nheads=3, seqlen=300)),
+    "siso_n128_small": ("siso_n128", dict(batch=1, nheads=2, seqlen=333)),
+    "mimo_r4_small": ("mimo_r4", dict(batch=1, nheads=3, seqlen=201)),
+    "long_small_segmented": ("long_n128_r4", dict(batch=1, nheads=2, seqlen=1100)),
+    "siso_n64_small_f32": ("siso_n64", dict(batch=1, nheads=2, seqlen=300, dtype="f32")),
+    "mimo_r4_small_f32_segmented": ("mimo_r4", dict(batch=1, nheads=1, seqlen=777, dtype="f32")),
+    "odd_shapes_f32": ("tiny_f32", dict(N=2, P=4, R=3, seqlen=37, nheads=3)),
+    "odd_shapes_bf16": ("tiny_f32", dict(N=6, P=8, R=2, seqlen=65, nheads=2, dtype="bf16")),
+    "single_token": ("siso_n64", dict(batch=2, nheads=2, seqlen=1)),
+}
+
+
+@pytest.mark.parametrize("case", sorted(SMALL))
+@pytest.mark.parametrize("with_state", [False, True])
+def test_scan_small_matches_oracle(case, with_state):
+    wname, over = SMALL[case]
+    w = WORKLOADS[wname].with_(**over)
+    inp = prefill_inputs(w, "cuda")
+    st = random_state(w.batch, w.nheads, w.P, w.N, w.R, inp["x"].dtype) if with_state else None
+    y, so = gpu_scan(inp, state_in=st)
+    yr, hr, Br, xr = oracle_full(inp, st)
+    tol = TOL[w.dtype]
+    assert norm_err(to_f64(y), yr) <= tol
+    assert norm_err(to_f64(so.h), hr) <= tol
+    np.testing.assert_array_equal(to_f64(so.B_prev), Br)     # carry is a plain copy
+    np.testing.assert_array_equal(to_f64(so.x_prev), xr)
+
+
+@pytest.mark.parametrize("wname", ["siso_n64", "siso_n128", "mimo_r4", "long_n128_r4"])
+def test_scan_full_size_sampled(wname):
+    w = WORKLOADS[wname]
+    inp = prefill_inputs(w, "cuda")
+    y, so = gpu_scan(inp)
+    pairs = [(0, 0), (w.batch - 1, w.nheads - 1)] if wname == "long_n128_r4" else \
+        [(0, 0), (w.batch // 2, w.nheads // 3), (w.batch - 1, w.nheads - 1)]
+    # oracle: all sampled sequences stacked along the batch axis, one thread each
+    stack = {k: torch.cat([inp[k][b:b + 1, :, h:h + 1] for b, h in pairs], dim=0) for k in KEYS}
+    yr, hr, _, _ = oracle.scan(*(to_f64(stack[k]) for k in KEYS), nthreads=len(pairs))
+    for i, (b, h) in enumerate(pairs):
+        ey = norm_err(to_f64(y[b:b + 1, :, h:h + 1]), yr[i:i + 1])
+        eh = norm_err(to_f64(so.h[b:b + 1, h:h + 1]), hr[i:i + 1])
+        assert ey <= TOL[w.dtype], (b, h, ey)
+        assert eh <= TOL[w.dtype], (b, h, eh)
+    assert torch.isfinite(y.float()).all()
+
+
+@pytest.mark.parametrize("wname", ["decode_n64_r1", "decode_n64_r4", "decode_n128_r1", "decode_n128_r4"])
+def test_decode_full_size_matches_oracle(wname):
+    w = WORKLOADS[wname]
+    st = decode_state(w, "cuda")
+    state = m3.State(st["h"].clone(), st["B_prev"].clone(), st["x_prev"].clone())
+    pool = decode_pool(w, "cuda", pool=3)
+    ref_h, ref_B, ref_x = to_f64(st["h"]), to_f64(st["B_prev"]), to_f64(st["x_prev"])
+    for step, tok in enumerate(pool):
+        y = m3.decode_step(*(tok[k] for k in KEYS), state=state)
+        assert m3.device_status() == m3.M3_OK
+        yr, ref_h, ref_B, ref_x = oracle.decode_step(*(to_f64(tok[k]) for k in KEYS), ref_h, ref_B, ref_x)
+        assert norm_err(to_f64(y), yr) <= TOL[w.dtype], step
+        assert norm_err(to_f64(state.h), ref_h) <= 1e-5, step      # fp32 state, exact-input update
+        np.testing.assert_array_equal(to_f64(state.B_prev), ref_B)
+        np.testing.assert_array_equal(to_f64(state.x_prev), ref_x)
+
+
+def test_decode_f32_tight():
+    w = WORKLOADS["tiny_f32"].with_(batch=3, nheads=5, N=32, P=16, R=2)
+    st = decode_state(w, "cuda")
+    state = m3.State(st["h"].clone(), st["B_prev"].clone(), st["x_prev"].clone())
+    tok = decode_pool(w, "cuda", pool=1)[0]
+    y = m3.decode_step(*(tok[k] for k in KEYS), state=state)
+    yr, hr, _, _ = oracle.decode_step(*(to_f64(tok[k]) for k in KEYS), to_f64(st["h"]), to_f64(st["B_prev"]),
+                                      to_f64(st["x_prev"]))
+    assert norm_err(to_f64(y), yr) <= 1e-5
+    assert norm_err(to_f64(state.h), hr) <= 1e-5
+
+
+# ---------------------------------------------------------------- GPU-side invariants
+
+def test_chunk_length_does_not_change_the_result():
+    w = WORKLOADS["mimo_r4"].with_(batch=1, nheads=2, seqlen=150, dtype="f32", R=2)
+    inp = prefill_inputs(w, "cuda")
+    ys = [gpu_scan(inp, chunk=q)[0] for q in (0, 1, 7, 32, 64)]
+    for y in ys[1:]:
+        assert norm_err(to_f64(y), to_f64(ys[0])) <= 1e-5
+
+
+def test_split_prefill_and_decode_resume_equal_full_prefill():
+    w = WORKLOADS["siso_n64"].with_(batch=2, nheads=2, seqlen=200)
+    inp = prefill_inputs(w, "cuda")
+    y_full, s_full = gpu_scan(inp)
+    L1 = 77
+    first = {k: v[:, :L1].contiguous() for k, v in inp.items()}
+    rest = {k: v[:, L1:].contiguous() for k, v in inp.items()}
+    y1, s1 = gpu_scan(first)
+    y2, s2 = gpu_scan(rest, state_in=s1)
+    tol = TOL[w.dtype]
+    assert norm_err(to_f64(torch.cat([y1, y2], 1)), to_f64(y_full)) <= tol
+    assert norm_err(to_f64(s2.h), to_f64(s_full.h)) <= 1e-4
+    # prefill L - k tokens, then k decode steps
+    k = 5
+    head = {kk: v[:, :-k].contiguous() for kk, v in inp.items()}
+    _, st = gpu_scan(head)
+    for t in range(w.seqlen - k, w.seqlen):
+        yt = m3.decode_step(*(inp[kk][:, t].contiguous() for kk in KEYS), state=st)
+        assert norm_err(to_f64(yt), to_f64(y_full[:, t])) <= tol
+    assert norm_err(to_f64(st.h), to_f64(s_full.h)) <= 1e-4
+
+
+def test_in_place_state_update_equals_out_of_place():
+    w = WORKLOADS["siso_n64"].with_(batch=2, nheads=3, seqlen=130)
+    inp = prefill_inputs(w, "cuda")
+    st = random_state(w.batch, w.nheads, w.P, w.N, w.R, inp["x"].dtype, seed=3)
+    st_copy = m3.State(st.h.clone(), st.B_prev.clone(), st.x_prev.clone())
+    y1, s1 = gpu_scan(inp, state_in=st_copy)
+    y2, s2 = gpu_scan(inp, state_in=st, inplace=True)
+    assert torch.equal(y1, y2)
+    assert torch.equal(s1.h, st.h) and torch.equal(s1.B_prev, st.B_prev) and torch.equal(s1.x_prev, st.x_prev)
+
+
+def test_in_place_segmented_long_sequence():
+    w = WORKLOADS["long_n128_r4"].with_(batch=1, nheads=1, seqlen=3000)
+    inp = prefill_inputs(w, "cuda")
+    st = random_state(1, 1, w.P, w.N, w.R, inp["x"].dtype, seed=4)
+    ref = oracle_full(inp, st)
+    y, _ = gpu_scan(inp, state_in=st, inplace=True)
+    assert norm_err(to_f64(y), ref[0]) <= TOL[w.dtype]
+    assert norm_err(to_f64(st.h), ref[1]) <= TOL[w.dtype]
+
+
+def test_empty_sequence_and_empty_batch():
+    w = WORKLOADS["siso_n64"].with_(batch=2, nheads=2, seqlen=0)
+    inp = prefill_inputs(w, "cuda")
+    st = random_state(2, 2, w.P, w.N, w.R, inp["x"].dtype, seed=5)
+    y, so = gpu_scan(inp, state_in=st)
+    assert y.numel() == 0
+    assert torch.equal(so.h, st.h) and torch.equal(so.B_prev, st.B_prev) and torch.equal(so.x_prev, st.x_prev)
+    _, so = gpu_scan(inp)          # no state in: zeros out
+    assert not so.h.any() and not so.B_prev.float().any()
+    w0 = WORKLOADS["siso_n64"].with_(batch=0, seqlen=16)
+    inp0 = prefill_inputs(w0, "cuda")
+    before = m3.launch_count()
+    y0, _ = gpu_scan(inp0)
+    assert y0.numel() == 0 and m3.launch_count() == before
+
+
+def test_theta_pi_parity_sign_flips_on_gpu():
+    """The parity mechanism (rotation by pi per 1 bit) through the CUDA path."""
+    L = 64
+    bits = torch.randint(0, 2, (L,), generator=torch.Generator().manual_seed(0))
+    x = torch.ones(1, L, 1, 1, 4)
+    B = torch.zeros(1, L, 1, 1, 2)
+    C = torch.zeros(1, L, 1, 1, 2)
+    C[..., 0] = 1.0
+    inp = {"x": x, "B": B, "C": C, "dt": torch.ones(1, L, 1), "A": torch.zeros(1, L, 1),
+           "lam": torch.ones(1, L, 1), "theta": (torch.pi * bits.float()).reshape(1, L, 1, 1)}
+    inp = {k: v.cuda() for k, v in inp.items()}
+    h0 = torch.zeros(1, 1, 2, 4, device="cuda")
+    h0[0, 0, 0] = 1.0
+    y, _ = gpu_scan(inp, state_in=m3.State(h0))
+    expect = (-1.0) ** torch.cumsum(bits, 0).double()
+    np.testing.assert_allclose(to_f64(y[0, :, 0, 0, 0]), expect.numpy(), atol=1e-5)
