@@ -21,12 +21,16 @@
  *
  * Conventions shared by every call
  *   - All tensor pointers are caller-owned DEVICE memory on the current CUDA
- *     device, row-major and contiguous, base address 16-byte aligned.  The
+ *     device, row-major and contiguous.  The fp32 state h and the workspace
+ *     must be 16-byte aligned; every other pointer must be aligned to its
+ *     element size (a misaligned or NULL pointer is M3_ERR_INVALID_ARG).  The
  *     library allocates no device memory; the prefill workspace is supplied by
  *     the caller after a size query.
- *   - Element type of the per-token inputs and of y is dims->dtype (fp32 or
- *     bf16).  The state h is always fp32.  The carry (B_prev, x_prev) has the
- *     input dtype.
+ *   - Element type of the per-token inputs is dims->dtype (fp32 or bf16).
+ *     The outputs y and the state h are always fp32: rounding y to bf16 would
+ *     by itself cost up to half a bf16 ulp of the largest |y|, about 1-2 % of
+ *     rms(y), which is the whole error budget of a bf16-input run.  The carry
+ *     (B_prev, x_prev) has the input dtype.
  *   - dt, A, lambda are already activated (dt >= 0, A <= 0, 0 <= lambda <= 1
  *     for a stable recurrence; other values are computed as given); theta is
  *     in radians.
@@ -34,6 +38,8 @@
  *     default stream).  The return value reports argument validation and
  *     launch status; on an argument error nothing is launched or written.
  *     Device-side wait limits report through mamba3_device_status().
+ *   - batch = 0 is a successful call that touches nothing (pointers are not
+ *     inspected).
  *   - Inputs must not overlap outputs, except that a state may be updated in
  *     place where a call says so.
  *   - Supported shapes: N even with 2 <= N <= 256, 1 <= P <= 128, P a
@@ -101,7 +107,7 @@ m3_status mamba3_scan_fwd_workspace(const m3_dims *dims, size_t *bytes);
  *   dt, A, lambda [batch][L][H]     theta [batch][L][H][N/2]
  *   state_in: initial state and carry, or NULL for h0 = 0 and no carry.
  * Outputs:
- *   y      [batch][L][H][R][P] dtype, y_t = C_t^T h_t (rounded once to dtype);
+ *   y      [batch][L][H][R][P] fp32, y_t = C_t^T h_t;
  *   state_out: final state h_L (fp32) and carry (B_{L-1}, x_{L-1}); NULL = not
  *     written.  state_out may equal state_in (in-place update); otherwise the
  *     two must not overlap.
@@ -122,7 +128,7 @@ m3_status mamba3_scan_fwd(const m3_dims *dims, const void *x, const void *B, con
  *   dt, A, lambda [batch][H]; theta [batch][H][N/2].
  * state: h (fp32) and carry; on return h is the state after this token and
  *   the carry is (B, x) of this token.  All three pointers are required.
- * Output: y [batch][H][R][P] dtype.
+ * Output: y [batch][H][R][P] fp32.
  * dims->seqlen and dims->chunk are ignored.
  */
 m3_status mamba3_decode_step(const m3_dims *dims, const void *x, const void *B, const void *C,

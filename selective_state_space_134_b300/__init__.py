@@ -4,8 +4,10 @@ The compute lives in ``libmamba3.so`` (hand-written CUDA behind the C ABI of
 ``include/mamba3.h``); :mod:`.mamba3` is its ctypes binding and :mod:`.synth`
 the seeded synthetic-input generator.
 """
-from .mamba3 import (M3_BF16, M3_F32, M3_OK, Mamba3Error, State, decode_step, device_status, dims,
-                     launch_count, lib, scan_fwd, scan_fwd_workspace, status_string)
+from .mamba3 import (KERNEL_DECODE, KERNEL_PREFILL_OUTPUT, KERNEL_PREFILL_STATE, KERNEL_SEGMENT_PASS, M3_BF16,
+                     M3_F32, M3_OK, Mamba3Error, State, decode_step, device_status, dims, launch_count, lib,
+                     scan_fwd, scan_fwd_workspace, status_string, trace_begin, trace_end)
 
-__all__ = ["M3_BF16", "M3_F32", "M3_OK", "Mamba3Error", "State", "decode_step", "device_status", "dims",
-           "launch_count", "lib", "scan_fwd", "scan_fwd_workspace", "status_string"]
+__all__ = ["KERNEL_DECODE", "KERNEL_PREFILL_OUTPUT", "KERNEL_PREFILL_STATE", "KERNEL_SEGMENT_PASS", "M3_BF16",
+           "M3_F32", "M3_OK", "Mamba3Error", "State", "decode_step", "device_status", "dims", "launch_count",
+           "lib", "scan_fwd", "scan_fwd_workspace", "status_string", "trace_begin", "trace_end"]

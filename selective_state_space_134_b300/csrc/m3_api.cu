@@ -87,7 +87,9 @@ m3_status check_dims(const m3_dims *d, bool prefill) {
     return M3_OK;
 }
 
-bool ptr_ok(const void *p) { return p && aligned16(p); }
+// Per-token inputs, y and the carry need only element alignment; the fp32
+// state and the workspace are read as float4 and need 16 bytes.
+bool ptr_ok(const void *p, size_t align) { return p && (reinterpret_cast<uintptr_t>(p) % align) == 0; }
 
 m3_status plan_scan(const m3_dims &d, ScanPlan *pl) {
     if (!simt_plan(d, sm_count(), pl)) return M3_ERR_UNSUPPORTED;
@@ -118,30 +120,25 @@ m3_status mamba3_scan_fwd(const m3_dims *dims, const void *x, const void *B, con
     if (st != M3_OK) return st;
     const m3_dims &d = *dims;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const bool work = d.batch > 0 && d.seqlen > 0;
+    if (d.batch == 0) return M3_OK;   // nothing to read or write; pointers are not inspected
+    const bool work = d.seqlen > 0;
+    const size_t es = elem_size(d.dtype);
     if (work) {
-        for (const void *p : {x, B, C, dt, A, lambda, theta, (const void *)y})
-            if (!ptr_ok(p)) return M3_ERR_INVALID_ARG;
+        for (const void *p : {x, B, C, dt, A, lambda, theta})
+            if (!ptr_ok(p, es)) return M3_ERR_INVALID_ARG;
+        if (!ptr_ok(y, 4)) return M3_ERR_INVALID_ARG;
     }
-    if (state_in) {
-        if (!ptr_ok(state_in->h)) return M3_ERR_INVALID_ARG;
-        if ((state_in->B_prev == nullptr) != (state_in->x_prev == nullptr)) return M3_ERR_INVALID_ARG;
-        if (state_in->B_prev && (!aligned16(state_in->B_prev) || !aligned16(state_in->x_prev)))
-            return M3_ERR_INVALID_ARG;
-    }
-    if (state_out) {
-        if (!ptr_ok(state_out->h)) return M3_ERR_INVALID_ARG;
-        if ((state_out->B_prev == nullptr) != (state_out->x_prev == nullptr)) return M3_ERR_INVALID_ARG;
-        if (state_out->B_prev && (!aligned16(state_out->B_prev) || !aligned16(state_out->x_prev)))
-            return M3_ERR_INVALID_ARG;
+    for (const m3_state *st : {state_in, state_out}) {
+        if (!st) continue;
+        if (!ptr_ok(st->h, 16)) return M3_ERR_INVALID_ARG;
+        if ((st->B_prev == nullptr) != (st->x_prev == nullptr)) return M3_ERR_INVALID_ARG;
+        if (st->B_prev && (!ptr_ok(st->B_prev, es) || !ptr_ok(st->x_prev, es))) return M3_ERR_INVALID_ARG;
     }
     ScanPlan pl;
     if ((st = plan_scan(d, &pl)) != M3_OK) return st;
-    if (d.batch == 0) return M3_OK;
 
     const size_t bh = (size_t)d.batch * d.nheads;
     const size_t hbytes = bh * d.dstate * d.headdim * sizeof(float);
-    const size_t es = elem_size(d.dtype);
     const size_t bbytes = bh * d.rank * d.dstate * es, xbytes = bh * d.rank * d.headdim * es;
     if (!work) {
         // L = 0: the state and carry pass through unchanged (zeros without state_in)
@@ -192,12 +189,15 @@ m3_status mamba3_decode_step(const m3_dims *dims, const void *x, const void *B, 
                              const m3_state *state, void *y, void *stream) {
     m3_status st = check_dims(dims, false);
     if (st != M3_OK) return st;
-    if (!state) return M3_ERR_INVALID_ARG;
-    for (const void *p : {x, B, C, dt, A, lambda, theta, (const void *)y, (const void *)state->h,
-                          (const void *)state->B_prev, (const void *)state->x_prev})
-        if (!ptr_ok(p)) return M3_ERR_INVALID_ARG;
     const m3_dims &d = *dims;
-    if (d.batch == 0) return M3_OK;
+    if (d.batch == 0) return M3_OK;   // nothing to read or write; pointers are not inspected
+    if (!state) return M3_ERR_INVALID_ARG;
+    const size_t es = elem_size(d.dtype);
+    for (const void *p : {x, B, C, dt, A, lambda, theta, (const void *)state->B_prev,
+                          (const void *)state->x_prev})
+        if (!ptr_ok(p, es)) return M3_ERR_INVALID_ARG;
+    if (!ptr_ok(y, 4)) return M3_ERR_INVALID_ARG;
+    if (!ptr_ok(state->h, 16)) return M3_ERR_INVALID_ARG;
     cudaError_t e = decode_step(d.dtype, d.batch, d.nheads, d.headdim, d.dstate, d.rank, x, B, C, dt,
                                 A, lambda, theta, state->h, state->B_prev, state->x_prev, y,
                                 static_cast<cudaStream_t>(stream));

@@ -4,7 +4,7 @@
 // (linkstar.cloud/article/869, sections "第一刀" and "第二刀"):
 //   h   <- rho R(dt theta_k) [h + (1 - lambda) dt B_prev x_prev^T] + lambda dt B x^T,
 //   rho  = exp(dt A),   R(a) = [[cos a, -sin a], [sin a, cos a]],
-//   y    = C^T h   (R x P),   carry <- (B, x).
+//   y    = C^T h   (R x P, fp32),   carry <- (B, x).
 // B x^T is the rank-R product of B (N x R) and x^T (R x P) ("第三刀").
 //
 // The state streams through once (read + write, 8 N P bytes per head); it is
@@ -31,7 +31,7 @@ __global__ void __launch_bounds__(kThreads)
 decode_kernel(int H, int P, int N, int R, const T *__restrict__ x, const T *__restrict__ Bm,
               const T *__restrict__ Cm, const T *__restrict__ dtp, const T *__restrict__ Ap,
               const T *__restrict__ lp, const T *__restrict__ thp, float *__restrict__ hs,
-              T *__restrict__ Bprev, T *__restrict__ xprev, T *__restrict__ y) {
+              T *__restrict__ Bprev, T *__restrict__ xprev, float *__restrict__ y) {
     extern __shared__ float sm[];
     const int K = N / 2, RN = R * N, RP = R * P;
     float *sB = sm, *sC = sB + RN, *sBp = sC + RN, *sx = sBp + RN, *sxp = sx + RP;
@@ -132,7 +132,7 @@ decode_kernel(int H, int P, int N, int R, const T *__restrict__ x, const T *__re
     for (int i = tid; i < RP; i += kThreads) {
         float v = 0.f;
         for (int g = 0; g < KG; ++g) v += red[g * RP + i];
-        y[bh * RP + i] = from_f<T>(v);
+        y[bh * RP + i] = v;
     }
 }
 
@@ -155,7 +155,7 @@ cudaError_t launch_decode(int batch, int H, int P, int N, int R, const void *x, 
         if (e != cudaSuccess) return e;                                                           \
         kern<<<grid, kThreads, smem, s>>>(H, P, N, R, (const T *)x, (const T *)B, (const T *)C,  \
                                           (const T *)dt, (const T *)A, (const T *)lam,            \
-                                          (const T *)theta, h, (T *)Bprev, (T *)xprev, (T *)y);   \
+                                          (const T *)theta, h, (T *)Bprev, (T *)xprev, (float *)y);   \
     } while (0)
     trace_mark(M3_KERNEL_DECODE, s, 0);
     if (pairs_per_thread <= 4)

@@ -132,14 +132,14 @@ def scan_fwd(x, B, C, dt, A, lam, theta, state_in: Optional[State] = None,
              workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     """Chunked prefill.  x [b,L,H,R,P]; B, C [b,L,H,R,N]; dt, A, lam [b,L,H]; theta [b,L,H,N/2].
 
-    Returns y [b,L,H,R,P] (input dtype).  ``state_out`` (may be ``state_in``) receives the final
+    Returns y [b,L,H,R,P] (fp32).  ``state_out`` (may be ``state_in``) receives the final
     state and carry.  The workspace is allocated here through torch unless given.
     """
     b, L, H, R, P = x.shape
     N = B.shape[-1]
     d = dims(b, L, H, P, N, R, x.dtype, chunk)
     if y is None:
-        y = torch.empty_like(x)
+        y = torch.empty(x.shape, dtype=torch.float32, device=x.device)
     ws_bytes = scan_fwd_workspace(d)
     if workspace is None and ws_bytes > 0:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=x.device)
@@ -158,13 +158,13 @@ def decode_step(x, B, C, dt, A, lam, theta, state: State, y: Optional[torch.Tens
                 stream=None) -> torch.Tensor:
     """One token for every (b, h).  x [b,H,R,P]; B, C [b,H,R,N]; dt, A, lam [b,H]; theta [b,H,N/2].
 
-    Updates ``state`` in place and returns y [b,H,R,P].
+    Updates ``state`` in place and returns y [b,H,R,P] (fp32).
     """
     b, H, R, P = x.shape
     N = B.shape[-1]
     d = dims(b, 1, H, P, N, R, x.dtype)
     if y is None:
-        y = torch.empty_like(x)
+        y = torch.empty(x.shape, dtype=torch.float32, device=x.device)
     st = state.c()
     rc = lib().mamba3_decode_step(ctypes.byref(d), _ptr(x), _ptr(B), _ptr(C), _ptr(dt), _ptr(A),
                                   _ptr(lam), _ptr(theta), ctypes.byref(st), _ptr(y), _stream_ptr(stream))

@@ -91,12 +91,14 @@ def test_scan_rejects_bad_pointers_before_launch():
     assert call_scan(None, ptrs) == api.M3_ERR_INVALID_ARG
     for k in ("x", "B", "C", "dt", "A", "lam", "theta", "y"):
         assert call_scan(d, ptrs, {k: None}) == api.M3_ERR_INVALID_ARG, k
-        assert call_scan(d, ptrs, {k: ptrs.get() + 4}) == api.M3_ERR_INVALID_ARG, k   # misaligned
+        assert call_scan(d, ptrs, {k: ptrs.get() + 2}) == api.M3_ERR_INVALID_ARG, k   # misaligned fp32
     # state with a carry half missing
     st = api.m3_state(ptrs.get(), ptrs.get(), None)
     assert call_scan(d, ptrs, state_in=ctypes.byref(st)) == api.M3_ERR_INVALID_ARG
     assert call_scan(d, ptrs, state_out=ctypes.byref(st)) == api.M3_ERR_INVALID_ARG
     st = api.m3_state(None, None, None)
+    assert call_scan(d, ptrs, state_in=ctypes.byref(st)) == api.M3_ERR_INVALID_ARG
+    st = api.m3_state(ptrs.get() + 4, None, None)      # fp32 state needs 16 bytes
     assert call_scan(d, ptrs, state_in=ctypes.byref(st)) == api.M3_ERR_INVALID_ARG
     assert m3.launch_count() == before
 
