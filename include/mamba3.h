@@ -120,6 +120,35 @@ m3_status mamba3_scan_fwd(const m3_dims *dims, const void *x, const void *B, con
                           const m3_state *state_in, void *y, const m3_state *state_out,
                           void *workspace, size_t workspace_bytes, void *stream);
 
+/* Size of the static scratch array behind mamba3_scan_fwd_noalloc (16 MiB). */
+#define M3_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/*
+ * mamba3_scan_fwd without a caller-provided workspace, for callers that cannot
+ * allocate device memory: a runtime or engine that owns and pre-plans every
+ * device allocation and forbids extra ones, a latency-critical path that
+ * cannot afford cudaMalloc's implicit synchronisation, or a plain C caller
+ * with no allocator at hand.  (The Mamba-3 pages have no counterpart; this is
+ * an interface convenience, not part of the method.)
+ *
+ * Same arguments, results and errors as mamba3_scan_fwd minus the workspace.
+ * The scratch is a static device array of M3_NOALLOC_SCRATCH_BYTES inside the
+ * library; every GPU that loads the library holds it until the process exits.
+ * A problem whose workspace query exceeds that size returns M3_ERR_WORKSPACE
+ * before anything is launched.  The call allocates nothing (no cudaMalloc,
+ * cudaFree or allocating library routine).
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - All calls share the one array and it keeps the last call's contents
+ *     (nothing in it needs to start at zero).  Calls that overlap on the GPU
+ *     (concurrent streams, other host threads) race on it: serialise them.
+ */
+m3_status mamba3_scan_fwd_noalloc(const m3_dims *dims, const void *x, const void *B, const void *C,
+                                  const void *dt, const void *A, const void *lambda, const void *theta,
+                                  const m3_state *state_in, void *y, const m3_state *state_out,
+                                  void *stream);
+
 /*
  * One-token recurrent step for every (b, h), updating `state` in place
  * (linkstar.cloud article, section "第一刀": the recursion used at inference).

@@ -190,3 +190,30 @@ def trace_end():
 def device_status(stream=None) -> int:
     """Synchronises the stream and returns (and clears) the device status (M3_OK or M3_ERR_TIMEOUT)."""
     return int(lib().mamba3_device_status(_stream_ptr(stream)))
+
+
+def scan_fwd_noalloc(x, B, C, dt, A, lam, theta, state_in: Optional[State] = None,
+                     state_out: Optional[State] = None, chunk: int = 0, y: Optional[torch.Tensor] = None,
+                     stream=None) -> torch.Tensor:
+    """mamba3_scan_fwd_noalloc: the prefill with the library's static scratch instead of a workspace.
+
+    For callers that cannot allocate device memory (see include/mamba3.h); y is still passed in
+    or, as a convenience of this binding, allocated here through torch.
+    """
+    L_ = lib()
+    fn = L_.mamba3_scan_fwd_noalloc
+    fn.argtypes = [ctypes.POINTER(m3_dims)] + [ctypes.c_void_p] * 7 + \
+        [ctypes.POINTER(m3_state), ctypes.c_void_p, ctypes.POINTER(m3_state), ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    b, L, H, R, P = x.shape
+    N = B.shape[-1]
+    d = dims(b, L, H, P, N, R, x.dtype, chunk)
+    if y is None:
+        y = torch.empty(x.shape, dtype=torch.float32, device=x.device)
+    st_in = state_in.c() if state_in is not None else None
+    st_out = state_out.c() if state_out is not None else None
+    rc = fn(ctypes.byref(d), _ptr(x), _ptr(B), _ptr(C), _ptr(dt), _ptr(A), _ptr(lam), _ptr(theta),
+            ctypes.byref(st_in) if st_in is not None else None, _ptr(y),
+            ctypes.byref(st_out) if st_out is not None else None, _stream_ptr(stream))
+    _check(rc, "mamba3_scan_fwd_noalloc")
+    return y
