@@ -91,8 +91,19 @@ m3_status check_dims(const m3_dims *d, bool prefill) {
 // state and the workspace are read as float4 and need 16 bytes.
 bool ptr_ok(const void *p, size_t align) { return p && (reinterpret_cast<uintptr_t>(p) % align) == 0; }
 
-m3_status plan_scan(const m3_dims &d, ScanPlan *pl) {
-    if (!simt_plan(d, sm_count(), pl)) return M3_ERR_UNSUPPORTED;
+// The workspace covers both plans, so a call may take either path: the
+// tensor-core one when the shape is supported and the pointers are 16-byte
+// aligned (TMA), the SIMT one otherwise.
+m3_status plan_scan(const m3_dims &d, ScanPlan *simt, ScanPlan *tc, bool *has_tc, size_t *ws) {
+    const int sms = sm_count();
+    const bool ok_simt = simt_plan(d, sms, simt);
+    *has_tc = tc_plan(d, sms, tc);
+    if (!ok_simt && !*has_tc) return M3_ERR_UNSUPPORTED;
+    size_t w = 0;
+    if (ok_simt) w = simt->ws_bytes;
+    else simt->path = -1;
+    if (*has_tc && tc->ws_bytes > w) w = tc->ws_bytes;
+    *ws = w;
     return M3_OK;
 }
 
@@ -106,9 +117,9 @@ m3_status mamba3_scan_fwd_workspace(const m3_dims *dims, size_t *bytes) {
     if (!bytes) return M3_ERR_INVALID_ARG;
     m3_status st = check_dims(dims, true);
     if (st != M3_OK) return st;
-    ScanPlan pl;
-    if ((st = plan_scan(*dims, &pl)) != M3_OK) return st;
-    *bytes = pl.ws_bytes;
+    ScanPlan simt, tc;
+    bool has_tc = false;
+    if ((st = plan_scan(*dims, &simt, &tc, &has_tc, bytes)) != M3_OK) return st;
     return M3_OK;
 }
 
@@ -134,8 +145,15 @@ m3_status mamba3_scan_fwd(const m3_dims *dims, const void *x, const void *B, con
         if ((st->B_prev == nullptr) != (st->x_prev == nullptr)) return M3_ERR_INVALID_ARG;
         if (st->B_prev && (!ptr_ok(st->B_prev, es) || !ptr_ok(st->x_prev, es))) return M3_ERR_INVALID_ARG;
     }
-    ScanPlan pl;
-    if ((st = plan_scan(d, &pl)) != M3_OK) return st;
+    ScanPlan simt, tc;
+    bool has_tc = false;
+    size_t ws_need = 0;
+    if ((st = plan_scan(d, &simt, &tc, &has_tc, &ws_need)) != M3_OK) return st;
+    bool use_tc = has_tc;
+    for (const void *p : {x, B, C, theta, (const void *)y})
+        if (!aligned16(p)) use_tc = false;
+    if (!use_tc && simt.path < 0) return M3_ERR_UNSUPPORTED;
+    const ScanPlan &pl = use_tc ? tc : simt;
 
     const size_t bh = (size_t)d.batch * d.nheads;
     const size_t hbytes = bh * d.dstate * d.headdim * sizeof(float);
@@ -161,7 +179,7 @@ m3_status mamba3_scan_fwd(const m3_dims *dims, const void *x, const void *B, con
         }
         return e == cudaSuccess ? M3_OK : M3_ERR_CUDA;
     }
-    if (pl.ws_bytes > 0 && (!workspace || workspace_bytes < pl.ws_bytes || !aligned16(workspace)))
+    if (ws_need > 0 && (!workspace || workspace_bytes < ws_need || !aligned16(workspace)))
         return M3_ERR_WORKSPACE;
 
     ScanArgs a{};
@@ -180,7 +198,7 @@ m3_status mamba3_scan_fwd(const m3_dims *dims, const void *x, const void *B, con
         a.ws_state = static_cast<float *>(workspace);
         a.ws_tot = reinterpret_cast<float *>(static_cast<char *>(workspace) + ((state_b + 255) / 256) * 256);
     }
-    cudaError_t e = simt_scan(a, pl, s);
+    cudaError_t e = use_tc ? tc_scan(a, pl, s) : simt_scan(a, pl, s);
     return e == cudaSuccess ? M3_OK : M3_ERR_CUDA;
 }
 

@@ -66,6 +66,11 @@ size_t scan_workspace_bytes(int batch, int H, int N, int P, int nseg);
 bool simt_plan(const m3_dims &d, int sms, ScanPlan *plan);   // false = unsupported
 cudaError_t simt_scan(const ScanArgs &a, const ScanPlan &plan, cudaStream_t s);
 
+// Tensor-core path (bf16, P = 64, N in {64, 128}, R in {1, 2, 4, 8}).
+bool tc_supported(const m3_dims &d);
+bool tc_plan(const m3_dims &d, int sms, ScanPlan *plan);      // false = unsupported
+cudaError_t tc_scan(const ScanArgs &a, const ScanPlan &plan, cudaStream_t s);
+
 // Segment state passing (shared by both paths).
 cudaError_t segment_pass(const ScanArgs &a, const ScanPlan &plan, cudaStream_t s);
 
