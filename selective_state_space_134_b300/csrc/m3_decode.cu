@@ -14,6 +14,7 @@
 // The per-token inputs (B, C, carry, x) are staged in shared memory as fp32.
 // y is reduced over N inside the thread, then across threads in shared memory.
 #include "m3_internal.cuh"
+#include "m3_tc.cuh"
 
 namespace m3 {
 namespace {
@@ -136,6 +137,228 @@ decode_kernel(int H, int P, int N, int R, const T *__restrict__ x, const T *__re
     }
 }
 
+// ---------------------------------------------------------------- streaming kernel
+// Persistent variant for the common shapes (P in {32, 64, 128}, N a multiple
+// of 16).  Each CTA walks heads blockIdx.x, blockIdx.x + gridDim.x, ... and
+// keeps several in flight: one elected thread moves a head's state and token
+// inputs into a shared-memory stage with bulk asynchronous copies (completion
+// on the stage's mbarrier), the CTA updates the state in place there, and the
+// same thread writes the state and the new carry back with bulk copies.  Bytes
+// in flight therefore do not depend on registers or occupancy, and two CTAs
+// per SM overlap one's barrier with the other's arithmetic.  Thread (kg, cg)
+// owns the four columns 4cg..4cg+3 (128-bit shared-memory accesses) of the
+// pairs k = kg, kg + NPG, ..., computes their rotation factors itself, and
+// reads B, B_prev and C as bf16 pairs shared by its four columns; y is summed
+// over the NPG pair groups in shared memory.
+constexpr int kStreamThreads = 256;
+constexpr uint32_t kStreamWaitPolls = 1u << 22;   // per mbarrier wait; far above any legal wait
+
+struct StreamLayout {
+    uint32_t st, B, C, Bp, x, xp, th, stage;   // byte offsets inside a stage, stage size
+    uint32_t red, bar, flag, total;            // offsets after the stages, total bytes
+    __host__ __device__ StreamLayout(int N, int P, int R, int e, int nst) {
+        auto up = [](uint32_t v) { return (v + 127u) & ~127u; };
+        const uint32_t bn = (uint32_t)(R * N * e), xn = (uint32_t)(R * P * e);
+        st = 0;
+        B = up(st + (uint32_t)(N * P * 4));
+        C = up(B + bn);
+        Bp = up(C + bn);
+        x = up(Bp + bn);
+        xp = up(x + xn);
+        th = up(xp + xn);
+        stage = up(th + (uint32_t)(N / 2 * e));
+        red = stage * nst;                                     // y partial sums [NPG][R][P]
+        bar = up(red + (uint32_t)(kStreamThreads * 4 * R * 4));
+        flag = bar + 8u * nst;
+        total = flag + 16;
+    }
+};
+
+__device__ __forceinline__ void pair_f(const float *q, float &a, float &b) {
+    const float2 v = *reinterpret_cast<const float2 *>(q);
+    a = v.x;
+    b = v.y;
+}
+__device__ __forceinline__ void pair_f(const __nv_bfloat16 *q, float &a, float &b) {
+    const uint32_t v = *reinterpret_cast<const uint32_t *>(q);
+    a = __uint_as_float(v << 16);
+    b = __uint_as_float(v & 0xFFFF0000u);
+}
+__device__ __forceinline__ void quad_f(const float *q, float (&o)[4]) {
+    const float4 v = *reinterpret_cast<const float4 *>(q);
+    o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
+}
+__device__ __forceinline__ void quad_f(const __nv_bfloat16 *q, float (&o)[4]) {
+    const uint2 v = *reinterpret_cast<const uint2 *>(q);
+    o[0] = __uint_as_float(v.x << 16); o[1] = __uint_as_float(v.x & 0xFFFF0000u);
+    o[2] = __uint_as_float(v.y << 16); o[3] = __uint_as_float(v.y & 0xFFFF0000u);
+}
+// sin / cos: Cody-Waite reduction by 2 pi (two-constant split) to [-pi, pi],
+// then the hardware approximations there
+__device__ __forceinline__ void sincos_reduced(float a, float *s, float *c) {
+    const float n = rintf(a * 0.15915494309189535f);
+    float r = fmaf(-n, 6.28318548202514648f, a);
+    r = fmaf(-n, -1.7484555314695172e-7f, r);
+    __sincosf(r, s, c);
+}
+
+template <typename T, int R>
+__global__ void __launch_bounds__(kStreamThreads, 2)
+decode_stream_kernel(int nbh, int P, int N, int nst, const T *__restrict__ x, const T *__restrict__ Bm,
+                     const T *__restrict__ Cm, const T *__restrict__ dtp, const T *__restrict__ Ap,
+                     const T *__restrict__ lp, const T *__restrict__ thp, float *__restrict__ hs,
+                     T *__restrict__ Bprev, T *__restrict__ xprev, float *__restrict__ y, unsigned *status) {
+    using namespace tc;
+    extern __shared__ __align__(128) unsigned char smem_s[];
+    unsigned char *sm = smem_s;
+    const StreamLayout Lo(N, P, R, (int)sizeof(T), nst);
+    const int K = N / 2, tid = threadIdx.x;
+    const int NCG = P / 4, NPG = kStreamThreads / NCG, cg = tid % NCG, kg = tid / NCG;
+    float *red = reinterpret_cast<float *>(sm + Lo.red);
+    uint64_t *full = reinterpret_cast<uint64_t *>(sm + Lo.bar);
+    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(sm + Lo.flag);
+
+    const int first = blockIdx.x, step = gridDim.x;
+    const int mine = first < nbh ? (nbh - first + step - 1) / step : 0;
+    const uint32_t bn = (uint32_t)(R * N * sizeof(T)), xn = (uint32_t)(R * P * sizeof(T));
+    const uint32_t hn = (uint32_t)(N * P * 4), tn = (uint32_t)(K * sizeof(T));
+
+    auto issue = [&](int j) {   // head j of this CTA -> stage j % nst (elected thread)
+        const size_t bh = (size_t)first + (size_t)j * step;
+        unsigned char *sg = sm + (size_t)(j % nst) * Lo.stage;
+        uint64_t *bar = full + (j % nst);
+        mbar_expect_tx(bar, hn + 3 * bn + 2 * xn + tn);
+        bulk_load(sg + Lo.st, hs + bh * N * P, hn, bar);
+        bulk_load(sg + Lo.B, Bm + bh * R * N, bn, bar);
+        bulk_load(sg + Lo.C, Cm + bh * R * N, bn, bar);
+        bulk_load(sg + Lo.Bp, Bprev + bh * R * N, bn, bar);
+        bulk_load(sg + Lo.x, x + bh * R * P, xn, bar);
+        bulk_load(sg + Lo.xp, xprev + bh * R * P, xn, bar);
+        bulk_load(sg + Lo.th, thp + bh * K, tn, bar);
+    };
+
+    if (tid == 0) {
+        for (int i = 0; i < nst; ++i) mbar_init(full + i, 1);
+        mbar_init_fence();
+        *abort_flag = 0;
+    }
+    __syncthreads();
+    int issued = 0;
+    if (tid == 0)
+        for (; issued < nst - 1 && issued < mine; ++issued) issue(issued);
+
+    // per-head scalars one head ahead, in registers (every thread loads the same address)
+    float d_n = 0.f, a_n = 0.f, l_n = 0.f;
+    if (mine > 0) {
+        d_n = to_f(dtp[first]);
+        a_n = to_f(Ap[first]);
+        l_n = to_f(lp[first]);
+    }
+    int j = 0;
+    for (; j < mine; ++j) {
+        const size_t bh = (size_t)first + (size_t)j * step;
+        const float d = d_n, av = a_n, l = l_n;
+        if (j + 1 < mine) {
+            const size_t nb = bh + step;
+            d_n = to_f(dtp[nb]);
+            a_n = to_f(Ap[nb]);
+            l_n = to_f(lp[nb]);
+        }
+        unsigned char *sg = sm + (size_t)(j % nst) * Lo.stage;
+        const bool ok = mbar_wait(full + (j % nst), (uint32_t)((j / nst) & 1), kStreamWaitPolls);
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) atomicOr(status, kStatusTimeout);
+            *abort_flag = 1;
+            break;
+        }
+        const T *sB = reinterpret_cast<const T *>(sg + Lo.B), *sC = reinterpret_cast<const T *>(sg + Lo.C);
+        const T *sBp = reinterpret_cast<const T *>(sg + Lo.Bp), *sx = reinterpret_cast<const T *>(sg + Lo.x);
+        const T *sxp = reinterpret_cast<const T *>(sg + Lo.xp), *sth = reinterpret_cast<const T *>(sg + Lo.th);
+        float *st = reinterpret_cast<float *>(sg + Lo.st);
+
+        const float rho = expf(d * av), left = (1.f - l) * d, right = l * d;
+        float xr[R][4], xq[R][4];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            quad_f(sx + r * P + 4 * cg, xr[r]);
+            quad_f(sxp + r * P + 4 * cg, xq[r]);
+        }
+        float yacc[R][4];
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) yacc[r][c] = 0.f;
+        for (int k = kg; k < K; k += NPG) {
+            float sa, ca;
+            sincos_reduced(d * to_f(sth[k]), &sa, &ca);
+            const float cr = rho * ca, sr = rho * sa;
+            float4 *r0 = reinterpret_cast<float4 *>(st + (size_t)(2 * k) * P + 4 * cg);
+            float4 *r1 = reinterpret_cast<float4 *>(st + (size_t)(2 * k + 1) * P + 4 * cg);
+            const float4 e0 = *r0, e1 = *r1;
+            float a0[4] = {e0.x, e0.y, e0.z, e0.w}, a1[4] = {e1.x, e1.y, e1.z, e1.w};
+            float u0[4] = {0.f, 0.f, 0.f, 0.f}, u1[4] = {0.f, 0.f, 0.f, 0.f};
+            float v0[4] = {0.f, 0.f, 0.f, 0.f}, v1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                float b0, b1, q0, q1;
+                pair_f(sB + r * N + 2 * k, b0, b1);
+                pair_f(sBp + r * N + 2 * k, q0, q1);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    u0[c] = fmaf(q0, xq[r][c], u0[c]);
+                    u1[c] = fmaf(q1, xq[r][c], u1[c]);
+                    v0[c] = fmaf(b0, xr[r][c], v0[c]);
+                    v1[c] = fmaf(b1, xr[r][c], v1[c]);
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const float s0 = fmaf(left, u0[c], a0[c]), s1 = fmaf(left, u1[c], a1[c]);
+                a0[c] = fmaf(cr, s0, fmaf(-sr, s1, right * v0[c]));
+                a1[c] = fmaf(sr, s0, fmaf(cr, s1, right * v1[c]));
+            }
+            *r0 = make_float4(a0[0], a0[1], a0[2], a0[3]);
+            *r1 = make_float4(a1[0], a1[1], a1[2], a1[3]);
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                float c0, c1;
+                pair_f(sC + r * N + 2 * k, c0, c1);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) yacc[r][c] = fmaf(c0, a0[c], fmaf(c1, a1[c], yacc[r][c]));
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+            *reinterpret_cast<float4 *>(red + (kg * R + r) * P + 4 * cg) =
+                make_float4(yacc[r][0], yacc[r][1], yacc[r][2], yacc[r][3]);
+        fence_proxy_async();   // the state writes above feed the bulk store below
+        __syncthreads();
+        if (tid == 0) {
+            bulk_store(hs + bh * N * P, st, hn);
+            bulk_store(Bprev + bh * R * N, sB, bn);     // new carry = this token's (B, x)
+            bulk_store(xprev + bh * R * P, sx, xn);
+            bulk_commit();
+            if (issued < mine) {
+                bulk_wait_read<1>();   // the stage about to be refilled has been written out
+                issue(issued);
+                ++issued;
+            }
+        }
+        for (int i = tid; i < R * P; i += kStreamThreads) {
+            float v = 0.f;
+            for (int q = 0; q < NPG; ++q) v += red[q * R * P + i];
+            y[bh * R * P + i] = v;
+        }
+    }
+    if (tid == 0) {
+        if (*abort_flag) {
+            // let the copies already issued land before the CTA's shared memory goes away
+            for (int i = j; i < issued; ++i) mbar_wait(full + (i % nst), (uint32_t)((i / nst) & 1), kStreamWaitPolls);
+        }
+        bulk_wait<0>();
+    }
+}
+
 template <typename T>
 cudaError_t launch_decode(int batch, int H, int P, int N, int R, const void *x, const void *B,
                           const void *C, const void *dt, const void *A, const void *lam,
@@ -168,12 +391,74 @@ cudaError_t launch_decode(int batch, int H, int P, int N, int R, const void *x, 
     return cudaGetLastError();
 }
 
+
+template <typename T, int R>
+cudaError_t launch_stream(int nbh, int P, int N, const void *x, const void *B, const void *C, const void *dt,
+                          const void *A, const void *lam, const void *theta, float *h, void *Bprev, void *xprev,
+                          void *y, cudaStream_t s) {
+    const int e = (int)sizeof(T);
+    // two CTAs per SM with as many stages as fit (2..6), else one CTA per SM
+    int per_sm = 2, nst = 6;
+    while (nst > 2 && StreamLayout(N, P, R, e, nst).total > 113u * 1024u) --nst;
+    if (StreamLayout(N, P, R, e, nst).total > 113u * 1024u) {
+        per_sm = 1;
+        nst = 6;
+        while (nst > 2 && StreamLayout(N, P, R, e, nst).total > 224u * 1024u) --nst;
+    }
+    const StreamLayout Lo(N, P, R, e, nst);
+    if (Lo.total > 224u * 1024u) return cudaErrorInvalidValue;
+    unsigned *status = device_status_word();
+    if (!status) return cudaErrorUnknown;
+    auto kern = decode_stream_kernel<T, R>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Lo.total);
+    if (err != cudaSuccess) return err;
+    const int grid = nbh < per_sm * sm_count() ? nbh : per_sm * sm_count();
+    trace_mark(M3_KERNEL_DECODE, s, 0);
+    kern<<<grid, kStreamThreads, Lo.total, s>>>(nbh, P, N, nst, (const T *)x, (const T *)B, (const T *)C,
+                                                (const T *)dt, (const T *)A, (const T *)lam, (const T *)theta, h,
+                                                (T *)Bprev, (T *)xprev, (float *)y, status);
+    trace_mark(M3_KERNEL_DECODE, s, 1);
+    count_launch();
+    return cudaGetLastError();
+}
+
+// Shapes the streaming kernel takes: every per-head block a multiple of 16 bytes
+// at 16-byte aligned addresses, and a whole number of state columns per warp.
+bool stream_ok(int e, int P, int N, int R, const void *const *ptrs, int nptr) {
+    if (P != 32 && P != 64 && P != 128) return false;
+    if ((N * e / 2) % 16 != 0 || (R * N * e) % 16 != 0 || (R * P * e) % 16 != 0) return false;
+    if (R != 1 && R != 2 && R != 4 && R != 8) return false;
+    for (int i = 0; i < nptr; ++i)
+        if (reinterpret_cast<uintptr_t>(ptrs[i]) & 15u) return false;
+    return true;
+}
+
+template <typename T>
+cudaError_t stream_dispatch(int nbh, int P, int N, int R, const void *x, const void *B, const void *C,
+                            const void *dt, const void *A, const void *lam, const void *theta, float *h,
+                            void *Bprev, void *xprev, void *y, cudaStream_t s) {
+    switch (R) {
+        case 1: return launch_stream<T, 1>(nbh, P, N, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, s);
+        case 2: return launch_stream<T, 2>(nbh, P, N, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, s);
+        case 4: return launch_stream<T, 4>(nbh, P, N, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, s);
+        default: return launch_stream<T, 8>(nbh, P, N, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, s);
+    }
+}
+
 }  // namespace
 
 cudaError_t decode_step(int dtype, int batch, int H, int P, int N, int R, const void *x,
                         const void *B, const void *C, const void *dt, const void *A,
                         const void *lam, const void *theta, float *h, void *Bprev, void *xprev,
                         void *y, cudaStream_t s) {
+    const int e = dtype == M3_F32 ? 4 : 2;
+    const void *ptrs[] = {x, B, C, theta, h, Bprev, xprev};
+    const int nbh = batch * H;
+    if (nbh > 0 && stream_ok(e, P, N, R, ptrs, 7)) {
+        if (dtype == M3_F32)
+            return stream_dispatch<float>(nbh, P, N, R, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, s);
+        return stream_dispatch<__nv_bfloat16>(nbh, P, N, R, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, s);
+    }
     if (dtype == M3_F32)
         return launch_decode<float>(batch, H, P, N, R, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, s);
     return launch_decode<__nv_bfloat16>(batch, H, P, N, R, x, B, C, dt, A, lam, theta, h, Bprev,
