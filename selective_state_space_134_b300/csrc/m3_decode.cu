@@ -151,7 +151,7 @@ decode_kernel(int H, int P, int N, int R, const T *__restrict__ x, const T *__re
 // reads B, B_prev and C as bf16 pairs shared by its four columns; y is summed
 // over the NPG pair groups in shared memory.
 constexpr int kStreamThreads = 256;
-constexpr uint32_t kStreamWaitPolls = 1u << 22;   // per mbarrier wait; far above any legal wait
+constexpr uint64_t kStreamWaitNs = 2000000000ull;   // 2 s per mbarrier wait; far above any legal wait
 
 struct StreamLayout {
     uint32_t st, B, C, Bp, x, xp, th, stage;   // byte offsets inside a stage, stage size
@@ -265,7 +265,7 @@ decode_stream_kernel(int nbh, int P, int N, int nst, const T *__restrict__ x, co
             l_n = to_f(lp[nb]);
         }
         unsigned char *sg = sm + (size_t)(j % nst) * Lo.stage;
-        const bool ok = mbar_wait(full + (j % nst), (uint32_t)((j / nst) & 1), kStreamWaitPolls);
+        const bool ok = mbar_wait(full + (j % nst), (uint32_t)((j / nst) & 1), kStreamWaitNs);
         if (__syncthreads_or(!ok)) {
             if (tid == 0) atomicOr(status, kStatusTimeout);
             *abort_flag = 1;
@@ -353,7 +353,7 @@ decode_stream_kernel(int nbh, int P, int N, int nst, const T *__restrict__ x, co
     if (tid == 0) {
         if (*abort_flag) {
             // let the copies already issued land before the CTA's shared memory goes away
-            for (int i = j; i < issued; ++i) mbar_wait(full + (i % nst), (uint32_t)((i / nst) & 1), kStreamWaitPolls);
+            for (int i = j; i < issued; ++i) mbar_wait(full + (i % nst), (uint32_t)((i / nst) & 1), kStreamWaitNs);
         }
         bulk_wait<0>();
     }

@@ -1,103 +1,107 @@
 // Chunked prefill of the Mamba-3 recurrence on the sm_100-family tensor cores
-// (tcgen05 MMA, accumulators in TMEM, inputs brought in by TMA).
+// (tcgen05 MMA with TMEM accumulators, operands brought in by TMA), as a
+// warp-specialised pipeline.
 //
-// One CTA walks the chunks of one segment of one (b, h) sequence, in order,
-// with the N x P fp32 state in registers.  Per chunk of Q tokens (QR = Q R
-// rows (t, r); linkstar.cloud/article/869, sections "第一刀" (parallel form),
-// "RoPE技巧" and "第三刀" (MIMO)):
-//   prologue   chunk-local cumsums cA_t (warp shuffle scan) and phi_t, rotation
-//              of B and C by R(-phi_t) into bf16 hi + lo tiles; X^_j = s_j x_j
-//              with s_j = exp(cA_e - cA_j) w_j (hi + lo);
-//   MMA  S   = C~ B~^T                 (QR x QR, K = N)      score
-//   MMA  Yi  = C~ H                    (QR x P,  K = N)      state -> output
-//   MMA  Sn  = B~^T X^                 (N x P,   K = QR)     chunk's state contribution
-//   epi  Pm  = S o M, M_tj = exp(cA_t - cA_j) w_j (j < t), lambda_t dt_t (j = t)  -> TMEM (bf16 hi+lo)
-//   epi  H  <- R(phi_e) [exp(cA_e) H + Sn]                   (fp32 registers)
-//   MMA  Ya  = Pm X                    (QR x P, K = QR, A operand read from TMEM)
-//   epi  y   = Ya + exp(cA_t) Yi       (fp32 out)
-// Every product whose operands are not exact in bf16 (rotated B and C, masked
-// scores, the state, scaled x) is formed from bf16 hi + lo parts as
-// hi*hi + hi*lo + lo*hi, accumulated in fp32: the outputs are heavy-tailed
-// (max |y| ~ 16 rms(y) on these inputs), so one plain bf16 rounding of an
-// operand would by itself cost ~3e-2 of rms(y).
+// One CTA walks the chunks of one segment of one (b, h) sequence in order.
+// Per chunk of Q tokens (QR = Q R rows (t, r); linkstar.cloud/article/869,
+// sections "第一刀" (parallel form), "RoPE技巧" and "第三刀" (MIMO)):
+//   prologue  chunk-local cumsums cA_t (warp shuffle scan) and phi_t; B and C
+//             turned by R(-phi_t) in place into fp16 tiles; X^_j = s_j x_j with
+//             s_j = exp(cA_e - cA_j) w_j; mask column factors
+//   MMA 1     S  = C~ B~^T        (QR x QR, K = N)    score
+//             Yi = C~ H           (QR x P,  K = N)    state -> output
+//             Sn = B~^T X^        (N x P,   K = QR)   the chunk's state contribution
+//   epilogue  P = S o M, M_tj = exp(cA_t - cA_j) w_j (j < t), lambda_t dt_t (j = t),
+//             into TMEM as fp16;  H <- R(phi_e) [exp(cA_e) H + Sn]
+//   MMA 2     Ya = P X            (QR x P,  K = QR, A operand read from TMEM)
+//   epilogue  y = Ya + exp(cA_t) Yi   (fp32)
 //
-// Tiles: B~ and C~ are K-major with the 128-byte swizzle (64-column slabs);
-// the same B~ bytes serve as the MN-major A operand of the Sn MMA.  X comes
-// straight from TMA in the MN-major 128-byte-swizzle layout.  N = 64 uses
-// QR = 128 row chunks (M = 128 MMAs); N = 128 uses QR = 64 (M = 64) so that
-// tiles, TMA staging and double-buffered X fit in shared memory.
+// Roles: warp 0 issues the TMA loads (two raw slots), warp 1 allocates TMEM and
+// issues the MMAs, warps 2-9 run the prologue of chunk c+1 while warps 10-17
+// run the epilogues of chunk c; they hand chunks over through mbarriers.  The
+// fp32 state H stays in TMEM next to the accumulators.
+//
+// Precision.  Every MMA operand (B~, C~, X^, H, P and x) is fp16 (11-bit
+// significand, fp32 accumulation) scaled by a per-chunk power of two that
+// puts a bound of the tile just under 2^14, so the result does not depend on
+// the magnitude of the inputs (x itself converts exactly); the scales are
+// undone exactly in the fp32 epilogues.
+// The decay is always formed as exp2 of a difference of chunk-local
+// cumulative sums (exponent <= 0) and factored per 32-column block, so no
+// partial product overflows.
 #include "m3_internal.cuh"
 #include "m3_tc.cuh"
 
 #include <mutex>
+#include <type_traits>
 
 namespace m3 {
 namespace {
 
 using namespace tc;
 
-constexpr int kThreads = 256;
 constexpr int kP = 64;
-constexpr uint32_t kWaitPolls = 1u << 22;   // per mbarrier wait; far above any legal wait
+constexpr int kWarps = 18;
+constexpr int kThreads = kWarps * 32;
+constexpr int kProW0 = 2, kProWarps = 8, kEpiW0 = 10, kEpiWarps = 8;
+constexpr int kProThreads = kProWarps * 32, kEpiThreads = kEpiWarps * 32;
+constexpr int kBarPro = 1, kBarEpi = 2;          // named barriers of the two groups
+constexpr uint64_t kWaitNs = 2000000000ull;      // 2 s per mbarrier wait; far above any legal wait
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int N, int R>
 struct Cfg {
-    static constexpr int QR = (N == 64) ? 128 : 64;    // rows per chunk
-    static constexpr int Q = QR / R;                   // tokens per chunk
-    static constexpr int K = N / 2;                    // complex pairs
-    static constexpr int NSLAB = N / 64;               // 64-column slabs of B~ / C~
-    static constexpr int NSEG = 8 / NSLAB;             // token segments of the angle scan
-    static constexpr int TPS = Q / NSEG;               // tokens per segment
-    static constexpr uint32_t TILE = QR * N * 2;       // one B~ or C~ part
-    static constexpr uint32_t XT = QR * kP * 2;        // one X tile
-    static constexpr uint32_t HT = N * kP * 2;         // one state tile part
-    static constexpr uint32_t RAWB = QR * N * 2;       // TMA staging of B or C
-    static constexpr uint32_t RAWT = Q * K * 2;        // TMA staging of theta
-    static_assert(Q % NSEG == 0, "token segments must tile the chunk");
+    static constexpr int QR = (N == 64) ? 128 : 64;   // rows (t, r) per chunk
+    static constexpr int Q = QR / R;                  // tokens per chunk
+    static constexpr int K = N / 2;                   // complex pairs
+    static constexpr int NSLAB = N / 64;              // 64-column (128-byte) slabs of B and C
+    static constexpr int NSEG = kProWarps / NSLAB;    // token segments of the prologue
+    static constexpr int TPS = Q / NSEG;              // tokens per segment
+    static constexpr int TB = 32 / R;                 // tokens per 32-column block of the score
+    static constexpr uint32_t BT = QR * N * 2;        // B or C tile
+    static constexpr uint32_t XT = QR * kP * 2;       // X or X^ tile
+    static constexpr uint32_t TT = Q * K * 2;         // theta tile
+    static constexpr uint32_t HT = N * kP * 2;        // fp16 state tile
+    static_assert(Q % NSEG == 0 && TPS >= 1, "token segments must tile the chunk");
     static_assert(K == 32 * NSLAB, "one lane per pair within a slab");
+    static_assert(Q <= kProThreads, "one prologue thread per token");
 };
 
 // Shared-memory map (byte offsets from a 1024-aligned base).
 template <int N, int R, bool OUT>
 struct Smem {
     using C = Cfg<N, R>;
-    static constexpr uint32_t oBh = 0;
-    static constexpr uint32_t oBl = oBh + C::TILE;
-    static constexpr uint32_t oCh = oBl + C::TILE;
-    static constexpr uint32_t oCl = oCh + (OUT ? C::TILE : 0);
-    static constexpr uint32_t oX = oCl + (OUT ? C::TILE : 0);       // 2 buffers
-    static constexpr uint32_t oXh = oX + 2 * C::XT;
-    static constexpr uint32_t oXl = oXh + C::XT;
-    static constexpr uint32_t oHh = oXl + C::XT;
-    static constexpr uint32_t oHl = oHh + (OUT ? C::HT : 0);
-    static constexpr uint32_t oRawB = oHl + (OUT ? C::HT : 0);
-    static constexpr uint32_t oRawC = oRawB + C::RAWB;
-    static constexpr uint32_t oRawT = oRawC + (OUT ? C::RAWB : 0);
-    static constexpr uint32_t oSmall = ((oRawT + C::RAWT + 127) / 128) * 128;
-    // small arrays (floats unless noted)
-    static constexpr uint32_t oCA = oSmall;                 // cA in log2 units [Q]
-    static constexpr uint32_t oG = oCA + 4 * C::Q;          // lambda dt [Q]
-    static constexpr uint32_t oW = oG + 4 * C::Q;           // w [Q]
-    static constexpr uint32_t oDT = oW + 4 * C::Q;          // dt [Q]
-    static constexpr uint32_t oPart = oDT + 4 * C::Q;       // [NSEG][K]
-    static constexpr uint32_t oCos = oPart + 4 * C::NSEG * C::K;
-    static constexpr uint32_t oSin = oCos + 4 * C::K;
-    static constexpr uint32_t oTot = oSin + 4 * C::K;       // [1 + K] segment totals (pass 1)
-    static constexpr uint32_t oBar = ((oTot + 4 * (1 + C::K) + 7) / 8) * 8;   // 3 mbarriers
-    static constexpr uint32_t oTmem = oBar + 24;
+    // raw slot: B, C (turned into fp16 B~, C~ in place), X (bf16), theta
+    static constexpr uint32_t sB = 0;
+    static constexpr uint32_t sC = sB + C::BT;
+    static constexpr uint32_t sX = sC + (OUT ? C::BT : 0);
+    static constexpr uint32_t sT = sX + C::XT;
+    static constexpr uint32_t SLOT = ((sT + C::TT + 1023) / 1024) * 1024;
+    static constexpr uint32_t oXh = 2 * SLOT;                  // X^ [2] (fp16)
+    static constexpr uint32_t oXp = oXh + 2 * C::XT;           // X' [2] (fp16), OUT only
+    static constexpr uint32_t oH = oXp + (OUT ? 2 * C::XT : 0); // H (fp16), OUT only
+    static constexpr uint32_t oVec = oH + (OUT ? C::HT : 0);   // per-parity vectors
+    // per parity (floats): cA2[Q] g[Q] w[Q] vj[Q] dt[Q] cosE[K] sinE[K] sig[8]
+    static constexpr uint32_t VF = 5 * C::Q + 2 * C::K + 8;
+    static constexpr uint32_t oPart = oVec + 2 * 4 * VF;       // angle partials [8][K]
+    static constexpr uint32_t oMx = oPart + 4 * kProWarps * C::K;   // prologue maxima [8][4]
+    static constexpr uint32_t oMxH = oMx + 4 * kProWarps * 4;       // epilogue maxima [2][8]
+    static constexpr uint32_t oSigH = oMxH + 4 * 2 * kEpiWarps;     // H scale [2] and inverse [2]
+    static constexpr uint32_t oTot = oSigH + 16;                    // segment totals [1 + K]
+    static constexpr uint32_t oBar = ((oTot + 4 * (1 + C::K) + 7) / 8) * 8;
+    static constexpr int kNumBars = 16;
+    static constexpr uint32_t oTmem = oBar + 8 * kNumBars;
     static constexpr uint32_t oFlag = oTmem + 4;
     static constexpr uint32_t kBytes = oFlag + 4;
-    static constexpr uint32_t kAlloc = kBytes + 1024;       // slack for the 1024-byte alignment
+    static constexpr uint32_t kAlloc = kBytes + 1024;          // slack for the 1024-byte alignment
 };
 
-// Byte offset of element (row, col) in a 128-byte-swizzled tile of 128-byte rows
-// (K-major tiles: col < 64 within a slab; MN-major tiles: col = the MN index).
+// Byte offset of element (row, col) in a 128-byte-swizzled tile of 128-byte rows.
 __device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t col) {
     return row * 128u + ((((col >> 3) ^ row) & 7u) << 4) + ((col & 7u) << 1);
 }
 
-__device__ __forceinline__ void fast_sincos(float x, float *s, float *c) {
+__device__ __forceinline__ void sincos_reduced(float x, float *s, float *c) {
     // Cody-Waite reduction by 2 pi (two-constant split), then the hardware sin/cos on [-pi, pi]
     const float n = rintf(x * 0.15915494309189535f);
     float r = fmaf(-n, 6.28318548202514648f, x);
@@ -111,8 +115,54 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
+// 2^(13 - floor(log2 m)): maps m to [2^13, 2^14).  1 for m = 0 or non-finite m.
+__device__ __forceinline__ float pow2_scale(float m) {
+    if (!(m > 0.f) || !(m <= 3.0e38f)) return 1.f;
+    const int e = (int)((__float_as_uint(m) >> 23) & 0xFFu) - 127;
+    int s = 13 - e;
+    s = s < -126 ? -126 : (s > 127 ? 127 : s);
+    return __uint_as_float((uint32_t)(s + 127) << 23);
+}
+__device__ __forceinline__ float pow2_inv(float s) {   // exact inverse of a power of two
+    return __uint_as_float((uint32_t)(254 - (int)(__float_as_uint(s) >> 23)) << 23);
+}
+
+// fp16 pair (lo element in the low half), round to nearest even
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// fp16 x fp16 -> fp32, dense; a_mn / b_mn: 1 = MN-major operand.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int a_mn, int b_mn) {
+    return (1u << 4) | (static_cast<uint32_t>(a_mn) << 15) | (static_cast<uint32_t>(b_mn) << 16) |
+           (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void named_sync(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *m) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(m)) : "memory");
+}
+__device__ __forceinline__ float warp_max(float v) {   // v >= 0
+    return __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(v)));
+}
+
 struct TcMaps {
     CUtensorMap B, C, X, T;
+};
+
+enum Bar {
+    kRawFull = 0,      // [2] TMA -> prologue (transaction bytes)
+    kRawEmpty = 2,     // [2] MMAs done with a raw slot -> producer
+    kTilesFull = 4,    // [2] prologue -> MMA
+    kStateReady = 6,   // [2] epilogue wrote H (and read S, Sn) -> MMA
+    kMma1 = 8,         // [2] first MMAs done -> epilogue
+    kPReady = 10,      // [2] epilogue wrote P -> MMA
+    kMma2 = 12,        // [2] Ya done -> epilogue
+    kEpiDone = 14      // [2] epilogue done with a chunk -> prologue
 };
 
 template <int N, int R, bool OUT>
@@ -121,44 +171,75 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                   unsigned *status) {
     using Cf = Cfg<N, R>;
     using S = Smem<N, R, OUT>;
-    constexpr int QR = Cf::QR, Q = Cf::Q, K = Cf::K, NSLAB = Cf::NSLAB, TPS = Cf::TPS;
-    constexpr bool kM64Rows = (QR == 64);   // rows of S / Y use the M = 64 TMEM lane layout
-    constexpr bool kM64State = (N == 64);   // rows of Sn use the M = 64 TMEM lane layout
-    constexpr uint32_t kTmemCols = OUT ? 512 : 64;
-    // TMEM columns
-    constexpr uint32_t cS = 0, cYa = 128, cYi = 192, cSn = OUT ? 256 : 0, cPh = 320, cPl = 384;
+    constexpr int QR = Cf::QR, Q = Cf::Q, K = Cf::K, NSLAB = Cf::NSLAB, TPS = Cf::TPS, TB = Cf::TB;
+    constexpr uint32_t kTmemCols = OUT ? 512 : 128;
+    // TMEM columns: score, state contribution, Yi (two buffers), Ya, P (fp16 pairs), fp32 state
+    constexpr uint32_t cS = 0, cSn = OUT ? 128 : 0, cYi0 = 192, cYa = 320, cP = 384, cH = OUT ? 448 : 64;
+    constexpr bool kRowsM64 = (QR == 64);    // S / Yi / Ya use the M = 64 lane layout
+    constexpr bool kStateM64 = (N == 64);    // Sn uses the M = 64 lane layout
 
     extern __shared__ __align__(16) unsigned char smem_raw[];
     unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    float *cA2 = reinterpret_cast<float *>(sm + S::oCA);
-    float *gv = reinterpret_cast<float *>(sm + S::oG);
-    float *wv = reinterpret_cast<float *>(sm + S::oW);
-    float *dts = reinterpret_cast<float *>(sm + S::oDT);
-    float *part = reinterpret_cast<float *>(sm + S::oPart);
-    float *cosE = reinterpret_cast<float *>(sm + S::oCos);
-    float *sinE = reinterpret_cast<float *>(sm + S::oSin);
-    float *tot = reinterpret_cast<float *>(sm + S::oTot);
-    uint64_t *bar_ld = reinterpret_cast<uint64_t *>(sm + S::oBar);
-    uint64_t *bar_mma1 = bar_ld + 1;
-    uint64_t *bar_mma2 = bar_ld + 2;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + S::oBar);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + S::oTmem);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(sm + S::oFlag);
+    float *part = reinterpret_cast<float *>(sm + S::oPart);
+    float *mx = reinterpret_cast<float *>(sm + S::oMx);
+    float *mxH = reinterpret_cast<float *>(sm + S::oMxH);
+    float *sigH = reinterpret_cast<float *>(sm + S::oSigH);   // [0..1] scale, [2..3] inverse
+    float *tot = reinterpret_cast<float *>(sm + S::oTot);
+    auto vec = [&](int p) { return reinterpret_cast<float *>(sm + S::oVec) + p * S::VF; };
+    // per-parity vector fields
+    auto v_cA = [&](int p) { return vec(p); };
+    auto v_g = [&](int p) { return vec(p) + Q; };
+    auto v_w = [&](int p) { return vec(p) + 2 * Q; };
+    auto v_vj = [&](int p) { return vec(p) + 3 * Q; };
+    auto v_dt = [&](int p) { return vec(p) + 4 * Q; };
+    auto v_cos = [&](int p) { return vec(p) + 5 * Q; };
+    auto v_sin = [&](int p) { return vec(p) + 5 * Q + K; };
+    // scales: sB, sC, sX, tauP / (sB sC), 1 / (sB sX), 1 / sC, 1 / (tauP sX')
+    auto v_sig = [&](int p) { return vec(p) + 5 * Q + 2 * K; };
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int quad = warp & 3, half = warp >> 2;
     const int H = a.H, L = a.L;
     const int g = blockIdx.x % nlaunch, bh = blockIdx.x / nlaunch, b = bh / H, h = bh % H;
     const int t_begin = g * seglen, t_end = min(L, t_begin + seglen);
+    const int nchunks = t_end > t_begin ? (t_end - t_begin + Q - 1) / Q : 0;
     const __nv_bfloat16 *dtp = static_cast<const __nv_bfloat16 *>(a.dt);
     const __nv_bfloat16 *Ap = static_cast<const __nv_bfloat16 *>(a.A);
     const __nv_bfloat16 *lp = static_cast<const __nv_bfloat16 *>(a.lam);
     auto tok = [&](int t) { return ((size_t)b * L + t) * H + h; };
 
-    // ---- set-up: barriers, TMEM, state
+    // bounded wait; after any timeout every later wait returns at once
+    // (backoff: single-thread roles nap between polls so that they do not take
+    // issue slots from the warps doing arithmetic)
+    auto wait = [&](int i, uint32_t parity, bool backoff = false) {
+        uint64_t *m = bars + i;
+        const uint64_t t0 = global_ns();
+        for (uint32_t n = 0;; ++n) {
+            if (mbar_try_wait(m, parity)) return;
+            if (backoff) __nanosleep(64);
+            if ((n & 7u) == 7u) {
+                if (*abort_flag) return;
+                if (global_ns() - t0 > kWaitNs) break;
+            }
+        }
+        *abort_flag = 1;
+        atomicOr(status, kStatusTimeout);
+    };
+
+    // ---- set-up
     if (tid == 0) {
-        mbar_init(bar_ld, 1);
-        mbar_init(bar_mma1, 1);
-        mbar_init(bar_mma2, 1);
+        for (int p = 0; p < 2; ++p) {
+            mbar_init(bars + kRawFull + p, 1);
+            mbar_init(bars + kRawEmpty + p, 1);
+            mbar_init(bars + kTilesFull + p, kProThreads);
+            mbar_init(bars + kStateReady + p, kEpiThreads);
+            mbar_init(bars + kMma1 + p, 1);
+            mbar_init(bars + kPReady + p, kEpiThreads);
+            mbar_init(bars + kMma2 + p, 1);
+            mbar_init(bars + kEpiDone + p, kEpiThreads);
+        }
         mbar_init_fence();
         *abort_flag = 0;
         tma_prefetch_desc(&maps.B);
@@ -167,387 +248,555 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
         if (OUT) tma_prefetch_desc(&maps.C);
     }
     for (int i = tid; i < 1 + K; i += kThreads) tot[i] = 0.f;
-    if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
+    if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
     fence_before();
     __syncthreads();
     fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    auto issue_loads = [&](int s0, int buf) {
-        constexpr uint32_t bytes = Cf::RAWB * (OUT ? 2 : 1) + Cf::XT + Cf::RAWT;
-        mbar_expect_tx(bar_ld, bytes);
-        const int row0 = b * L + s0;
-        tma_load_4d(sm + S::oRawB, &maps.B, 0, 0, h, row0, bar_ld);
-        if (OUT) tma_load_4d(sm + S::oRawC, &maps.C, 0, 0, h, row0, bar_ld);
-        tma_load_4d(sm + S::oX + buf * Cf::XT, &maps.X, 0, 0, h, row0, bar_ld);
-        tma_load_3d(sm + S::oRawT, &maps.T, 0, h, row0, bar_ld);
-    };
-    if (tid == 0 && t_begin < t_end) issue_loads(t_begin, 0);
-
-    // State rows owned by this thread: row n of the N x P state, 32 columns [32 half, +32).
-    const bool st_owner = kM64State ? (lane < 16) : true;
-    const int st_row = kM64State ? quad * 16 + lane : quad * 32 + lane;
-    float hreg[32];
-    {
-        const int n = st_row;
-        if (!OUT || !st_owner) {
+    if (warp == 0) {
+        // ================================================================ producer
+        if (lane == 0) {
+            for (int it = 0; it < nchunks; ++it) {
+                const int p = it & 1;
+                if (it >= 2) wait(kRawEmpty + p, ((it - 2) >> 1) & 1, true);
+                unsigned char *slot = sm + p * S::SLOT;
+                constexpr uint32_t bytes = Cf::BT * (OUT ? 2 : 1) + Cf::XT + Cf::TT;
+                mbar_expect_tx(bars + kRawFull + p, bytes);
+                const int row0 = b * L + t_begin + it * Q;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) hreg[j] = 0.f;
-        } else if (nseg == 1) {
-            const float left0 = (1.f - to_f(lp[tok(0)])) * to_f(dtp[tok(0)]);
-            const __nv_bfloat16 *bq = static_cast<const __nv_bfloat16 *>(a.Bprev);
-            const __nv_bfloat16 *xq = static_cast<const __nv_bfloat16 *>(a.xprev);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int p = 32 * half + j;
-                float v = a.h0 ? a.h0[((size_t)bh * N + n) * kP + p] : 0.f;
-                if (bq && xq) {
-                    float u = 0.f;
-                    for (int r = 0; r < R; ++r)
-                        u += to_f(bq[((size_t)bh * R + r) * N + n]) * to_f(xq[((size_t)bh * R + r) * kP + p]);
-                    v += left0 * u;
+                for (int sl = 0; sl < NSLAB; ++sl) {
+                    tma_load_4d(slot + S::sB + sl * QR * 128, &maps.B, 64 * sl, 0, h, row0, bars + kRawFull + p);
+                    if (OUT)
+                        tma_load_4d(slot + S::sC + sl * QR * 128, &maps.C, 64 * sl, 0, h, row0, bars + kRawFull + p);
                 }
-                hreg[j] = v;
+                tma_load_4d(slot + S::sX, &maps.X, 0, 0, h, row0, bars + kRawFull + p);
+                tma_load_3d(slot + S::sT, &maps.T, 0, h, row0, bars + kRawFull + p);
             }
-        } else {
-            const float *src = a.ws_state + (((size_t)bh * nseg + g) * N + n) * kP + 32 * half;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) hreg[j] = src[j];
-        }
-    }
-    // bf16 hi / lo copy of the state for the C~ H MMA (MN-major, 128-byte swizzle, rows n)
-    auto write_state_tile = [&]() {
-        if (!OUT || !st_owner) return;
-        const int n = st_row;
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-            uint32_t hi[4], lo[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) split2(hreg[8 * q4 + 2 * e], hreg[8 * q4 + 2 * e + 1], hi[e], lo[e]);
-            const uint32_t off = sw128(n, 32 * half + 8 * q4);
-            *reinterpret_cast<uint4 *>(sm + S::oHh + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-            *reinterpret_cast<uint4 *>(sm + S::oHl + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-        }
-    };
-    write_state_tile();
-
-    auto fail = [&]() {
-        *abort_flag = 1;
-        atomicOr(status, kStatusTimeout);
-    };
-
-    int it = 0;
-    for (int s0 = t_begin; s0 < t_end; s0 += Q, ++it) {
-        const int Qc = min(Q, t_end - s0), e = Qc - 1, buf = it & 1;
-        const bool last_chunk = s0 + Q >= t_end;
-
-        // ---------------- prologue: per-token scalars (plain loads overlap the TMA wait)
-        if (tid < Q) {
-            float d = 0.f, av = 0.f, gg = 0.f, ww = 0.f;
-            if (tid < Qc) {
-                const size_t ti = tok(s0 + tid);
-                d = to_f(dtp[ti]);
-                av = d * to_f(Ap[ti]) * kLog2e;
-                const float l = to_f(lp[ti]);
-                gg = l * d;
-                float nxt = 0.f;
-                if (s0 + tid + 1 < L) {
-                    const size_t tn = tok(s0 + tid + 1);
-                    nxt = (1.f - to_f(lp[tn])) * to_f(dtp[tn]);
+            if (*abort_flag) {
+                // let the copies already issued land before the CTA's shared memory goes away
+                for (int it = nchunks - 2 < 0 ? 0 : nchunks - 2; it < nchunks; ++it) {
+                    mbar_wait(bars + kRawFull + (it & 1), (it >> 1) & 1, kWaitNs);
                 }
-                ww = gg + nxt;
-            }
-            dts[tid] = d;
-            cA2[tid] = av;
-            gv[tid] = gg;
-            wv[tid] = ww;
-        }
-        if (!mbar_wait(bar_ld, it & 1, kWaitPolls)) fail();
-        __syncthreads();
-        if (*abort_flag) break;
-
-        const __nv_bfloat16 *rawT = reinterpret_cast<const __nv_bfloat16 *>(sm + S::oRawT);
-        const int slab = warp % NSLAB, seg = warp / NSLAB, k = 32 * slab + lane;
-        // chunk-local prefix of dt A (one warp, shuffle scan); per-segment angle sums (all warps)
-        if (warp == 0) {
-            float carry = 0.f;
-            for (int base = 0; base < Q; base += 32) {
-                float v = (base + lane < Q) ? cA2[base + lane] : 0.f;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const float t = __shfl_up_sync(0xffffffffu, v, o);
-                    if (lane >= o) v += t;
-                }
-                v += carry;
-                if (base + lane < Q) cA2[base + lane] = v;
-                carry = __shfl_sync(0xffffffffu, v, 31);
             }
         }
-        {
-            float ps = 0.f;
+        __syncwarp();
+    } else if (warp == 1) {
+        // ================================================================ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idS = idesc_f16(QR, QR, 0, 0);
+            constexpr uint32_t idYi = idesc_f16(QR, kP, 0, 1);
+            constexpr uint32_t idSn = idesc_f16(N, kP, 1, 1);
+            constexpr uint32_t idYa = idesc_f16(QR, kP, 0, 1);
+            for (int it = 0; it < nchunks; ++it) {
+                const int p = it & 1;
+                const uint32_t ph = (it >> 1) & 1;
+                wait(kTilesFull + p, ph, true);
+                wait(kStateReady + p, ph, true);
+                fence_after();
+                unsigned char *slot = sm + p * S::SLOT;
+                const uint32_t bA = smem_u32(slot + S::sB), xh = smem_u32(sm + S::oXh + p * Cf::XT);
+                if (OUT) {
+                    const uint32_t cA = smem_u32(slot + S::sC), hA = smem_u32(sm + S::oH);
+                    const uint32_t cYi = cYi0 + 64 * p;
 #pragma unroll
-            for (int i = 0; i < TPS; ++i) {
-                const int t = seg * TPS + i;
-                if (t < Qc) ps += dts[t] * __bfloat162float(rawT[t * K + k]);
-            }
-            part[seg * K + k] = ps;
-        }
-        __syncthreads();
-        if (!OUT && tid < K) {
-            float s = 0.f;
-            for (int sg = 0; sg < Cf::NSEG; ++sg) s += part[sg * K + tid];
-            tot[1 + tid] += s;
-        }
-        if (!OUT && tid == 0) tot[0] += cA2[e];
-
-        // ---------------- rotation of B (and C) by R(-phi_t), split into bf16 hi + lo
-        {
-            float phi = 0.f;
-            for (int sg = 0; sg < seg; ++sg) phi += part[sg * K + k];
-            const uint32_t *rawB = reinterpret_cast<const uint32_t *>(sm + S::oRawB);
-            const uint32_t *rawC = reinterpret_cast<const uint32_t *>(sm + S::oRawC);
-            const uint32_t slab_off = slab * (QR * 128);
-            const uint32_t col = 2 * (lane);   // column within the slab (n % 64), even
-#pragma unroll
-            for (int i = 0; i < TPS; ++i) {
-                const int t = seg * TPS + i;
-                float c = 1.f, s = 0.f;
-                const bool valid = t < Qc;
-                if (valid) {
-                    phi += dts[t] * __bfloat162float(rawT[t * K + k]);
-                    fast_sincos(phi, &s, &c);
-                    if (t == e) {
-                        cosE[k] = c;
-                        sinE[k] = s;
+                    for (int ks = 0; ks < N / 16; ++ks) {
+                        // K-major, 128-byte swizzle: slab ks / 4, 32 bytes per 16-column step inside it
+                        const uint32_t ko = (ks / 4) * (QR * 128) + (ks % 4) * 32;
+                        const uint64_t dC = make_desc(cA + ko, 16, 1024, kSwizzle128B);
+                        mma_ss(tmem + cS, dC, make_desc(bA + ko, 16, 1024, kSwizzle128B), idS, ks > 0);
+                        // state operand: MN-major (p), K = n rows in 8-row groups of 1024 bytes
+                        mma_ss(tmem + cYi, dC, make_desc(hA + ks * 2048, 0, 1024, kSwizzle128B), idYi, ks > 0);
                     }
                 }
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    const int row = t * R + r;
-                    const uint32_t off = slab_off + sw128(row, col);
-                    uint32_t hi = 0, lo = 0;
-                    if (valid) {
-                        const uint32_t v = rawB[(row * N) / 2 + k];
-                        const float b0 = bf16_lo_f(v), b1 = bf16_hi_f(v);
-                        split2(c * b0 + s * b1, c * b1 - s * b0, hi, lo);
-                    }
-                    *reinterpret_cast<uint32_t *>(sm + S::oBh + off) = hi;
-                    *reinterpret_cast<uint32_t *>(sm + S::oBl + off) = lo;
-                    if (OUT) {
-                        uint32_t chi = 0, clo = 0;
-                        if (valid) {
-                            const uint32_t v = rawC[(row * N) / 2 + k];
-                            const float c0 = bf16_lo_f(v), c1 = bf16_hi_f(v);
-                            split2(c * c0 + s * c1, c * c1 - s * c0, chi, clo);
-                        }
-                        *reinterpret_cast<uint32_t *>(sm + S::oCh + off) = chi;
-                        *reinterpret_cast<uint32_t *>(sm + S::oCl + off) = clo;
-                    }
-                }
-            }
-        }
-        // ---------------- X^ = s_j x_j (hi + lo); zero the rows past the chunk end in X
-        {
-            unsigned char *xb = sm + S::oX + buf * Cf::XT;
-            const float ce = cA2[e];
-            for (int item = tid; item < QR * 8; item += kThreads) {
-                const int row = item >> 3, c8 = item & 7, t = row / R;
-                const uint32_t off = sw128(row, 8 * c8);
-                uint4 hi = make_uint4(0, 0, 0, 0), lo = hi;
-                if (t < Qc) {
-                    const float sj = fast_exp2(ce - cA2[t]) * wv[t];
-                    const uint4 v = *reinterpret_cast<const uint4 *>(xb + off);
-                    split2(sj * bf16_lo_f(v.x), sj * bf16_hi_f(v.x), hi.x, lo.x);
-                    split2(sj * bf16_lo_f(v.y), sj * bf16_hi_f(v.y), hi.y, lo.y);
-                    split2(sj * bf16_lo_f(v.z), sj * bf16_hi_f(v.z), hi.z, lo.z);
-                    split2(sj * bf16_lo_f(v.w), sj * bf16_hi_f(v.w), hi.w, lo.w);
-                } else if (OUT) {
-                    *reinterpret_cast<uint4 *>(xb + off) = make_uint4(0, 0, 0, 0);
-                }
-                *reinterpret_cast<uint4 *>(sm + S::oXh + off) = hi;
-                *reinterpret_cast<uint4 *>(sm + S::oXl + off) = lo;
-            }
-        }
-        fence_proxy_async();
-        fence_before();
-        __syncthreads();
-        fence_after();
-
-        // ---------------- MMAs of this chunk; then prefetch the next chunk's inputs
-        if (tid == 0) {
-            const uint32_t bh_ = smem_u32(sm + S::oBh), bl_ = smem_u32(sm + S::oBl);
-            if (OUT) {
-                const uint32_t ch_ = smem_u32(sm + S::oCh), cl_ = smem_u32(sm + S::oCl);
-                const uint32_t hh_ = smem_u32(sm + S::oHh), hl_ = smem_u32(sm + S::oHl);
-                constexpr uint32_t idS = idesc_bf16(QR, QR, 0, 0);
-                constexpr uint32_t idYi = idesc_bf16(QR, kP, 0, 1);
-#pragma unroll
-                for (int ks = 0; ks < N / 16; ++ks) {
-                    // K-major, 128-byte swizzle: slab (ks / 4), 32 bytes per 16-column step inside it
-                    const uint32_t ko = (ks / 4) * (QR * 128) + (ks % 4) * 32;
-                    const uint64_t dCh = make_desc(ch_ + ko, 16, 1024, kSwizzle128B);
-                    const uint64_t dCl = make_desc(cl_ + ko, 16, 1024, kSwizzle128B);
-                    const uint64_t dBh = make_desc(bh_ + ko, 16, 1024, kSwizzle128B);
-                    const uint64_t dBl = make_desc(bl_ + ko, 16, 1024, kSwizzle128B);
-                    mma_ss(tmem + cS, dCh, dBh, idS, ks > 0);
-                    mma_ss(tmem + cS, dCh, dBl, idS, 1);
-                    mma_ss(tmem + cS, dCl, dBh, idS, 1);
-                    // state operand: MN-major (p), K = n rows in 8-row groups of 1024 bytes
-                    const uint64_t dHh = make_desc(hh_ + ks * 2048, 0, 1024, kSwizzle128B);
-                    const uint64_t dHl = make_desc(hl_ + ks * 2048, 0, 1024, kSwizzle128B);
-                    mma_ss(tmem + cYi, dCh, dHh, idYi, ks > 0);
-                    mma_ss(tmem + cYi, dCh, dHl, idYi, 1);
-                    mma_ss(tmem + cYi, dCl, dHh, idYi, 1);
-                }
-            }
-            {
-                const uint32_t xh_ = smem_u32(sm + S::oXh), xl_ = smem_u32(sm + S::oXl);
-                constexpr uint32_t idSn = idesc_bf16(N, kP, 1, 1);
 #pragma unroll
                 for (int ks = 0; ks < QR / 16; ++ks) {
                     // B~ read as the MN-major A operand (M = n in 64-wide slabs, K = rows j)
-                    const uint64_t dAh = make_desc(bh_ + ks * 2048, QR * 128, 1024, kSwizzle128B);
-                    const uint64_t dAl = make_desc(bl_ + ks * 2048, QR * 128, 1024, kSwizzle128B);
-                    const uint64_t dXh = make_desc(xh_ + ks * 2048, 0, 1024, kSwizzle128B);
-                    const uint64_t dXl = make_desc(xl_ + ks * 2048, 0, 1024, kSwizzle128B);
-                    mma_ss(tmem + cSn, dAh, dXh, idSn, ks > 0);
-                    mma_ss(tmem + cSn, dAh, dXl, idSn, 1);
-                    mma_ss(tmem + cSn, dAl, dXh, idSn, 1);
+                    mma_ss(tmem + cSn, make_desc(bA + ks * 2048, QR * 128, 1024, kSwizzle128B),
+                           make_desc(xh + ks * 2048, 0, 1024, kSwizzle128B), idSn, ks > 0);
+                }
+                mma_commit(bars + kMma1 + p);
+                if (OUT) {
+                    wait(kPReady + p, ph, true);
+                    fence_after();
+                    const uint32_t xb = smem_u32(sm + S::oXp + p * Cf::XT);
+#pragma unroll
+                    for (int ks = 0; ks < QR / 16; ++ks)
+                        mma_ts(tmem + cYa, tmem + cP + ks * 8, make_desc(xb + ks * 2048, 0, 1024, kSwizzle128B),
+                               idYa, ks > 0);
+                    mma_commit(bars + kMma2 + p);
+                }
+                mma_commit(bars + kRawEmpty + p);
+            }
+            if (*abort_flag && nchunks > 0) {
+                // let the last MMAs finish before TMEM is released
+                const int it = nchunks - 1;
+                mbar_wait(bars + kRawEmpty + (it & 1), (it >> 1) & 1, kWaitNs);
+            }
+        }
+        __syncwarp();
+    } else if (warp < kEpiW0) {
+        // ================================================================ prologue
+        const int ptid = tid - kProW0 * 32, pw = warp - kProW0;
+        const int slab = pw % NSLAB, seg = pw / NSLAB, k = 32 * slab + lane;
+        // per-token scalars of the next chunk, loaded one chunk ahead into registers
+        // (raw values: nothing waits on these loads until the chunk is processed)
+        __nv_bfloat16 r_dt, r_A, r_l, r_ln, r_dtn;
+        auto fetch = [&](int it) {
+            const __nv_bfloat16 z = __float2bfloat16_rn(0.f);
+            r_dt = r_A = r_l = r_ln = r_dtn = z;
+            const int t = t_begin + it * Q + ptid;
+            if (ptid < Q && it < nchunks && t < t_end) {
+                const size_t ti = tok(t);
+                r_dt = dtp[ti];
+                r_A = Ap[ti];
+                r_l = lp[ti];
+                if (t + 1 < L) {
+                    const size_t tn = tok(t + 1);
+                    r_ln = lp[tn];
+                    r_dtn = dtp[tn];
+                } else {
+                    r_ln = __float2bfloat16_rn(1.f);   // (1 - lambda) dt = 0 past the sequence end
                 }
             }
-            mma_commit(bar_mma1);
-            if (!last_chunk) issue_loads(s0 + Q, buf ^ 1);
-        }
-        if (!mbar_wait(bar_mma1, it & 1, kWaitPolls)) fail();
-        fence_after();
-
-        // ---------------- epilogue 1: masked score -> TMEM (bf16 hi + lo); state update
-        if (OUT) {
-            constexpr int COLS = QR / 2;                      // score columns per thread
-            const bool rvalid = kM64Rows ? (lane < 16) : true;
-            const int row = kM64Rows ? quad * 16 + lane : quad * 32 + lane;
-            const int ti = row / R;
-            const float cai = cA2[min(ti, Q - 1)];
-            const float gi = gv[min(ti, Q - 1)];
-            const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+        };
+        fetch(0);
+        float acc_cA = 0.f;   // pass 1: total log2-decay of the segment (prologue thread 0)
+        for (int it = 0; it < nchunks; ++it) {
+            const int p = it & 1;
+            const int s0 = t_begin + it * Q, Qc = min(Q, t_end - s0), e = Qc - 1;
+            unsigned char *slot = sm + p * S::SLOT;
+            float *cA2 = v_cA(p), *gv = v_g(p), *wv = v_w(p), *vj = v_vj(p), *dts = v_dt(p);
+            if (it >= 2) wait(kEpiDone + p, ((it - 2) >> 1) & 1);
+            // ---- P1: token scalars
+            const float c_dt = to_f(r_dt), c_a = c_dt * to_f(r_A) * kLog2e, c_g = to_f(r_l) * c_dt;
+            const float c_w = c_g + (1.f - to_f(r_ln)) * to_f(r_dtn);
+            if (ptid < Q) {
+                dts[ptid] = c_dt;
+                cA2[ptid] = c_a;
+                gv[ptid] = c_g;
+                wv[ptid] = c_w;
+            }
+            fetch(it + 1);
+            // one thread waits for the chunk's TMA; the named barrier (which costs the
+            // other warps no issue slots) releases the rest
+            if (ptid == 0) wait(kRawFull + p, (it >> 1) & 1);
+            named_sync(kBarPro, kProThreads);
+            // ---- P2: cumsum (warp 0), angle partial sums, bounds of |B|, |C|, |x|, w
+            if (pw == 0) {
+                float carry = 0.f;
+                for (int base = 0; base < Q; base += 32) {
+                    float v = (base + lane < Q) ? cA2[base + lane] : 0.f;
 #pragma unroll
-            for (int cc = 0; cc < COLS; cc += 32) {
-                uint32_t sv[32];
-                tmem_ld32(tmem + lane_base + cS + half * COLS + cc, sv);
-                uint32_t ph[16], pl[16];
-#pragma unroll
-                for (int j = 0; j < 32; j += 2) {
-                    float pm[2];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int col = half * COLS + cc + j + u, tj = col / R;
-                        float m = 0.f;
-                        if (tj < ti) m = fast_exp2(cai - cA2[tj]) * wv[tj];
-                        else if (tj == ti) m = gi;
-                        pm[u] = rvalid ? __uint_as_float(sv[j + u]) * m : 0.f;
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const float t = __shfl_up_sync(0xffffffffu, v, o);
+                        if (lane >= o) v += t;
                     }
-                    split2(pm[0], pm[1], ph[j / 2], pl[j / 2]);
+                    v += carry;
+                    if (base + lane < Q) cA2[base + lane] = v;
+                    carry = __shfl_sync(0xffffffffu, v, 31);
                 }
-                const uint32_t pcol = (half * COLS + cc) / 2;
-                tmem_st16(tmem + lane_base + cPh + pcol, ph);
-                tmem_st16(tmem + lane_base + cPl + pcol, pl);
+            }
+            const __nv_bfloat16 *rawT = reinterpret_cast<const __nv_bfloat16 *>(slot + S::sT);
+            float mW = ptid < Qc ? fabsf(c_w) : 0.f;
+            // this thread's tokens: dt (0 past the sequence end) and its pair's angle rate
+            float dd[TPS], th[TPS];
+#pragma unroll
+            for (int i = 0; i < TPS; ++i) {
+                const int t = seg * TPS + i;
+                dd[i] = dts[t];
+                th[i] = __bfloat162float(rawT[t * K + k]);
+            }
+            {
+                float ps = 0.f;
+#pragma unroll
+                for (int i = 0; i < TPS; ++i) ps = fmaf(dd[i], th[i], ps);
+                part[seg * K + k] = ps;
+            }
+            // bounds of |B|, |C|, |x| over the raw tiles: packed maxima of the bf16 magnitudes
+            // (their bit patterns order like the values)
+            auto tile_max = [&](const unsigned char *base, auto bytes_c) {
+                constexpr uint32_t bytes = decltype(bytes_c)::value;
+                static_assert(bytes % (16u * kProThreads) == 0, "whole 16-byte words per thread");
+                uint32_t m2 = 0;
+#pragma unroll
+                for (uint32_t o = 0; o < bytes; o += 16u * kProThreads) {
+                    const uint4 v = *reinterpret_cast<const uint4 *>(base + o + 16u * ptid);
+                    m2 = __vmaxu2(m2, v.x & 0x7FFF7FFFu);
+                    m2 = __vmaxu2(m2, v.y & 0x7FFF7FFFu);
+                    m2 = __vmaxu2(m2, v.z & 0x7FFF7FFFu);
+                    m2 = __vmaxu2(m2, v.w & 0x7FFF7FFFu);
+                }
+                return fmaxf(bf16_lo_f(m2), bf16_hi_f(m2));
+            };
+            using BTc = std::integral_constant<uint32_t, Cf::BT>;
+            using XTc = std::integral_constant<uint32_t, Cf::XT>;
+            float mB = tile_max(slot + S::sB, BTc{});
+            float mC = OUT ? tile_max(slot + S::sC, BTc{}) : 0.f;
+            float mX = tile_max(slot + S::sX, XTc{});
+            mB = warp_max(mB);
+            mC = warp_max(mC);
+            mX = warp_max(mX);
+            mW = warp_max(mW);
+            if (lane == 0) {
+                mx[pw * 4 + 0] = mB;
+                mx[pw * 4 + 1] = mC;
+                mx[pw * 4 + 2] = mX;
+                mx[pw * 4 + 3] = mW;
+            }
+            named_sync(kBarPro, kProThreads);
+            // ---- P3: scales, rotation of B and C in place (fp16), X^, mask column factors
+            float MB = 0.f, MC = 0.f, MX = 0.f, MW = 0.f;
+#pragma unroll
+            for (int q = 0; q < kProWarps; ++q) {
+                MB = fmaxf(MB, mx[q * 4 + 0]);
+                MC = fmaxf(MC, mx[q * 4 + 1]);
+                MX = fmaxf(MX, mx[q * 4 + 2]);
+                MW = fmaxf(MW, mx[q * 4 + 3]);
+            }
+            // |B~| <= sqrt 2 max|B| (rotation of a pair);  |X^| <= max w max|x|;
+            // |P| <= N max|B~| max|C~| max(w, lambda dt)
+            const float sgB = pow2_scale(1.5f * MB), sgC = pow2_scale(1.5f * MC), sgX = pow2_scale(MX * MW);
+            const float sgXp = pow2_scale(MX), tauP = pow2_scale((float)N * 2.25f * MB * MC * MW);
+            if (ptid == 0) {
+                float *sg = v_sig(p);
+                sg[0] = sgB;
+                sg[1] = sgC;
+                sg[2] = sgX;
+                sg[3] = tauP * pow2_inv(sgB) * pow2_inv(sgC);
+                sg[4] = pow2_inv(sgB) * pow2_inv(sgX);
+                sg[5] = pow2_inv(sgC);
+                sg[6] = pow2_inv(tauP) * pow2_inv(sgXp);
+                if (!OUT) acc_cA += cA2[e];
+            }
+            {
+                float phi = 0.f;
+                for (int sg = 0; sg < seg; ++sg) phi += part[sg * K + k];
+                unsigned char *bs = slot + S::sB + slab * (QR * 128);
+                unsigned char *cs = slot + S::sC + slab * (QR * 128);
+                // angles of all the thread's tokens first (a short FMA chain), then
+                // independent rotations the scheduler can overlap
+                float ph[TPS];
+#pragma unroll
+                for (int i = 0; i < TPS; ++i) {
+                    phi = fmaf(dd[i], th[i], phi);
+                    ph[i] = phi;
+                }
+                const int ie = e - seg * TPS;   // the chunk's last token, if it is this thread's
+                if (ie >= 0 && ie < TPS) {
+                    float pe = 0.f;
+#pragma unroll
+                    for (int i = 0; i < TPS; ++i) pe = (i == ie) ? ph[i] : pe;
+                    float se, ce2;
+                    sincos_reduced(pe, &se, &ce2);
+                    v_cos(p)[k] = ce2;
+                    v_sin(p)[k] = se;
+                    if (!OUT) tot[1 + k] += pe;
+                }
+                // all raw words first: the in-place stores below then cannot hold back a load
+                uint32_t rb[TPS * R], rc[TPS * R];
+#pragma unroll
+                for (int i = 0; i < TPS * R; ++i) {
+                    const uint32_t off = sw128(seg * TPS * R + i, 2 * lane);
+                    rb[i] = *reinterpret_cast<const uint32_t *>(bs + off);
+                    if (OUT) rc[i] = *reinterpret_cast<const uint32_t *>(cs + off);
+                }
+#pragma unroll
+                for (int i = 0; i < TPS; ++i) {
+                    const int t = seg * TPS + i;
+                    const bool valid = t < Qc;
+                    float c, s;
+                    sincos_reduced(ph[i], &s, &c);
+                    const float cb = c * sgB, sb = s * sgB, cc = c * sgC, sc = s * sgC;
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        const uint32_t off = sw128(t * R + r, 2 * lane);
+                        const uint32_t vb = rb[i * R + r];
+                        const float b0 = bf16_lo_f(vb), b1 = bf16_hi_f(vb);
+                        *reinterpret_cast<uint32_t *>(bs + off) =
+                            valid ? pack_f16x2(fmaf(cb, b0, sb * b1), fmaf(cb, b1, -sb * b0)) : 0u;
+                        if (OUT) {
+                            const uint32_t vc = rc[i * R + r];
+                            const float c0 = bf16_lo_f(vc), c1 = bf16_hi_f(vc);
+                            *reinterpret_cast<uint32_t *>(cs + off) =
+                                valid ? pack_f16x2(fmaf(cc, c0, sc * c1), fmaf(cc, c1, -sc * c0)) : 0u;
+                        }
+                    }
+                }
+            }
+            {
+                unsigned char *xh = sm + S::oXh + p * Cf::XT;
+                unsigned char *xp = sm + S::oXp + p * Cf::XT;
+                const float ce = cA2[e];
+                static_assert((QR * 8) % kProThreads == 0, "whole items per thread");
+                constexpr int kItems = QR * 8 / kProThreads;
+                uint4 xv[kItems];
+#pragma unroll
+                for (int i = 0; i < kItems; ++i) {
+                    const int item = ptid + i * kProThreads;
+                    xv[i] = *reinterpret_cast<const uint4 *>(slot + S::sX + sw128(item >> 3, 8 * (item & 7)));
+                }
+#pragma unroll
+                for (int i = 0; i < kItems; ++i) {
+                    const int item = ptid + i * kProThreads;
+                    const int row = item >> 3, c8 = item & 7, t = row / R;
+                    const uint32_t off = sw128(row, 8 * c8);
+                    uint4 o = make_uint4(0, 0, 0, 0), q = o;
+                    if (t < Qc) {
+                        const float sj = fast_exp2(ce - cA2[t]) * wv[t] * sgX;
+                        const uint4 v = xv[i];
+                        const float f[8] = {bf16_lo_f(v.x), bf16_hi_f(v.x), bf16_lo_f(v.y), bf16_hi_f(v.y),
+                                            bf16_lo_f(v.z), bf16_hi_f(v.z), bf16_lo_f(v.w), bf16_hi_f(v.w)};
+                        o = make_uint4(pack_f16x2(sj * f[0], sj * f[1]), pack_f16x2(sj * f[2], sj * f[3]),
+                                       pack_f16x2(sj * f[4], sj * f[5]), pack_f16x2(sj * f[6], sj * f[7]));
+                        if (OUT)   // x' = sX' x, exact in fp16
+                            q = make_uint4(pack_f16x2(sgXp * f[0], sgXp * f[1]), pack_f16x2(sgXp * f[2], sgXp * f[3]),
+                                           pack_f16x2(sgXp * f[4], sgXp * f[5]), pack_f16x2(sgXp * f[6], sgXp * f[7]));
+                    }
+                    *reinterpret_cast<uint4 *>(xh + off) = o;
+                    if (OUT) *reinterpret_cast<uint4 *>(xp + off) = q;   // rows past the end stay zero
+                }
+                if (ptid < Q) {
+                    const int bt = (ptid / TB) * TB;
+                    vj[ptid] = ptid < Qc ? fast_exp2(cA2[bt] - cA2[ptid]) * wv[ptid] : 0.f;
+                }
+            }
+            fence_proxy_async();
+            mbar_arrive(bars + kTilesFull + p);
+        }
+        if (!OUT) {
+            named_sync(kBarPro, kProThreads);
+            if (!*abort_flag) {
+                float *dst = a.ws_tot + ((size_t)bh * (nseg - 1) + g) * (1 + K);
+                if (ptid == 0) dst[0] = acc_cA / kLog2e;
+                for (int i = ptid; i < K; i += kProThreads) dst[1 + i] = tot[1 + i];
             }
         }
+    } else {
+        // ================================================================ epilogue
+        const int ew = warp - kEpiW0, eq = warp & 3, eh = ew >> 2;   // lane quadrant, column half
+        const uint32_t lane_base = static_cast<uint32_t>(eq * 32) << 16;
+        // state rows owned: row n of the N x P state, columns [32 eh, 32 eh + 32)
+        const bool st_owner = kStateM64 ? (lane < 16) : true;
+        const int st_row = kStateM64 ? eq * 16 + lane : eq * 32 + lane;
+        // score / output rows owned
+        const bool row_ok = kRowsM64 ? (lane < 16) : true;
+        const int row = kRowsM64 ? eq * 16 + lane : eq * 32 + lane;
+        const int ti = row / R, ri = row % R;
+        // The fp32 state lives in TMEM columns [cH, cH + 64): row n in the lane of the Sn
+        // accumulator's row n, column p; this thread holds columns [32 eh, 32 eh + 32).
+        const uint32_t hcol = tmem + lane_base + cH + 32 * eh;
+        float hmax = 0.f;   // this thread's max |h| (state rows it owns)
         {
-            uint32_t sn[32];
-            const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-            tmem_ld32(tmem + lane_base + cSn + 32 * half, sn);
-            const float rho = fast_exp2(cA2[e]);
-            const int n = st_row, kk = n >> 1;
-            const float c = st_owner ? cosE[kk] : 1.f, s = st_owner ? sinE[kk] : 0.f;
-            const bool odd = n & 1;
+            const int n = st_row;
+            const float left0 = (OUT && nseg == 1) ? (1.f - to_f(lp[tok(0)])) * to_f(dtp[tok(0)]) : 0.f;
+            const __nv_bfloat16 *bq = static_cast<const __nv_bfloat16 *>(a.Bprev);
+            const __nv_bfloat16 *xq = static_cast<const __nv_bfloat16 *>(a.xprev);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const float v = rho * hreg[j] + __uint_as_float(sn[j]);
-                const float pv = __shfl_xor_sync(0xffffffffu, v, 1);
-                hreg[j] = odd ? fmaf(s, pv, c * v) : fmaf(-s, pv, c * v);
-            }
-            write_state_tile();
-            if (last_chunk && st_owner) {
-                float *dst = nullptr;
-                if (!OUT) dst = a.ws_state + (((size_t)bh * nseg + g + 1) * N + n) * kP;
-                else if (g == nseg - 1 && a.h_out) dst = a.h_out + ((size_t)bh * N + n) * kP;
-                if (dst) {
+            for (int h16 = 0; h16 < 32; h16 += 16) {
+                uint32_t w[16];
 #pragma unroll
-                    for (int j = 0; j < 32; j += 4)
-                        *reinterpret_cast<float4 *>(dst + 32 * half + j) =
-                            make_float4(hreg[j], hreg[j + 1], hreg[j + 2], hreg[j + 3]);
+                for (int j = 0; j < 16; ++j) {
+                    const int pp = 32 * eh + h16 + j;
+                    float v = 0.f;
+                    if (OUT && st_owner) {
+                        if (nseg == 1) {
+                            v = a.h0 ? a.h0[((size_t)bh * N + n) * kP + pp] : 0.f;
+                            if (bq && xq) {
+                                float u = 0.f;
+                                for (int r = 0; r < R; ++r)
+                                    u += to_f(bq[((size_t)bh * R + r) * N + n]) * to_f(xq[((size_t)bh * R + r) * kP + pp]);
+                                v += left0 * u;
+                            }
+                        } else {
+                            v = a.ws_state[(((size_t)bh * nseg + g) * N + n) * kP + pp];
+                        }
+                    }
+                    hmax = fmaxf(hmax, fabsf(v));
+                    w[j] = __float_as_uint(v);
                 }
+                tmem_st16(hcol + h16, w);
             }
         }
+        // fp16 copy of the state (scaled) for the C~ H MMA (MN-major, 128-byte swizzle, rows n)
+        auto publish_state = [&](int slot_parity, float m) {
+            if (!OUT) return;
+            m = warp_max(m);
+            if (lane == 0) mxH[slot_parity * kEpiWarps + ew] = m;
+            named_sync(kBarEpi, kEpiThreads);
+            float M = 0.f;
+#pragma unroll
+            for (int q = 0; q < kEpiWarps; ++q) M = fmaxf(M, mxH[slot_parity * kEpiWarps + q]);
+            const float sg = pow2_scale(M);
+            if (ew == 0 && lane == 0) {
+                sigH[slot_parity] = sg;
+                sigH[2 + slot_parity] = pow2_inv(sg);
+            }
+            uint32_t hv[32];
+            tmem_ld16_nw(hcol, hv);
+            tmem_ld16_nw(hcol + 16, hv + 16);
+            tmem_wait_ld(hv);
+            if (st_owner) {
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    uint32_t w4[4];
+#pragma unroll
+                    for (int e2 = 0; e2 < 4; ++e2)
+                        w4[e2] = pack_f16x2(__uint_as_float(hv[8 * q4 + 2 * e2]) * sg,
+                                            __uint_as_float(hv[8 * q4 + 2 * e2 + 1]) * sg);
+                    *reinterpret_cast<uint4 *>(sm + S::oH + sw128(st_row, 32 * eh + 8 * q4)) =
+                        make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                }
+            }
+        };
+        publish_state(0, hmax);
         fence_proxy_async();
         fence_before();
-        __syncthreads();
-        fence_after();
+        mbar_arrive(bars + kStateReady + 0);
 
-        if (OUT) {
-            // ---------------- Ya = Pm X (A operand from TMEM), then y = Ya + exp(cA_t) Yi
-            if (tid == 0) {
-                const uint32_t xb_ = smem_u32(sm + S::oX + buf * Cf::XT);
-                constexpr uint32_t idYa = idesc_bf16(QR, kP, 0, 1);
-#pragma unroll
-                for (int ks = 0; ks < QR / 16; ++ks) {
-                    const uint64_t dX = make_desc(xb_ + ks * 2048, 0, 1024, kSwizzle128B);
-                    mma_ts(tmem + cYa, tmem + cPh + ks * 8, dX, idYa, ks > 0);
-                    mma_ts(tmem + cYa, tmem + cPl + ks * 8, dX, idYa, 1);
-                }
-                mma_commit(bar_mma2);
+        for (int it = 0; it < nchunks; ++it) {
+            const int p = it & 1;
+            const uint32_t ph = (it >> 1) & 1;
+            const int s0 = t_begin + it * Q, Qc = min(Q, t_end - s0), e = Qc - 1;
+            const float *cA2 = v_cA(p), *gv = v_g(p), *vj = v_vj(p), *sg = v_sig(p);
+            const bool last_chunk = it == nchunks - 1;
+            // one thread waits for the chunk's vectors and first MMAs; the named barrier
+            // releases the other epilogue warps without them polling
+            if (ew == 0 && lane == 0) {
+                wait(kTilesFull + p, ph);
+                wait(kMma1 + p, ph);
             }
-            if (!mbar_wait(bar_mma2, it & 1, kWaitPolls)) fail();
+            named_sync(kBarEpi, kEpiThreads);
             fence_after();
-            {
-                const bool rvalid = kM64Rows ? (lane < 16) : true;
-                const int row = kM64Rows ? quad * 16 + lane : quad * 32 + lane;
-                const int ti = row / R, r = row % R;
-                const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-                uint32_t ya[32], yi[32];
-                tmem_ld32(tmem + lane_base + cYa + 32 * half, ya);
-                tmem_ld32(tmem + lane_base + cYi + 32 * half, yi);
-                if (rvalid && ti < Qc) {
-                    const float sc = fast_exp2(cA2[ti]);
-                    float *yp = static_cast<float *>(a.y) + (tok(s0 + ti) * R + r) * kP + 32 * half;
+            // ---- masked score -> TMEM (fp16, scaled by tauP)
+            if (OUT) {
+                constexpr int COLS = QR / 2;    // score columns per thread
+                const int t = min(ti, Q - 1);
+                const float ca = cA2[t], invBC = sg[3];   // tauP / (sB sC)
+                const float gd = row_ok ? gv[t] * invBC : 0.f;
+                // largest token among this warp's rows: blocks past it are all zero (warp-uniform)
+                const int tmax = (kRowsM64 ? eq * 16 + 15 : eq * 32 + 31) / R;
 #pragma unroll
-                    for (int j = 0; j < 32; j += 4)
-                        *reinterpret_cast<float4 *>(yp + j) = make_float4(
-                            fmaf(sc, __uint_as_float(yi[j]), __uint_as_float(ya[j])),
-                            fmaf(sc, __uint_as_float(yi[j + 1]), __uint_as_float(ya[j + 1])),
-                            fmaf(sc, __uint_as_float(yi[j + 2]), __uint_as_float(ya[j + 2])),
-                            fmaf(sc, __uint_as_float(yi[j + 3]), __uint_as_float(ya[j + 3])));
+                for (int cc = 0; cc < COLS; cc += 32) {
+                    const int cb = eh * COLS + cc;   // first score column of this 32-column block
+                    const int btok = (cb / 32) * TB; // first token of the block
+                    uint32_t p16[16];
+                    if (btok > tmax) {
+#pragma unroll
+                        for (int q = 0; q < 16; ++q) p16[q] = 0u;
+                    } else {
+                        uint32_t sv[32];
+                        tmem_ld16_nw(tmem + lane_base + cS + cb, sv);
+                        tmem_ld16_nw(tmem + lane_base + cS + cb + 16, sv + 16);
+                        // exp2(cA_t - cA_btok) <= 1 wherever it is used (btok <= tj < t)
+                        const float u = (row_ok && btok < ti) ? fast_exp2(ca - cA2[btok]) * invBC : 0.f;
+                        float um[TB];
+#pragma unroll
+                        for (int q = 0; q < TB; ++q) um[q] = u * vj[btok + q];
+                        tmem_wait_ld(sv);
+#pragma unroll
+                        for (int q = 0; q < 16; ++q) {
+                            float pm[2];
+#pragma unroll
+                            for (int z = 0; z < 2; ++z) {
+                                const int jq = (2 * q + z) / R;   // token offset in the block
+                                const int tj = btok + jq;
+                                const float m = (tj < ti) ? um[jq] : ((tj == ti) ? gd : 0.f);
+                                pm[z] = __uint_as_float(sv[2 * q + z]) * m;
+                            }
+                            p16[q] = pack_f16x2(pm[0], pm[1]);
+                        }
+                    }
+                    tmem_st16(tmem + lane_base + cP + cb / 2, p16);
+                }
+                fence_before();
+                mbar_arrive(bars + kPReady + p);
+            }
+            // ---- state update: H <- R(phi_e) [exp(cA_e) H + Sn]
+            {
+                const float rho = fast_exp2(cA2[e]), invBX = sg[4];
+                const int n = st_row, kk = n >> 1;
+                const float c = st_owner ? v_cos(p)[kk] : 1.f, s = st_owner ? v_sin(p)[kk] : 0.f;
+                const bool odd = n & 1;
+                float *dst = nullptr;
+                if (last_chunk && st_owner && !*abort_flag) {
+                    if (!OUT) dst = a.ws_state + (((size_t)bh * nseg + g + 1) * N + n) * kP + 32 * eh;
+                    else if (g == nseg - 1 && a.h_out) dst = a.h_out + ((size_t)bh * N + n) * kP + 32 * eh;
+                }
+                float m = 0.f;
+#pragma unroll
+                for (int h16 = 0; h16 < 32; h16 += 16) {
+                    uint32_t sh[32];   // [0, 16): Sn, [16, 32): H
+                    tmem_ld16_nw(tmem + lane_base + cSn + 32 * eh + h16, sh);
+                    tmem_ld16_nw(hcol + h16, sh + 16);
+                    tmem_wait_ld(sh);
+                    uint32_t hv[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float v = fmaf(rho, __uint_as_float(sh[16 + j]), __uint_as_float(sh[j]) * invBX);
+                        const float pv = __shfl_xor_sync(0xffffffffu, v, 1);
+                        const float nv = odd ? fmaf(s, pv, c * v) : fmaf(-s, pv, c * v);
+                        m = fmaxf(m, st_owner ? fabsf(nv) : 0.f);
+                        hv[j] = __float_as_uint(nv);
+                    }
+                    tmem_st16(hcol + h16, hv);
+                    if (dst) {
+#pragma unroll
+                        for (int j = 0; j < 16; j += 4)
+                            *reinterpret_cast<float4 *>(dst + h16 + j) =
+                                make_float4(__uint_as_float(hv[j]), __uint_as_float(hv[j + 1]),
+                                            __uint_as_float(hv[j + 2]), __uint_as_float(hv[j + 3]));
+                    }
+                }
+                publish_state((it + 1) & 1, m);
+                fence_proxy_async();
+                fence_before();
+                mbar_arrive(bars + kStateReady + ((it + 1) & 1));
+            }
+            // ---- y = Ya + exp(cA_t) Yi
+            if (OUT) {
+                if (ew == 0 && lane == 0) wait(kMma2 + p, ph);
+                named_sync(kBarEpi, kEpiThreads);
+                fence_after();
+                const bool store = row_ok && ti < Qc && !*abort_flag;
+                const float sc = fast_exp2(cA2[min(ti, Q - 1)]) * sg[5] * sigH[2 + p], sa = sg[6];
+                float *yp = static_cast<float *>(a.y) + (tok(s0 + min(ti, Qc - 1)) * R + ri) * kP + 32 * eh;
+#pragma unroll
+                for (int half16 = 0; half16 < 32; half16 += 16) {
+                    uint32_t yy[32];   // [0, 16): Ya, [16, 32): Yi
+                    tmem_ld16_nw(tmem + lane_base + cYa + 32 * eh + half16, yy);
+                    tmem_ld16_nw(tmem + lane_base + cYi0 + 64 * p + 32 * eh + half16, yy + 16);
+                    tmem_wait_ld(yy);
+                    const uint32_t *ya = yy, *yi = yy + 16;
+                    if (store) {
+#pragma unroll
+                        for (int j = 0; j < 16; j += 4)
+                            *reinterpret_cast<float4 *>(yp + half16 + j) = make_float4(
+                                fmaf(sc, __uint_as_float(yi[j]), sa * __uint_as_float(ya[j])),
+                                fmaf(sc, __uint_as_float(yi[j + 1]), sa * __uint_as_float(ya[j + 1])),
+                                fmaf(sc, __uint_as_float(yi[j + 2]), sa * __uint_as_float(ya[j + 2])),
+                                fmaf(sc, __uint_as_float(yi[j + 3]), sa * __uint_as_float(ya[j + 3])));
+                    }
                 }
             }
             fence_before();
-            __syncthreads();
-            fence_after();
+            mbar_arrive(bars + kEpiDone + p);
         }
-        if (*abort_flag) break;
-    }
-
-    // ---------------- segment outputs
-    if (!*abort_flag) {
-        if (!OUT) {
-            float *dst = a.ws_tot + ((size_t)bh * (nseg - 1) + g) * (1 + K);
-            for (int i = tid; i < 1 + K; i += kThreads) dst[i] = (i == 0) ? tot[0] / kLog2e : tot[i];
-        } else if (g == nseg - 1 && a.Bprev_out && a.xprev_out && L > 0) {
+        // ---- carry out (last segment)
+        if (OUT && g == nseg - 1 && a.Bprev_out && a.xprev_out && L > 0 && !*abort_flag) {
+            const int et = tid - kEpiW0 * 32;
             const size_t tl = tok(L - 1);
             const __nv_bfloat16 *Bm = static_cast<const __nv_bfloat16 *>(a.B);
             const __nv_bfloat16 *xm = static_cast<const __nv_bfloat16 *>(a.x);
             __nv_bfloat16 *bo = static_cast<__nv_bfloat16 *>(a.Bprev_out);
             __nv_bfloat16 *xo = static_cast<__nv_bfloat16 *>(a.xprev_out);
-            for (int i = tid; i < R * N; i += kThreads) bo[(size_t)bh * R * N + i] = Bm[tl * R * N + i];
-            for (int i = tid; i < R * kP; i += kThreads) xo[(size_t)bh * R * kP + i] = xm[tl * R * kP + i];
+            for (int i = et; i < R * N; i += kEpiThreads) bo[(size_t)bh * R * N + i] = Bm[tl * R * N + i];
+            for (int i = et; i < R * kP; i += kEpiThreads) xo[(size_t)bh * R * kP + i] = xm[tl * R * kP + i];
         }
-    } else if (tid == 0) {
-        // a wait gave up: let any outstanding bulk copy land before the CTA's shared memory goes away
-        mbar_wait(bar_ld, it & 1, kWaitPolls);
     }
     fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
 // ---------------------------------------------------------------- host side
@@ -569,17 +818,17 @@ EncodeFn encode_fn() {
     return fn;
 }
 
-// 4-d map over a [b*L][H][R][inner] bf16 tensor, box = {inner, R, 1, Q}
-bool map4(CUtensorMap *m, const void *base, int inner, int R, int H, long long rows, int Q, bool swz) {
+// 4-d map over a [b*L][H][R][inner] bf16 tensor, box = {64, R, 1, Q}, 128-byte swizzle
+bool map4(CUtensorMap *m, const void *base, int inner, int R, int H, long long rows, int Q) {
     EncodeFn enc = encode_fn();
     if (!enc) return false;
     const cuuint64_t dims[4] = {(cuuint64_t)inner, (cuuint64_t)R, (cuuint64_t)H, (cuuint64_t)rows};
     const cuuint64_t strides[3] = {(cuuint64_t)inner * 2, (cuuint64_t)inner * 2 * R, (cuuint64_t)inner * 2 * R * H};
-    const cuuint32_t box[4] = {(cuuint32_t)inner, (cuuint32_t)R, 1, (cuuint32_t)Q};
+    const cuuint32_t box[4] = {64, (cuuint32_t)R, 1, (cuuint32_t)Q};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, swz ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 // 3-d map over a [b*L][H][inner] bf16 tensor, box = {inner, 1, Q}
 bool map3(CUtensorMap *m, const void *base, int inner, int H, long long rows, int Q) {
@@ -597,6 +846,7 @@ bool map3(CUtensorMap *m, const void *base, int inner, int H, long long rows, in
 template <int N, int R, bool OUT>
 cudaError_t launch_pass(const TcMaps &maps, const ScanArgs &a, const ScanPlan &pl, int nlaunch, cudaStream_t s) {
     using Sm = Smem<N, R, OUT>;
+    static_assert(Sm::kAlloc <= 227 * 1024, "shared memory over the per-CTA limit");
     auto kern = tc_segment_kernel<N, R, OUT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Sm::kAlloc);
     if (e != cudaSuccess) return e;
@@ -616,8 +866,8 @@ cudaError_t run_tc(const ScanArgs &a, const ScanPlan &pl, cudaStream_t s) {
     using Cf = Cfg<N, R>;
     const long long rows = (long long)a.batch * a.L;
     TcMaps maps;
-    if (!map4(&maps.B, a.B, N, R, a.H, rows, Cf::Q, false) || !map4(&maps.C, a.C, N, R, a.H, rows, Cf::Q, false) ||
-        !map4(&maps.X, a.x, kP, R, a.H, rows, Cf::Q, true) || !map3(&maps.T, a.theta, N / 2, a.H, rows, Cf::Q))
+    if (!map4(&maps.B, a.B, N, R, a.H, rows, Cf::Q) || !map4(&maps.C, a.C, N, R, a.H, rows, Cf::Q) ||
+        !map4(&maps.X, a.x, kP, R, a.H, rows, Cf::Q) || !map3(&maps.T, a.theta, N / 2, a.H, rows, Cf::Q))
         return cudaErrorInvalidValue;
     cudaError_t e;
     if (pl.nseg > 1) {
