@@ -456,7 +456,8 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
             }
             // |B~| <= sqrt 2 max|B| (rotation of a pair);  |X^| <= max w max|x|;
             // |P| <= N max|B~| max|C~| max(w, lambda dt)
-            const float sgB = pow2_scale(1.5f * MB), sgC = pow2_scale(1.5f * MC), sgX = pow2_scale(MX * MW);
+            // one scale for B~ and C~ (their rotations then share the scaled cos / sin)
+            const float sgB = pow2_scale(1.5f * fmaxf(MB, MC)), sgC = sgB, sgX = pow2_scale(MX * MW);
             const float sgXp = pow2_scale(MX), tauP = pow2_scale((float)N * 2.25f * MB * MC * MW);
             if (ptid == 0) {
                 float *sg = v_sig(p);
@@ -507,7 +508,7 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                     const bool valid = t < Qc;
                     float c, s;
                     sincos_reduced(ph[i], &s, &c);
-                    const float cb = c * sgB, sb = s * sgB, cc = c * sgC, sc = s * sgC;
+                    const float cb = c * sgB, sb = s * sgB;
 #pragma unroll
                     for (int r = 0; r < R; ++r) {
                         const uint32_t off = sw128(t * R + r, 2 * lane);
@@ -519,7 +520,7 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                             const uint32_t vc = rc[i * R + r];
                             const float c0 = bf16_lo_f(vc), c1 = bf16_hi_f(vc);
                             *reinterpret_cast<uint32_t *>(cs + off) =
-                                valid ? pack_f16x2(fmaf(cc, c0, sc * c1), fmaf(cc, c1, -sc * c0)) : 0u;
+                                valid ? pack_f16x2(fmaf(cb, c0, sb * c1), fmaf(cb, c1, -sb * c0)) : 0u;
                         }
                     }
                 }
@@ -674,8 +675,10 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                 const int t = min(ti, Q - 1);
                 const float ca = cA2[t], invBC = sg[3];   // tauP / (sB sC)
                 const float gd = row_ok ? gv[t] * invBC : 0.f;
-                // largest token among this warp's rows: blocks past it are all zero (warp-uniform)
+                // token range of this warp's rows (warp-uniform): blocks past tmax are zero,
+                // blocks ending before tmin need no causal test
                 const int tmax = (kRowsM64 ? eq * 16 + 15 : eq * 32 + 31) / R;
+                const int tmin = (kRowsM64 ? eq * 16 : eq * 32) / R;
 #pragma unroll
                 for (int cc = 0; cc < COLS; cc += 32) {
                     const int cb = eh * COLS + cc;   // first score column of this 32-column block
@@ -694,17 +697,24 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
 #pragma unroll
                         for (int q = 0; q < TB; ++q) um[q] = u * vj[btok + q];
                         tmem_wait_ld(sv);
+                        if (btok + TB <= tmin) {
 #pragma unroll
-                        for (int q = 0; q < 16; ++q) {
-                            float pm[2];
+                            for (int q = 0; q < 16; ++q)
+                                p16[q] = pack_f16x2(__uint_as_float(sv[2 * q]) * um[(2 * q) / R],
+                                                    __uint_as_float(sv[2 * q + 1]) * um[(2 * q + 1) / R]);
+                        } else {
 #pragma unroll
-                            for (int z = 0; z < 2; ++z) {
-                                const int jq = (2 * q + z) / R;   // token offset in the block
-                                const int tj = btok + jq;
-                                const float m = (tj < ti) ? um[jq] : ((tj == ti) ? gd : 0.f);
-                                pm[z] = __uint_as_float(sv[2 * q + z]) * m;
+                            for (int q = 0; q < 16; ++q) {
+                                float pm[2];
+#pragma unroll
+                                for (int z = 0; z < 2; ++z) {
+                                    const int jq = (2 * q + z) / R;   // token offset in the block
+                                    const int tj = btok + jq;
+                                    const float m = (tj < ti) ? um[jq] : ((tj == ti) ? gd : 0.f);
+                                    pm[z] = __uint_as_float(sv[2 * q + z]) * m;
+                                }
+                                p16[q] = pack_f16x2(pm[0], pm[1]);
                             }
-                            p16[q] = pack_f16x2(pm[0], pm[1]);
                         }
                     }
                     tmem_st16(tmem + lane_base + cP + cb / 2, p16);
