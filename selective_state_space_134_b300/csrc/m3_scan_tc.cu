@@ -80,7 +80,8 @@ struct Smem {
     static constexpr uint32_t oXh = 2 * SLOT;                  // X^ [2] (fp16)
     static constexpr uint32_t oXp = oXh + 2 * C::XT;           // X' [2] (fp16), OUT only
     static constexpr uint32_t oH = oXp + (OUT ? 2 * C::XT : 0); // H (fp16), OUT only
-    static constexpr uint32_t oVec = oH + (OUT ? C::HT : 0);   // per-parity vectors
+    static constexpr uint32_t oYs = oH + (OUT ? C::HT : 0);    // y staging: 2 halves [QR][32] fp32, OUT only
+    static constexpr uint32_t oVec = oYs + (OUT ? C::QR * kP * 4 : 0);   // per-parity vectors
     // per parity (floats): cA2[Q] g[Q] w[Q] vj[Q] dt[Q] cosE[K] sinE[K] sig[8]
     static constexpr uint32_t VF = 5 * C::Q + 2 * C::K + 8;
     static constexpr uint32_t oPart = oVec + 2 * 4 * VF;       // angle partials [8][K]
@@ -88,7 +89,8 @@ struct Smem {
     static constexpr uint32_t oMxH = oMx + 4 * kProWarps * 4;       // epilogue maxima [2][8]
     static constexpr uint32_t oSigH = oMxH + 4 * 2 * kEpiWarps;     // H scale [2] and inverse [2]
     static constexpr uint32_t oTot = oSigH + 16;                    // segment totals [1 + K]
-    static constexpr uint32_t oBar = ((oTot + 4 * (1 + C::K) + 7) / 8) * 8;
+    static constexpr uint32_t oWtot = oTot + 4 * (1 + C::K);                    // per-warp dt A totals [4]
+    static constexpr uint32_t oBar = ((oWtot + 16 + 7) / 8) * 8;
     static constexpr int kNumBars = 16;
     static constexpr uint32_t oTmem = oBar + 8 * kNumBars;
     static constexpr uint32_t oFlag = oTmem + 4;
@@ -96,9 +98,13 @@ struct Smem {
     static constexpr uint32_t kAlloc = kBytes + 1024;          // slack for the 1024-byte alignment
 };
 
-// Byte offset of element (row, col) in a 128-byte-swizzled tile of 128-byte rows.
+// Byte offset of element (row, col) in a 128-byte-swizzled tile of 128-byte rows
+// (16-bit elements; sw128f: 32-bit elements).
 __device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t col) {
     return row * 128u + ((((col >> 3) ^ row) & 7u) << 4) + ((col & 7u) << 1);
+}
+__device__ __forceinline__ uint32_t sw128f(uint32_t row, uint32_t col) {
+    return row * 128u + ((((col >> 2) ^ row) & 7u) << 4) + ((col & 3u) << 2);
 }
 
 __device__ __forceinline__ void sincos_reduced(float x, float *s, float *c) {
@@ -151,7 +157,7 @@ __device__ __forceinline__ float warp_max(float v) {   // v >= 0
 }
 
 struct TcMaps {
-    CUtensorMap B, C, X, T;
+    CUtensorMap B, C, X, T, Y;
 };
 
 enum Bar {
@@ -188,6 +194,7 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
     float *mxH = reinterpret_cast<float *>(sm + S::oMxH);
     float *sigH = reinterpret_cast<float *>(sm + S::oSigH);   // [0..1] scale, [2..3] inverse
     float *tot = reinterpret_cast<float *>(sm + S::oTot);
+    float *wtot = reinterpret_cast<float *>(sm + S::oWtot);
     auto vec = [&](int p) { return reinterpret_cast<float *>(sm + S::oVec) + p * S::VF; };
     // per-parity vector fields
     auto v_cA = [&](int p) { return vec(p); };
@@ -245,7 +252,10 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
         tma_prefetch_desc(&maps.B);
         tma_prefetch_desc(&maps.X);
         tma_prefetch_desc(&maps.T);
-        if (OUT) tma_prefetch_desc(&maps.C);
+        if (OUT) {
+            tma_prefetch_desc(&maps.C);
+            tma_prefetch_desc(&maps.Y);
+        }
     }
     for (int i = tid; i < 1 + K; i += kThreads) tot[i] = 0.f;
     if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
@@ -371,9 +381,19 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
             // ---- P1: token scalars
             const float c_dt = to_f(r_dt), c_a = c_dt * to_f(r_A) * kLog2e, c_g = to_f(r_l) * c_dt;
             const float c_w = c_g + (1.f - to_f(r_ln)) * to_f(r_dtn);
+            // inclusive scan of dt A within each warp of tokens (shuffles); the warp totals
+            // are added after the barrier
+            float c_scan = c_a;
+            if (pw * 32 < Q) {
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float t = __shfl_up_sync(0xffffffffu, c_scan, o);
+                    if (lane >= o) c_scan += t;
+                }
+                if (lane == 31) wtot[pw] = c_scan;
+            }
             if (ptid < Q) {
                 dts[ptid] = c_dt;
-                cA2[ptid] = c_a;
                 gv[ptid] = c_g;
                 wv[ptid] = c_w;
             }
@@ -382,20 +402,12 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
             // other warps no issue slots) releases the rest
             if (ptid == 0) wait(kRawFull + p, (it >> 1) & 1);
             named_sync(kBarPro, kProThreads);
-            // ---- P2: cumsum (warp 0), angle partial sums, bounds of |B|, |C|, |x|, w
-            if (pw == 0) {
-                float carry = 0.f;
-                for (int base = 0; base < Q; base += 32) {
-                    float v = (base + lane < Q) ? cA2[base + lane] : 0.f;
+            // ---- P2: chunk-local cumsum of dt A, angle partial sums, bounds of |B|, |C|, |x|, w
+            if (ptid < Q) {
+                float off = 0.f;
 #pragma unroll
-                    for (int o = 1; o < 32; o <<= 1) {
-                        const float t = __shfl_up_sync(0xffffffffu, v, o);
-                        if (lane >= o) v += t;
-                    }
-                    v += carry;
-                    if (base + lane < Q) cA2[base + lane] = v;
-                    carry = __shfl_sync(0xffffffffu, v, 31);
-                }
+                for (int q = 0; q < (Q + 31) / 32 - 1; ++q) off += (q < pw) ? wtot[q] : 0.f;
+                cA2[ptid] = c_scan + off;
             }
             const __nv_bfloat16 *rawT = reinterpret_cast<const __nv_bfloat16 *>(slot + S::sT);
             float mW = ptid < Qc ? fabsf(c_w) : 0.f;
@@ -446,13 +458,13 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
             }
             named_sync(kBarPro, kProThreads);
             // ---- P3: scales, rotation of B and C in place (fp16), X^, mask column factors
-            float MB = 0.f, MC = 0.f, MX = 0.f, MW = 0.f;
-#pragma unroll
-            for (int q = 0; q < kProWarps; ++q) {
-                MB = fmaxf(MB, mx[q * 4 + 0]);
-                MC = fmaxf(MC, mx[q * 4 + 1]);
-                MX = fmaxf(MX, mx[q * 4 + 2]);
-                MW = fmaxf(MW, mx[q * 4 + 3]);
+            float MB, MC, MX, MW;
+            {
+                const bool rd = lane < kProWarps;
+                MB = warp_max(rd ? mx[lane * 4 + 0] : 0.f);
+                MC = warp_max(rd ? mx[lane * 4 + 1] : 0.f);
+                MX = warp_max(rd ? mx[lane * 4 + 2] : 0.f);
+                MW = warp_max(rd ? mx[lane * 4 + 3] : 0.f);
             }
             // |B~| <= sqrt 2 max|B| (rotation of a pair);  |X^| <= max w max|x|;
             // |P| <= N max|B~| max|C~| max(w, lambda dt)
@@ -472,7 +484,8 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
             }
             {
                 float phi = 0.f;
-                for (int sg = 0; sg < seg; ++sg) phi += part[sg * K + k];
+#pragma unroll
+                for (int sg = 0; sg < Cf::NSEG - 1; ++sg) phi += (sg < seg) ? part[sg * K + k] : 0.f;
                 unsigned char *bs = slot + S::sB + slab * (QR * 128);
                 unsigned char *cs = slot + S::sC + slab * (QR * 128);
                 // angles of all the thread's tokens first (a short FMA chain), then
@@ -484,16 +497,6 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                     ph[i] = phi;
                 }
                 const int ie = e - seg * TPS;   // the chunk's last token, if it is this thread's
-                if (ie >= 0 && ie < TPS) {
-                    float pe = 0.f;
-#pragma unroll
-                    for (int i = 0; i < TPS; ++i) pe = (i == ie) ? ph[i] : pe;
-                    float se, ce2;
-                    sincos_reduced(pe, &se, &ce2);
-                    v_cos(p)[k] = ce2;
-                    v_sin(p)[k] = se;
-                    if (!OUT) tot[1 + k] += pe;
-                }
                 // all raw words first: the in-place stores below then cannot hold back a load
                 uint32_t rb[TPS * R], rc[TPS * R];
 #pragma unroll
@@ -508,6 +511,11 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                     const bool valid = t < Qc;
                     float c, s;
                     sincos_reduced(ph[i], &s, &c);
+                    if (i == ie) {   // the chunk's last token: rotation of the state at the chunk end
+                        v_cos(p)[k] = c;
+                        v_sin(p)[k] = s;
+                        if (!OUT) tot[1 + k] += ph[i];
+                    }
                     const float cb = c * sgB, sb = s * sgB;
 #pragma unroll
                     for (int r = 0; r < R; ++r) {
@@ -695,7 +703,13 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                         const float u = (row_ok && btok < ti) ? fast_exp2(ca - cA2[btok]) * invBC : 0.f;
                         float um[TB];
 #pragma unroll
-                        for (int q = 0; q < TB; ++q) um[q] = u * vj[btok + q];
+                        for (int q = 0; q < TB; q += 4) {
+                            const float4 v4 = *reinterpret_cast<const float4 *>(vj + btok + q);
+                            um[q] = u * v4.x;
+                            if (q + 1 < TB) um[q + 1] = u * v4.y;
+                            if (q + 2 < TB) um[q + 2] = u * v4.z;
+                            if (q + 3 < TB) um[q + 3] = u * v4.w;
+                        }
                         tmem_wait_ld(sv);
                         if (btok + TB <= tmin) {
 #pragma unroll
@@ -765,12 +779,17 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
             }
             // ---- y = Ya + exp(cA_t) Yi
             if (OUT) {
-                if (ew == 0 && lane == 0) wait(kMma2 + p, ph);
+                if (ew == 0 && lane == 0) {
+                    wait(kMma2 + p, ph);
+                    bulk_wait_read<0>();   // the previous chunk's y stores have left the staging tile
+                }
                 named_sync(kBarEpi, kEpiThreads);
                 fence_after();
-                const bool store = row_ok && ti < Qc && !*abort_flag;
                 const float sc = fast_exp2(cA2[min(ti, Q - 1)]) * sg[5] * sigH[2 + p], sa = sg[6];
-                float *yp = static_cast<float *>(a.y) + (tok(s0 + min(ti, Qc - 1)) * R + ri) * kP + 32 * eh;
+                // y rows go through a shared-memory tile (this thread: row `row`, columns
+                // [32 eh, 32 eh + 32) of half eh) and leave by TMA: rows past the sequence end
+                // are clipped by the map, and the global writes are whole lines
+                unsigned char *ys = sm + S::oYs + eh * (QR * 128);
 #pragma unroll
                 for (int half16 = 0; half16 < 32; half16 += 16) {
                     uint32_t yy[32];   // [0, 16): Ya, [16, 32): Yi
@@ -778,20 +797,30 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                     tmem_ld16_nw(tmem + lane_base + cYi0 + 64 * p + 32 * eh + half16, yy + 16);
                     tmem_wait_ld(yy);
                     const uint32_t *ya = yy, *yi = yy + 16;
-                    if (store) {
+                    if (row_ok) {
 #pragma unroll
                         for (int j = 0; j < 16; j += 4)
-                            *reinterpret_cast<float4 *>(yp + half16 + j) = make_float4(
+                            *reinterpret_cast<float4 *>(ys + sw128f(row, half16 + j)) = make_float4(
                                 fmaf(sc, __uint_as_float(yi[j]), sa * __uint_as_float(ya[j])),
                                 fmaf(sc, __uint_as_float(yi[j + 1]), sa * __uint_as_float(ya[j + 1])),
                                 fmaf(sc, __uint_as_float(yi[j + 2]), sa * __uint_as_float(ya[j + 2])),
                                 fmaf(sc, __uint_as_float(yi[j + 3]), sa * __uint_as_float(ya[j + 3])));
                     }
                 }
+                fence_proxy_async();
+                named_sync(kBarEpi, kEpiThreads);
+                if (ew == 0 && lane == 0) {
+                    if (!*abort_flag) {
+                        tma_store_5d(&maps.Y, sm + S::oYs, 0, 0, h, s0, b);
+                        tma_store_5d(&maps.Y, sm + S::oYs + QR * 128, 32, 0, h, s0, b);
+                    }
+                    bulk_commit();
+                }
             }
             fence_before();
             mbar_arrive(bars + kEpiDone + p);
         }
+        if (OUT && ew == 0 && lane == 0) bulk_wait<0>();
         // ---- carry out (last segment)
         if (OUT && g == nseg - 1 && a.Bprev_out && a.xprev_out && L > 0 && !*abort_flag) {
             const int et = tid - kEpiW0 * 32;
@@ -853,6 +882,20 @@ bool map3(CUtensorMap *m, const void *base, int inner, int H, long long rows, in
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 5-d map over the fp32 y [batch][L][H][R][64], box = {32, R, 1, Q, 1}, 128-byte swizzle
+bool map_y(CUtensorMap *m, void *base, int R, int H, int L, int batch, int Q) {
+    EncodeFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[5] = {64, (cuuint64_t)R, (cuuint64_t)H, (cuuint64_t)L, (cuuint64_t)batch};
+    const cuuint64_t strides[4] = {64 * 4, (cuuint64_t)R * 64 * 4, (cuuint64_t)H * R * 64 * 4,
+                                   (cuuint64_t)L * H * R * 64 * 4};
+    const cuuint32_t box[5] = {32, (cuuint32_t)R, 1, (cuuint32_t)Q, 1};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int N, int R, bool OUT>
 cudaError_t launch_pass(const TcMaps &maps, const ScanArgs &a, const ScanPlan &pl, int nlaunch, cudaStream_t s) {
     using Sm = Smem<N, R, OUT>;
@@ -877,7 +920,8 @@ cudaError_t run_tc(const ScanArgs &a, const ScanPlan &pl, cudaStream_t s) {
     const long long rows = (long long)a.batch * a.L;
     TcMaps maps;
     if (!map4(&maps.B, a.B, N, R, a.H, rows, Cf::Q) || !map4(&maps.C, a.C, N, R, a.H, rows, Cf::Q) ||
-        !map4(&maps.X, a.x, kP, R, a.H, rows, Cf::Q) || !map3(&maps.T, a.theta, N / 2, a.H, rows, Cf::Q))
+        !map4(&maps.X, a.x, kP, R, a.H, rows, Cf::Q) || !map3(&maps.T, a.theta, N / 2, a.H, rows, Cf::Q) ||
+        !map_y(&maps.Y, a.y, R, a.H, a.L, a.batch, Cf::Q))
         return cudaErrorInvalidValue;
     cudaError_t e;
     if (pl.nseg > 1) {
