@@ -108,8 +108,10 @@ __device__ __forceinline__ uint32_t sw128f(uint32_t row, uint32_t col) {
 }
 
 __device__ __forceinline__ void sincos_reduced(float x, float *s, float *c) {
-    // Cody-Waite reduction by 2 pi (two-constant split), then the hardware sin/cos on [-pi, pi]
-    const float n = rintf(x * 0.15915494309189535f);
+    // Cody-Waite reduction by 2 pi (two-constant split), then the hardware sin/cos on [-pi, pi].
+    // n = round(x / 2 pi) by the 1.5 * 2^23 addition (exact for |x / 2 pi| < 2^22), which runs
+    // on the FMA pipe instead of the quarter-rate conversion unit
+    const float n = (x * 0.15915494309189535f + 12582912.f) - 12582912.f;
     float r = fmaf(-n, 6.28318548202514648f, x);
     r = fmaf(-n, -1.7484555314695172e-7f, r);
     __sincosf(r, s, c);
