@@ -255,8 +255,10 @@ def time_decode(m3, w, calls, warmup):
     return e0.elapsed_time(e1) / calls, tr_ms / max(n_tr, 1)
 
 
-def e2e_prefill(m3, w, inp, steps, warmup):
-    """Same metric through host buffers: pinned H2D of the inputs, scan, D2H of y and the state."""
+def e2e_prefill(m3, w, inp, steps, warmup, slices=16):
+    """Same metric through host buffers, via the library's staged prefill: every step copies the
+    inputs in from pinned host memory and y and the final state h back out, the copies of each
+    token range overlapped with the kernels and copies of the others."""
     host = {k: v.cpu().pin_memory() for k, v in inp.items()}
     dtype = inp["x"].dtype
     dev = {k: torch.empty_like(v) for k, v in inp.items()}
@@ -264,29 +266,32 @@ def e2e_prefill(m3, w, inp, steps, warmup):
     y = torch.empty(inp["x"].shape, dtype=torch.float32, device="cuda")
     y_host = torch.empty(y.shape, dtype=y.dtype).pin_memory()
     h_host = torch.empty(st.h.shape, dtype=st.h.dtype).pin_memory()
+    slices = max(1, min(slices, w.seqlen))
+    need = m3.mamba3.scan_fwd_staged_workspace(m3.dims(w.batch, w.seqlen, w.nheads, w.P, w.N, w.R, dtype), slices)
+    work = torch.empty(max(need, 1), dtype=torch.uint8, device="cuda")
+    main, side = torch.cuda.current_stream(), torch.cuda.Stream()
 
     def step():
-        for k in KEYS:
-            dev[k].copy_(host[k], non_blocking=True)
-        m3.scan_fwd(*(dev[k] for k in KEYS), state_out=st, y=y)
-        y_host.copy_(y, non_blocking=True)
-        h_host.copy_(st.h, non_blocking=True)
+        m3.mamba3.scan_fwd_staged(host, dev, y_host, y, state_out=st, host_h=h_host, slices=slices,
+                                  workspace=work, stream=main, copy_stream=side)
 
     for _ in range(warmup):
         step()
+    main.wait_stream(side)
     torch.cuda.synchronize()
-    t0 = time.perf_counter()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
+    e0.record(main)
     for _ in range(steps):
         step()
-    e1.record()
+    main.wait_stream(side)
+    e1.record(main)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
     h2d = sum(v.numel() * v.element_size() for v in host.values())
     d2h = y.numel() * y.element_size() + st.h.numel() * 4
     return {"value": w.batch * w.seqlen / (ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": ms}
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "api": "mamba3_scan_fwd_staged",
+            "slices": slices}
 
 
 def cpu_oracle_rate(w, inp, max_seconds=12.0):
@@ -371,16 +376,7 @@ def run_ours(args):
     extra = {}
     if rank == 0 and not args.quick:
         # decode: the four (N, R) variants, 1024 calls each
-        dec = {}
-        for name in ("decode_n64_r1", "decode_n64_r4", "decode_n128_r1", "decode_n128_r4"):
-            wd = WORKLOADS[name]
-            ms_call, k_ms = time_decode(m3, wd, 1024, 16)
-            gbs = decode_bytes(wd) / (k_ms * 1e-3) / 1e9
-            dec[name] = {"tokens_per_s": wd.batch / (ms_call * 1e-3), "us_per_call": round(ms_call * 1e3, 2),
-                         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s",
-                                      "frac": round(gbs / hbm_peak, 4),
-                                      "traffic": traffic_for("decode", name),
-                                      "algorithmic_bytes": decode_bytes(wd), "kernel_ms": k_ms}}
+        dec = decode_results(m3, hbm_peak)
         extra["decode"] = {"metric": "decode tokens/s", "unit": "tokens/s", "workloads": dec}
         # other prefill workloads
         pre = {}
@@ -450,6 +446,31 @@ def run_reference(args):
     }))
 
 
+def decode_results(m3, hbm_peak, calls=1024, warmup=16):
+    """The four decode workloads: tokens/s, us per call and the kernel's HBM roofline."""
+    from selective_state_space_134_b300.synth import WORKLOADS
+    dec = {}
+    for name in ("decode_n64_r1", "decode_n64_r4", "decode_n128_r1", "decode_n128_r4"):
+        wd = WORKLOADS[name]
+        ms_call, k_ms = time_decode(m3, wd, calls, warmup)
+        gbs = decode_bytes(wd) / (k_ms * 1e-3) / 1e9
+        dec[name] = {"tokens_per_s": wd.batch / (ms_call * 1e-3), "us_per_call": round(ms_call * 1e3, 2),
+                     "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+                                  "frac": round(gbs / hbm_peak, 4),
+                                  "traffic": traffic_for("decode", name),
+                                  "algorithmic_bytes": decode_bytes(wd), "kernel_ms": k_ms}}
+    return dec
+
+
+def run_decode_only(args):
+    torch.cuda.set_device(0)
+    import selective_state_space_134_b300 as m3
+    m3.lib()
+    hbm_peak, _, _ = peaks()
+    print(json.dumps({"metric": "decode tokens/s", "unit": "tokens/s", "higher_is_better": True,
+                      "workloads": decode_results(m3, hbm_peak)}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -457,10 +478,14 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--quick", action="store_true", help="headline only (no decode / other workloads / oracle)")
+    ap.add_argument("--decode-only", action="store_true",
+                    help="one JSON line with the four decode workloads only (profiling runs)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.decode_only:
+        run_decode_only(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -120,6 +120,48 @@ m3_status mamba3_scan_fwd(const m3_dims *dims, const void *x, const void *B, con
                           const m3_state *state_in, void *y, const m3_state *state_out,
                           void *workspace, size_t workspace_bytes, void *stream);
 
+/* The seven per-token input tensors of a prefill (layouts as in mamba3_scan_fwd). */
+typedef struct {
+    const void *x, *B, *C, *dt, *A, *lambda, *theta;
+} m3_token_inputs;
+
+/*
+ * Workspace bytes mamba3_scan_fwd_staged needs for `dims` cut into `slices`
+ * token slices (0 is a valid answer).  Errors as mamba3_scan_fwd_workspace;
+ * slices < 1 is M3_ERR_INVALID_ARG.
+ */
+m3_status mamba3_scan_fwd_staged_workspace(const m3_dims *dims, int slices, size_t *bytes);
+
+/*
+ * The prefill from and to host memory, with the host <-> device copies
+ * overlapped: the sequences are cut into `slices` consecutive token ranges
+ * (at most L); range i of every sequence is copied in and scanned on `stream`
+ * (starting from range i-1's final state and carry), and its y is copied out
+ * on `copy_stream` while range i+1 is copied in.  The host buffers should be
+ * pinned (page-locked) for the copies to be asynchronous.
+ *   host_in, host_y:   the inputs and y in host memory, full layouts;
+ *   dev_in, dev_y:     device buffers of the same sizes (caller-owned staging;
+ *                      range i occupies the block of batch * L_i tokens that
+ *                      follows the earlier ranges' blocks);
+ *   dev_state_in:      initial state and carry on the device, or NULL (zero);
+ *   dev_state_out:     final state and carry on the device; required (with its
+ *                      carry) when slices > 1, as it carries the state between
+ *                      the ranges; may equal dev_state_in;
+ *   host_h_out:        if non-NULL (needs dev_state_out), the final state h is
+ *                      also copied to this host buffer [batch][H][N][P] fp32;
+ *   workspace:         at least mamba3_scan_fwd_staged_workspace(dims, slices).
+ * Work on `stream` first waits for the copies already queued on `copy_stream`
+ * (a previous call's outputs), so consecutive calls may share the buffers.
+ * Returns when everything is enqueued; `copy_stream` holds the last copies
+ * (synchronise it before reading the host outputs).  Argument errors are
+ * reported before anything is enqueued; a failing range reports M3_ERR_CUDA.
+ * Not from the Mamba-3 pages: a host-side convenience around mamba3_scan_fwd.
+ */
+m3_status mamba3_scan_fwd_staged(const m3_dims *dims, const m3_token_inputs *host_in, const m3_token_inputs *dev_in,
+                                 void *host_y, void *dev_y, const m3_state *dev_state_in,
+                                 const m3_state *dev_state_out, float *host_h_out, void *workspace,
+                                 size_t workspace_bytes, int slices, void *stream, void *copy_stream);
+
 /* Size of the static scratch array behind mamba3_scan_fwd_noalloc (16 MiB). */
 #define M3_NOALLOC_SCRATCH_BYTES (16u << 20)
 

@@ -202,6 +202,117 @@ m3_status mamba3_scan_fwd(const m3_dims *dims, const void *x, const void *B, con
     return e == cudaSuccess ? M3_OK : M3_ERR_CUDA;
 }
 
+// Token range [l0, l1) of slice i when L tokens are cut into ns slices.
+static void slice_range(int L, int ns, int i, int *l0, int *l1) {
+    const int base = L / ns, extra = L % ns;
+    *l0 = i * base + (i < extra ? i : extra);
+    *l1 = *l0 + base + (i < extra ? 1 : 0);
+}
+
+m3_status mamba3_scan_fwd_staged_workspace(const m3_dims *dims, int slices, size_t *bytes) {
+    if (!bytes || !dims || slices < 1) return M3_ERR_INVALID_ARG;
+    m3_status st = check_dims(dims, true);
+    if (st != M3_OK) return st;
+    const int L = dims->seqlen;
+    const int ns = slices < L ? slices : (L > 0 ? L : 1);
+    size_t need = 0;
+    for (int ls : {(L + ns - 1) / ns, L / ns}) {   // slices hold ceil(L / ns) or floor(L / ns) tokens
+        if (ls < 1) continue;
+        m3_dims sd = *dims;
+        sd.seqlen = ls;
+        size_t w = 0;
+        if ((st = mamba3_scan_fwd_workspace(&sd, &w)) != M3_OK) return st;
+        if (w > need) need = w;
+    }
+    *bytes = need;
+    return M3_OK;
+}
+
+m3_status mamba3_scan_fwd_staged(const m3_dims *dims, const m3_token_inputs *host_in, const m3_token_inputs *dev_in,
+                                 void *host_y, void *dev_y, const m3_state *dev_state_in,
+                                 const m3_state *dev_state_out, float *host_h_out, void *workspace,
+                                 size_t workspace_bytes, int slices, void *stream, void *copy_stream) {
+    m3_status st = check_dims(dims, true);
+    if (st != M3_OK) return st;
+    if (!host_in || !dev_in || slices < 1) return M3_ERR_INVALID_ARG;
+    const m3_dims &d = *dims;
+    if (d.batch == 0) return M3_OK;
+    if (host_h_out && !dev_state_out) return M3_ERR_INVALID_ARG;
+    const int L = d.seqlen, ns = slices < L ? slices : (L > 0 ? L : 1);
+    if (ns > 1 && !(dev_state_out && dev_state_out->B_prev)) return M3_ERR_INVALID_ARG;   // carries the slices
+    for (const void *p : {host_in->x, host_in->B, host_in->C, host_in->dt, host_in->A, host_in->lambda,
+                          host_in->theta, dev_in->x, dev_in->B, dev_in->C, dev_in->dt, dev_in->A, dev_in->lambda,
+                          dev_in->theta})
+        if (!p) return M3_ERR_INVALID_ARG;
+    if (L > 0 && (!dev_y || !host_y)) return M3_ERR_INVALID_ARG;
+    size_t need = 0;
+    if ((st = mamba3_scan_fwd_staged_workspace(dims, slices, &need)) != M3_OK) return st;
+    if (need > 0 && (!workspace || workspace_bytes < need)) return M3_ERR_WORKSPACE;
+    const size_t es = elem_size(d.dtype);
+    const size_t H = (size_t)d.nheads, P = (size_t)d.headdim, N = (size_t)d.dstate, R = (size_t)d.rank;
+    const size_t nb = (size_t)d.batch;
+    // bytes per token (all heads) of every tensor
+    const size_t tx = H * R * P * es, tB = H * R * N * es, ts = H * es, tth = H * (N / 2) * es, ty = H * R * P * 4;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream), cs = static_cast<cudaStream_t>(copy_stream);
+    // the previous call's copies out read buffers this call rewrites: start after them
+    {
+        cudaEvent_t ev;
+        if (cudaEventCreateWithFlags(&ev, cudaEventDisableTiming) != cudaSuccess) return M3_ERR_CUDA;
+        cudaError_t e = cudaEventRecord(ev, cs);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ev, 0);
+        cudaEventDestroy(ev);
+        if (e != cudaSuccess) return M3_ERR_CUDA;
+    }
+    if (L == 0) {
+        st = mamba3_scan_fwd(dims, dev_in->x, dev_in->B, dev_in->C, dev_in->dt, dev_in->A, dev_in->lambda,
+                             dev_in->theta, dev_state_in, dev_y, dev_state_out, workspace, workspace_bytes, stream);
+        if (st == M3_OK && host_h_out &&
+            cudaMemcpyAsync(host_h_out, dev_state_out->h, nb * H * N * P * 4, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+            st = M3_ERR_CUDA;
+        return st;
+    }
+    // Slice i holds tokens [l0, l1) of every sequence; its device copy is the contiguous
+    // [batch][l1 - l0][...] block at offset batch * l0 * (bytes per token) of each device buffer.
+    for (int i = 0; i < ns; ++i) {
+        int l0, l1;
+        slice_range(L, ns, i, &l0, &l1);
+        const size_t ls = (size_t)(l1 - l0);
+        const struct { const void *h; const void *dv; size_t tb; } in[7] = {
+            {host_in->x, dev_in->x, tx}, {host_in->B, dev_in->B, tB}, {host_in->C, dev_in->C, tB},
+            {host_in->dt, dev_in->dt, ts}, {host_in->A, dev_in->A, ts}, {host_in->lambda, dev_in->lambda, ts},
+            {host_in->theta, dev_in->theta, tth}};
+        const void *dp[7];
+        for (int k = 0; k < 7; ++k) {
+            char *dst = static_cast<char *>(const_cast<void *>(in[k].dv)) + nb * (size_t)l0 * in[k].tb;
+            const char *src = static_cast<const char *>(in[k].h) + (size_t)l0 * in[k].tb;
+            dp[k] = dst;
+            if (cudaMemcpy2DAsync(dst, ls * in[k].tb, src, (size_t)L * in[k].tb, ls * in[k].tb, nb,
+                                  cudaMemcpyHostToDevice, s) != cudaSuccess)
+                return M3_ERR_CUDA;
+        }
+        m3_dims sd = d;
+        sd.seqlen = (int)ls;
+        char *ydev = static_cast<char *>(dev_y) + nb * (size_t)l0 * ty;
+        st = mamba3_scan_fwd(&sd, dp[0], dp[1], dp[2], dp[3], dp[4], dp[5], dp[6],
+                             i == 0 ? dev_state_in : dev_state_out, ydev, dev_state_out, workspace, workspace_bytes,
+                             stream);
+        if (st != M3_OK) return st;
+        cudaEvent_t ev;
+        if (cudaEventCreateWithFlags(&ev, cudaEventDisableTiming) != cudaSuccess) return M3_ERR_CUDA;
+        cudaError_t e = cudaEventRecord(ev, s);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, ev, 0);
+        cudaEventDestroy(ev);   // released once the wait has been satisfied
+        if (e != cudaSuccess) return M3_ERR_CUDA;
+        if (cudaMemcpy2DAsync(static_cast<char *>(host_y) + (size_t)l0 * ty, (size_t)L * ty, ydev, ls * ty, ls * ty, nb,
+                              cudaMemcpyDeviceToHost, cs) != cudaSuccess)
+            return M3_ERR_CUDA;
+    }
+    if (host_h_out &&
+        cudaMemcpyAsync(host_h_out, dev_state_out->h, nb * H * N * P * 4, cudaMemcpyDeviceToHost, cs) != cudaSuccess)
+        return M3_ERR_CUDA;
+    return M3_OK;
+}
+
 m3_status mamba3_decode_step(const m3_dims *dims, const void *x, const void *B, const void *C,
                              const void *dt, const void *A, const void *lambda, const void *theta,
                              const m3_state *state, void *y, void *stream) {

@@ -32,6 +32,10 @@ class m3_state(ctypes.Structure):
     _fields_ = [("h", ctypes.c_void_p), ("B_prev", ctypes.c_void_p), ("x_prev", ctypes.c_void_p)]
 
 
+class m3_token_inputs(ctypes.Structure):
+    _fields_ = [(k, ctypes.c_void_p) for k in ("x", "B", "C", "dt", "A", "lam", "theta")]
+
+
 class Mamba3Error(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
@@ -66,6 +70,12 @@ def lib() -> ctypes.CDLL:
         L.mamba3_trace_begin.restype = ctypes.c_int
         L.mamba3_trace_end.argtypes = [ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_double)]
         L.mamba3_trace_end.restype = ctypes.c_int
+        L.mamba3_scan_fwd_staged_workspace.argtypes = [dp, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)]
+        L.mamba3_scan_fwd_staged_workspace.restype = ctypes.c_int
+        ip = ctypes.POINTER(m3_token_inputs)
+        L.mamba3_scan_fwd_staged.argtypes = [dp, ip, ip, vp, vp, sp, sp, vp, vp, ctypes.c_size_t, ctypes.c_int,
+                                             vp, vp]
+        L.mamba3_scan_fwd_staged.restype = ctypes.c_int
         L.mamba3_version.argtypes = []
         L.mamba3_version.restype = ctypes.c_int
         _lib = L
@@ -217,3 +227,55 @@ def scan_fwd_noalloc(x, B, C, dt, A, lam, theta, state_in: Optional[State] = Non
             ctypes.byref(st_out) if st_out is not None else None, _stream_ptr(stream))
     _check(rc, "mamba3_scan_fwd_noalloc")
     return y
+
+
+TOKEN_KEYS = ("x", "B", "C", "dt", "A", "lam", "theta")
+_side_streams = {}
+
+
+def _side_stream(device) -> "torch.cuda.Stream":
+    """A second stream per device for the copies out of scan_fwd_staged."""
+    key = torch.device(device).index if torch.device(device).index is not None else torch.cuda.current_device()
+    if key not in _side_streams:
+        _side_streams[key] = torch.cuda.Stream(device=key)
+    return _side_streams[key]
+
+
+def scan_fwd_staged_workspace(d: m3_dims, slices: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().mamba3_scan_fwd_staged_workspace(ctypes.byref(d), int(slices), ctypes.byref(n)),
+           "mamba3_scan_fwd_staged_workspace")
+    return int(n.value)
+
+
+def scan_fwd_staged(host: dict, dev: dict, host_y: torch.Tensor, dev_y: torch.Tensor,
+                    state_out: Optional[State] = None, host_h: Optional[torch.Tensor] = None,
+                    state_in: Optional[State] = None, slices: int = 4, workspace: Optional[torch.Tensor] = None,
+                    stream=None, copy_stream=None):
+    """mamba3_scan_fwd_staged: the prefill from pinned host tensors to host tensors, the copies
+    overlapped with the kernels over `slices` batch slices.
+
+    ``host`` / ``dev``: dicts of the seven token inputs (keys x, B, C, dt, A, lam, theta) in pinned host
+    memory and same-shaped device staging buffers.  ``host_y`` / ``dev_y``: y in host and device memory.
+    ``state_out`` (device) receives the final state and carry, copied to ``host_h`` when given.
+    Returns after enqueueing; synchronise ``copy_stream`` before reading the host outputs.
+    """
+    x = host["x"]
+    b, L, H, R, P = x.shape
+    N = host["B"].shape[-1]
+    d = dims(b, L, H, P, N, R, x.dtype)
+    need = scan_fwd_staged_workspace(d, slices)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev_y.device)
+    hi = m3_token_inputs(*(_ptr(host[k]) for k in TOKEN_KEYS))
+    di = m3_token_inputs(*(_ptr(dev[k]) for k in TOKEN_KEYS))
+    st_in = state_in.c() if state_in is not None else None
+    st_out = state_out.c() if state_out is not None else None
+    if copy_stream is None:
+        copy_stream = _side_stream(dev_y.device)
+    rc = lib().mamba3_scan_fwd_staged(ctypes.byref(d), ctypes.byref(hi), ctypes.byref(di), _ptr(host_y), _ptr(dev_y),
+                                      ctypes.byref(st_in) if st_in is not None else None,
+                                      ctypes.byref(st_out) if st_out is not None else None, _ptr(host_h),
+                                      _ptr(workspace), workspace.numel() if workspace is not None else 0,
+                                      int(slices), _stream_ptr(stream), _stream_ptr(copy_stream))
+    _check(rc, "mamba3_scan_fwd_staged")

@@ -136,3 +136,24 @@ def test_decode_rejects_bad_arguments_before_launch():
     assert lib.mamba3_decode_step(ctypes.byref(dd), *[good[k] for k in ("x", "B", "C", "dt", "A", "lam", "theta")],
                                   None, good["y"], None) == api.M3_ERR_UNSUPPORTED
     assert m3.launch_count() == before
+
+
+def test_staged_prefill_rejects_bad_arguments_before_any_copy():
+    lib = m3.lib()
+    d = m3.dims(2, 16, 2, 64, 64, 1, torch.bfloat16)
+    n = ctypes.c_size_t(0)
+    assert lib.mamba3_scan_fwd_staged_workspace(ctypes.byref(d), 0, ctypes.byref(n)) == api.M3_ERR_INVALID_ARG
+    assert lib.mamba3_scan_fwd_staged_workspace(ctypes.byref(d), 4, ctypes.byref(n)) == api.M3_OK
+    ins = api.m3_token_inputs(*([None] * 7))
+    before = m3.launch_count()
+    # no input tables / zero slices / h copy without a device state
+    assert lib.mamba3_scan_fwd_staged(ctypes.byref(d), None, None, None, None, None, None, None, None, 0, 1,
+                                      None, None) == api.M3_ERR_INVALID_ARG
+    assert lib.mamba3_scan_fwd_staged(ctypes.byref(d), ctypes.byref(ins), ctypes.byref(ins), None, None, None,
+                                      None, None, None, 0, 0, None, None) == api.M3_ERR_INVALID_ARG
+    assert lib.mamba3_scan_fwd_staged(ctypes.byref(d), ctypes.byref(ins), ctypes.byref(ins), None, None, None,
+                                      None, 0x1000, None, 0, 1, None, None) == api.M3_ERR_INVALID_ARG
+    # several token ranges need a device state (with its carry) to hand on
+    assert lib.mamba3_scan_fwd_staged(ctypes.byref(d), ctypes.byref(ins), ctypes.byref(ins), None, None, None,
+                                      None, None, None, 0, 2, None, None) == api.M3_ERR_INVALID_ARG
+    assert m3.launch_count() == before
