@@ -67,6 +67,20 @@ int sm_count() {
     return g_sms[dev];
 }
 
+void *tensor_map_encoder() {
+    static std::once_flag once;
+    static void *fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = p;
+    });
+    return fn;
+}
+
 }  // namespace m3
 
 using namespace m3;

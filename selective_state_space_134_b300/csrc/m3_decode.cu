@@ -13,6 +13,12 @@
 // state loads issued before any arithmetic so that many bytes are in flight.
 // The per-token inputs (B, C, carry, x) are staged in shared memory as fp32.
 // y is reduced over N inside the thread, then across threads in shared memory.
+//
+// That generic kernel takes any shape.  Two persistent kernels below take the
+// common ones and stage whole heads in shared memory with asynchronous bulk
+// copies: a streaming FMA kernel (fp32 or bf16 inputs, P in {32, 64, 128}) and
+// a tensor-core kernel (bf16 inputs, P = 64, N in {64, 128}) that runs the
+// rank-R products and the readout on warp-level MMAs.
 #include "m3_internal.cuh"
 #include "m3_tc.cuh"
 
@@ -445,6 +451,336 @@ cudaError_t stream_dispatch(int nbh, int P, int N, int R, const void *x, const v
     }
 }
 
+
+// ---------------------------------------------------------------- tensor-core variant (bf16 inputs, P = 64)
+// The same streaming pipeline, with the rank-R products B_prev x_prev^T and B x^T
+// and the readout y = C^T h on warp-level bf16 MMAs (fp32 accumulation) instead
+// of per-thread FMAs; the rotation factors are computed once per pair into a
+// shared table.  A pipeline unit is HPU adjacent heads (their state rows, token
+// inputs and carries are contiguous).  Warp w owns the 16 state columns
+// p0 = 16 (w % 4) ... p0 + 15 and, with HPU = 2, all N rows of head w / 4 of the
+// unit; with HPU = 1, rows (w / 4) N / 2 ... of the one head, the two halves' y
+// summed through shared memory.  Per 8-row tile at n0:
+//   U = x_prev^T B_prev, V = x^T B    (m16n8k8: M = p, N = n, K = r padded to 8)
+// lands in the MMA accumulator layout, in which lane (g, t) holds the columns
+// p0 + g, p0 + g + 8 of the rows n0 + 2t, n0 + 2t + 1: exactly one complex pair,
+// so the update needs no data exchange.  The new state, split into bf16
+// hi + lo parts (error below 2^-16 of |h|), is the A operand of
+//   Y^T += h^T C^T     (m16n8k16: M = p, N = r padded to 8, K = n).
+// The state is staged by 2-d TMA with the 128-byte swizzle (boxes of 32 columns
+// x HPU N rows): the MMA layout's accesses are then free of bank conflicts.
+constexpr int kMmaThreads = 256;
+constexpr int kMmaP = 64;
+
+struct MmaLayout {
+    uint32_t B, C, Bp, x, xp, stage;     // byte offsets inside a stage (the state at 0), stage size
+    uint32_t rot, red, bar, flag, total;
+    __host__ __device__ MmaLayout(int N, int R, int hpu, int nst) {
+        auto up = [](uint32_t v, uint32_t a) { return (v + a - 1u) & ~(a - 1u); };
+        const uint32_t bn = (uint32_t)(hpu * R * N * 2), xn = (uint32_t)(hpu * R * kMmaP * 2);
+        B = (uint32_t)(hpu * N * kMmaP * 4);
+        C = up(B + bn, 128u);
+        Bp = up(C + bn, 128u);
+        x = up(Bp + bn, 128u);
+        xp = up(x + xn, 128u);
+        stage = up(xp + xn, 1024u);
+        rot = stage * nst;                                   // (rho cos, rho sin) per pair of the unit
+        red = up(rot + (uint32_t)(hpu * N / 2 * 8), 128u);   // HPU = 1: row group 0's y partials,
+        bar = red + (hpu == 1 ? 4u * 32u * 16u : 0u);        //   [4 p-tiles][32 lanes] float4
+        flag = bar + 8u * nst;
+        total = flag + 16u + 1024u;                          // slack to put the stages on a 1024-byte boundary
+    }
+};
+
+template <int R, int N, int HPU>
+__global__ void __launch_bounds__(kMmaThreads, 2)
+decode_mma_kernel(const __grid_constant__ CUtensorMap hmap, int nunit, int nst, const __nv_bfloat16 *__restrict__ x,
+                  const __nv_bfloat16 *__restrict__ Bm, const __nv_bfloat16 *__restrict__ Cm,
+                  const __nv_bfloat16 *__restrict__ dtp, const __nv_bfloat16 *__restrict__ Ap,
+                  const __nv_bfloat16 *__restrict__ lp, const __nv_bfloat16 *__restrict__ thp,
+                  __nv_bfloat16 *__restrict__ Bprev, __nv_bfloat16 *__restrict__ xprev, float *__restrict__ y,
+                  unsigned *status) {
+    using namespace tc;
+    constexpr int P = kMmaP, K = N / 2, NW = HPU == 2 ? N : N / 2, NKS = NW / 16;
+    constexpr int NR = HPU * N, KU = HPU * K, KT = kMmaThreads - KU;   // rows, pairs per unit; table threads
+    static_assert((HPU == 1 || HPU == 2) && N % 32 == 0 && NR <= 256 && KU <= kMmaThreads && R >= 1 && R <= 8,
+                  "shape outside the tensor-core decode");
+    extern __shared__ __align__(1024) unsigned char smem_m[];
+    unsigned char *sm = smem_m + ((1024u - (smem_u32(smem_m) & 1023u)) & 1023u);
+    const MmaLayout Lo(N, R, HPU, nst);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = lane >> 2, t = lane & 3, pt = warp & 3, grp = warp >> 2;
+    const int p0 = 16 * pt, hh = HPU == 2 ? grp : 0, nb0 = HPU == 2 ? 0 : grp * NW;   // head in unit, first row
+    const int ti = tid - KT, th_head = ti / K;                           // rotation-table entry of this thread
+    float2 *rot = reinterpret_cast<float2 *>(sm + Lo.rot);
+    float4 *red = reinterpret_cast<float4 *>(sm + Lo.red);
+    uint64_t *full = reinterpret_cast<uint64_t *>(sm + Lo.bar);
+    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(sm + Lo.flag);
+
+    const int first = blockIdx.x, step = gridDim.x;
+    const int mine = first < nunit ? (nunit - first + step - 1) / step : 0;
+    constexpr uint32_t bn = HPU * R * N * 2, xn = HPU * R * P * 2, hn = NR * P * 4;
+
+    auto issue = [&](int j) {   // unit j of this CTA -> stage j % nst (elected thread)
+        const int bh0 = (first + j * step) * HPU;
+        unsigned char *sg = sm + (size_t)(j % nst) * Lo.stage;
+        uint64_t *bar = full + (j % nst);
+        mbar_expect_tx(bar, hn + 3 * bn + 2 * xn);
+        tma_load_2d(sg, &hmap, 0, bh0 * N, bar);
+        tma_load_2d(sg + NR * 128, &hmap, 32, bh0 * N, bar);
+        bulk_load(sg + Lo.B, Bm + (size_t)bh0 * R * N, bn, bar);
+        bulk_load(sg + Lo.C, Cm + (size_t)bh0 * R * N, bn, bar);
+        bulk_load(sg + Lo.Bp, Bprev + (size_t)bh0 * R * N, bn, bar);
+        bulk_load(sg + Lo.x, x + (size_t)bh0 * R * P, xn, bar);
+        bulk_load(sg + Lo.xp, xprev + (size_t)bh0 * R * P, xn, bar);
+    };
+
+    if (tid == 0) {
+        tma_prefetch_desc(&hmap);
+        for (int i = 0; i < nst; ++i) mbar_init(full + i, 1);
+        mbar_init_fence();
+        *abort_flag = 0;
+    }
+    __syncthreads();
+    int issued = 0;
+    if (tid == 0)
+        for (; issued < nst - 1 && issued < mine; ++issued) issue(issued);
+
+    // swizzled byte offsets of this lane's four state elements, relative to unit row
+    // hh N + n0 + 2t (n0 a multiple of 8): columns p0 + g, p0 + g + 8 of that row and the next
+    const uint32_t lb = (uint32_t)(pt >> 1) * NR * 128u + ((uint32_t)(g & 3) << 2);
+    const uint32_t c0 = 4u * (uint32_t)(pt & 1) + (uint32_t)(g >> 2), c1 = c0 + 2u;
+    const uint32_t o00 = lb + ((c0 ^ (2u * t)) << 4), o01 = lb + 128u + ((c0 ^ (2u * t + 1u)) << 4);
+    const uint32_t o10 = lb + ((c1 ^ (2u * t)) << 4), o11 = lb + 128u + ((c1 ^ (2u * t + 1u)) << 4);
+    const bool rlane = 2 * t < R;   // lanes holding rank rows 2t (and 2t + 1 when R > 1)
+
+    // per-head scalars of this warp's head and of this thread's table entry, one unit ahead
+    float d_n = 0.f, l_n = 0.f, dq_n = 0.f, aq_n = 0.f, th_n = 0.f;
+    auto prefetch = [&](int unit) {
+        const int bh0 = unit * HPU;
+        d_n = to_f(dtp[bh0 + hh]);
+        l_n = to_f(lp[bh0 + hh]);
+        if (ti >= 0) {
+            dq_n = to_f(dtp[bh0 + th_head]);
+            aq_n = to_f(Ap[bh0 + th_head]);
+            th_n = to_f(thp[(size_t)bh0 * K + ti]);
+        }
+    };
+    if (mine > 0) prefetch(first);
+    int j = 0;
+    for (; j < mine; ++j) {
+        const int bh0 = (first + j * step) * HPU;
+        const float d = d_n, l = l_n, dq = dq_n, aq = aq_n, th = th_n;
+        if (j + 1 < mine) prefetch(first + (j + 1) * step);
+        // the last warps fill the rotation table (warp 0 also issues the copies); it is read after
+        // the barrier below, and its last reads came before the previous one
+        if (ti >= 0) {
+            const float rho = expf(dq * aq);
+            float sa, ca;
+            sincos_reduced(dq * th, &sa, &ca);
+            rot[ti] = make_float2(rho * ca, rho * sa);
+        }
+        unsigned char *sg = sm + (size_t)(j % nst) * Lo.stage;
+        const bool ok = mbar_wait(full + (j % nst), (uint32_t)((j / nst) & 1), kStreamWaitNs);
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) atomicOr(status, kStatusTimeout);
+            *abort_flag = 1;
+            break;
+        }
+        const unsigned short *sB = reinterpret_cast<const unsigned short *>(sg + Lo.B) + hh * R * N;
+        const unsigned short *sBp = reinterpret_cast<const unsigned short *>(sg + Lo.Bp) + hh * R * N;
+        const unsigned short *sC = reinterpret_cast<const unsigned short *>(sg + Lo.C) + hh * R * N;
+        const unsigned short *sx = reinterpret_cast<const unsigned short *>(sg + Lo.x) + hh * R * P;
+        const unsigned short *sxp = reinterpret_cast<const unsigned short *>(sg + Lo.xp) + hh * R * P;
+        const float2 *hrot = rot + hh * K;
+        unsigned char *hst = sg + (uint32_t)(hh * N) * 128u;
+        const float left = (1.f - l) * d, right = l * d;
+
+        // A operands of the rank-R products: x^T rows p0 + g, p0 + g + 8, rank columns 2t, 2t + 1
+        uint32_t ax0 = 0, ax1 = 0, aq0 = 0, aq1 = 0;
+        if (rlane) {
+            const int r0 = 2 * t * P + p0 + g;
+            ax0 = sx[r0];
+            ax1 = sx[r0 + 8];
+            aq0 = sxp[r0];
+            aq1 = sxp[r0 + 8];
+            if (R > 1) {
+                ax0 |= (uint32_t)sx[r0 + P] << 16;
+                ax1 |= (uint32_t)sx[r0 + P + 8] << 16;
+                aq0 |= (uint32_t)sxp[r0 + P] << 16;
+                aq1 |= (uint32_t)sxp[r0 + P + 8] << 16;
+            }
+        }
+        float yacc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ks = 0; ks < NKS; ++ks) {
+            uint32_t ahi[4], alo[4];
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const int n0 = nb0 + 16 * ks + 8 * hf;
+                uint32_t bb = 0, bq = 0;   // B operands: rank rows 2t, 2t + 1 of state row n0 + g
+                if (rlane) {
+                    const int q = 2 * t * N + n0 + g;
+                    bb = sB[q];
+                    bq = sBp[q];
+                    if (R > 1) {
+                        bb |= (uint32_t)sB[q + N] << 16;
+                        bq |= (uint32_t)sBp[q + N] << 16;
+                    }
+                }
+                float u[4] = {0.f, 0.f, 0.f, 0.f}, v[4] = {0.f, 0.f, 0.f, 0.f};
+                mma_m16n8k8(u, aq0, aq1, bq);
+                mma_m16n8k8(v, ax0, ax1, bb);
+                const float2 rt = hrot[n0 / 2 + t];
+                unsigned char *rb = hst + (uint32_t)(n0 + 2 * t) * 128u;
+                float *q00 = reinterpret_cast<float *>(rb + o00), *q01 = reinterpret_cast<float *>(rb + o01);
+                float *q10 = reinterpret_cast<float *>(rb + o10), *q11 = reinterpret_cast<float *>(rb + o11);
+                float s0 = fmaf(left, u[0], *q00), s1 = fmaf(left, u[1], *q01);
+                const float n00 = fmaf(rt.x, s0, fmaf(-rt.y, s1, right * v[0]));
+                const float n01 = fmaf(rt.y, s0, fmaf(rt.x, s1, right * v[1]));
+                s0 = fmaf(left, u[2], *q10);
+                s1 = fmaf(left, u[3], *q11);
+                const float n10 = fmaf(rt.x, s0, fmaf(-rt.y, s1, right * v[2]));
+                const float n11 = fmaf(rt.y, s0, fmaf(rt.x, s1, right * v[3]));
+                *q00 = n00;
+                *q01 = n01;
+                *q10 = n10;
+                *q11 = n11;
+                split2(n00, n01, ahi[2 * hf], alo[2 * hf]);           // row p0 + g
+                split2(n10, n11, ahi[2 * hf + 1], alo[2 * hf + 1]);   // row p0 + g + 8
+            }
+            uint32_t b0 = 0, b1 = 0;   // C^T: state rows 2t, 2t + 1 (+ 8) of this K step, rank column g
+            if (g < R) {
+                const unsigned short *cp = sC + g * N + nb0 + 16 * ks + 2 * t;
+                b0 = *reinterpret_cast<const uint32_t *>(cp);
+                b1 = *reinterpret_cast<const uint32_t *>(cp + 8);
+            }
+            mma_m16n8k16(yacc, ahi, b0, b1);
+            mma_m16n8k16(yacc, alo, b0, b1);
+        }
+        // y[r][p] for r = 2t, 2t + 1 and p = p0 + g, p0 + g + 8
+        float *yo = y + (size_t)(bh0 + hh) * R * P + 2 * t * P + p0 + g;
+        if (HPU == 2 && rlane) {
+            yo[0] = yacc[0];
+            yo[8] = yacc[2];
+            if (R > 1) {
+                yo[P] = yacc[1];
+                yo[P + 8] = yacc[3];
+            }
+        }
+        if (HPU == 1 && grp == 0) red[pt * 32 + lane] = make_float4(yacc[0], yacc[1], yacc[2], yacc[3]);
+        fence_proxy_async();   // the state writes above feed the tensor stores below
+        __syncthreads();
+        if (tid == 0) {
+            tma_store_2d(&hmap, sg, 0, bh0 * N);
+            tma_store_2d(&hmap, sg + NR * 128, 32, bh0 * N);
+            bulk_store(Bprev + (size_t)bh0 * R * N, sg + Lo.B, bn);   // new carry = this token's (B, x)
+            bulk_store(xprev + (size_t)bh0 * R * P, sg + Lo.x, xn);
+            bulk_commit();
+            if (issued < mine) {
+                bulk_wait_read<1>();   // the stage about to be refilled has been written out
+                issue(issued);
+                ++issued;
+            }
+        }
+        if (HPU == 1 && grp == 1 && rlane) {
+            const float4 o = red[pt * 32 + lane];
+            yo[0] = yacc[0] + o.x;
+            yo[8] = yacc[2] + o.z;
+            if (R > 1) {
+                yo[P] = yacc[1] + o.y;
+                yo[P + 8] = yacc[3] + o.w;
+            }
+        }
+    }
+    if (tid == 0) {
+        if (*abort_flag) {
+            for (int i = j; i < issued; ++i) mbar_wait(full + (i % nst), (uint32_t)((i / nst) & 1), kStreamWaitNs);
+        }
+        bulk_wait<0>();
+    }
+}
+
+// 2-d map over the fp32 state viewed as [nbh * N rows][64 columns]; box = 32 columns x box_rows,
+// 128-byte swizzle
+bool map_state(CUtensorMap *m, float *h, long long rows, int box_rows) {
+    tc::EncodeFn enc = tc::encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)kMmaP, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)kMmaP * 4};
+    const cuuint32_t box[2] = {32, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, h, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int R, int N, int HPU>
+cudaError_t launch_mma(int nbh, const void *x, const void *B, const void *C, const void *dt, const void *A,
+                       const void *lam, const void *theta, float *h, void *Bprev, void *xprev, void *y,
+                       cudaStream_t s) {
+    CUtensorMap hmap;
+    if (!map_state(&hmap, h, (long long)nbh * N, HPU * N)) return cudaErrorInvalidValue;
+    // two CTAs per SM with as many stages as fit (2..6), else one CTA per SM
+    int per_sm = 2, nst = 6;
+    while (nst > 2 && MmaLayout(N, R, HPU, nst).total > 113u * 1024u) --nst;
+    if (MmaLayout(N, R, HPU, nst).total > 113u * 1024u) {
+        per_sm = 1;
+        nst = 6;
+        while (nst > 2 && MmaLayout(N, R, HPU, nst).total > 224u * 1024u) --nst;
+    }
+    const MmaLayout Lo(N, R, HPU, nst);
+    if (Lo.total > 224u * 1024u) return cudaErrorInvalidValue;
+    unsigned *status = device_status_word();
+    if (!status) return cudaErrorUnknown;
+    auto kern = decode_mma_kernel<R, N, HPU>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Lo.total);
+    if (err != cudaSuccess) return err;
+    const int nunit = nbh / HPU;
+    const int grid = nunit < per_sm * sm_count() ? nunit : per_sm * sm_count();
+    using bf = __nv_bfloat16;
+    trace_mark(M3_KERNEL_DECODE, s, 0);
+    kern<<<grid, kMmaThreads, Lo.total, s>>>(hmap, nunit, nst, (const bf *)x, (const bf *)B, (const bf *)C,
+                                            (const bf *)dt, (const bf *)A, (const bf *)lam, (const bf *)theta,
+                                            (bf *)Bprev, (bf *)xprev, (float *)y, status);
+    trace_mark(M3_KERNEL_DECODE, s, 1);
+    count_launch();
+    return cudaGetLastError();
+}
+
+// The tensor-core variant takes bf16 inputs with P = 64, N in {64, 128}, R in {1, 2, 4, 8},
+// the streaming kernel's alignment, and state row indices within int range.  (For R = 1 the
+// padded rank products waste tensor work, but that work is far from binding and the per-pair
+// FMAs it replaces are not.)
+bool mma_ok(int dtype, int P, int N, int R, long long nbh) {
+    return dtype == M3_BF16 && P == kMmaP && (N == 64 || N == 128) && (R == 1 || R == 2 || R == 4 || R == 8) &&
+           nbh * N < (1ll << 31);
+}
+
+// N = 64 pairs adjacent heads into one unit when the head count is even.
+cudaError_t mma_dispatch(int nbh, int N, int R, const void *x, const void *B, const void *C, const void *dt,
+                         const void *A, const void *lam, const void *theta, float *h, void *Bprev, void *xprev,
+                         void *y, cudaStream_t s) {
+    const bool pair = N == 64 && nbh % 2 == 0;
+#define M3_MMA(RR, NN, HH)                                                                                         \
+    if (R == RR && N == NN && (HH == 2) == pair)                                                                 \
+    return launch_mma<RR, NN, HH>(nbh, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, s)
+    M3_MMA(1, 64, 2);
+    M3_MMA(2, 64, 2);
+    M3_MMA(4, 64, 2);
+    M3_MMA(8, 64, 2);
+    M3_MMA(1, 64, 1);
+    M3_MMA(2, 64, 1);
+    M3_MMA(4, 64, 1);
+    M3_MMA(8, 64, 1);
+    M3_MMA(1, 128, 1);
+    M3_MMA(2, 128, 1);
+    M3_MMA(4, 128, 1);
+    M3_MMA(8, 128, 1);
+#undef M3_MMA
+    return cudaErrorInvalidValue;
+}
+
 }  // namespace
 
 cudaError_t decode_step(int dtype, int batch, int H, int P, int N, int R, const void *x,
@@ -455,6 +791,8 @@ cudaError_t decode_step(int dtype, int batch, int H, int P, int N, int R, const 
     const void *ptrs[] = {x, B, C, theta, h, Bprev, xprev};
     const int nbh = batch * H;
     if (nbh > 0 && stream_ok(e, P, N, R, ptrs, 7)) {
+        if (mma_ok(dtype, P, N, R, nbh))
+            return mma_dispatch(nbh, N, R, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, s);
         if (dtype == M3_F32)
             return stream_dispatch<float>(nbh, P, N, R, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, s);
         return stream_dispatch<__nv_bfloat16>(nbh, P, N, R, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, s);

@@ -28,6 +28,7 @@ void count_launch();                 // +1 to the library's launch counter
 void trace_mark(int kernel, cudaStream_t s, int phase);
 unsigned *device_status_word();      // address of this device's status word (nullptr on error)
 int sm_count();                      // SMs of the current device (cached)
+void *tensor_map_encoder();          // the driver's cuTensorMapEncodeTiled (nullptr if unavailable)
 
 // ---------------------------------------------------------------- prefill plan
 // Prefill runs over segments of `seglen` tokens (a multiple of the chunk Q).

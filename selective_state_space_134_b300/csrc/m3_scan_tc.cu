@@ -841,24 +841,6 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
 }
 
 // ---------------------------------------------------------------- host side
-using EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                              const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeFn encode_fn() {
-    static std::once_flag once;
-    static EncodeFn fn = nullptr;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeFn>(p);
-    });
-    return fn;
-}
-
 // 4-d map over a [b*L][H][R][inner] bf16 tensor, box = {64, R, 1, Q}, 128-byte swizzle
 bool map4(CUtensorMap *m, const void *base, int inner, int R, int H, long long rows, int Q) {
     EncodeFn enc = encode_fn();

@@ -10,6 +10,8 @@
 #include <stdint.h>
 
 namespace m3 {
+void *tensor_map_encoder();   // the driver's cuTensorMapEncodeTiled, or nullptr
+
 namespace tc {
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -188,6 +190,17 @@ __device__ __forceinline__ void tma_store_5d(const CUtensorMap *map, const void 
         ::"l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
         : "memory");
 }
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int c0, int c1, uint64_t *mbar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(mbar))
+        : "memory");
+}
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void *src, int c0, int c1) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];"
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(src)), "r"(c0), "r"(c1)
+                 : "memory");
+}
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -229,6 +242,27 @@ __device__ __forceinline__ void split2(float a, float b, uint32_t &hi, uint32_t 
     hi = pack_bf16x2(a, b);
     lo = pack_bf16x2(a - bf16_lo_f(hi), b - bf16_hi_f(hi));
 }
+
+// ---- warp-level bf16 MMA with fp32 accumulation (mma.sync; fragment layouts per the PTX ISA:
+// lane = 4 g + t holds A rows g / g + 8 at columns 2t, 2t + 1 (+ 8), B column g at rows 2t, 2t + 1
+// (+ 8), and D rows g / g + 8 at columns 2t, 2t + 1)
+__device__ __forceinline__ void mma_m16n8k8(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t b0) {
+    asm("mma.sync.aligned.m16n8k8.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5}, {%6}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(b0));
+}
+__device__ __forceinline__ void mma_m16n8k16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// ---- host: the driver's tensor-map encoder (cuTensorMapEncodeTiled), looked up once
+using EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                              const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+inline EncodeFn encode_fn() { return reinterpret_cast<EncodeFn>(m3::tensor_map_encoder()); }
 
 }  // namespace tc
 }  // namespace m3

@@ -113,6 +113,25 @@ def test_decode_full_size_matches_oracle(wname):
         np.testing.assert_array_equal(to_f64(state.x_prev), ref_x)
 
 
+@pytest.mark.parametrize("R,N,H", [(1, 64, 45), (2, 64, 45), (8, 64, 45), (4, 64, 45), (1, 64, 46), (2, 64, 46),
+                                   (8, 64, 46), (1, 128, 45), (2, 128, 45), (8, 128, 45)])
+def test_decode_tensor_core_ranks_match_oracle(R, N, H):
+    # bf16, P = 64: the tensor-core decode; 7 x 45 = 315 heads (one head per unit) and
+    # 7 x 46 = 322 heads (N = 64: two heads per unit) leave a ragged last round of units
+    w = WORKLOADS["decode_n64_r4"].with_(batch=7, nheads=H, N=N, R=R)
+    st = decode_state(w, "cuda")
+    state = m3.State(st["h"].clone(), st["B_prev"].clone(), st["x_prev"].clone())
+    ref_h, ref_B, ref_x = to_f64(st["h"]), to_f64(st["B_prev"]), to_f64(st["x_prev"])
+    for step, tok in enumerate(decode_pool(w, "cuda", pool=2)):
+        y = m3.decode_step(*(tok[k] for k in KEYS), state=state)
+        assert m3.device_status() == m3.M3_OK
+        yr, ref_h, ref_B, ref_x = oracle.decode_step(*(to_f64(tok[k]) for k in KEYS), ref_h, ref_B, ref_x)
+        assert norm_err(to_f64(y), yr) <= 1e-4, step     # hi + lo split of h: far inside the bf16 bar
+        assert norm_err(to_f64(state.h), ref_h) <= 1e-5, step
+        np.testing.assert_array_equal(to_f64(state.B_prev), ref_B)
+        np.testing.assert_array_equal(to_f64(state.x_prev), ref_x)
+
+
 def test_decode_f32_tight():
     w = WORKLOADS["tiny_f32"].with_(batch=3, nheads=5, N=32, P=16, R=2)
     st = decode_state(w, "cuda")
