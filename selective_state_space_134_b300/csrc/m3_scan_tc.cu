@@ -117,6 +117,10 @@ __device__ __forceinline__ void sincos_reduced(float x, float *s, float *c) {
     __sincosf(r, s, c);
 }
 
+// packed fp32 pairs (one instruction for two lanes of arithmetic)
+__device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
+__device__ __forceinline__ float2 f2u(uint32_t a, uint32_t b) { return make_float2(__uint_as_float(a), __uint_as_float(b)); }
+
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -499,38 +503,62 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                     ph[i] = phi;
                 }
                 const int ie = e - seg * TPS;   // the chunk's last token, if it is this thread's
-                // all raw words first: the in-place stores below then cannot hold back a load
+                // raw words are loaded kLA tokens ahead of their use (each load precedes, in
+                // program order, the in-place stores it could alias, so none waits on a store)
                 uint32_t rb[TPS * R], rc[TPS * R];
-#pragma unroll
-                for (int i = 0; i < TPS * R; ++i) {
-                    const uint32_t off = sw128(seg * TPS * R + i, 2 * lane);
-                    rb[i] = *reinterpret_cast<const uint32_t *>(bs + off);
-                    if (OUT) rc[i] = *reinterpret_cast<const uint32_t *>(cs + off);
-                }
-#pragma unroll
-                for (int i = 0; i < TPS; ++i) {
-                    const int t = seg * TPS + i;
-                    const bool valid = t < Qc;
-                    float c, s;
-                    sincos_reduced(ph[i], &s, &c);
-                    if (i == ie) {   // the chunk's last token: rotation of the state at the chunk end
-                        v_cos(p)[k] = c;
-                        v_sin(p)[k] = s;
-                        if (!OUT) tot[1 + k] += ph[i];
-                    }
-                    const float cb = c * sgB, sb = s * sgB;
+                constexpr int kLA = TPS < 4 ? TPS : 4;
+                auto load_tok = [&](int i) {
 #pragma unroll
                     for (int r = 0; r < R; ++r) {
-                        const uint32_t off = sw128(t * R + r, 2 * lane);
-                        const uint32_t vb = rb[i * R + r];
-                        const float b0 = bf16_lo_f(vb), b1 = bf16_hi_f(vb);
-                        *reinterpret_cast<uint32_t *>(bs + off) =
-                            valid ? pack_f16x2(fmaf(cb, b0, sb * b1), fmaf(cb, b1, -sb * b0)) : 0u;
+                        const uint32_t off = sw128((seg * TPS + i) * R + r, 2 * lane);
+                        rb[i * R + r] = *reinterpret_cast<const uint32_t *>(bs + off);
+                        if (OUT) rc[i * R + r] = *reinterpret_cast<const uint32_t *>(cs + off);
+                    }
+                };
+#pragma unroll
+                for (int i = 0; i < kLA; ++i) load_tok(i);
+                // two tokens at a time on packed fp32 (the range reduction of sincos_reduced and
+                // the rotations; same operations, same roundings)
+                static_assert(TPS % 2 == 0, "token pairs");
+#pragma unroll
+                for (int i = 0; i < TPS; i += 2) {
+                    if (i + kLA < TPS) load_tok(i + kLA);
+                    if (i + kLA + 1 < TPS) load_tok(i + kLA + 1);
+                    const float2 x2 = make_float2(ph[i], ph[i + 1]);
+                    const float2 n2 = __fadd2_rn(__ffma2_rn(x2, f2(0.15915494309189535f), f2(12582912.f)),
+                                                 f2(-12582912.f));
+                    float2 r2 = __ffma2_rn(n2, f2(-6.28318548202514648f), x2);
+                    r2 = __ffma2_rn(n2, f2(1.7484555314695172e-7f), r2);
+                    float c0, s0, c1, s1;
+                    __sincosf(r2.x, &s0, &c0);
+                    __sincosf(r2.y, &s1, &c1);
+                    if (i == ie || i + 1 == ie) {   // the chunk's last token: rotation of the state at the chunk end
+                        const bool first = i == ie;
+                        v_cos(p)[k] = first ? c0 : c1;
+                        v_sin(p)[k] = first ? s0 : s1;
+                        if (!OUT) tot[1 + k] += first ? ph[i] : ph[i + 1];
+                    }
+                    const float2 cb = __fmul2_rn(make_float2(c0, c1), f2(sgB));
+                    const float2 sb = __fmul2_rn(make_float2(s0, s1), f2(sgB));
+                    const float2 nsb = __fmul2_rn(make_float2(s0, s1), f2(-sgB));
+                    const int t = seg * TPS + i;
+                    const bool valid0 = t < Qc, valid1 = t + 1 < Qc;
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        const uint32_t off0 = sw128(t * R + r, 2 * lane), off1 = sw128((t + 1) * R + r, 2 * lane);
+                        const uint32_t vb0 = rb[i * R + r], vb1 = rb[(i + 1) * R + r];
+                        const float2 b0 = f2u(vb0 << 16, vb1 << 16), b1 = f2u(vb0 & 0xFFFF0000u, vb1 & 0xFFFF0000u);
+                        const float2 o0 = __ffma2_rn(cb, b0, __fmul2_rn(sb, b1));
+                        const float2 o1 = __ffma2_rn(cb, b1, __fmul2_rn(nsb, b0));
+                        *reinterpret_cast<uint32_t *>(bs + off0) = valid0 ? pack_f16x2(o0.x, o1.x) : 0u;
+                        *reinterpret_cast<uint32_t *>(bs + off1) = valid1 ? pack_f16x2(o0.y, o1.y) : 0u;
                         if (OUT) {
-                            const uint32_t vc = rc[i * R + r];
-                            const float c0 = bf16_lo_f(vc), c1 = bf16_hi_f(vc);
-                            *reinterpret_cast<uint32_t *>(cs + off) =
-                                valid ? pack_f16x2(fmaf(cb, c0, sb * c1), fmaf(cb, c1, -sb * c0)) : 0u;
+                            const uint32_t vc0 = rc[i * R + r], vc1 = rc[(i + 1) * R + r];
+                            const float2 e0 = f2u(vc0 << 16, vc1 << 16), e1 = f2u(vc0 & 0xFFFF0000u, vc1 & 0xFFFF0000u);
+                            const float2 q0 = __ffma2_rn(cb, e0, __fmul2_rn(sb, e1));
+                            const float2 q1 = __ffma2_rn(cb, e1, __fmul2_rn(nsb, e0));
+                            *reinterpret_cast<uint32_t *>(cs + off0) = valid0 ? pack_f16x2(q0.x, q1.x) : 0u;
+                            *reinterpret_cast<uint32_t *>(cs + off1) = valid1 ? pack_f16x2(q0.y, q1.y) : 0u;
                         }
                     }
                 }
@@ -558,11 +586,19 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                         const uint4 v = xv[i];
                         const float f[8] = {bf16_lo_f(v.x), bf16_hi_f(v.x), bf16_lo_f(v.y), bf16_hi_f(v.y),
                                             bf16_lo_f(v.z), bf16_hi_f(v.z), bf16_lo_f(v.w), bf16_hi_f(v.w)};
-                        o = make_uint4(pack_f16x2(sj * f[0], sj * f[1]), pack_f16x2(sj * f[2], sj * f[3]),
-                                       pack_f16x2(sj * f[4], sj * f[5]), pack_f16x2(sj * f[6], sj * f[7]));
-                        if (OUT)   // x' = sX' x, exact in fp16
-                            q = make_uint4(pack_f16x2(sgXp * f[0], sgXp * f[1]), pack_f16x2(sgXp * f[2], sgXp * f[3]),
-                                           pack_f16x2(sgXp * f[4], sgXp * f[5]), pack_f16x2(sgXp * f[6], sgXp * f[7]));
+                        uint32_t ow[4], qw[4];
+#pragma unroll
+                        for (int z = 0; z < 4; ++z) {
+                            const float2 fz = make_float2(f[2 * z], f[2 * z + 1]);
+                            const float2 a = __fmul2_rn(f2(sj), fz);
+                            ow[z] = pack_f16x2(a.x, a.y);
+                            if (OUT) {   // x' = sX' x, exact in fp16
+                                const float2 b2 = __fmul2_rn(f2(sgXp), fz);
+                                qw[z] = pack_f16x2(b2.x, b2.y);
+                            }
+                        }
+                        o = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+                        if (OUT) q = make_uint4(qw[0], qw[1], qw[2], qw[3]);
                     }
                     *reinterpret_cast<uint4 *>(xh + off) = o;
                     if (OUT) *reinterpret_cast<uint4 *>(xp + off) = q;   // rows past the end stay zero
@@ -652,9 +688,10 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                 for (int q4 = 0; q4 < 4; ++q4) {
                     uint32_t w4[4];
 #pragma unroll
-                    for (int e2 = 0; e2 < 4; ++e2)
-                        w4[e2] = pack_f16x2(__uint_as_float(hv[8 * q4 + 2 * e2]) * sg,
-                                            __uint_as_float(hv[8 * q4 + 2 * e2 + 1]) * sg);
+                    for (int e2 = 0; e2 < 4; ++e2) {
+                        const float2 v2 = __fmul2_rn(f2u(hv[8 * q4 + 2 * e2], hv[8 * q4 + 2 * e2 + 1]), f2(sg));
+                        w4[e2] = pack_f16x2(v2.x, v2.y);
+                    }
                     *reinterpret_cast<uint4 *>(sm + S::oH + sw128(st_row, 32 * eh + 8 * q4)) =
                         make_uint4(w4[0], w4[1], w4[2], w4[3]);
                 }
@@ -715,21 +752,23 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                         tmem_wait_ld(sv);
                         if (btok + TB <= tmin) {
 #pragma unroll
-                            for (int q = 0; q < 16; ++q)
-                                p16[q] = pack_f16x2(__uint_as_float(sv[2 * q]) * um[(2 * q) / R],
-                                                    __uint_as_float(sv[2 * q + 1]) * um[(2 * q + 1) / R]);
+                            for (int q = 0; q < 16; ++q) {
+                                const float2 v2 = __fmul2_rn(f2u(sv[2 * q], sv[2 * q + 1]),
+                                                             make_float2(um[(2 * q) / R], um[(2 * q + 1) / R]));
+                                p16[q] = pack_f16x2(v2.x, v2.y);
+                            }
                         } else {
 #pragma unroll
                             for (int q = 0; q < 16; ++q) {
-                                float pm[2];
+                                float mz[2];
 #pragma unroll
                                 for (int z = 0; z < 2; ++z) {
                                     const int jq = (2 * q + z) / R;   // token offset in the block
                                     const int tj = btok + jq;
-                                    const float m = (tj < ti) ? um[jq] : ((tj == ti) ? gd : 0.f);
-                                    pm[z] = __uint_as_float(sv[2 * q + z]) * m;
+                                    mz[z] = (tj < ti) ? um[jq] : ((tj == ti) ? gd : 0.f);
                                 }
-                                p16[q] = pack_f16x2(pm[0], pm[1]);
+                                const float2 v2 = __fmul2_rn(f2u(sv[2 * q], sv[2 * q + 1]), make_float2(mz[0], mz[1]));
+                                p16[q] = pack_f16x2(v2.x, v2.y);
                             }
                         }
                     }
@@ -757,13 +796,17 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                     tmem_ld16_nw(hcol + h16, sh + 16);
                     tmem_wait_ld(sh);
                     uint32_t hv[16];
+                    const float sgn_s = odd ? s : -s;
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const float v = fmaf(rho, __uint_as_float(sh[16 + j]), __uint_as_float(sh[j]) * invBX);
-                        const float pv = __shfl_xor_sync(0xffffffffu, v, 1);
-                        const float nv = odd ? fmaf(s, pv, c * v) : fmaf(-s, pv, c * v);
-                        m = fmaxf(m, st_owner ? fabsf(nv) : 0.f);
-                        hv[j] = __float_as_uint(nv);
+                    for (int j = 0; j < 16; j += 2) {
+                        const float2 v = __ffma2_rn(f2(rho), f2u(sh[16 + j], sh[16 + j + 1]),
+                                                    __fmul2_rn(f2u(sh[j], sh[j + 1]), f2(invBX)));
+                        const float2 pv = make_float2(__shfl_xor_sync(0xffffffffu, v.x, 1),
+                                                      __shfl_xor_sync(0xffffffffu, v.y, 1));
+                        const float2 nv = __ffma2_rn(f2(sgn_s), pv, __fmul2_rn(f2(c), v));
+                        m = fmaxf(m, st_owner ? fmaxf(fabsf(nv.x), fabsf(nv.y)) : 0.f);
+                        hv[j] = __float_as_uint(nv.x);
+                        hv[j + 1] = __float_as_uint(nv.y);
                     }
                     tmem_st16(hcol + h16, hv);
                     if (dst) {
@@ -801,12 +844,12 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                     const uint32_t *ya = yy, *yi = yy + 16;
                     if (row_ok) {
 #pragma unroll
-                        for (int j = 0; j < 16; j += 4)
-                            *reinterpret_cast<float4 *>(ys + sw128f(row, half16 + j)) = make_float4(
-                                fmaf(sc, __uint_as_float(yi[j]), sa * __uint_as_float(ya[j])),
-                                fmaf(sc, __uint_as_float(yi[j + 1]), sa * __uint_as_float(ya[j + 1])),
-                                fmaf(sc, __uint_as_float(yi[j + 2]), sa * __uint_as_float(ya[j + 2])),
-                                fmaf(sc, __uint_as_float(yi[j + 3]), sa * __uint_as_float(ya[j + 3])));
+                        for (int j = 0; j < 16; j += 4) {
+                            const float2 u0 = __ffma2_rn(f2(sc), f2u(yi[j], yi[j + 1]), __fmul2_rn(f2(sa), f2u(ya[j], ya[j + 1])));
+                            const float2 u1 = __ffma2_rn(f2(sc), f2u(yi[j + 2], yi[j + 3]),
+                                                         __fmul2_rn(f2(sa), f2u(ya[j + 2], ya[j + 3])));
+                            *reinterpret_cast<float4 *>(ys + sw128f(row, half16 + j)) = make_float4(u0.x, u0.y, u1.x, u1.y);
+                        }
                     }
                 }
                 fence_proxy_async();
