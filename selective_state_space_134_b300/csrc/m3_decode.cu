@@ -379,8 +379,7 @@ cudaError_t launch_decode(int batch, int H, int P, int N, int R, const void *x, 
 #define M3_DECODE_LAUNCH(PPT)                                                                     \
     do {                                                                                          \
         auto kern = decode_kernel<T, PPT>;                                                        \
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,   \
-                                             (int)smem);                                          \
+        cudaError_t e = allow_dynamic_smem<decode_kernel<T, PPT>>(smem);                          \
         if (e != cudaSuccess) return e;                                                           \
         kern<<<grid, kThreads, smem, s>>>(H, P, N, R, (const T *)x, (const T *)B, (const T *)C,  \
                                           (const T *)dt, (const T *)A, (const T *)lam,            \
@@ -416,7 +415,7 @@ cudaError_t launch_stream(int nbh, int P, int N, const void *x, const void *B, c
     unsigned *status = device_status_word();
     if (!status) return cudaErrorUnknown;
     auto kern = decode_stream_kernel<T, R>;
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Lo.total);
+    cudaError_t err = allow_dynamic_smem<decode_stream_kernel<T, R>>(Lo.total);
     if (err != cudaSuccess) return err;
     const int grid = nbh < per_sm * sm_count() ? nbh : per_sm * sm_count();
     trace_mark(M3_KERNEL_DECODE, s, 0);
@@ -719,8 +718,23 @@ template <int R, int N, int HPU>
 cudaError_t launch_mma(int nbh, const void *x, const void *B, const void *C, const void *dt, const void *A,
                        const void *lam, const void *theta, float *h, void *Bprev, void *xprev, void *y,
                        cudaStream_t s) {
-    CUtensorMap hmap;
-    if (!map_state(&hmap, h, (long long)nbh * N, HPU * N)) return cudaErrorInvalidValue;
+    // the map depends only on (h, rows, box); a decode loop reuses one state buffer
+    struct MapCache {
+        const float *h = nullptr;
+        long long rows = 0;
+        int box = 0;
+        CUtensorMap map;
+    };
+    thread_local MapCache cache;
+    const long long rows = (long long)nbh * N;
+    if (cache.h != h || cache.rows != rows || cache.box != HPU * N) {
+        cache.h = nullptr;
+        if (!map_state(&cache.map, h, rows, HPU * N)) return cudaErrorInvalidValue;
+        cache.h = h;
+        cache.rows = rows;
+        cache.box = HPU * N;
+    }
+    const CUtensorMap &hmap = cache.map;
     // two CTAs per SM with as many stages as fit (2..6), else one CTA per SM
     int per_sm = 2, nst = 6;
     while (nst > 2 && MmaLayout(N, R, HPU, nst).total > 113u * 1024u) --nst;
@@ -734,7 +748,7 @@ cudaError_t launch_mma(int nbh, const void *x, const void *B, const void *C, con
     unsigned *status = device_status_word();
     if (!status) return cudaErrorUnknown;
     auto kern = decode_mma_kernel<R, N, HPU>;
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Lo.total);
+    cudaError_t err = allow_dynamic_smem<decode_mma_kernel<R, N, HPU>>(Lo.total);
     if (err != cudaSuccess) return err;
     const int nunit = nbh / HPU;
     const int grid = nunit < per_sm * sm_count() ? nunit : per_sm * sm_count();

@@ -1,6 +1,7 @@
 // Internal declarations of the Mamba-3 recurrence library (not part of the C ABI).
 #pragma once
 
+#include <atomic>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -28,6 +29,25 @@ void count_launch();                 // +1 to the library's launch counter
 void trace_mark(int kernel, cudaStream_t s, int phase);
 unsigned *device_status_word();      // address of this device's status word (nullptr on error)
 int sm_count();                      // SMs of the current device (cached)
+
+// Raises a kernel's dynamic shared-memory limit to at least `bytes` on the current device.  The
+// driver call (microseconds of host time) is made only when the limit has to grow.
+constexpr int kSmemLimitDevices = 64;
+template <auto Kern>
+cudaError_t allow_dynamic_smem(size_t bytes) {
+    static std::atomic<int> limit[kSmemLimitDevices];
+    int dev = -1;
+    cudaGetDevice(&dev);
+    const bool cached = dev >= 0 && dev < kSmemLimitDevices;
+    if (cached && limit[dev].load(std::memory_order_acquire) >= (int)bytes) return cudaSuccess;
+    const cudaError_t e = cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess && cached) {
+        int cur = limit[dev].load(std::memory_order_relaxed);
+        while (cur < (int)bytes && !limit[dev].compare_exchange_weak(cur, (int)bytes)) {
+        }
+    }
+    return e;
+}
 void *tensor_map_encoder();          // the driver's cuTensorMapEncodeTiled (nullptr if unavailable)
 
 // ---------------------------------------------------------------- prefill plan

@@ -289,7 +289,7 @@ cudaError_t launch_simt(const ScanArgs &a, const ScanPlan &pl, cudaStream_t s) {
         const SimtSmem l1(pl.Q, a.R, a.N, a.P, false);
         const size_t bytes1 = l1.total * sizeof(float);
         auto k1 = simt_segment_kernel<T, false>;
-        cudaError_t err = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes1);
+        cudaError_t err = allow_dynamic_smem<simt_segment_kernel<T, false>>(bytes1);
         if (err != cudaSuccess) return err;
         trace_mark(M3_KERNEL_PREFILL_STATE, s, 0);
         k1<<<(unsigned)(bh * (pl.nseg - 1)), kThreads, bytes1, s>>>(a, pl.Q, pl.seglen, pl.nseg, pl.nseg - 1);
@@ -301,7 +301,7 @@ cudaError_t launch_simt(const ScanArgs &a, const ScanPlan &pl, cudaStream_t s) {
     const SimtSmem l3(pl.Q, a.R, a.N, a.P, true);
     const size_t bytes3 = l3.total * sizeof(float);
     auto k3 = simt_segment_kernel<T, true>;
-    cudaError_t err = cudaFuncSetAttribute(k3, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes3);
+    cudaError_t err = allow_dynamic_smem<simt_segment_kernel<T, true>>(bytes3);
     if (err != cudaSuccess) return err;
     trace_mark(M3_KERNEL_PREFILL_OUTPUT, s, 0);
     k3<<<(unsigned)(bh * pl.nseg), kThreads, bytes3, s>>>(a, pl.Q, pl.seglen, pl.nseg, pl.nseg);

@@ -928,7 +928,7 @@ cudaError_t launch_pass(const TcMaps &maps, const ScanArgs &a, const ScanPlan &p
     using Sm = Smem<N, R, OUT>;
     static_assert(Sm::kAlloc <= 227 * 1024, "shared memory over the per-CTA limit");
     auto kern = tc_segment_kernel<N, R, OUT>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Sm::kAlloc);
+    cudaError_t e = allow_dynamic_smem<tc_segment_kernel<N, R, OUT>>(Sm::kAlloc);
     if (e != cudaSuccess) return e;
     unsigned *status = device_status_word();
     if (!status) return cudaErrorUnknown;
