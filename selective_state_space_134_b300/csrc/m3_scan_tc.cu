@@ -332,6 +332,7 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                            make_desc(xh + ks * 2048, 0, 1024, kSwizzle128B), idSn, ks > 0);
                 }
                 mma_commit(bars + kMma1 + p);
+                mma_commit(bars + kRawEmpty + p);   // MMA 2 reads only TMEM and x'
                 if (OUT) {
                     wait(kPReady + p, ph, true);
                     fence_after();
@@ -342,12 +343,11 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                                idYa, ks > 0);
                     mma_commit(bars + kMma2 + p);
                 }
-                mma_commit(bars + kRawEmpty + p);
             }
             if (*abort_flag && nchunks > 0) {
                 // let the last MMAs finish before TMEM is released
                 const int it = nchunks - 1;
-                mbar_wait(bars + kRawEmpty + (it & 1), (it >> 1) & 1, kWaitNs);
+                mbar_wait(bars + (OUT ? kMma2 : kMma1) + (it & 1), (it >> 1) & 1, kWaitNs);
             }
         }
         __syncwarp();
