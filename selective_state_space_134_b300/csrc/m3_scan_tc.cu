@@ -978,9 +978,10 @@ bool tc_plan(const m3_dims &d, int sms, ScanPlan *pl) {
     const int L = d.seqlen;
     int nseg = 1;
     if (seqs > 0 && L > 0 && seqs < (long long)(0.8 * sms)) {
-        // fill the SMs (one CTA each); segments of at least 8 chunks
+        // fill the SMs with one wave of CTAs (one per SM; a second, partial wave would
+        // double the time of the output pass); segments of at least 8 chunks
         const int max_seg = (L + 8 * Q - 1) / (8 * Q);
-        long long want = (sms + seqs - 1) / seqs;
+        long long want = sms / seqs;
         nseg = (int)(want < max_seg ? want : max_seg);
         if (nseg < 1) nseg = 1;
     }
