@@ -208,7 +208,9 @@ m3_status mamba3_scan_fwd(const m3_dims *dims, const void *x, const void *B, con
     a.Bprev_out = state_out ? state_out->B_prev : nullptr;
     a.xprev_out = state_out ? state_out->x_prev : nullptr;
     if (pl.ws_bytes > 0) {
-        const size_t state_b = bh * pl.nseg * d.dstate * d.headdim * sizeof(float);
+        // state slots per sequence: one per state-pass piece boundary (see scan_workspace_bytes)
+        const size_t slots = pl.nseg > 1 ? (size_t)(pl.nseg - 1) * pl.nsub + 1 : 1;
+        const size_t state_b = bh * slots * d.dstate * d.headdim * sizeof(float);
         a.ws_state = static_cast<float *>(workspace);
         a.ws_tot = reinterpret_cast<float *>(static_cast<char *>(workspace) + ((state_b + 255) / 256) * 256);
     }

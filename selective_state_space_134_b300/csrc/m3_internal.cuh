@@ -63,6 +63,7 @@ struct ScanPlan {
     int Q;        // tokens per chunk
     int nseg;     // segments per sequence
     int seglen;   // tokens per segment (multiple of Q), last one may be shorter
+    int nsub;     // state-pass pieces per segment (the pass that feeds the segment starts)
     int path;     // kPathSimt or kPathTc
     size_t ws_bytes;
 };

@@ -346,6 +346,7 @@ bool simt_plan(const m3_dims &d, int sms, ScanPlan *pl) {
     nseg = L > 0 ? (L + seglen - 1) / seglen : 1;
     pl->Q = Q;
     pl->nseg = nseg;
+    pl->nsub = 1;
     pl->seglen = seglen;
     pl->path = kPathSimt;
     pl->ws_bytes = scan_workspace_bytes(d.batch, d.nheads, N, P, nseg);

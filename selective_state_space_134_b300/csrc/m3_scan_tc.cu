@@ -179,8 +179,8 @@ enum Bar {
 
 template <int N, int R, bool OUT>
 __global__ void __launch_bounds__(kThreads, 1)
-tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, int nseg, int nlaunch,
-                  unsigned *status) {
+tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, int nseg, int nlaunch, int ws_stride,
+                  int ws_step, unsigned *status) {
     using Cf = Cfg<N, R>;
     using S = Smem<N, R, OUT>;
     constexpr int QR = Cf::QR, Q = Cf::Q, K = Cf::K, NSLAB = Cf::NSLAB, TPS = Cf::TPS, TB = Cf::TB;
@@ -614,7 +614,7 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
         if (!OUT) {
             named_sync(kBarPro, kProThreads);
             if (!*abort_flag) {
-                float *dst = a.ws_tot + ((size_t)bh * (nseg - 1) + g) * (1 + K);
+                float *dst = a.ws_tot + ((size_t)bh * (ws_stride - 1) + g) * (1 + K);
                 if (ptid == 0) dst[0] = acc_cA / kLog2e;
                 for (int i = ptid; i < K; i += kProThreads) dst[1 + i] = tot[1 + i];
             }
@@ -656,7 +656,7 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                                 v += left0 * u;
                             }
                         } else {
-                            v = a.ws_state[(((size_t)bh * nseg + g) * N + n) * kP + pp];
+                            v = a.ws_state[(((size_t)bh * ws_stride + (size_t)g * ws_step) * N + n) * kP + pp];
                         }
                     }
                     hmax = fmaxf(hmax, fabsf(v));
@@ -785,7 +785,7 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                 const bool odd = n & 1;
                 float *dst = nullptr;
                 if (last_chunk && st_owner && !*abort_flag) {
-                    if (!OUT) dst = a.ws_state + (((size_t)bh * nseg + g + 1) * N + n) * kP + 32 * eh;
+                    if (!OUT) dst = a.ws_state + (((size_t)bh * ws_stride + g + 1) * N + n) * kP + 32 * eh;
                     else if (g == nseg - 1 && a.h_out) dst = a.h_out + ((size_t)bh * N + n) * kP + 32 * eh;
                 }
                 float m = 0.f;
@@ -924,7 +924,9 @@ bool map_y(CUtensorMap *m, void *base, int R, int H, int L, int batch, int Q) {
 }
 
 template <int N, int R, bool OUT>
-cudaError_t launch_pass(const TcMaps &maps, const ScanArgs &a, const ScanPlan &pl, int nlaunch, cudaStream_t s) {
+// ws_stride: workspace state slots per sequence; ws_step: slots per segment of this pass
+cudaError_t launch_pass(const TcMaps &maps, const ScanArgs &a, const ScanPlan &pl, int nlaunch, int ws_stride,
+                        int ws_step, cudaStream_t s) {
     using Sm = Smem<N, R, OUT>;
     static_assert(Sm::kAlloc <= 227 * 1024, "shared memory over the per-CTA limit");
     auto kern = tc_segment_kernel<N, R, OUT>;
@@ -935,7 +937,8 @@ cudaError_t launch_pass(const TcMaps &maps, const ScanArgs &a, const ScanPlan &p
     const long long grid = (long long)a.batch * a.H * nlaunch;
     const int kid = OUT ? M3_KERNEL_PREFILL_OUTPUT : M3_KERNEL_PREFILL_STATE;
     trace_mark(kid, s, 0);
-    kern<<<(unsigned)grid, kThreads, Sm::kAlloc, s>>>(maps, a, pl.seglen, pl.nseg, nlaunch, status);
+    kern<<<(unsigned)grid, kThreads, Sm::kAlloc, s>>>(maps, a, pl.seglen, pl.nseg, nlaunch, ws_stride, ws_step,
+                                                      status);
     trace_mark(kid, s, 1);
     count_launch();
     return cudaGetLastError();
@@ -951,11 +954,18 @@ cudaError_t run_tc(const ScanArgs &a, const ScanPlan &pl, cudaStream_t s) {
         !map_y(&maps.Y, a.y, R, a.H, a.L, a.batch, Cf::Q))
         return cudaErrorInvalidValue;
     cudaError_t e;
+    // The state pass works on pieces of seglen / nsub tokens (one CTA each) covering segments
+    // 0 .. nseg - 2; the segment pass chains the pieces' end states; the output pass starts
+    // segment g from the state at piece g * nsub.
+    const int npieces = pl.nseg > 1 ? (pl.nseg - 1) * pl.nsub + 1 : 1;
     if (pl.nseg > 1) {
-        if ((e = launch_pass<N, R, false>(maps, a, pl, pl.nseg - 1, s)) != cudaSuccess) return e;
-        if ((e = segment_pass(a, pl, s)) != cudaSuccess) return e;
+        ScanPlan pp = pl;
+        pp.nseg = npieces;
+        pp.seglen = pl.seglen / pl.nsub;
+        if ((e = launch_pass<N, R, false>(maps, a, pp, npieces - 1, npieces, 1, s)) != cudaSuccess) return e;
+        if ((e = segment_pass(a, pp, s)) != cudaSuccess) return e;
     }
-    return launch_pass<N, R, true>(maps, a, pl, pl.nseg, s);
+    return launch_pass<N, R, true>(maps, a, pl, pl.nseg, npieces, pl.nsub, s);
 }
 
 int tc_chunk(int N, int R) { return (N == 64 ? 128 : 64) / R; }
@@ -988,11 +998,22 @@ bool tc_plan(const m3_dims &d, int sms, ScanPlan *pl) {
     int seglen = L > 0 ? (L + nseg - 1) / nseg : Q;
     seglen = ((seglen + Q - 1) / Q) * Q;
     nseg = L > 0 ? (L + seglen - 1) / seglen : 1;
+    // the state pass covers segments 0 .. nseg - 2: split them into as many whole pieces of
+    // at least 8 chunks as one wave of CTAs holds
+    int nsub = 1;
+    if (nseg > 1) {
+        const long long cap = sms / (seqs * (nseg - 1));
+        const int chunks = seglen / Q;
+        for (int c = 2; c <= cap && chunks / c >= 8; ++c)
+            if (chunks % c == 0) nsub = c;
+    }
     pl->Q = Q;
     pl->nseg = nseg;
     pl->seglen = seglen;
+    pl->nsub = nsub;
     pl->path = kPathTc;
-    pl->ws_bytes = scan_workspace_bytes(d.batch, d.nheads, d.dstate, d.headdim, nseg);
+    pl->ws_bytes = scan_workspace_bytes(d.batch, d.nheads, d.dstate, d.headdim,
+                                        nseg > 1 ? (nseg - 1) * nsub + 1 : 1);
     return true;
 }
 

@@ -96,6 +96,22 @@ def test_scan_full_size_sampled(wname):
     assert torch.isfinite(y.float()).all()
 
 
+@pytest.mark.parametrize("with_state", [False, True])
+def test_segmented_prefill_with_state_pass_pieces(with_state):
+    # 64 sequences, L = 1000, N = 128, R = 4 (16-token chunks): two segments of 512 tokens
+    # (one wave of CTAs), the state pass cut into two pieces of 256 tokens, a ragged last
+    # segment; every sequence against the oracle
+    w = WORKLOADS["long_n128_r4"].with_(batch=1, nheads=64, seqlen=1000)
+    inp = prefill_inputs(w, "cuda")
+    st = random_state(w.batch, w.nheads, w.P, w.N, w.R, inp["x"].dtype) if with_state else None
+    y, so = gpu_scan(inp, state_in=st)
+    yr, hr, Br, xr = oracle_full(inp, st)
+    assert norm_err(to_f64(y), yr) <= TOL[w.dtype]
+    assert norm_err(to_f64(so.h), hr) <= TOL[w.dtype]
+    np.testing.assert_array_equal(to_f64(so.B_prev), Br)
+    np.testing.assert_array_equal(to_f64(so.x_prev), xr)
+
+
 @pytest.mark.parametrize("wname", ["decode_n64_r1", "decode_n64_r4", "decode_n128_r1", "decode_n128_r4"])
 def test_decode_full_size_matches_oracle(wname):
     w = WORKLOADS[wname]
