@@ -467,20 +467,27 @@ cudaError_t stream_dispatch(int nbh, int P, int N, int R, const void *x, const v
 // hi + lo parts (error below 2^-16 of |h|), is the A operand of
 //   Y^T += h^T C^T     (m16n8k16: M = p, N = r padded to 8, K = n).
 // The state is staged by 2-d TMA with the 128-byte swizzle (boxes of 32 columns
-// x HPU N rows): the MMA layout's accesses are then free of bank conflicts.
+// x HPU N rows): the MMA layout's accesses are then free of bank conflicts.  When
+// a unit has a multiple of 8 rank rows (HPU R), B, C and B_prev are staged the
+// same way (boxes of 64 columns x HPU R rows, no padding needed); otherwise by
+// bulk copies in their linear layout, where rank rows N * 2 bytes apart share
+// banks.
 constexpr int kMmaThreads = 256;
 constexpr int kMmaP = 64;
 
 struct MmaLayout {
     uint32_t B, C, Bp, x, xp, stage;     // byte offsets inside a stage (the state at 0), stage size
+    uint32_t half;                       // swizzled B, C, B_prev: bytes per 64-column half tile
     uint32_t rot, red, bar, flag, total;
     __host__ __device__ MmaLayout(int N, int R, int hpu, int nst) {
         auto up = [](uint32_t v, uint32_t a) { return (v + a - 1u) & ~(a - 1u); };
-        const uint32_t bn = (uint32_t)(hpu * R * N * 2), xn = (uint32_t)(hpu * R * kMmaP * 2);
+        const uint32_t xn = (uint32_t)(hpu * R * kMmaP * 2);
+        half = (uint32_t)(hpu * R * 128);   // a multiple of 1024 when the tiles are swizzled
+        const uint32_t tile = up(half * (uint32_t)(N / 64), 128u);
         B = (uint32_t)(hpu * N * kMmaP * 4);
-        C = up(B + bn, 128u);
-        Bp = up(C + bn, 128u);
-        x = up(Bp + bn, 128u);
+        C = B + tile;
+        Bp = C + tile;
+        x = Bp + tile;
         xp = up(x + xn, 128u);
         stage = up(xp + xn, 1024u);
         rot = stage * nst;                                   // (rho cos, rho sin) per pair of the unit
@@ -491,9 +498,21 @@ struct MmaLayout {
     }
 };
 
+// Byte offset of (row, col) in a B / C / B_prev tile: 64-column halves of `half` bytes, each
+// rows of 128 bytes with the 16-byte chunks of row r XOR-ed by r mod 8 (the TMA 128-byte swizzle)
+// (linear layout: row-major [rows][N] bf16)
+template <bool SWZ, int N>
+__device__ __forceinline__ uint32_t rank_off(uint32_t half, int row, int col) {
+    if (!SWZ) return (uint32_t)(row * N + col) * 2u;
+    const uint32_t c = (uint32_t)col & 63u, r = (uint32_t)row;
+    return ((uint32_t)col >> 6) * half + r * 128u + ((((c >> 3) ^ r) & 7u) << 4) + ((c & 7u) << 1);
+}
+
 template <int R, int N, int HPU>
 __global__ void __launch_bounds__(kMmaThreads, 2)
-decode_mma_kernel(const __grid_constant__ CUtensorMap hmap, int nunit, int nst, const __nv_bfloat16 *__restrict__ x,
+decode_mma_kernel(const __grid_constant__ CUtensorMap hmap, const __grid_constant__ CUtensorMap bmap,
+                  const __grid_constant__ CUtensorMap cmap, const __grid_constant__ CUtensorMap bpmap, int nunit,
+                  int nst, const __nv_bfloat16 *__restrict__ x,
                   const __nv_bfloat16 *__restrict__ Bm, const __nv_bfloat16 *__restrict__ Cm,
                   const __nv_bfloat16 *__restrict__ dtp, const __nv_bfloat16 *__restrict__ Ap,
                   const __nv_bfloat16 *__restrict__ lp, const __nv_bfloat16 *__restrict__ thp,
@@ -504,6 +523,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap hmap, int nunit, int nst, 
     constexpr int NR = HPU * N, KU = HPU * K, KT = kMmaThreads - KU;   // rows, pairs per unit; table threads
     static_assert((HPU == 1 || HPU == 2) && N % 32 == 0 && NR <= 256 && KU <= kMmaThreads && R >= 1 && R <= 8,
                   "shape outside the tensor-core decode");
+    constexpr bool SWZ = (HPU * R) % 8 == 0;   // B, C, B_prev through swizzled TMA tiles
     extern __shared__ __align__(1024) unsigned char smem_m[];
     unsigned char *sm = smem_m + ((1024u - (smem_u32(smem_m) & 1023u)) & 1023u);
     const MmaLayout Lo(N, R, HPU, nst);
@@ -527,15 +547,29 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap hmap, int nunit, int nst, 
         mbar_expect_tx(bar, hn + 3 * bn + 2 * xn);
         tma_load_2d(sg, &hmap, 0, bh0 * N, bar);
         tma_load_2d(sg + NR * 128, &hmap, 32, bh0 * N, bar);
-        bulk_load(sg + Lo.B, Bm + (size_t)bh0 * R * N, bn, bar);
-        bulk_load(sg + Lo.C, Cm + (size_t)bh0 * R * N, bn, bar);
-        bulk_load(sg + Lo.Bp, Bprev + (size_t)bh0 * R * N, bn, bar);
+        if (SWZ) {
+#pragma unroll
+            for (int hf = 0; hf < N / 64; ++hf) {
+                tma_load_2d(sg + Lo.B + hf * Lo.half, &bmap, 64 * hf, bh0 * R, bar);
+                tma_load_2d(sg + Lo.C + hf * Lo.half, &cmap, 64 * hf, bh0 * R, bar);
+                tma_load_2d(sg + Lo.Bp + hf * Lo.half, &bpmap, 64 * hf, bh0 * R, bar);
+            }
+        } else {
+            bulk_load(sg + Lo.B, Bm + (size_t)bh0 * R * N, bn, bar);
+            bulk_load(sg + Lo.C, Cm + (size_t)bh0 * R * N, bn, bar);
+            bulk_load(sg + Lo.Bp, Bprev + (size_t)bh0 * R * N, bn, bar);
+        }
         bulk_load(sg + Lo.x, x + (size_t)bh0 * R * P, xn, bar);
         bulk_load(sg + Lo.xp, xprev + (size_t)bh0 * R * P, xn, bar);
     };
 
     if (tid == 0) {
         tma_prefetch_desc(&hmap);
+        if (SWZ) {
+            tma_prefetch_desc(&bmap);
+            tma_prefetch_desc(&cmap);
+            tma_prefetch_desc(&bpmap);
+        }
         for (int i = 0; i < nst; ++i) mbar_init(full + i, 1);
         mbar_init_fence();
         *abort_flag = 0;
@@ -586,9 +620,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap hmap, int nunit, int nst, 
             *abort_flag = 1;
             break;
         }
-        const unsigned short *sB = reinterpret_cast<const unsigned short *>(sg + Lo.B) + hh * R * N;
-        const unsigned short *sBp = reinterpret_cast<const unsigned short *>(sg + Lo.Bp) + hh * R * N;
-        const unsigned short *sC = reinterpret_cast<const unsigned short *>(sg + Lo.C) + hh * R * N;
+        const unsigned char *sB = sg + Lo.B, *sBp = sg + Lo.Bp, *sC = sg + Lo.C;
         const unsigned short *sx = reinterpret_cast<const unsigned short *>(sg + Lo.x) + hh * R * P;
         const unsigned short *sxp = reinterpret_cast<const unsigned short *>(sg + Lo.xp) + hh * R * P;
         const float2 *hrot = rot + hh * K;
@@ -619,12 +651,13 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap hmap, int nunit, int nst, 
                 const int n0 = nb0 + 16 * ks + 8 * hf;
                 uint32_t bb = 0, bq = 0;   // B operands: rank rows 2t, 2t + 1 of state row n0 + g
                 if (rlane) {
-                    const int q = 2 * t * N + n0 + g;
-                    bb = sB[q];
-                    bq = sBp[q];
+                    const int row = hh * R + 2 * t;
+                    const uint32_t o0 = rank_off<SWZ, N>(Lo.half, row, n0 + g), o1 = rank_off<SWZ, N>(Lo.half, row + 1, n0 + g);
+                    bb = *reinterpret_cast<const unsigned short *>(sB + o0);
+                    bq = *reinterpret_cast<const unsigned short *>(sBp + o0);
                     if (R > 1) {
-                        bb |= (uint32_t)sB[q + N] << 16;
-                        bq |= (uint32_t)sBp[q + N] << 16;
+                        bb |= (uint32_t)*reinterpret_cast<const unsigned short *>(sB + o1) << 16;
+                        bq |= (uint32_t)*reinterpret_cast<const unsigned short *>(sBp + o1) << 16;
                     }
                 }
                 float u[4] = {0.f, 0.f, 0.f, 0.f}, v[4] = {0.f, 0.f, 0.f, 0.f};
@@ -650,9 +683,9 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap hmap, int nunit, int nst, 
             }
             uint32_t b0 = 0, b1 = 0;   // C^T: state rows 2t, 2t + 1 (+ 8) of this K step, rank column g
             if (g < R) {
-                const unsigned short *cp = sC + g * N + nb0 + 16 * ks + 2 * t;
-                b0 = *reinterpret_cast<const uint32_t *>(cp);
-                b1 = *reinterpret_cast<const uint32_t *>(cp + 8);
+                const int row = hh * R + g, c0 = nb0 + 16 * ks + 2 * t;
+                b0 = *reinterpret_cast<const uint32_t *>(sC + rank_off<SWZ, N>(Lo.half, row, c0));
+                b1 = *reinterpret_cast<const uint32_t *>(sC + rank_off<SWZ, N>(Lo.half, row, c0 + 8));
             }
             mma_m16n8k16(yacc, ahi, b0, b1);
             mma_m16n8k16(yacc, alo, b0, b1);
@@ -673,7 +706,12 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap hmap, int nunit, int nst, 
         if (tid == 0) {
             tma_store_2d(&hmap, sg, 0, bh0 * N);
             tma_store_2d(&hmap, sg + NR * 128, 32, bh0 * N);
-            bulk_store(Bprev + (size_t)bh0 * R * N, sg + Lo.B, bn);   // new carry = this token's (B, x)
+            if (SWZ) {   // new carry = this token's (B, x)
+#pragma unroll
+                for (int hf = 0; hf < N / 64; ++hf) tma_store_2d(&bpmap, sg + Lo.B + hf * Lo.half, 64 * hf, bh0 * R);
+            } else {
+                bulk_store(Bprev + (size_t)bh0 * R * N, sg + Lo.B, bn);
+            }
             bulk_store(xprev + (size_t)bh0 * R * P, sg + Lo.x, xn);
             bulk_commit();
             if (issued < mine) {
@@ -700,6 +738,20 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap hmap, int nunit, int nst, 
     }
 }
 
+// 2-d map over a [rows][cols] bf16 array (B, C or B_prev as [nbh * R][N]); box = 64 columns x
+// box_rows, 128-byte swizzle
+bool map_rank(CUtensorMap *m, const void *base, long long rows, int cols, int box_rows) {
+    tc::EncodeFn enc = tc::encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 2-d map over the fp32 state viewed as [nbh * N rows][64 columns]; box = 32 columns x box_rows,
 // 128-byte swizzle
 bool map_state(CUtensorMap *m, float *h, long long rows, int box_rows) {
@@ -718,23 +770,33 @@ template <int R, int N, int HPU>
 cudaError_t launch_mma(int nbh, const void *x, const void *B, const void *C, const void *dt, const void *A,
                        const void *lam, const void *theta, float *h, void *Bprev, void *xprev, void *y,
                        cudaStream_t s) {
-    // the map depends only on (h, rows, box); a decode loop reuses one state buffer
+    constexpr bool kSwz = (HPU * R) % 8 == 0;
+    // the state and carry maps depend only on (h, B_prev, shape); a decode loop reuses one state
     struct MapCache {
         const float *h = nullptr;
+        const void *bp = nullptr;
         long long rows = 0;
-        int box = 0;
-        CUtensorMap map;
+        int n = 0, r = 0, hpu = 0;
+        CUtensorMap hmap, bpmap;
     };
     thread_local MapCache cache;
     const long long rows = (long long)nbh * N;
-    if (cache.h != h || cache.rows != rows || cache.box != HPU * N) {
+    if (cache.h != h || cache.bp != Bprev || cache.rows != rows || cache.n != N || cache.r != R || cache.hpu != HPU) {
         cache.h = nullptr;
-        if (!map_state(&cache.map, h, rows, HPU * N)) return cudaErrorInvalidValue;
+        if (!map_state(&cache.hmap, h, rows, HPU * N)) return cudaErrorInvalidValue;
+        if (kSwz && !map_rank(&cache.bpmap, Bprev, (long long)nbh * R, N, HPU * R)) return cudaErrorInvalidValue;
         cache.h = h;
+        cache.bp = Bprev;
         cache.rows = rows;
-        cache.box = HPU * N;
+        cache.n = N;
+        cache.r = R;
+        cache.hpu = HPU;
     }
-    const CUtensorMap &hmap = cache.map;
+    CUtensorMap bmap = cache.hmap, cmap = cache.hmap;   // unused unless swizzled
+    if (kSwz && (!map_rank(&bmap, B, (long long)nbh * R, N, HPU * R) ||
+                 !map_rank(&cmap, C, (long long)nbh * R, N, HPU * R)))
+        return cudaErrorInvalidValue;
+    if (!kSwz) cache.bpmap = cache.hmap;
     // two CTAs per SM with as many stages as fit (2..6), else one CTA per SM
     int per_sm = 2, nst = 6;
     while (nst > 2 && MmaLayout(N, R, HPU, nst).total > 113u * 1024u) --nst;
@@ -754,7 +816,7 @@ cudaError_t launch_mma(int nbh, const void *x, const void *B, const void *C, con
     const int grid = nunit < per_sm * sm_count() ? nunit : per_sm * sm_count();
     using bf = __nv_bfloat16;
     trace_mark(M3_KERNEL_DECODE, s, 0);
-    kern<<<grid, kMmaThreads, Lo.total, s>>>(hmap, nunit, nst, (const bf *)x, (const bf *)B, (const bf *)C,
+    kern<<<grid, kMmaThreads, Lo.total, s>>>(cache.hmap, bmap, cmap, cache.bpmap, nunit, nst, (const bf *)x, (const bf *)B, (const bf *)C,
                                             (const bf *)dt, (const bf *)A, (const bf *)lam, (const bf *)theta,
                                             (bf *)Bprev, (bf *)xprev, (float *)y, status);
     trace_mark(M3_KERNEL_DECODE, s, 1);

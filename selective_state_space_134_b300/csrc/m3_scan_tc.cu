@@ -107,16 +107,6 @@ __device__ __forceinline__ uint32_t sw128f(uint32_t row, uint32_t col) {
     return row * 128u + ((((col >> 2) ^ row) & 7u) << 4) + ((col & 3u) << 2);
 }
 
-__device__ __forceinline__ void sincos_reduced(float x, float *s, float *c) {
-    // Cody-Waite reduction by 2 pi (two-constant split), then the hardware sin/cos on [-pi, pi].
-    // n = round(x / 2 pi) by the 1.5 * 2^23 addition (exact for |x / 2 pi| < 2^22), which runs
-    // on the FMA pipe instead of the quarter-rate conversion unit
-    const float n = (x * 0.15915494309189535f + 12582912.f) - 12582912.f;
-    float r = fmaf(-n, 6.28318548202514648f, x);
-    r = fmaf(-n, -1.7484555314695172e-7f, r);
-    __sincosf(r, s, c);
-}
-
 // packed fp32 pairs (one instruction for two lanes of arithmetic)
 __device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
 __device__ __forceinline__ float2 f2u(uint32_t a, uint32_t b) { return make_float2(__uint_as_float(a), __uint_as_float(b)); }
@@ -517,8 +507,10 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                 };
 #pragma unroll
                 for (int i = 0; i < kLA; ++i) load_tok(i);
-                // two tokens at a time on packed fp32 (the range reduction of sincos_reduced and
-                // the rotations; same operations, same roundings)
+                // two tokens at a time on packed fp32.  sin / cos: Cody-Waite reduction by 2 pi
+                // (two-constant split) to [-pi, pi], n = round(x / 2 pi) by the 1.5 * 2^23
+                // addition (exact for |x / 2 pi| < 2^22, and on the FMA pipe rather than the
+                // conversion unit), then the hardware approximations there
                 static_assert(TPS % 2 == 0, "token pairs");
 #pragma unroll
                 for (int i = 0; i < TPS; i += 2) {
@@ -629,7 +621,7 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
         // score / output rows owned
         const bool row_ok = kRowsM64 ? (lane < 16) : true;
         const int row = kRowsM64 ? eq * 16 + lane : eq * 32 + lane;
-        const int ti = row / R, ri = row % R;
+        const int ti = row / R;
         // The fp32 state lives in TMEM columns [cH, cH + 64): row n in the lane of the Sn
         // accumulator's row n, column p; this thread holds columns [32 eh, 32 eh + 32).
         const uint32_t hcol = tmem + lane_base + cH + 32 * eh;
