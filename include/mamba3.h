@@ -62,7 +62,8 @@ typedef enum {
     M3_ERR_UNSUPPORTED = 2,   /* shape or dtype outside the supported set */
     M3_ERR_WORKSPACE = 3,     /* workspace missing or smaller than the queried size */
     M3_ERR_CUDA = 4,          /* a CUDA runtime call or kernel launch failed */
-    M3_ERR_TIMEOUT = 5        /* a device-side wait gave up (see mamba3_device_status) */
+    M3_ERR_TIMEOUT = 5,       /* a device-side wait gave up (see mamba3_device_status) */
+    M3_ERR_INDEX = 6          /* a pooled decode read a slot index outside [0, pool_size) */
 } m3_status;
 
 typedef enum { M3_F32 = 0, M3_BF16 = 1 } m3_dtype;
@@ -207,10 +208,37 @@ m3_status mamba3_decode_step(const m3_dims *dims, const void *x, const void *B, 
                              const m3_state *state, void *y, void *stream);
 
 /*
+ * One decode step for a batch whose states live in a caller-owned state pool
+ * (serving: sequences join and leave, each keeps its slot).  Not from the
+ * Mamba-3 pages: the step is exactly mamba3_decode_step, with the state of
+ * batch row b read from and written back to pool slot slot[b].
+ *
+ * slot:  device int32 [batch].  slot[b] in [0, pool_size) selects the pool
+ *   state of row b; slot[b] < 0 marks an inactive row: nothing of it is read
+ *   from the pool or written (its y row is left as it was).  Active rows must
+ *   name distinct slots (two rows on one slot race).  A slot >= pool_size is
+ *   skipped like an inactive row and sets M3_ERR_INDEX in the device status
+ *   word (see mamba3_device_status).
+ * pool:  h [pool_size][H][N][P] fp32, B_prev [pool_size][H][R][N], x_prev
+ *   [pool_size][H][R][P] (input dtype), updated in place for the active rows.
+ * x, B, C, dt, A, lambda, theta, y: as mamba3_decode_step, indexed by batch
+ *   row.
+ * Supported shapes: those of the tensor-core decode kernel (bf16 inputs,
+ * P = 64, N in {64, 128}, R in {1, 2, 4, 8}, 16-byte-aligned pointers); others
+ * return M3_ERR_UNSUPPORTED.  pool_size < 1 or a NULL pointer is
+ * M3_ERR_INVALID_ARG; nothing is launched on an argument error.
+ */
+m3_status mamba3_decode_step_pooled(const m3_dims *dims, const int *slot, const void *x, const void *B,
+                                    const void *C, const void *dt, const void *A, const void *lambda,
+                                    const void *theta, const m3_state *pool, int pool_size, void *y,
+                                    void *stream);
+
+/*
  * Synchronises `stream`, then reads and clears the library's device status
  * word on the current device.  Returns M3_OK, or M3_ERR_TIMEOUT when a kernel
  * gave up a bounded wait since the last call (its outputs are then invalid),
- * or M3_ERR_CUDA when the synchronisation itself failed.
+ * M3_ERR_INDEX when a pooled decode met a slot index outside the pool (that
+ * row was skipped), or M3_ERR_CUDA when the synchronisation itself failed.
  */
 m3_status mamba3_device_status(void *stream);
 

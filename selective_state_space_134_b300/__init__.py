@@ -5,9 +5,11 @@ The compute lives in ``libmamba3.so`` (hand-written CUDA behind the C ABI of
 the seeded synthetic-input generator.
 """
 from .mamba3 import (KERNEL_DECODE, KERNEL_PREFILL_OUTPUT, KERNEL_PREFILL_STATE, KERNEL_SEGMENT_PASS, M3_BF16,
-                     M3_F32, M3_OK, Mamba3Error, State, decode_step, device_status, dims, launch_count, lib,
+                     M3_ERR_INDEX, M3_F32, M3_OK, Mamba3Error, State, decode_step, decode_step_pooled, device_status,
+                     dims, launch_count, lib,
                      scan_fwd, scan_fwd_workspace, status_string, trace_begin, trace_end)
 
 __all__ = ["KERNEL_DECODE", "KERNEL_PREFILL_OUTPUT", "KERNEL_PREFILL_STATE", "KERNEL_SEGMENT_PASS", "M3_BF16",
-           "M3_F32", "M3_OK", "Mamba3Error", "State", "decode_step", "device_status", "dims", "launch_count",
+           "M3_ERR_INDEX", "M3_F32", "M3_OK", "Mamba3Error", "State", "decode_step", "decode_step_pooled",
+           "device_status", "dims", "launch_count",
            "lib", "scan_fwd", "scan_fwd_workspace", "status_string", "trace_begin", "trace_end"]

@@ -349,6 +349,29 @@ m3_status mamba3_decode_step(const m3_dims *dims, const void *x, const void *B, 
     return e == cudaSuccess ? M3_OK : M3_ERR_CUDA;
 }
 
+m3_status mamba3_decode_step_pooled(const m3_dims *dims, const int *slot, const void *x, const void *B,
+                                    const void *C, const void *dt, const void *A, const void *lambda,
+                                    const void *theta, const m3_state *pool, int pool_size, void *y,
+                                    void *stream) {
+    m3_status st = check_dims(dims, false);
+    if (st != M3_OK) return st;
+    const m3_dims &d = *dims;
+    if (d.batch == 0) return M3_OK;   // nothing to read or write; pointers are not inspected
+    if (!pool || pool_size < 1 || !ptr_ok(slot, 4)) return M3_ERR_INVALID_ARG;
+    const size_t es = elem_size(d.dtype);
+    for (const void *p : {x, B, C, dt, A, lambda, theta, (const void *)pool->B_prev, (const void *)pool->x_prev})
+        if (!ptr_ok(p, es)) return M3_ERR_INVALID_ARG;
+    if (!ptr_ok(y, 4)) return M3_ERR_INVALID_ARG;
+    if (!ptr_ok(pool->h, 16)) return M3_ERR_INVALID_ARG;
+    const void *ptrs[] = {x, B, C, theta, pool->h, pool->B_prev, pool->x_prev};
+    if (!decode_pooled_ok(d.dtype, d.batch, d.nheads, d.headdim, d.dstate, d.rank, pool_size, ptrs, 7))
+        return M3_ERR_UNSUPPORTED;
+    cudaError_t e = decode_step_pooled(d.batch, d.nheads, d.headdim, d.dstate, d.rank, slot, pool_size, x, B, C,
+                                       dt, A, lambda, theta, pool->h, pool->B_prev, pool->x_prev, y,
+                                       static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? M3_OK : M3_ERR_CUDA;
+}
+
 m3_status mamba3_device_status(void *stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return M3_ERR_CUDA;
     unsigned *w = device_status_word();
@@ -359,7 +382,8 @@ m3_status mamba3_device_status(void *stream) {
         const unsigned zero = 0;
         if (cudaMemcpy(w, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return M3_ERR_CUDA;
     }
-    return (v & kStatusTimeout) ? M3_ERR_TIMEOUT : M3_OK;
+    if (v & kStatusTimeout) return M3_ERR_TIMEOUT;
+    return (v & kStatusBadIndex) ? M3_ERR_INDEX : M3_OK;
 }
 
 const char *mamba3_status_string(int status) {
@@ -370,6 +394,7 @@ const char *mamba3_status_string(int status) {
         case M3_ERR_WORKSPACE: return "workspace missing or too small";
         case M3_ERR_CUDA: return "CUDA error";
         case M3_ERR_TIMEOUT: return "device-side wait timed out";
+        case M3_ERR_INDEX: return "pooled decode slot index outside the pool";
         default: return "unknown status";
     }
 }

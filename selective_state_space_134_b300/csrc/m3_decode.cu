@@ -512,7 +512,7 @@ template <int R, int N, int HPU>
 __global__ void __launch_bounds__(kMmaThreads, 2)
 decode_mma_kernel(const __grid_constant__ CUtensorMap hmap, const __grid_constant__ CUtensorMap bmap,
                   const __grid_constant__ CUtensorMap cmap, const __grid_constant__ CUtensorMap bpmap, int nunit,
-                  int nst, const __nv_bfloat16 *__restrict__ x,
+                  int nst, const int *__restrict__ slot, int pool, int H, const __nv_bfloat16 *__restrict__ x,
                   const __nv_bfloat16 *__restrict__ Bm, const __nv_bfloat16 *__restrict__ Cm,
                   const __nv_bfloat16 *__restrict__ dtp, const __nv_bfloat16 *__restrict__ Ap,
                   const __nv_bfloat16 *__restrict__ lp, const __nv_bfloat16 *__restrict__ thp,
@@ -540,27 +540,39 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap hmap, const __grid_constan
     const int mine = first < nunit ? (nunit - first + step - 1) / step : 0;
     constexpr uint32_t bn = HPU * R * N * 2, xn = HPU * R * P * 2, hn = NR * P * 4;
 
+    // Head of the state (pool) holding token head bh0 of a unit: bh0 itself, or with a slot
+    // table (pooled decode), slot[b] * H + h; -1 for an inactive or out-of-range row.  The
+    // heads of a unit share b (H is even whenever a unit holds two heads).
+    auto state_head = [&](int bh0) -> int {
+        if (!slot) return bh0;
+        const int b = bh0 / H, sl = slot[b];
+        return sl >= 0 && sl < pool ? sl * H + (bh0 - b * H) : -1;
+    };
     auto issue = [&](int j) {   // unit j of this CTA -> stage j % nst (elected thread)
-        const int bh0 = (first + j * step) * HPU;
+        const int bh0 = (first + j * step) * HPU, sh0 = state_head(bh0);
         unsigned char *sg = sm + (size_t)(j % nst) * Lo.stage;
         uint64_t *bar = full + (j % nst);
+        if (sh0 < 0) {   // inactive row: the stage's phase completes with no bytes
+            mbar_expect_tx(bar, 0);
+            return;
+        }
         mbar_expect_tx(bar, hn + 3 * bn + 2 * xn);
-        tma_load_2d(sg, &hmap, 0, bh0 * N, bar);
-        tma_load_2d(sg + NR * 128, &hmap, 32, bh0 * N, bar);
+        tma_load_2d(sg, &hmap, 0, sh0 * N, bar);
+        tma_load_2d(sg + NR * 128, &hmap, 32, sh0 * N, bar);
         if (SWZ) {
 #pragma unroll
             for (int hf = 0; hf < N / 64; ++hf) {
                 tma_load_2d(sg + Lo.B + hf * Lo.half, &bmap, 64 * hf, bh0 * R, bar);
                 tma_load_2d(sg + Lo.C + hf * Lo.half, &cmap, 64 * hf, bh0 * R, bar);
-                tma_load_2d(sg + Lo.Bp + hf * Lo.half, &bpmap, 64 * hf, bh0 * R, bar);
+                tma_load_2d(sg + Lo.Bp + hf * Lo.half, &bpmap, 64 * hf, sh0 * R, bar);
             }
         } else {
             bulk_load(sg + Lo.B, Bm + (size_t)bh0 * R * N, bn, bar);
             bulk_load(sg + Lo.C, Cm + (size_t)bh0 * R * N, bn, bar);
-            bulk_load(sg + Lo.Bp, Bprev + (size_t)bh0 * R * N, bn, bar);
+            bulk_load(sg + Lo.Bp, Bprev + (size_t)sh0 * R * N, bn, bar);
         }
         bulk_load(sg + Lo.x, x + (size_t)bh0 * R * P, xn, bar);
-        bulk_load(sg + Lo.xp, xprev + (size_t)bh0 * R * P, xn, bar);
+        bulk_load(sg + Lo.xp, xprev + (size_t)sh0 * R * P, xn, bar);
     };
 
     if (tid == 0) {
@@ -620,99 +632,106 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap hmap, const __grid_constan
             *abort_flag = 1;
             break;
         }
-        const unsigned char *sB = sg + Lo.B, *sBp = sg + Lo.Bp, *sC = sg + Lo.C;
-        const unsigned short *sx = reinterpret_cast<const unsigned short *>(sg + Lo.x) + hh * R * P;
-        const unsigned short *sxp = reinterpret_cast<const unsigned short *>(sg + Lo.xp) + hh * R * P;
-        const float2 *hrot = rot + hh * K;
-        unsigned char *hst = sg + (uint32_t)(hh * N) * 128u;
-        const float left = (1.f - l) * d, right = l * d;
-
-        // A operands of the rank-R products: x^T rows p0 + g, p0 + g + 8, rank columns 2t, 2t + 1
-        uint32_t ax0 = 0, ax1 = 0, aq0 = 0, aq1 = 0;
-        if (rlane) {
-            const int r0 = 2 * t * P + p0 + g;
-            ax0 = sx[r0];
-            ax1 = sx[r0 + 8];
-            aq0 = sxp[r0];
-            aq1 = sxp[r0 + 8];
-            if (R > 1) {
-                ax0 |= (uint32_t)sx[r0 + P] << 16;
-                ax1 |= (uint32_t)sx[r0 + P + 8] << 16;
-                aq0 |= (uint32_t)sxp[r0 + P] << 16;
-                aq1 |= (uint32_t)sxp[r0 + P + 8] << 16;
-            }
-        }
+        const int sh0 = state_head(bh0);   // < 0: inactive row, nothing to read or write
+        if (tid == 0 && slot && sh0 < 0 && slot[bh0 / H] >= pool) atomicOr(status, kStatusBadIndex);
         float yacc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int ks = 0; ks < NKS; ++ks) {
-            uint32_t ahi[4], alo[4];
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                const int n0 = nb0 + 16 * ks + 8 * hf;
-                uint32_t bb = 0, bq = 0;   // B operands: rank rows 2t, 2t + 1 of state row n0 + g
-                if (rlane) {
-                    const int row = hh * R + 2 * t;
-                    const uint32_t o0 = rank_off<SWZ, N>(Lo.half, row, n0 + g), o1 = rank_off<SWZ, N>(Lo.half, row + 1, n0 + g);
-                    bb = *reinterpret_cast<const unsigned short *>(sB + o0);
-                    bq = *reinterpret_cast<const unsigned short *>(sBp + o0);
-                    if (R > 1) {
-                        bb |= (uint32_t)*reinterpret_cast<const unsigned short *>(sB + o1) << 16;
-                        bq |= (uint32_t)*reinterpret_cast<const unsigned short *>(sBp + o1) << 16;
-                    }
-                }
-                float u[4] = {0.f, 0.f, 0.f, 0.f}, v[4] = {0.f, 0.f, 0.f, 0.f};
-                mma_m16n8k8(u, aq0, aq1, bq);
-                mma_m16n8k8(v, ax0, ax1, bb);
-                const float2 rt = hrot[n0 / 2 + t];
-                unsigned char *rb = hst + (uint32_t)(n0 + 2 * t) * 128u;
-                float *q00 = reinterpret_cast<float *>(rb + o00), *q01 = reinterpret_cast<float *>(rb + o01);
-                float *q10 = reinterpret_cast<float *>(rb + o10), *q11 = reinterpret_cast<float *>(rb + o11);
-                float s0 = fmaf(left, u[0], *q00), s1 = fmaf(left, u[1], *q01);
-                const float n00 = fmaf(rt.x, s0, fmaf(-rt.y, s1, right * v[0]));
-                const float n01 = fmaf(rt.y, s0, fmaf(rt.x, s1, right * v[1]));
-                s0 = fmaf(left, u[2], *q10);
-                s1 = fmaf(left, u[3], *q11);
-                const float n10 = fmaf(rt.x, s0, fmaf(-rt.y, s1, right * v[2]));
-                const float n11 = fmaf(rt.y, s0, fmaf(rt.x, s1, right * v[3]));
-                *q00 = n00;
-                *q01 = n01;
-                *q10 = n10;
-                *q11 = n11;
-                split2(n00, n01, ahi[2 * hf], alo[2 * hf]);           // row p0 + g
-                split2(n10, n11, ahi[2 * hf + 1], alo[2 * hf + 1]);   // row p0 + g + 8
-            }
-            uint32_t b0 = 0, b1 = 0;   // C^T: state rows 2t, 2t + 1 (+ 8) of this K step, rank column g
-            if (g < R) {
-                const int row = hh * R + g, c0 = nb0 + 16 * ks + 2 * t;
-                b0 = *reinterpret_cast<const uint32_t *>(sC + rank_off<SWZ, N>(Lo.half, row, c0));
-                b1 = *reinterpret_cast<const uint32_t *>(sC + rank_off<SWZ, N>(Lo.half, row, c0 + 8));
-            }
-            mma_m16n8k16(yacc, ahi, b0, b1);
-            mma_m16n8k16(yacc, alo, b0, b1);
-        }
         // y[r][p] for r = 2t, 2t + 1 and p = p0 + g, p0 + g + 8
         float *yo = y + (size_t)(bh0 + hh) * R * P + 2 * t * P + p0 + g;
-        if (HPU == 2 && rlane) {
-            yo[0] = yacc[0];
-            yo[8] = yacc[2];
-            if (R > 1) {
-                yo[P] = yacc[1];
-                yo[P + 8] = yacc[3];
+        if (sh0 >= 0) {
+            const unsigned char *sB = sg + Lo.B, *sBp = sg + Lo.Bp, *sC = sg + Lo.C;
+            const unsigned short *sx = reinterpret_cast<const unsigned short *>(sg + Lo.x) + hh * R * P;
+            const unsigned short *sxp = reinterpret_cast<const unsigned short *>(sg + Lo.xp) + hh * R * P;
+            const float2 *hrot = rot + hh * K;
+            unsigned char *hst = sg + (uint32_t)(hh * N) * 128u;
+            const float left = (1.f - l) * d, right = l * d;
+
+            // A operands of the rank-R products: x^T rows p0 + g, p0 + g + 8, rank columns 2t, 2t + 1
+            uint32_t ax0 = 0, ax1 = 0, aq0 = 0, aq1 = 0;
+            if (rlane) {
+                const int r0 = 2 * t * P + p0 + g;
+                ax0 = sx[r0];
+                ax1 = sx[r0 + 8];
+                aq0 = sxp[r0];
+                aq1 = sxp[r0 + 8];
+                if (R > 1) {
+                    ax0 |= (uint32_t)sx[r0 + P] << 16;
+                    ax1 |= (uint32_t)sx[r0 + P + 8] << 16;
+                    aq0 |= (uint32_t)sxp[r0 + P] << 16;
+                    aq1 |= (uint32_t)sxp[r0 + P + 8] << 16;
+                }
             }
+#pragma unroll
+            for (int ks = 0; ks < NKS; ++ks) {
+                uint32_t ahi[4], alo[4];
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    const int n0 = nb0 + 16 * ks + 8 * hf;
+                    uint32_t bb = 0, bq = 0;   // B operands: rank rows 2t, 2t + 1 of state row n0 + g
+                    if (rlane) {
+                        const int row = hh * R + 2 * t;
+                        const uint32_t o0 = rank_off<SWZ, N>(Lo.half, row, n0 + g), o1 = rank_off<SWZ, N>(Lo.half, row + 1, n0 + g);
+                        bb = *reinterpret_cast<const unsigned short *>(sB + o0);
+                        bq = *reinterpret_cast<const unsigned short *>(sBp + o0);
+                        if (R > 1) {
+                            bb |= (uint32_t)*reinterpret_cast<const unsigned short *>(sB + o1) << 16;
+                            bq |= (uint32_t)*reinterpret_cast<const unsigned short *>(sBp + o1) << 16;
+                        }
+                    }
+                    float u[4] = {0.f, 0.f, 0.f, 0.f}, v[4] = {0.f, 0.f, 0.f, 0.f};
+                    mma_m16n8k8(u, aq0, aq1, bq);
+                    mma_m16n8k8(v, ax0, ax1, bb);
+                    const float2 rt = hrot[n0 / 2 + t];
+                    unsigned char *rb = hst + (uint32_t)(n0 + 2 * t) * 128u;
+                    float *q00 = reinterpret_cast<float *>(rb + o00), *q01 = reinterpret_cast<float *>(rb + o01);
+                    float *q10 = reinterpret_cast<float *>(rb + o10), *q11 = reinterpret_cast<float *>(rb + o11);
+                    float s0 = fmaf(left, u[0], *q00), s1 = fmaf(left, u[1], *q01);
+                    const float n00 = fmaf(rt.x, s0, fmaf(-rt.y, s1, right * v[0]));
+                    const float n01 = fmaf(rt.y, s0, fmaf(rt.x, s1, right * v[1]));
+                    s0 = fmaf(left, u[2], *q10);
+                    s1 = fmaf(left, u[3], *q11);
+                    const float n10 = fmaf(rt.x, s0, fmaf(-rt.y, s1, right * v[2]));
+                    const float n11 = fmaf(rt.y, s0, fmaf(rt.x, s1, right * v[3]));
+                    *q00 = n00;
+                    *q01 = n01;
+                    *q10 = n10;
+                    *q11 = n11;
+                    split2(n00, n01, ahi[2 * hf], alo[2 * hf]);           // row p0 + g
+                    split2(n10, n11, ahi[2 * hf + 1], alo[2 * hf + 1]);   // row p0 + g + 8
+                }
+                uint32_t b0 = 0, b1 = 0;   // C^T: state rows 2t, 2t + 1 (+ 8) of this K step, rank column g
+                if (g < R) {
+                    const int row = hh * R + g, c0 = nb0 + 16 * ks + 2 * t;
+                    b0 = *reinterpret_cast<const uint32_t *>(sC + rank_off<SWZ, N>(Lo.half, row, c0));
+                    b1 = *reinterpret_cast<const uint32_t *>(sC + rank_off<SWZ, N>(Lo.half, row, c0 + 8));
+                }
+                mma_m16n8k16(yacc, ahi, b0, b1);
+                mma_m16n8k16(yacc, alo, b0, b1);
+            }
+            if (HPU == 2 && rlane) {
+                yo[0] = yacc[0];
+                yo[8] = yacc[2];
+                if (R > 1) {
+                    yo[P] = yacc[1];
+                    yo[P + 8] = yacc[3];
+                }
+            }
+            if (HPU == 1 && grp == 0) red[pt * 32 + lane] = make_float4(yacc[0], yacc[1], yacc[2], yacc[3]);
         }
-        if (HPU == 1 && grp == 0) red[pt * 32 + lane] = make_float4(yacc[0], yacc[1], yacc[2], yacc[3]);
         fence_proxy_async();   // the state writes above feed the tensor stores below
         __syncthreads();
         if (tid == 0) {
-            tma_store_2d(&hmap, sg, 0, bh0 * N);
-            tma_store_2d(&hmap, sg + NR * 128, 32, bh0 * N);
-            if (SWZ) {   // new carry = this token's (B, x)
+            if (sh0 >= 0) {
+                tma_store_2d(&hmap, sg, 0, sh0 * N);
+                tma_store_2d(&hmap, sg + NR * 128, 32, sh0 * N);
+                if (SWZ) {   // new carry = this token's (B, x)
 #pragma unroll
-                for (int hf = 0; hf < N / 64; ++hf) tma_store_2d(&bpmap, sg + Lo.B + hf * Lo.half, 64 * hf, bh0 * R);
-            } else {
-                bulk_store(Bprev + (size_t)bh0 * R * N, sg + Lo.B, bn);
+                    for (int hf = 0; hf < N / 64; ++hf)
+                        tma_store_2d(&bpmap, sg + Lo.B + hf * Lo.half, 64 * hf, sh0 * R);
+                } else {
+                    bulk_store(Bprev + (size_t)sh0 * R * N, sg + Lo.B, bn);
+                }
+                bulk_store(xprev + (size_t)sh0 * R * P, sg + Lo.x, xn);
             }
-            bulk_store(xprev + (size_t)bh0 * R * P, sg + Lo.x, xn);
             bulk_commit();
             if (issued < mine) {
                 bulk_wait_read<1>();   // the stage about to be refilled has been written out
@@ -720,7 +739,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap hmap, const __grid_constan
                 ++issued;
             }
         }
-        if (HPU == 1 && grp == 1 && rlane) {
+        if (sh0 >= 0 && HPU == 1 && grp == 1 && rlane) {
             const float4 o = red[pt * 32 + lane];
             yo[0] = yacc[0] + o.x;
             yo[8] = yacc[2] + o.z;
@@ -767,10 +786,12 @@ bool map_state(CUtensorMap *m, float *h, long long rows, int box_rows) {
 }
 
 template <int R, int N, int HPU>
-cudaError_t launch_mma(int nbh, const void *x, const void *B, const void *C, const void *dt, const void *A,
-                       const void *lam, const void *theta, float *h, void *Bprev, void *xprev, void *y,
-                       cudaStream_t s) {
+// nbh: token heads (batch * H); with a slot table the state arrays hold pool_heads heads
+cudaError_t launch_mma(int nbh, int H, const int *slot, int pool, const void *x, const void *B, const void *C,
+                       const void *dt, const void *A, const void *lam, const void *theta, float *h, void *Bprev,
+                       void *xprev, void *y, cudaStream_t s) {
     constexpr bool kSwz = (HPU * R) % 8 == 0;
+    const long long pool_heads = slot ? (long long)pool * H : (long long)nbh;
     // the state and carry maps depend only on (h, B_prev, shape); a decode loop reuses one state
     struct MapCache {
         const float *h = nullptr;
@@ -780,11 +801,11 @@ cudaError_t launch_mma(int nbh, const void *x, const void *B, const void *C, con
         CUtensorMap hmap, bpmap;
     };
     thread_local MapCache cache;
-    const long long rows = (long long)nbh * N;
+    const long long rows = pool_heads * N;
     if (cache.h != h || cache.bp != Bprev || cache.rows != rows || cache.n != N || cache.r != R || cache.hpu != HPU) {
         cache.h = nullptr;
         if (!map_state(&cache.hmap, h, rows, HPU * N)) return cudaErrorInvalidValue;
-        if (kSwz && !map_rank(&cache.bpmap, Bprev, (long long)nbh * R, N, HPU * R)) return cudaErrorInvalidValue;
+        if (kSwz && !map_rank(&cache.bpmap, Bprev, pool_heads * R, N, HPU * R)) return cudaErrorInvalidValue;
         cache.h = h;
         cache.bp = Bprev;
         cache.rows = rows;
@@ -816,9 +837,10 @@ cudaError_t launch_mma(int nbh, const void *x, const void *B, const void *C, con
     const int grid = nunit < per_sm * sm_count() ? nunit : per_sm * sm_count();
     using bf = __nv_bfloat16;
     trace_mark(M3_KERNEL_DECODE, s, 0);
-    kern<<<grid, kMmaThreads, Lo.total, s>>>(cache.hmap, bmap, cmap, cache.bpmap, nunit, nst, (const bf *)x, (const bf *)B, (const bf *)C,
-                                            (const bf *)dt, (const bf *)A, (const bf *)lam, (const bf *)theta,
-                                            (bf *)Bprev, (bf *)xprev, (float *)y, status);
+    kern<<<grid, kMmaThreads, Lo.total, s>>>(cache.hmap, bmap, cmap, cache.bpmap, nunit, nst, slot, pool, H,
+                                            (const bf *)x, (const bf *)B, (const bf *)C, (const bf *)dt,
+                                            (const bf *)A, (const bf *)lam, (const bf *)theta, (bf *)Bprev,
+                                            (bf *)xprev, (float *)y, status);
     trace_mark(M3_KERNEL_DECODE, s, 1);
     count_launch();
     return cudaGetLastError();
@@ -833,14 +855,15 @@ bool mma_ok(int dtype, int P, int N, int R, long long nbh) {
            nbh * N < (1ll << 31);
 }
 
-// N = 64 pairs adjacent heads into one unit when the head count is even.
-cudaError_t mma_dispatch(int nbh, int N, int R, const void *x, const void *B, const void *C, const void *dt,
-                         const void *A, const void *lam, const void *theta, float *h, void *Bprev, void *xprev,
-                         void *y, cudaStream_t s) {
-    const bool pair = N == 64 && nbh % 2 == 0;
+// N = 64 pairs adjacent heads into one unit when the head count is even (with a slot table:
+// when H is even, so that the two heads share a batch row and thus a pool slot).
+cudaError_t mma_dispatch(int nbh, int H, const int *slot, int pool, int N, int R, const void *x, const void *B,
+                         const void *C, const void *dt, const void *A, const void *lam, const void *theta, float *h,
+                         void *Bprev, void *xprev, void *y, cudaStream_t s) {
+    const bool pair = N == 64 && (slot ? H % 2 == 0 : nbh % 2 == 0);
 #define M3_MMA(RR, NN, HH)                                                                                         \
     if (R == RR && N == NN && (HH == 2) == pair)                                                                 \
-    return launch_mma<RR, NN, HH>(nbh, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, s)
+    return launch_mma<RR, NN, HH>(nbh, H, slot, pool, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, s)
     M3_MMA(1, 64, 2);
     M3_MMA(2, 64, 2);
     M3_MMA(4, 64, 2);
@@ -868,7 +891,7 @@ cudaError_t decode_step(int dtype, int batch, int H, int P, int N, int R, const 
     const int nbh = batch * H;
     if (nbh > 0 && stream_ok(e, P, N, R, ptrs, 7)) {
         if (mma_ok(dtype, P, N, R, nbh))
-            return mma_dispatch(nbh, N, R, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, s);
+            return mma_dispatch(nbh, H, nullptr, batch, N, R, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, s);
         if (dtype == M3_F32)
             return stream_dispatch<float>(nbh, P, N, R, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, s);
         return stream_dispatch<__nv_bfloat16>(nbh, P, N, R, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, s);
@@ -877,6 +900,18 @@ cudaError_t decode_step(int dtype, int batch, int H, int P, int N, int R, const 
         return launch_decode<float>(batch, H, P, N, R, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, s);
     return launch_decode<__nv_bfloat16>(batch, H, P, N, R, x, B, C, dt, A, lam, theta, h, Bprev,
                                         xprev, y, s);
+}
+
+bool decode_pooled_ok(int dtype, int batch, int H, int P, int N, int R, int pool, const void *const *ptrs, int nptr) {
+    return mma_ok(dtype, P, N, R, (long long)(batch > pool ? batch : pool) * H) && stream_ok(2, P, N, R, ptrs, nptr);
+}
+
+cudaError_t decode_step_pooled(int batch, int H, int P, int N, int R, const int *slot, int pool, const void *x,
+                               const void *B, const void *C, const void *dt, const void *A, const void *lam,
+                               const void *theta, float *h, void *Bprev, void *xprev, void *y, cudaStream_t s) {
+    (void)P;
+    if (batch == 0) return cudaSuccess;
+    return mma_dispatch(batch * H, H, slot, pool, N, R, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, s);
 }
 
 }  // namespace m3

@@ -20,7 +20,7 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float
 }
 
 // Device status word bits (read and cleared by mamba3_device_status).
-enum : unsigned { kStatusTimeout = 1u };
+enum : unsigned { kStatusTimeout = 1u, kStatusBadIndex = 2u };
 
 // ---------------------------------------------------------------- launch plumbing
 void count_launch();                 // +1 to the library's launch counter
@@ -101,5 +101,10 @@ cudaError_t decode_step(int dtype, int batch, int H, int P, int N, int R, const 
                         const void *B, const void *C, const void *dt, const void *A,
                         const void *lam, const void *theta, float *h, void *Bprev, void *xprev,
                         void *y, cudaStream_t s);
+// Pooled decode (slot table on the device): supported shapes and the launch.
+bool decode_pooled_ok(int dtype, int batch, int H, int P, int N, int R, int pool, const void *const *ptrs, int nptr);
+cudaError_t decode_step_pooled(int batch, int H, int P, int N, int R, const int *slot, int pool, const void *x,
+                               const void *B, const void *C, const void *dt, const void *A, const void *lam,
+                               const void *theta, float *h, void *Bprev, void *xprev, void *y, cudaStream_t s);
 
 }  // namespace m3

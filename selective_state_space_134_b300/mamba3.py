@@ -17,7 +17,7 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libmamba3.so")
 
-M3_OK, M3_ERR_INVALID_ARG, M3_ERR_UNSUPPORTED, M3_ERR_WORKSPACE, M3_ERR_CUDA, M3_ERR_TIMEOUT = range(6)
+M3_OK, M3_ERR_INVALID_ARG, M3_ERR_UNSUPPORTED, M3_ERR_WORKSPACE, M3_ERR_CUDA, M3_ERR_TIMEOUT, M3_ERR_INDEX = range(7)
 M3_F32, M3_BF16 = 0, 1
 _DTYPE_CODE = {torch.float32: M3_F32, torch.bfloat16: M3_BF16}
 
@@ -60,6 +60,8 @@ def lib() -> ctypes.CDLL:
         L.mamba3_scan_fwd.restype = ctypes.c_int
         L.mamba3_decode_step.argtypes = [dp] + [vp] * 7 + [sp, vp, vp]
         L.mamba3_decode_step.restype = ctypes.c_int
+        L.mamba3_decode_step_pooled.argtypes = [dp] + [vp] * 8 + [sp, ctypes.c_int, vp, vp]
+        L.mamba3_decode_step_pooled.restype = ctypes.c_int
         L.mamba3_device_status.argtypes = [vp]
         L.mamba3_device_status.restype = ctypes.c_int
         L.mamba3_status_string.argtypes = [ctypes.c_int]
@@ -182,6 +184,28 @@ def decode_step(x, B, C, dt, A, lam, theta, state: State, y: Optional[torch.Tens
     return y
 
 
+def decode_step_pooled(x, B, C, dt, A, lam, theta, slot: torch.Tensor, pool: State,
+                       y: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """mamba3_decode_step_pooled: one token per batch row, states in a pool.
+
+    slot [b] int32 on the device: pool slot of each row (< 0: inactive row, left untouched).
+    pool: State with h [S,H,N,P], B_prev [S,H,R,N], x_prev [S,H,R,P], updated in place.
+    Returns y [b,H,R,P] (fp32; rows of inactive slots keep what ``y`` held).
+    """
+    b, H, R, P = x.shape
+    N = B.shape[-1]
+    if slot.dtype != torch.int32:
+        raise ValueError("slot must be int32")
+    d = dims(b, 1, H, P, N, R, x.dtype)
+    if y is None:
+        y = torch.zeros(x.shape, dtype=torch.float32, device=x.device)
+    rc = lib().mamba3_decode_step_pooled(ctypes.byref(d), _ptr(slot), _ptr(x), _ptr(B), _ptr(C), _ptr(dt),
+                                         _ptr(A), _ptr(lam), _ptr(theta), ctypes.byref(pool.c()),
+                                         int(pool.h.shape[0]), _ptr(y), _stream_ptr(stream))
+    _check(rc, "mamba3_decode_step_pooled")
+    return y
+
+
 KERNEL_PREFILL_STATE, KERNEL_SEGMENT_PASS, KERNEL_PREFILL_OUTPUT, KERNEL_DECODE = range(4)
 
 
@@ -198,7 +222,8 @@ def trace_end():
 
 
 def device_status(stream=None) -> int:
-    """Synchronises the stream and returns (and clears) the device status (M3_OK or M3_ERR_TIMEOUT)."""
+    """Synchronises the stream and returns (and clears) the device status (M3_OK, M3_ERR_TIMEOUT or
+    M3_ERR_INDEX)."""
     return int(lib().mamba3_device_status(_stream_ptr(stream)))
 
 

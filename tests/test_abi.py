@@ -138,6 +138,33 @@ def test_decode_rejects_bad_arguments_before_launch():
     assert m3.launch_count() == before
 
 
+def test_pooled_decode_rejects_bad_arguments_before_launch():
+    ptrs = Ptrs()
+    lib = m3.lib()
+    before = m3.launch_count()
+    d = m3.dims(2, 1, 2, 64, 64, 4, torch.bfloat16)
+    good = {k: ptrs.get() for k in ("slot", "x", "B", "C", "dt", "A", "lam", "theta", "y")}
+
+    def call(over=None, pool="good", size=8, dd=d):
+        a = dict(good)
+        a.update(over or {})
+        st = api.m3_state(ptrs.get(), ptrs.get(), ptrs.get()) if pool == "good" else pool
+        return lib.mamba3_decode_step_pooled(ctypes.byref(dd), a["slot"], a["x"], a["B"], a["C"], a["dt"], a["A"],
+                                             a["lam"], a["theta"], ctypes.byref(st) if st is not None else None,
+                                             size, a["y"], None)
+
+    assert call(pool=None) == api.M3_ERR_INVALID_ARG
+    assert call(size=0) == api.M3_ERR_INVALID_ARG
+    assert call(pool=api.m3_state(ptrs.get(), None, ptrs.get())) == api.M3_ERR_INVALID_ARG
+    for k in good:
+        assert call({k: None}) == api.M3_ERR_INVALID_ARG, k
+    # shapes outside the tensor-core decode: fp32 inputs, P = 32
+    assert call(dd=m3.dims(2, 1, 2, 64, 64, 4, torch.float32)) == api.M3_ERR_UNSUPPORTED
+    assert call(dd=m3.dims(2, 1, 2, 32, 64, 4, torch.bfloat16)) == api.M3_ERR_UNSUPPORTED
+    assert m3.launch_count() == before
+    assert m3.status_string(api.M3_ERR_INDEX) == "pooled decode slot index outside the pool"
+
+
 def test_staged_prefill_rejects_bad_arguments_before_any_copy():
     lib = m3.lib()
     d = m3.dims(2, 16, 2, 64, 64, 1, torch.bfloat16)

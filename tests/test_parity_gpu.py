@@ -148,6 +148,53 @@ def test_decode_tensor_core_ranks_match_oracle(R, N, H):
         np.testing.assert_array_equal(to_f64(state.x_prev), ref_x)
 
 
+@pytest.mark.parametrize("N,R,H", [(64, 4, 8), (64, 1, 8), (128, 4, 8), (64, 8, 5)])
+def test_decode_pooled_matches_oracle(N, R, H):
+    # six batch rows on a pool of 11 states: active rows name distinct slots, two rows are
+    # inactive (-1); H = 8 pairs adjacent heads for N = 64, H = 5 keeps one head per unit
+    S = 11
+    slots = [7, -1, 0, 10, 3, -1]
+    w = WORKLOADS["decode_n64_r4"].with_(batch=len(slots), nheads=H, N=N, R=R)
+    ps = decode_state(w.with_(batch=S), "cuda")
+    pool = m3.State(ps["h"].clone(), ps["B_prev"].clone(), ps["x_prev"].clone())
+    tok = decode_pool(w, "cuda", pool=1)[0]
+    slot = torch.tensor(slots, dtype=torch.int32, device="cuda")
+    y = torch.full((w.batch, H, R, w.P), 12345.0, device="cuda")
+    m3.decode_step_pooled(*(tok[k] for k in KEYS), slot=slot, pool=pool, y=y)
+    assert m3.device_status() == m3.M3_OK
+    for b, sl in enumerate(slots):
+        if sl < 0:
+            assert bool((y[b] == 12345.0).all()), b          # inactive row: y untouched
+            continue
+        one = {k: to_f64(tok[k][b:b + 1]) for k in KEYS}
+        yr, hr, Br, xr = oracle.decode_step(*(one[k] for k in KEYS), to_f64(ps["h"][sl:sl + 1]),
+                                            to_f64(ps["B_prev"][sl:sl + 1]), to_f64(ps["x_prev"][sl:sl + 1]))
+        assert norm_err(to_f64(y[b:b + 1]), yr) <= 1e-4, b
+        assert norm_err(to_f64(pool.h[sl:sl + 1]), hr) <= 1e-5, b
+        np.testing.assert_array_equal(to_f64(pool.B_prev[sl:sl + 1]), Br)
+        np.testing.assert_array_equal(to_f64(pool.x_prev[sl:sl + 1]), xr)
+    for sl in set(range(S)) - set(slots):                          # slots no row names: bitwise unchanged
+        assert torch.equal(pool.h[sl], ps["h"][sl]) and torch.equal(pool.B_prev[sl], ps["B_prev"][sl])
+        assert torch.equal(pool.x_prev[sl], ps["x_prev"][sl])
+
+
+def test_decode_pooled_slot_outside_pool_is_reported_and_skipped():
+    # the kernel checks every slot against the pool size before touching the pool
+    S = 4
+    w = WORKLOADS["decode_n64_r4"].with_(batch=3, nheads=4, N=64, R=4)
+    ps = decode_state(w.with_(batch=S), "cuda")
+    pool = m3.State(ps["h"].clone(), ps["B_prev"].clone(), ps["x_prev"].clone())
+    tok = decode_pool(w, "cuda", pool=1)[0]
+    slot = torch.tensor([2, S, 0], dtype=torch.int32, device="cuda")
+    y = torch.full((3, 4, 4, 64), -7.0, device="cuda")
+    m3.decode_step_pooled(*(tok[k] for k in KEYS), slot=slot, pool=pool, y=y)
+    assert m3.device_status() == m3.M3_ERR_INDEX
+    assert m3.device_status() == m3.M3_OK                          # read and cleared
+    assert bool((y[1] == -7.0).all())
+    assert torch.equal(pool.h[1], ps["h"][1]) and torch.equal(pool.h[3], ps["h"][3])
+    assert not torch.equal(pool.h[2], ps["h"][2])                  # the valid rows ran
+
+
 def test_decode_f32_tight():
     w = WORKLOADS["tiny_f32"].with_(batch=3, nheads=5, N=32, P=16, R=2)
     st = decode_state(w, "cuda")
