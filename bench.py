@@ -255,6 +255,33 @@ def time_decode(m3, w, calls, warmup):
     return e0.elapsed_time(e1) / calls, tr_ms / max(n_tr, 1)
 
 
+def time_decode_pooled(m3, w, calls, warmup, pool_factor=2):
+    """The decode step on states kept in a pool of pool_factor x batch slots: the batch rows name a
+    seeded random set of distinct slots (serving with a state pool)."""
+    from selective_state_space_134_b300.synth import decode_pool, decode_state
+    S = pool_factor * w.batch
+    ps = decode_state(w.with_(batch=S), "cuda")
+    pool = m3.State(ps["h"], ps["B_prev"], ps["x_prev"])
+    g = torch.Generator().manual_seed(1234)
+    slot = torch.randperm(S, generator=g)[: w.batch].to(torch.int32).to("cuda")
+    toks = decode_pool(w, "cuda")
+    ys = [torch.empty(p["x"].shape, dtype=torch.float32, device="cuda") for p in toks]
+    argsets = [[p[k] for k in KEYS] for p in toks]
+    for i in range(warmup):
+        m3.decode_step_pooled(*argsets[i % len(toks)], slot=slot, pool=pool, y=ys[i % len(toks)])
+    torch.cuda.synchronize()
+    m3.trace_begin(m3.KERNEL_DECODE, calls)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(calls):
+        m3.decode_step_pooled(*argsets[i % len(toks)], slot=slot, pool=pool, y=ys[i % len(toks)])
+    e1.record()
+    torch.cuda.synchronize()
+    n_tr, tr_ms = m3.trace_end()
+    assert m3.device_status() == m3.M3_OK
+    return e0.elapsed_time(e1) / calls, tr_ms / max(n_tr, 1)
+
+
 def e2e_prefill(m3, w, inp, steps, warmup, slices=16):
     """Same metric through host buffers, via the library's staged prefill: every step copies the
     inputs in from pinned host memory and y and the final state h back out, the copies of each
@@ -447,7 +474,8 @@ def run_reference(args):
 
 
 def decode_results(m3, hbm_peak, calls=1024, warmup=16):
-    """The four decode workloads: tokens/s, us per call and the kernel's HBM roofline."""
+    """The four decode workloads (and N=64 R=4 on a state pool): tokens/s, us per call and the
+    kernel's HBM roofline."""
     from selective_state_space_134_b300.synth import WORKLOADS
     dec = {}
     for name in ("decode_n64_r1", "decode_n64_r4", "decode_n128_r1", "decode_n128_r4"):
@@ -459,6 +487,16 @@ def decode_results(m3, hbm_peak, calls=1024, warmup=16):
                                   "frac": round(gbs / hbm_peak, 4),
                                   "traffic": traffic_for("decode", name),
                                   "algorithmic_bytes": decode_bytes(wd), "kernel_ms": k_ms}}
+    # the same step on a state pool (2 x batch slots, rows on a random set of distinct slots)
+    wd = WORKLOADS["decode_n64_r4"]
+    ms_call, k_ms = time_decode_pooled(m3, wd, calls, warmup)
+    gbs = decode_bytes(wd) / (k_ms * 1e-3) / 1e9
+    dec["decode_n64_r4_pooled"] = {
+        "tokens_per_s": wd.batch / (ms_call * 1e-3), "us_per_call": round(ms_call * 1e3, 2),
+        "pool_slots": 2 * wd.batch,
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(gbs / hbm_peak, 4), "traffic": None,
+                     "algorithmic_bytes": decode_bytes(wd), "kernel_ms": k_ms}}
     return dec
 
 

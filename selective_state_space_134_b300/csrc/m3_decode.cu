@@ -18,7 +18,9 @@
 // common ones and stage whole heads in shared memory with asynchronous bulk
 // copies: a streaming FMA kernel (fp32 or bf16 inputs, P in {32, 64, 128}) and
 // a tensor-core kernel (bf16 inputs, P = 64, N in {64, 128}) that runs the
-// rank-R products and the readout on warp-level MMAs.
+// rank-R products and the readout on warp-level MMAs.  The tensor-core kernel
+// also serves the pooled step, whose states live in a caller-owned pool
+// indexed by a per-row slot table.
 #include "m3_internal.cuh"
 #include "m3_tc.cuh"
 
