@@ -510,7 +510,8 @@ __device__ __forceinline__ uint32_t rank_off(uint32_t half, int row, int col) {
     return ((uint32_t)col >> 6) * half + r * 128u + ((((c >> 3) ^ r) & 7u) << 4) + ((c & 7u) << 1);
 }
 
-template <int R, int N, int HPU>
+// POOL: the state rows come from a slot table (pooled decode); otherwise row bh is state bh.
+template <int R, int N, int HPU, bool POOL>
 __global__ void __launch_bounds__(kMmaThreads, 2)
 decode_mma_kernel(const __grid_constant__ CUtensorMap hmap, const __grid_constant__ CUtensorMap bmap,
                   const __grid_constant__ CUtensorMap cmap, const __grid_constant__ CUtensorMap bpmap, int nunit,
@@ -546,7 +547,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap hmap, const __grid_constan
     // table (pooled decode), slot[b] * H + h; -1 for an inactive or out-of-range row.  The
     // heads of a unit share b (H is even whenever a unit holds two heads).
     auto state_head = [&](int bh0) -> int {
-        if (!slot) return bh0;
+        if (!POOL) return bh0;
         const int b = bh0 / H, sl = slot[b];
         return sl >= 0 && sl < pool ? sl * H + (bh0 - b * H) : -1;
     };
@@ -635,7 +636,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap hmap, const __grid_constan
             break;
         }
         const int sh0 = state_head(bh0);   // < 0: inactive row, nothing to read or write
-        if (tid == 0 && slot && sh0 < 0 && slot[bh0 / H] >= pool) atomicOr(status, kStatusBadIndex);
+        if (POOL && tid == 0 && sh0 < 0 && slot[bh0 / H] >= pool) atomicOr(status, kStatusBadIndex);
         float yacc[4] = {0.f, 0.f, 0.f, 0.f};
         // y[r][p] for r = 2t, 2t + 1 and p = p0 + g, p0 + g + 8
         float *yo = y + (size_t)(bh0 + hh) * R * P + 2 * t * P + p0 + g;
@@ -832,8 +833,9 @@ cudaError_t launch_mma(int nbh, int H, const int *slot, int pool, const void *x,
     if (Lo.total > 224u * 1024u) return cudaErrorInvalidValue;
     unsigned *status = device_status_word();
     if (!status) return cudaErrorUnknown;
-    auto kern = decode_mma_kernel<R, N, HPU>;
-    cudaError_t err = allow_dynamic_smem<decode_mma_kernel<R, N, HPU>>(Lo.total);
+    auto kern = slot ? decode_mma_kernel<R, N, HPU, true> : decode_mma_kernel<R, N, HPU, false>;
+    cudaError_t err = slot ? allow_dynamic_smem<decode_mma_kernel<R, N, HPU, true>>(Lo.total)
+                           : allow_dynamic_smem<decode_mma_kernel<R, N, HPU, false>>(Lo.total);
     if (err != cudaSuccess) return err;
     const int nunit = nbh / HPU;
     const int grid = nunit < per_sm * sm_count() ? nunit : per_sm * sm_count();
