@@ -495,7 +495,7 @@ def decode_results(m3, hbm_peak, calls=1024, warmup=16):
         "tokens_per_s": wd.batch / (ms_call * 1e-3), "us_per_call": round(ms_call * 1e3, 2),
         "pool_slots": 2 * wd.batch,
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s",
-                     "frac": round(gbs / hbm_peak, 4), "traffic": None,
+                     "frac": round(gbs / hbm_peak, 4), "traffic": traffic_for("decode", "decode_n64_r4_pooled"),
                      "algorithmic_bytes": decode_bytes(wd), "kernel_ms": k_ms}}
     return dec
 
