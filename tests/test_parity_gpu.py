@@ -96,6 +96,33 @@ def test_scan_full_size_sampled(wname):
     assert torch.isfinite(y.float()).all()
 
 
+def _random_shapes(n, seed=2026):
+    import random
+    rng = random.Random(seed)
+    out = []
+    for _ in range(n):
+        N, R = rng.choice([64, 128]), rng.choice([1, 2, 4, 8])
+        H, b = rng.randint(1, 40), rng.randint(1, 2)
+        L = rng.randint(1, 1400)
+        out.append((N, R, H, b, L, rng.random() < 0.5))
+    return out
+
+
+@pytest.mark.parametrize("N,R,H,b,L,with_state", _random_shapes(8))
+def test_prefill_random_shapes_match_oracle(N, R, H, b, L, with_state):
+    # seeded shapes over the planner's cases: one or several segments, state-pass pieces,
+    # ragged last chunks and segments, every rank; all sequences against the oracle
+    w = WORKLOADS["mimo_r4"].with_(batch=b, nheads=H, seqlen=L, N=N, R=R)
+    inp = prefill_inputs(w, "cuda")
+    st = random_state(b, H, w.P, N, R, inp["x"].dtype, seed=L) if with_state else None
+    y, so = gpu_scan(inp, state_in=st)
+    yr, hr, Br, xr = oracle_full(inp, st)
+    assert norm_err(to_f64(y), yr) <= TOL[w.dtype]
+    assert norm_err(to_f64(so.h), hr) <= TOL[w.dtype]
+    np.testing.assert_array_equal(to_f64(so.B_prev), Br)
+    np.testing.assert_array_equal(to_f64(so.x_prev), xr)
+
+
 @pytest.mark.parametrize("with_state", [False, True])
 def test_segmented_prefill_with_state_pass_pieces(with_state):
     # 64 sequences, L = 1000, N = 128, R = 4 (16-token chunks): two segments of 512 tokens
