@@ -70,7 +70,15 @@ typedef enum { M3_F32 = 0, M3_BF16 = 1 } m3_dtype;
 
 /* Problem sizes.  P = head dim, N = real state size (N/2 complex pairs),
  * R = MIMO rank.  chunk = tokens per chunk of the prefill kernels, 0 = the
- * library's choice; the result does not depend on it beyond rounding. */
+ * library's choice; the result does not depend on it beyond rounding.
+ * ngroups = G: B and C are shared by groups of H / G consecutive heads
+ * (head h reads group h / (H / G)), so their per-token blocks are [G][R][N]
+ * instead of [H][R][N]; 0 (or H) = one B and C per head.  G must divide H
+ * (else M3_ERR_INVALID_ARG).  Grouped B and C are a layout of the inputs, not
+ * a change of the recurrence, and are not from the Mamba-3 pages.  They are
+ * supported on the tensor-core paths only (bf16 inputs, P = 64, N in
+ * {64, 128}, 16-byte-aligned pointers); elsewhere M3_ERR_UNSUPPORTED.  The
+ * state's carry stays per head. */
 typedef struct {
     int batch;
     int seqlen;      /* L; ignored by mamba3_decode_step */
@@ -80,6 +88,7 @@ typedef struct {
     int rank;        /* R */
     int chunk;
     int dtype;       /* m3_dtype */
+    int ngroups;     /* G, 0 = H */
 } m3_dims;
 
 /* Recurrent state of every (batch, head): the checkpoint between calls.

@@ -98,8 +98,12 @@ m3_status check_dims(const m3_dims *d, bool prefill) {
     if (d->headdim < 1 || d->headdim > 128 || (d->headdim % 4) != 0) return M3_ERR_UNSUPPORTED;
     if (d->dstate < 2 || d->dstate > 256 || (d->dstate % 2) != 0) return M3_ERR_UNSUPPORTED;
     if (d->rank < 1 || d->rank > 8) return M3_ERR_UNSUPPORTED;
+    if (d->ngroups < 0 || (d->ngroups > 0 && d->nheads % d->ngroups != 0)) return M3_ERR_INVALID_ARG;
     return M3_OK;
 }
+
+// B / C groups of a problem (ngroups = 0 means one per head)
+int groups_of(const m3_dims &d) { return d.ngroups > 0 ? d.ngroups : d.nheads; }
 
 // Per-token inputs, y and the carry need only element alignment; the fp32
 // state and the workspace are read as float4 and need 16 bytes.
@@ -166,6 +170,7 @@ m3_status mamba3_scan_fwd(const m3_dims *dims, const void *x, const void *B, con
     bool use_tc = has_tc;
     for (const void *p : {x, B, C, theta, (const void *)y})
         if (!aligned16(p)) use_tc = false;
+    if (!use_tc && groups_of(d) != d.nheads) return M3_ERR_UNSUPPORTED;   // grouped B / C: tensor cores only
     if (!use_tc && simt.path < 0) return M3_ERR_UNSUPPORTED;
     const ScanPlan &pl = use_tc ? tc : simt;
 
@@ -197,7 +202,7 @@ m3_status mamba3_scan_fwd(const m3_dims *dims, const void *x, const void *B, con
         return M3_ERR_WORKSPACE;
 
     ScanArgs a{};
-    a.dtype = d.dtype; a.batch = d.batch; a.L = d.seqlen; a.H = d.nheads;
+    a.dtype = d.dtype; a.batch = d.batch; a.L = d.seqlen; a.H = d.nheads; a.G = groups_of(d);
     a.P = d.headdim; a.N = d.dstate; a.R = d.rank;
     a.x = x; a.B = B; a.C = C; a.dt = dt; a.A = A; a.lam = lambda; a.theta = theta;
     a.h0 = state_in ? state_in->h : nullptr;
@@ -268,7 +273,8 @@ m3_status mamba3_scan_fwd_staged(const m3_dims *dims, const m3_token_inputs *hos
     const size_t H = (size_t)d.nheads, P = (size_t)d.headdim, N = (size_t)d.dstate, R = (size_t)d.rank;
     const size_t nb = (size_t)d.batch;
     // bytes per token (all heads) of every tensor
-    const size_t tx = H * R * P * es, tB = H * R * N * es, ts = H * es, tth = H * (N / 2) * es, ty = H * R * P * 4;
+    const size_t G = (size_t)groups_of(d);
+    const size_t tx = H * R * P * es, tB = G * R * N * es, ts = H * es, tth = H * (N / 2) * es, ty = H * R * P * 4;
     const cudaStream_t s = static_cast<cudaStream_t>(stream), cs = static_cast<cudaStream_t>(copy_stream);
     // the previous call's copies out read buffers this call rewrites: start after them
     {
@@ -343,7 +349,13 @@ m3_status mamba3_decode_step(const m3_dims *dims, const void *x, const void *B, 
         if (!ptr_ok(p, es)) return M3_ERR_INVALID_ARG;
     if (!ptr_ok(y, 4)) return M3_ERR_INVALID_ARG;
     if (!ptr_ok(state->h, 16)) return M3_ERR_INVALID_ARG;
-    cudaError_t e = decode_step(d.dtype, d.batch, d.nheads, d.headdim, d.dstate, d.rank, x, B, C, dt,
+    const int G = groups_of(d);
+    if (G != d.nheads) {
+        const void *ptrs[] = {x, B, C, theta, state->h, state->B_prev, state->x_prev};
+        if (!decode_tc_ok(d.dtype, d.headdim, d.dstate, d.rank, (long long)d.batch * d.nheads, ptrs, 7))
+            return M3_ERR_UNSUPPORTED;
+    }
+    cudaError_t e = decode_step(d.dtype, d.batch, d.nheads, G, d.headdim, d.dstate, d.rank, x, B, C, dt,
                                 A, lambda, theta, state->h, state->B_prev, state->x_prev, y,
                                 static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? M3_OK : M3_ERR_CUDA;
@@ -364,11 +376,11 @@ m3_status mamba3_decode_step_pooled(const m3_dims *dims, const int *slot, const 
     if (!ptr_ok(y, 4)) return M3_ERR_INVALID_ARG;
     if (!ptr_ok(pool->h, 16)) return M3_ERR_INVALID_ARG;
     const void *ptrs[] = {x, B, C, theta, pool->h, pool->B_prev, pool->x_prev};
-    if (!decode_pooled_ok(d.dtype, d.batch, d.nheads, d.headdim, d.dstate, d.rank, pool_size, ptrs, 7))
-        return M3_ERR_UNSUPPORTED;
-    cudaError_t e = decode_step_pooled(d.batch, d.nheads, d.headdim, d.dstate, d.rank, slot, pool_size, x, B, C,
-                                       dt, A, lambda, theta, pool->h, pool->B_prev, pool->x_prev, y,
-                                       static_cast<cudaStream_t>(stream));
+    const long long heads = (long long)(d.batch > pool_size ? d.batch : pool_size) * d.nheads;
+    if (!decode_tc_ok(d.dtype, d.headdim, d.dstate, d.rank, heads, ptrs, 7)) return M3_ERR_UNSUPPORTED;
+    cudaError_t e = decode_step_pooled(d.batch, d.nheads, groups_of(d), d.headdim, d.dstate, d.rank, slot,
+                                       pool_size, x, B, C, dt, A, lambda, theta, pool->h, pool->B_prev,
+                                       pool->x_prev, y, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? M3_OK : M3_ERR_CUDA;
 }
 

@@ -511,11 +511,13 @@ __device__ __forceinline__ uint32_t rank_off(uint32_t half, int row, int col) {
 }
 
 // POOL: the state rows come from a slot table (pooled decode); otherwise row bh is state bh.
-template <int R, int N, int HPU, bool POOL>
+// SWZ: B, C, B_prev through swizzled TMA tiles (a unit of 8k rank rows, one B / C per head).
+template <int R, int N, int HPU, bool POOL, bool SWZ>
 __global__ void __launch_bounds__(kMmaThreads, 2)
 decode_mma_kernel(const __grid_constant__ CUtensorMap hmap, const __grid_constant__ CUtensorMap bmap,
                   const __grid_constant__ CUtensorMap cmap, const __grid_constant__ CUtensorMap bpmap, int nunit,
-                  int nst, const int *__restrict__ slot, int pool, int H, const __nv_bfloat16 *__restrict__ x,
+                  int nst, const int *__restrict__ slot, int pool, int H, int G,
+                  const __nv_bfloat16 *__restrict__ x,
                   const __nv_bfloat16 *__restrict__ Bm, const __nv_bfloat16 *__restrict__ Cm,
                   const __nv_bfloat16 *__restrict__ dtp, const __nv_bfloat16 *__restrict__ Ap,
                   const __nv_bfloat16 *__restrict__ lp, const __nv_bfloat16 *__restrict__ thp,
@@ -526,7 +528,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap hmap, const __grid_constan
     constexpr int NR = HPU * N, KU = HPU * K, KT = kMmaThreads - KU;   // rows, pairs per unit; table threads
     static_assert((HPU == 1 || HPU == 2) && N % 32 == 0 && NR <= 256 && KU <= kMmaThreads && R >= 1 && R <= 8,
                   "shape outside the tensor-core decode");
-    constexpr bool SWZ = (HPU * R) % 8 == 0;   // B, C, B_prev through swizzled TMA tiles
+    static_assert(!SWZ || (HPU * R) % 8 == 0, "swizzled rank tiles need 8k rows");
     extern __shared__ __align__(1024) unsigned char smem_m[];
     unsigned char *sm = smem_m + ((1024u - (smem_u32(smem_m) & 1023u)) & 1023u);
     const MmaLayout Lo(N, R, HPU, nst);
@@ -570,8 +572,17 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap hmap, const __grid_constan
                 tma_load_2d(sg + Lo.Bp + hf * Lo.half, &bpmap, 64 * hf, sh0 * R, bar);
             }
         } else {
-            bulk_load(sg + Lo.B, Bm + (size_t)bh0 * R * N, bn, bar);
-            bulk_load(sg + Lo.C, Cm + (size_t)bh0 * R * N, bn, bar);
+            if (G == H) {
+                bulk_load(sg + Lo.B, Bm + (size_t)bh0 * R * N, bn, bar);
+                bulk_load(sg + Lo.C, Cm + (size_t)bh0 * R * N, bn, bar);
+            } else {   // grouped B / C: each head's rank rows from its group (head h: group h / (H / G))
+#pragma unroll
+                for (int hh = 0; hh < HPU; ++hh) {
+                    const int bh = bh0 + hh, gi = (bh / H) * G + (bh % H) / (H / G);
+                    bulk_load(sg + Lo.B + hh * R * N * 2, Bm + (size_t)gi * R * N, R * N * 2, bar);
+                    bulk_load(sg + Lo.C + hh * R * N * 2, Cm + (size_t)gi * R * N, R * N * 2, bar);
+                }
+            }
             bulk_load(sg + Lo.Bp, Bprev + (size_t)sh0 * R * N, bn, bar);
         }
         bulk_load(sg + Lo.x, x + (size_t)bh0 * R * P, xn, bar);
@@ -788,12 +799,12 @@ bool map_state(CUtensorMap *m, float *h, long long rows, int box_rows) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int R, int N, int HPU>
-// nbh: token heads (batch * H); with a slot table the state arrays hold pool_heads heads
-cudaError_t launch_mma(int nbh, int H, const int *slot, int pool, const void *x, const void *B, const void *C,
-                       const void *dt, const void *A, const void *lam, const void *theta, float *h, void *Bprev,
-                       void *xprev, void *y, cudaStream_t s) {
-    constexpr bool kSwz = (HPU * R) % 8 == 0;
+// nbh: token heads (batch * H); with a slot table the state arrays hold pool_heads heads; B and C
+// hold G groups of heads
+template <int R, int N, int HPU, bool kSwz>
+cudaError_t launch_mma_t(int nbh, int H, int G, const int *slot, int pool, const void *x, const void *B,
+                         const void *C, const void *dt, const void *A, const void *lam, const void *theta, float *h,
+                         void *Bprev, void *xprev, void *y, cudaStream_t s) {
     const long long pool_heads = slot ? (long long)pool * H : (long long)nbh;
     // the state and carry maps depend only on (h, B_prev, shape); a decode loop reuses one state
     struct MapCache {
@@ -833,21 +844,33 @@ cudaError_t launch_mma(int nbh, int H, const int *slot, int pool, const void *x,
     if (Lo.total > 224u * 1024u) return cudaErrorInvalidValue;
     unsigned *status = device_status_word();
     if (!status) return cudaErrorUnknown;
-    auto kern = slot ? decode_mma_kernel<R, N, HPU, true> : decode_mma_kernel<R, N, HPU, false>;
-    cudaError_t err = slot ? allow_dynamic_smem<decode_mma_kernel<R, N, HPU, true>>(Lo.total)
-                           : allow_dynamic_smem<decode_mma_kernel<R, N, HPU, false>>(Lo.total);
+    auto kern = slot ? decode_mma_kernel<R, N, HPU, true, kSwz> : decode_mma_kernel<R, N, HPU, false, kSwz>;
+    cudaError_t err = slot ? allow_dynamic_smem<decode_mma_kernel<R, N, HPU, true, kSwz>>(Lo.total)
+                           : allow_dynamic_smem<decode_mma_kernel<R, N, HPU, false, kSwz>>(Lo.total);
     if (err != cudaSuccess) return err;
     const int nunit = nbh / HPU;
     const int grid = nunit < per_sm * sm_count() ? nunit : per_sm * sm_count();
     using bf = __nv_bfloat16;
     trace_mark(M3_KERNEL_DECODE, s, 0);
-    kern<<<grid, kMmaThreads, Lo.total, s>>>(cache.hmap, bmap, cmap, cache.bpmap, nunit, nst, slot, pool, H,
+    kern<<<grid, kMmaThreads, Lo.total, s>>>(cache.hmap, bmap, cmap, cache.bpmap, nunit, nst, slot, pool, H, G,
                                             (const bf *)x, (const bf *)B, (const bf *)C, (const bf *)dt,
                                             (const bf *)A, (const bf *)lam, (const bf *)theta, (bf *)Bprev,
                                             (bf *)xprev, (float *)y, status);
     trace_mark(M3_KERNEL_DECODE, s, 1);
     count_launch();
     return cudaGetLastError();
+}
+
+template <int R, int N, int HPU>
+cudaError_t launch_mma(int nbh, int H, int G, const int *slot, int pool, const void *x, const void *B, const void *C,
+                       const void *dt, const void *A, const void *lam, const void *theta, float *h, void *Bprev,
+                       void *xprev, void *y, cudaStream_t s) {
+    if constexpr ((HPU * R) % 8 == 0) {
+        if (G == H)
+            return launch_mma_t<R, N, HPU, true>(nbh, H, G, slot, pool, x, B, C, dt, A, lam, theta, h, Bprev, xprev,
+                                                 y, s);
+    }
+    return launch_mma_t<R, N, HPU, false>(nbh, H, G, slot, pool, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, s);
 }
 
 // The tensor-core variant takes bf16 inputs with P = 64, N in {64, 128}, R in {1, 2, 4, 8},
@@ -861,13 +884,13 @@ bool mma_ok(int dtype, int P, int N, int R, long long nbh) {
 
 // N = 64 pairs adjacent heads into one unit when the head count is even (with a slot table:
 // when H is even, so that the two heads share a batch row and thus a pool slot).
-cudaError_t mma_dispatch(int nbh, int H, const int *slot, int pool, int N, int R, const void *x, const void *B,
-                         const void *C, const void *dt, const void *A, const void *lam, const void *theta, float *h,
-                         void *Bprev, void *xprev, void *y, cudaStream_t s) {
-    const bool pair = N == 64 && (slot ? H % 2 == 0 : nbh % 2 == 0);
+cudaError_t mma_dispatch(int nbh, int H, int G, const int *slot, int pool, int N, int R, const void *x,
+                         const void *B, const void *C, const void *dt, const void *A, const void *lam,
+                         const void *theta, float *h, void *Bprev, void *xprev, void *y, cudaStream_t s) {
+    const bool pair = N == 64 && (slot || G != H ? H % 2 == 0 : nbh % 2 == 0);
 #define M3_MMA(RR, NN, HH)                                                                                         \
     if (R == RR && N == NN && (HH == 2) == pair)                                                                 \
-    return launch_mma<RR, NN, HH>(nbh, H, slot, pool, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, s)
+    return launch_mma<RR, NN, HH>(nbh, H, G, slot, pool, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, s)
     M3_MMA(1, 64, 2);
     M3_MMA(2, 64, 2);
     M3_MMA(4, 64, 2);
@@ -886,16 +909,20 @@ cudaError_t mma_dispatch(int nbh, int H, const int *slot, int pool, int N, int R
 
 }  // namespace
 
-cudaError_t decode_step(int dtype, int batch, int H, int P, int N, int R, const void *x,
+cudaError_t decode_step(int dtype, int batch, int H, int G, int P, int N, int R, const void *x,
                         const void *B, const void *C, const void *dt, const void *A,
                         const void *lam, const void *theta, float *h, void *Bprev, void *xprev,
                         void *y, cudaStream_t s) {
     const int e = dtype == M3_F32 ? 4 : 2;
     const void *ptrs[] = {x, B, C, theta, h, Bprev, xprev};
     const int nbh = batch * H;
+    if (G != H) {   // grouped B / C: tensor-core kernel only (the caller checked decode_tc_ok)
+        if (nbh == 0) return cudaSuccess;
+        return mma_dispatch(nbh, H, G, nullptr, batch, N, R, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, s);
+    }
     if (nbh > 0 && stream_ok(e, P, N, R, ptrs, 7)) {
         if (mma_ok(dtype, P, N, R, nbh))
-            return mma_dispatch(nbh, H, nullptr, batch, N, R, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, s);
+            return mma_dispatch(nbh, H, H, nullptr, batch, N, R, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, s);
         if (dtype == M3_F32)
             return stream_dispatch<float>(nbh, P, N, R, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, s);
         return stream_dispatch<__nv_bfloat16>(nbh, P, N, R, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, s);
@@ -906,16 +933,17 @@ cudaError_t decode_step(int dtype, int batch, int H, int P, int N, int R, const 
                                         xprev, y, s);
 }
 
-bool decode_pooled_ok(int dtype, int batch, int H, int P, int N, int R, int pool, const void *const *ptrs, int nptr) {
-    return mma_ok(dtype, P, N, R, (long long)(batch > pool ? batch : pool) * H) && stream_ok(2, P, N, R, ptrs, nptr);
+bool decode_tc_ok(int dtype, int P, int N, int R, long long heads, const void *const *ptrs, int nptr) {
+    return mma_ok(dtype, P, N, R, heads) && stream_ok(2, P, N, R, ptrs, nptr);
 }
 
-cudaError_t decode_step_pooled(int batch, int H, int P, int N, int R, const int *slot, int pool, const void *x,
-                               const void *B, const void *C, const void *dt, const void *A, const void *lam,
-                               const void *theta, float *h, void *Bprev, void *xprev, void *y, cudaStream_t s) {
+cudaError_t decode_step_pooled(int batch, int H, int G, int P, int N, int R, const int *slot, int pool,
+                               const void *x, const void *B, const void *C, const void *dt, const void *A,
+                               const void *lam, const void *theta, float *h, void *Bprev, void *xprev, void *y,
+                               cudaStream_t s) {
     (void)P;
     if (batch == 0) return cudaSuccess;
-    return mma_dispatch(batch * H, H, slot, pool, N, R, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, s);
+    return mma_dispatch(batch * H, H, G, slot, pool, N, R, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, s);
 }
 
 }  // namespace m3

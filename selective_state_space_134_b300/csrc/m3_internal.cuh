@@ -71,6 +71,7 @@ enum { kPathSimt = 0, kPathTc = 1 };
 
 struct ScanArgs {
     int dtype, batch, L, H, P, N, R;
+    int G;                      // B / C groups (G = H: one per head)
     const void *x, *B, *C, *dt, *A, *lam, *theta;
     const float *h0;            // may be null (zero state)
     const void *Bprev, *xprev;  // may be null (no carry)
@@ -97,14 +98,15 @@ cudaError_t tc_scan(const ScanArgs &a, const ScanPlan &plan, cudaStream_t s);
 cudaError_t segment_pass(const ScanArgs &a, const ScanPlan &plan, cudaStream_t s);
 
 // Decode step.
-cudaError_t decode_step(int dtype, int batch, int H, int P, int N, int R, const void *x,
+cudaError_t decode_step(int dtype, int batch, int H, int G, int P, int N, int R, const void *x,
                         const void *B, const void *C, const void *dt, const void *A,
                         const void *lam, const void *theta, float *h, void *Bprev, void *xprev,
                         void *y, cudaStream_t s);
-// Pooled decode (slot table on the device): supported shapes and the launch.
-bool decode_pooled_ok(int dtype, int batch, int H, int P, int N, int R, int pool, const void *const *ptrs, int nptr);
-cudaError_t decode_step_pooled(int batch, int H, int P, int N, int R, const int *slot, int pool, const void *x,
-                               const void *B, const void *C, const void *dt, const void *A, const void *lam,
-                               const void *theta, float *h, void *Bprev, void *xprev, void *y, cudaStream_t s);
+// The tensor-core decode's shapes (pooled and grouped decode run only there), and the pooled launch.
+bool decode_tc_ok(int dtype, int P, int N, int R, long long heads, const void *const *ptrs, int nptr);
+cudaError_t decode_step_pooled(int batch, int H, int G, int P, int N, int R, const int *slot, int pool,
+                               const void *x, const void *B, const void *C, const void *dt, const void *A,
+                               const void *lam, const void *theta, float *h, void *Bprev, void *xprev, void *y,
+                               cudaStream_t s);
 
 }  // namespace m3

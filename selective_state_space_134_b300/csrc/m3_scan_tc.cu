@@ -270,11 +270,12 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                 constexpr uint32_t bytes = Cf::BT * (OUT ? 2 : 1) + Cf::XT + Cf::TT;
                 mbar_expect_tx(bars + kRawFull + p, bytes);
                 const int row0 = b * L + t_begin + it * Q;
+                const int hg = h / (H / a.G);   // B / C group of this head
 #pragma unroll
                 for (int sl = 0; sl < NSLAB; ++sl) {
-                    tma_load_4d(slot + S::sB + sl * QR * 128, &maps.B, 64 * sl, 0, h, row0, bars + kRawFull + p);
+                    tma_load_4d(slot + S::sB + sl * QR * 128, &maps.B, 64 * sl, 0, hg, row0, bars + kRawFull + p);
                     if (OUT)
-                        tma_load_4d(slot + S::sC + sl * QR * 128, &maps.C, 64 * sl, 0, h, row0, bars + kRawFull + p);
+                        tma_load_4d(slot + S::sC + sl * QR * 128, &maps.C, 64 * sl, 0, hg, row0, bars + kRawFull + p);
                 }
                 tma_load_4d(slot + S::sX, &maps.X, 0, 0, h, row0, bars + kRawFull + p);
                 tma_load_3d(slot + S::sT, &maps.T, 0, h, row0, bars + kRawFull + p);
@@ -862,11 +863,12 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
         if (OUT && g == nseg - 1 && a.Bprev_out && a.xprev_out && L > 0 && !*abort_flag) {
             const int et = tid - kEpiW0 * 32;
             const size_t tl = tok(L - 1);
+            const size_t tlg = ((size_t)b * L + L - 1) * a.G + h / (H / a.G);   // its B / C group row
             const __nv_bfloat16 *Bm = static_cast<const __nv_bfloat16 *>(a.B);
             const __nv_bfloat16 *xm = static_cast<const __nv_bfloat16 *>(a.x);
             __nv_bfloat16 *bo = static_cast<__nv_bfloat16 *>(a.Bprev_out);
             __nv_bfloat16 *xo = static_cast<__nv_bfloat16 *>(a.xprev_out);
-            for (int i = et; i < R * N; i += kEpiThreads) bo[(size_t)bh * R * N + i] = Bm[tl * R * N + i];
+            for (int i = et; i < R * N; i += kEpiThreads) bo[(size_t)bh * R * N + i] = Bm[tlg * R * N + i];
             for (int i = et; i < R * kP; i += kEpiThreads) xo[(size_t)bh * R * kP + i] = xm[tl * R * kP + i];
         }
     }
@@ -941,7 +943,7 @@ cudaError_t run_tc(const ScanArgs &a, const ScanPlan &pl, cudaStream_t s) {
     using Cf = Cfg<N, R>;
     const long long rows = (long long)a.batch * a.L;
     TcMaps maps;
-    if (!map4(&maps.B, a.B, N, R, a.H, rows, Cf::Q) || !map4(&maps.C, a.C, N, R, a.H, rows, Cf::Q) ||
+    if (!map4(&maps.B, a.B, N, R, a.G, rows, Cf::Q) || !map4(&maps.C, a.C, N, R, a.G, rows, Cf::Q) ||
         !map4(&maps.X, a.x, kP, R, a.H, rows, Cf::Q) || !map3(&maps.T, a.theta, N / 2, a.H, rows, Cf::Q) ||
         !map_y(&maps.Y, a.y, R, a.H, a.L, a.batch, Cf::Q))
         return cudaErrorInvalidValue;

@@ -25,7 +25,7 @@ _DTYPE_CODE = {torch.float32: M3_F32, torch.bfloat16: M3_BF16}
 class m3_dims(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int), ("seqlen", ctypes.c_int), ("nheads", ctypes.c_int),
                 ("headdim", ctypes.c_int), ("dstate", ctypes.c_int), ("rank", ctypes.c_int),
-                ("chunk", ctypes.c_int), ("dtype", ctypes.c_int)]
+                ("chunk", ctypes.c_int), ("dtype", ctypes.c_int), ("ngroups", ctypes.c_int)]
 
 
 class m3_state(ctypes.Structure):
@@ -128,9 +128,15 @@ class State:
                      torch.zeros(batch, nheads, R, P, dtype=dtype, device=device))
 
 
-def dims(batch, seqlen, nheads, P, N, R, dtype, chunk=0) -> m3_dims:
+def dims(batch, seqlen, nheads, P, N, R, dtype, chunk=0, ngroups=0) -> m3_dims:
+    """ngroups: B / C groups of heads (0 = one B and C per head)."""
     code = _DTYPE_CODE.get(dtype, dtype) if isinstance(dtype, torch.dtype) else int(dtype)
-    return m3_dims(batch, seqlen, nheads, P, N, R, chunk, code)
+    return m3_dims(batch, seqlen, nheads, P, N, R, chunk, code, ngroups)
+
+
+def _groups(H: int, G: int) -> int:
+    # the head axis of B / C: H = one per head (ngroups 0), else G groups
+    return 0 if G == H else G
 
 
 def scan_fwd_workspace(d: m3_dims) -> int:
@@ -142,14 +148,15 @@ def scan_fwd_workspace(d: m3_dims) -> int:
 def scan_fwd(x, B, C, dt, A, lam, theta, state_in: Optional[State] = None,
              state_out: Optional[State] = None, chunk: int = 0, y: Optional[torch.Tensor] = None,
              workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """Chunked prefill.  x [b,L,H,R,P]; B, C [b,L,H,R,N]; dt, A, lam [b,L,H]; theta [b,L,H,N/2].
+    """Chunked prefill.  x [b,L,H,R,P]; B, C [b,L,H,R,N] (or [b,L,G,R,N]: G groups of heads);
+    dt, A, lam [b,L,H]; theta [b,L,H,N/2].
 
     Returns y [b,L,H,R,P] (fp32).  ``state_out`` (may be ``state_in``) receives the final
     state and carry.  The workspace is allocated here through torch unless given.
     """
     b, L, H, R, P = x.shape
     N = B.shape[-1]
-    d = dims(b, L, H, P, N, R, x.dtype, chunk)
+    d = dims(b, L, H, P, N, R, x.dtype, chunk, _groups(H, B.shape[2]))
     if y is None:
         y = torch.empty(x.shape, dtype=torch.float32, device=x.device)
     ws_bytes = scan_fwd_workspace(d)
@@ -168,13 +175,14 @@ def scan_fwd(x, B, C, dt, A, lam, theta, state_in: Optional[State] = None,
 
 def decode_step(x, B, C, dt, A, lam, theta, state: State, y: Optional[torch.Tensor] = None,
                 stream=None) -> torch.Tensor:
-    """One token for every (b, h).  x [b,H,R,P]; B, C [b,H,R,N]; dt, A, lam [b,H]; theta [b,H,N/2].
+    """One token for every (b, h).  x [b,H,R,P]; B, C [b,H,R,N] (or [b,G,R,N]: G groups of heads);
+    dt, A, lam [b,H]; theta [b,H,N/2].
 
     Updates ``state`` in place and returns y [b,H,R,P] (fp32).
     """
     b, H, R, P = x.shape
     N = B.shape[-1]
-    d = dims(b, 1, H, P, N, R, x.dtype)
+    d = dims(b, 1, H, P, N, R, x.dtype, 0, _groups(H, B.shape[1]))
     if y is None:
         y = torch.empty(x.shape, dtype=torch.float32, device=x.device)
     st = state.c()
@@ -196,7 +204,7 @@ def decode_step_pooled(x, B, C, dt, A, lam, theta, slot: torch.Tensor, pool: Sta
     N = B.shape[-1]
     if slot.dtype != torch.int32:
         raise ValueError("slot must be int32")
-    d = dims(b, 1, H, P, N, R, x.dtype)
+    d = dims(b, 1, H, P, N, R, x.dtype, 0, _groups(H, B.shape[1]))
     if y is None:
         y = torch.zeros(x.shape, dtype=torch.float32, device=x.device)
     rc = lib().mamba3_decode_step_pooled(ctypes.byref(d), _ptr(slot), _ptr(x), _ptr(B), _ptr(C), _ptr(dt),
@@ -242,7 +250,7 @@ def scan_fwd_noalloc(x, B, C, dt, A, lam, theta, state_in: Optional[State] = Non
     fn.restype = ctypes.c_int
     b, L, H, R, P = x.shape
     N = B.shape[-1]
-    d = dims(b, L, H, P, N, R, x.dtype, chunk)
+    d = dims(b, L, H, P, N, R, x.dtype, chunk, _groups(H, B.shape[2]))
     if y is None:
         y = torch.empty(x.shape, dtype=torch.float32, device=x.device)
     st_in = state_in.c() if state_in is not None else None
@@ -288,7 +296,7 @@ def scan_fwd_staged(host: dict, dev: dict, host_y: torch.Tensor, dev_y: torch.Te
     x = host["x"]
     b, L, H, R, P = x.shape
     N = host["B"].shape[-1]
-    d = dims(b, L, H, P, N, R, x.dtype)
+    d = dims(b, L, H, P, N, R, x.dtype, 0, _groups(H, host["B"].shape[2]))
     need = scan_fwd_staged_workspace(d, slices)
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev_y.device)

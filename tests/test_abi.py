@@ -165,6 +165,31 @@ def test_pooled_decode_rejects_bad_arguments_before_launch():
     assert m3.status_string(api.M3_ERR_INDEX) == "pooled decode slot index outside the pool"
 
 
+def test_grouped_bc_validation():
+    lib = m3.lib()
+    n = ctypes.c_size_t(0)
+    # G must divide H; a negative G is an argument error
+    for g in (3, -1):
+        d = m3.dims(1, 64, 8, 64, 64, 1, torch.bfloat16, ngroups=g)
+        assert lib.mamba3_scan_fwd_workspace(ctypes.byref(d), ctypes.byref(n)) == api.M3_ERR_INVALID_ARG
+    # grouped B / C exist on the tensor-core path only: fp32 inputs or P = 32 are unsupported
+    for d in (m3.dims(1, 64, 8, 64, 64, 1, torch.float32, ngroups=2),
+              m3.dims(1, 64, 8, 32, 64, 1, torch.bfloat16, ngroups=2)):
+        assert lib.mamba3_scan_fwd_workspace(ctypes.byref(d), ctypes.byref(n)) == api.M3_ERR_UNSUPPORTED
+    d = m3.dims(1, 64, 8, 64, 64, 1, torch.bfloat16, ngroups=2)
+    assert lib.mamba3_scan_fwd_workspace(ctypes.byref(d), ctypes.byref(n)) == api.M3_OK
+    # decode: the same checks before any launch
+    ptrs = Ptrs()
+    before = m3.launch_count()
+    args = [ptrs.get() for _ in range(7)]
+    st = api.m3_state(ptrs.get(), ptrs.get(), ptrs.get())
+    for d, want in ((m3.dims(2, 1, 8, 64, 64, 1, torch.bfloat16, ngroups=3), api.M3_ERR_INVALID_ARG),
+                    (m3.dims(2, 1, 8, 64, 64, 1, torch.float32, ngroups=2), api.M3_ERR_UNSUPPORTED),
+                    (m3.dims(2, 1, 8, 16, 64, 1, torch.bfloat16, ngroups=2), api.M3_ERR_UNSUPPORTED)):
+        assert lib.mamba3_decode_step(ctypes.byref(d), *args, ctypes.byref(st), ptrs.get(), None) == want
+    assert m3.launch_count() == before
+
+
 def test_staged_prefill_rejects_bad_arguments_before_any_copy():
     lib = m3.lib()
     d = m3.dims(2, 16, 2, 64, 64, 1, torch.bfloat16)

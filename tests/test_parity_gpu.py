@@ -222,6 +222,52 @@ def test_decode_pooled_slot_outside_pool_is_reported_and_skipped():
     assert not torch.equal(pool.h[2], ps["h"][2])                  # the valid rows ran
 
 
+def _grouped(t, H, G, axis):
+    # B / C shared by groups of H / G heads: the first head's values of every group, and the
+    # per-head expansion the oracle reads (head h takes group h // (H / G))
+    idx = torch.arange(0, H, H // G, device=t.device)
+    g = t.index_select(axis, idx).contiguous()
+    return g, g.repeat_interleave(H // G, dim=axis)
+
+
+@pytest.mark.parametrize("wname,H,G,L", [("siso_n64", 8, 2, 700), ("siso_n64", 4, 1, 300),
+                                         ("long_n128_r4", 6, 3, 900), ("mimo_r4", 40, 8, 260)])
+def test_prefill_grouped_bc_matches_oracle(wname, H, G, L):
+    # grouped B / C (G groups of H / G heads) on the tensor-core prefill, one or several
+    # segments, with an initial state; against the oracle on the per-head expansion
+    w = WORKLOADS[wname].with_(batch=2, nheads=H, seqlen=L)
+    inp = prefill_inputs(w, "cuda")
+    full = dict(inp)
+    for k in ("B", "C"):
+        inp[k], full[k] = _grouped(inp[k], H, G, 2)
+    st = random_state(w.batch, H, w.P, w.N, w.R, inp["x"].dtype, seed=G)
+    y, so = gpu_scan(inp, state_in=st)
+    yr, hr, Br, xr = oracle_full(full, st)
+    assert norm_err(to_f64(y), yr) <= TOL[w.dtype]
+    assert norm_err(to_f64(so.h), hr) <= TOL[w.dtype]
+    np.testing.assert_array_equal(to_f64(so.B_prev), Br)       # per-head carry of the group's B
+    np.testing.assert_array_equal(to_f64(so.x_prev), xr)
+
+
+@pytest.mark.parametrize("N,R,H,G", [(64, 4, 8, 2), (64, 1, 8, 4), (128, 4, 6, 1), (64, 8, 8, 8)])
+def test_decode_grouped_bc_matches_oracle(N, R, H, G):
+    w = WORKLOADS["decode_n64_r4"].with_(batch=5, nheads=H, N=N, R=R)
+    st = decode_state(w, "cuda")
+    state = m3.State(st["h"].clone(), st["B_prev"].clone(), st["x_prev"].clone())
+    ref_h, ref_B, ref_x = to_f64(st["h"]), to_f64(st["B_prev"]), to_f64(st["x_prev"])
+    for step, tok in enumerate(decode_pool(w, "cuda", pool=2)):
+        full = dict(tok)
+        for k in ("B", "C"):
+            tok[k], full[k] = _grouped(tok[k], H, G, 1)
+        y = m3.decode_step(*(tok[k] for k in KEYS), state=state)
+        assert m3.device_status() == m3.M3_OK
+        yr, ref_h, ref_B, ref_x = oracle.decode_step(*(to_f64(full[k]) for k in KEYS), ref_h, ref_B, ref_x)
+        assert norm_err(to_f64(y), yr) <= 1e-4, step
+        assert norm_err(to_f64(state.h), ref_h) <= 1e-5, step
+        np.testing.assert_array_equal(to_f64(state.B_prev), ref_B)
+        np.testing.assert_array_equal(to_f64(state.x_prev), ref_x)
+
+
 def test_decode_f32_tight():
     w = WORKLOADS["tiny_f32"].with_(batch=3, nheads=5, N=32, P=16, R=2)
     st = decode_state(w, "cuda")
