@@ -39,15 +39,17 @@ HEADLINE = "siso_n64"
 KEYS = ("x", "B", "C", "dt", "A", "lam", "theta")
 
 
-def bytes_per_token_head(w) -> int:
-    """Algorithmic HBM bytes of prefill per (token, head): x; y (fp32); B, C; theta; dt, A, lambda."""
+def bytes_per_token_head(w, groups=0) -> float:
+    """Algorithmic HBM bytes of prefill per (token, head): x; y (fp32); B, C (shared by
+    nheads / groups heads when grouped); theta; dt, A, lambda."""
     e = 4 if w.dtype == "f32" else 2
-    return e * (w.P * w.R + 2 * w.N * w.R + w.N // 2 + 3) + 4 * w.P * w.R
+    share = groups / w.nheads if groups else 1.0
+    return e * (w.P * w.R + 2 * w.N * w.R * share + w.N // 2 + 3) + 4 * w.P * w.R
 
 
-def prefill_bytes(w) -> int:
+def prefill_bytes(w, groups=0) -> int:
     bh = w.batch * w.nheads
-    return w.token_heads * bytes_per_token_head(w) + bh * w.N * w.P * 4 + \
+    return int(w.token_heads * bytes_per_token_head(w, groups)) + bh * w.N * w.P * 4 + \
         bh * w.R * (w.N + w.P) * (4 if w.dtype == "f32" else 2)
 
 
@@ -168,14 +170,20 @@ def max_over_ranks(v: float, ws: int) -> float:
 
 
 # ------------------------------------------------------------------ our arm
-def time_prefill(m3, w, steps, warmup, trace_kernel=None):
-    """Device time of `steps` scan_fwd calls (inputs resident). Returns dict."""
+def time_prefill(m3, w, steps, warmup, trace_kernel=None, groups=0):
+    """Device time of `steps` scan_fwd calls (inputs resident). Returns dict.  groups > 0: B and C
+    shared by groups of nheads / groups heads (the first head's values of each group)."""
     from selective_state_space_134_b300.synth import prefill_inputs
     inp = prefill_inputs(w, "cuda")
+    if groups:
+        idx = torch.arange(0, w.nheads, w.nheads // groups, device="cuda")
+        for k in ("B", "C"):
+            inp[k] = inp[k].index_select(2, idx).contiguous()
     dtype = inp["x"].dtype
     st = m3.State.zeros(w.batch, w.nheads, w.P, w.N, w.R, dtype)
     y = torch.empty(inp["x"].shape, dtype=torch.float32, device="cuda")
-    ws_bytes = m3.scan_fwd_workspace(m3.dims(w.batch, w.seqlen, w.nheads, w.P, w.N, w.R, dtype))
+    ws_bytes = m3.scan_fwd_workspace(m3.dims(w.batch, w.seqlen, w.nheads, w.P, w.N, w.R, dtype,
+                                             ngroups=groups if groups != w.nheads else 0))
     work = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device="cuda")
     args = [inp[k] for k in KEYS]
 
@@ -201,10 +209,10 @@ def time_prefill(m3, w, steps, warmup, trace_kernel=None):
     return {"ms": ms, "launches": launches, "traced": traced, "inputs": inp, "ws": ws_bytes}
 
 
-def prefill_line(m3, w, res, steps, hbm_peak, peak_kind):
+def prefill_line(m3, w, res, steps, hbm_peak, peak_kind, groups=0):
     ms_step = res["ms"] / steps
     n_tr, tr_ms = res["traced"]
-    algo = prefill_bytes(w)
+    algo = prefill_bytes(w, groups)
     k_ms = tr_ms / n_tr if n_tr else ms_step
     achieved = algo / (k_ms * 1e-3) / 1e9
     return {
@@ -212,7 +220,7 @@ def prefill_line(m3, w, res, steps, hbm_peak, peak_kind):
         "ms_per_step": ms_step,
         "roofline": {"bound": "hbm", "kernel": "prefill output pass", "achieved": round(achieved, 1),
                      "peak": hbm_peak, "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
-                     "traffic": traffic_for("prefill_output", w.name),
+                     "traffic": traffic_for("prefill_output", w.name + (f"_g{groups}" if groups else "")),
                      "algorithmic_bytes": algo, "kernel_ms": k_ms,
                      "peak_source": peak_kind},
     }
@@ -414,6 +422,13 @@ def run_ours(args):
             pre[name]["launches_per_step"] = r["launches"] / steps
             del r
             torch.cuda.empty_cache()
+        # grouped B / C: siso_n64 with one B and C per 8 heads
+        wp = WORKLOADS[HEADLINE]
+        r = time_prefill(m3, wp, 20, 1, m3.KERNEL_PREFILL_OUTPUT, groups=4)
+        pre["siso_n64_grouped_g4"] = prefill_line(m3, wp, r, 20, hbm_peak, peak_kind, groups=4)
+        pre["siso_n64_grouped_g4"]["launches_per_step"] = r["launches"] / 20
+        del r
+        torch.cuda.empty_cache()
         extra["prefill"] = pre
 
     e2e = e2e_prefill(m3, w, inp, max(2, min(args.steps, 10)), 1) if rank == 0 else None
