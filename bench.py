@@ -1,6 +1,6 @@
 """Benchmark of the Mamba-3 layer recurrence on B300: prefill and decode tokens/s.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--quick]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--quick] [--decode-only]
 
 A step is one mamba3_scan_fwd over the SISO bf16 prefill workload (batch 4,
 32 heads, L = 4096, P = 64, N = 64, R = 1): the prefill hot path end to end
@@ -8,10 +8,14 @@ A step is one mamba3_scan_fwd over the SISO bf16 prefill workload (batch 4,
 state).  `value` = prefill tokens/s (batch x L / time; a token covers every
 head), inputs resident in HBM and larger than L2 (no flush needed).  The same
 line carries the decode-step measurement (batch 256, 32 heads, one token per
-call over 1024 calls), the other prefill workloads, the roofline of the
-dominant kernel (timed live through the library's event tracing), the
-end-to-end figure through host buffers, the clocks seen, and the fp64 CPU
-oracle timed on this host's cores.
+call over 1024 calls; also N = 64, R = 4 on a 512-slot state pool), the other
+prefill workloads (N = 128, MIMO R = 4, long context, and the headline shape
+with grouped B / C), the roofline of the dominant kernel (timed live through
+the library's event tracing; `traffic` from profiles/traffic.json while the
+library sources match its digest), the end-to-end figure through host
+buffers, the clocks seen, and the fp64 CPU oracle timed on this host's cores.
+--quick prints the headline alone; --decode-only prints the decode workloads
+alone.
 
 --impl reference times the CPU oracle itself on the same workload (the
 reference arm of this method: there is no GPU implementation to compare with).
