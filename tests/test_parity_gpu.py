@@ -368,11 +368,16 @@ def test_theta_pi_parity_sign_flips_on_gpu():
 
 
 @pytest.mark.parametrize("slices", [1, 3, 7])
-def test_staged_host_prefill_matches_device_prefill(slices):
+@pytest.mark.parametrize("groups", [0, 2])
+def test_staged_host_prefill_matches_device_prefill(slices, groups):
     """mamba3_scan_fwd_staged (host buffers, copies overlapped over token ranges, the state and
-    carry handed from range to range) gives the same y and final state as mamba3_scan_fwd."""
-    w = WORKLOADS["siso_n64"].with_(batch=5, nheads=3, seqlen=200)
+    carry handed from range to range) gives the same y and final state as mamba3_scan_fwd,
+    with per-head or grouped B / C."""
+    w = WORKLOADS["siso_n64"].with_(batch=5, nheads=4 if groups else 3, seqlen=200)
     inp = prefill_inputs(w, "cuda")
+    if groups:
+        for k in ("B", "C"):
+            inp[k] = _grouped(inp[k], w.nheads, groups, 2)[0]
     y_ref, s_ref = gpu_scan(inp)
     host = {k: v.cpu().pin_memory() for k, v in inp.items()}
     dev = {k: torch.empty_like(v) for k, v in inp.items()}
