@@ -44,25 +44,40 @@ KEYS = ("x", "B", "C", "dt", "A", "lam", "theta")
 
 
 def bytes_per_token_head(w, groups=0) -> float:
-    """Algorithmic HBM bytes of prefill per (token, head): x; y (fp32); B, C (shared by
-    nheads / groups heads when grouped); theta; dt, A, lambda."""
+    """Algorithmic HBM bytes of prefill per (token, head), every tensor at the input element
+    size e: e (2PR + 2NR + N/2 + 3) for x and y; B and C (shared by nheads / groups heads when
+    grouped); theta; dt, A, lambda."""
     e = 4 if w.dtype == "f32" else 2
     share = groups / w.nheads if groups else 1.0
-    return e * (w.P * w.R + 2 * w.N * w.R * share + w.N // 2 + 3) + 4 * w.P * w.R
+    return e * (2 * w.P * w.R + 2 * w.N * w.R * share + w.N // 2 + 3)
+
+
+def y_surplus_per_token_head(w, y_bytes=4) -> float:
+    """Bytes per (token, head) that a y wider than the input element (fp32 y for bf16 inputs)
+    moves beyond the algorithmic count; reported beside the roofline, never folded into it."""
+    e = 4 if w.dtype == "f32" else 2
+    return max(0, y_bytes - e) * w.P * w.R
 
 
 def prefill_bytes(w, groups=0) -> int:
+    """Whole prefill step: every (token, head), plus the final state (fp32) and carry written."""
     bh = w.batch * w.nheads
     return int(w.token_heads * bytes_per_token_head(w, groups)) + bh * w.N * w.P * 4 + \
         bh * w.R * (w.N + w.P) * (4 if w.dtype == "f32" else 2)
 
 
 def decode_bytes(w) -> int:
-    """Per call: state read + write, carry read + write, token inputs, y."""
+    """Per call: state read + write (fp32), carry read + write, token inputs and y at the input
+    element size."""
     e = 4 if w.dtype == "f32" else 2
     bh = w.batch * w.nheads
     return bh * (8 * w.N * w.P + 2 * e * w.R * (w.N + w.P) + e * (2 * w.R * w.N + w.R * w.P + w.N // 2 + 3)
-                 + 4 * w.R * w.P)
+                 + e * w.R * w.P)
+
+
+def decode_y_surplus(w, y_bytes=4) -> int:
+    e = 4 if w.dtype == "f32" else 2
+    return w.batch * w.nheads * max(0, y_bytes - e) * w.R * w.P
 
 
 def peaks():
@@ -213,19 +228,27 @@ def time_prefill(m3, w, steps, warmup, trace_kernel=None, groups=0):
     return {"ms": ms, "launches": launches, "traced": traced, "inputs": inp, "ws": ws_bytes}
 
 
-def prefill_line(m3, w, res, steps, hbm_peak, peak_kind, groups=0):
+def prefill_line(m3, w, res, steps, hbm_peak, peak_kind, groups=0, y_bytes=4):
+    """Tokens/s and the HBM roofline of one prefill workload.  `frac` covers the whole step (all
+    launches): algorithmic bytes / time per step.  The output pass's own rate (the same bytes over
+    its traced time) is reported beside it; for one-launch steps the two agree."""
     ms_step = res["ms"] / steps
     n_tr, tr_ms = res["traced"]
     algo = prefill_bytes(w, groups)
     k_ms = tr_ms / n_tr if n_tr else ms_step
-    achieved = algo / (k_ms * 1e-3) / 1e9
+    achieved = algo / (ms_step * 1e-3) / 1e9
+    achieved_k = algo / (k_ms * 1e-3) / 1e9
     return {
         "tokens_per_s": w.batch * w.seqlen / (ms_step * 1e-3),
         "ms_per_step": ms_step,
-        "roofline": {"bound": "hbm", "kernel": "prefill output pass", "achieved": round(achieved, 1),
+        "roofline": {"bound": "hbm", "kernel": "whole prefill step", "achieved": round(achieved, 1),
                      "peak": hbm_peak, "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
                      "traffic": traffic_for("prefill_output", w.name + (f"_g{groups}" if groups else "")),
-                     "algorithmic_bytes": algo, "kernel_ms": k_ms,
+                     "algorithmic_bytes": algo,
+                     "extra_bytes_wide_y": int(w.token_heads * y_surplus_per_token_head(w, y_bytes)),
+                     "y_bytes": y_bytes,
+                     "output_pass": {"kernel_ms": k_ms, "achieved": round(achieved_k, 1),
+                                     "frac": round(achieved_k / hbm_peak, 4)},
                      "peak_source": peak_kind},
     }
 
@@ -505,7 +528,8 @@ def decode_results(m3, hbm_peak, calls=1024, warmup=16):
                      "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s",
                                   "frac": round(gbs / hbm_peak, 4),
                                   "traffic": traffic_for("decode", name),
-                                  "algorithmic_bytes": decode_bytes(wd), "kernel_ms": k_ms}}
+                                  "algorithmic_bytes": decode_bytes(wd), "kernel_ms": k_ms,
+                                  "extra_bytes_wide_y": decode_y_surplus(wd)}}
     # the same step on a state pool (2 x batch slots, rows on a random set of distinct slots)
     wd = WORKLOADS["decode_n64_r4"]
     ms_call, k_ms = time_decode_pooled(m3, wd, calls, warmup)
@@ -515,7 +539,8 @@ def decode_results(m3, hbm_peak, calls=1024, warmup=16):
         "pool_slots": 2 * wd.batch,
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(gbs / hbm_peak, 4), "traffic": traffic_for("decode", "decode_n64_r4_pooled"),
-                     "algorithmic_bytes": decode_bytes(wd), "kernel_ms": k_ms}}
+                     "algorithmic_bytes": decode_bytes(wd), "kernel_ms": k_ms,
+                     "extra_bytes_wide_y": decode_y_surplus(wd)}}
     return dec
 
 

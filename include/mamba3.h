@@ -23,9 +23,12 @@
  *   - All tensor pointers are caller-owned DEVICE memory on the current CUDA
  *     device, row-major and contiguous.  The fp32 state h and the workspace
  *     must be 16-byte aligned; every other pointer must be aligned to its
- *     element size (a misaligned or NULL pointer is M3_ERR_INVALID_ARG).  The
- *     library allocates no device memory; the prefill workspace is supplied by
- *     the caller after a size query.
+ *     element size (a misaligned or NULL pointer is M3_ERR_INVALID_ARG).  No
+ *     call allocates device memory at run time; the prefill workspace is
+ *     supplied by the caller after a size query.  The one static reservation
+ *     is the M3_NOALLOC_SCRATCH_BYTES scratch array behind
+ *     mamba3_scan_fwd_noalloc, which the module holds on every device it is
+ *     loaded on.
  *   - Element type of the per-token inputs is dims->dtype (fp32 or bf16).
  *     The outputs y and the state h are always fp32: rounding y to bf16 would
  *     by itself cost up to half a bf16 ulp of the largest |y|, about 1-2 % of
@@ -241,6 +244,19 @@ m3_status mamba3_decode_step_pooled(const m3_dims *dims, const int *slot, const 
                                     const void *C, const void *dt, const void *A, const void *lambda,
                                     const void *theta, const m3_state *pool, int pool_size, void *y,
                                     void *stream);
+
+/* The decode kernels (one per class of shapes; the results agree within
+ * rounding).  Not from the Mamba-3 pages: an implementation detail exposed so
+ * that a caller or a test can see which kernel served a call. */
+typedef enum {
+    M3_DECODE_GENERIC = 0,   /* any supported shape: one CTA per head, global loads */
+    M3_DECODE_STREAM = 1,    /* P in {32, 64, 128}, 16-byte aligned blocks: staged FMA pipeline */
+    M3_DECODE_TENSOR = 2     /* bf16, P = 64, N in {64, 128}: warp-level MMA pipeline */
+} m3_decode_variant;
+
+/* The m3_decode_variant that served the most recent decode call (plain or
+ * pooled) in this process, on any thread or device; -1 before the first. */
+int mamba3_decode_last_variant(void);
 
 /*
  * Synchronises `stream`, then reads and clears the library's device status

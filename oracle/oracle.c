@@ -22,7 +22,7 @@
  *  - linkstar.cloud/article/869, section "第三刀：多输入多输出 / MIMO的思路":
  *      B_t is N x R and x_t is P x R, so B_t x_t^T is a rank-R matrix product.
  *
- * Readings taken where the pages are silent (stated once more in the design doc):
+ * Readings taken where the pages are silent:
  *  - complex pairs are adjacent real entries: S_k = h[2k] + i h[2k+1];
  *  - the left-endpoint (beta) term is propagated by the full complex
  *    transition, i.e. beta_t = (1 - lambda_t) dt_t exp(dt_t (A_t + i theta_k));

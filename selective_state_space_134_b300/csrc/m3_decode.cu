@@ -909,6 +909,8 @@ cudaError_t mma_dispatch(int nbh, int H, int G, const int *slot, int pool, int N
 
 }  // namespace
 
+std::atomic<int> g_last_decode_variant{-1};
+
 cudaError_t decode_step(int dtype, int batch, int H, int G, int P, int N, int R, const void *x,
                         const void *B, const void *C, const void *dt, const void *A,
                         const void *lam, const void *theta, float *h, void *Bprev, void *xprev,
@@ -918,15 +920,20 @@ cudaError_t decode_step(int dtype, int batch, int H, int G, int P, int N, int R,
     const int nbh = batch * H;
     if (G != H) {   // grouped B / C: tensor-core kernel only (the caller checked decode_tc_ok)
         if (nbh == 0) return cudaSuccess;
+        g_last_decode_variant.store(M3_DECODE_TENSOR, std::memory_order_relaxed);
         return mma_dispatch(nbh, H, G, nullptr, batch, N, R, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, s);
     }
     if (nbh > 0 && stream_ok(e, P, N, R, ptrs, 7)) {
-        if (mma_ok(dtype, P, N, R, nbh))
+        if (mma_ok(dtype, P, N, R, nbh)) {
+            g_last_decode_variant.store(M3_DECODE_TENSOR, std::memory_order_relaxed);
             return mma_dispatch(nbh, H, H, nullptr, batch, N, R, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, s);
+        }
+        g_last_decode_variant.store(M3_DECODE_STREAM, std::memory_order_relaxed);
         if (dtype == M3_F32)
             return stream_dispatch<float>(nbh, P, N, R, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, s);
         return stream_dispatch<__nv_bfloat16>(nbh, P, N, R, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, s);
     }
+    g_last_decode_variant.store(M3_DECODE_GENERIC, std::memory_order_relaxed);
     if (dtype == M3_F32)
         return launch_decode<float>(batch, H, P, N, R, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, s);
     return launch_decode<__nv_bfloat16>(batch, H, P, N, R, x, B, C, dt, A, lam, theta, h, Bprev,
@@ -943,7 +950,12 @@ cudaError_t decode_step_pooled(int batch, int H, int G, int P, int N, int R, con
                                cudaStream_t s) {
     (void)P;
     if (batch == 0) return cudaSuccess;
+    g_last_decode_variant.store(M3_DECODE_TENSOR, std::memory_order_relaxed);
     return mma_dispatch(batch * H, H, G, slot, pool, N, R, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, s);
 }
 
 }  // namespace m3
+
+extern "C" int mamba3_decode_last_variant(void) {
+    return m3::g_last_decode_variant.load(std::memory_order_relaxed);
+}

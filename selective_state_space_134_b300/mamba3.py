@@ -78,6 +78,8 @@ def lib() -> ctypes.CDLL:
         L.mamba3_scan_fwd_staged.argtypes = [dp, ip, ip, vp, vp, sp, sp, vp, vp, ctypes.c_size_t, ctypes.c_int,
                                              vp, vp]
         L.mamba3_scan_fwd_staged.restype = ctypes.c_int
+        L.mamba3_decode_last_variant.argtypes = []
+        L.mamba3_decode_last_variant.restype = ctypes.c_int
         L.mamba3_version.argtypes = []
         L.mamba3_version.restype = ctypes.c_int
         _lib = L
@@ -227,6 +229,14 @@ def trace_end():
     n, ms = ctypes.c_int(0), ctypes.c_double(0.0)
     _check(lib().mamba3_trace_end(ctypes.byref(n), ctypes.byref(ms)), "mamba3_trace_end")
     return int(n.value), float(ms.value)
+
+
+DECODE_GENERIC, DECODE_STREAM, DECODE_TENSOR = range(3)
+
+
+def decode_last_variant() -> int:
+    """Which decode kernel (DECODE_GENERIC / DECODE_STREAM / DECODE_TENSOR) served the last decode call."""
+    return int(lib().mamba3_decode_last_variant())
 
 
 def device_status(stream=None) -> int:

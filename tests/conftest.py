@@ -28,3 +28,24 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    # the measured parity errors closest to their bars (error / bar), so that a run's log shows the
+    # margin and which case sits nearest the bar
+    try:
+        from helpers import RECORD
+    except Exception:  # pragma: no cover
+        return
+    if not RECORD:
+        return
+    worst = {}
+    for test, what, err, tol in RECORD:
+        key = (test, what.split(" ")[0])
+        if key not in worst or err / tol > worst[key][0] / worst[key][1]:
+            worst[key] = (err, tol)
+    rows = sorted(worst.items(), key=lambda kv: -kv[1][0] / kv[1][1])
+    tr = terminalreporter
+    tr.write_sep("-", f"parity margins: {len(RECORD)} checked comparisons, the closest to the bar last")
+    for (test, what), (err, tol) in reversed(rows[:15]):
+        tr.write_line(f"{err / tol:6.3f} of bar  err {err:.3e}  bar {tol:.0e}  {what:2s} {test}")

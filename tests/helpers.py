@@ -1,4 +1,6 @@
 """Shared helpers of the tests: error metric, oracle on sampled (b, h) slices."""
+import os
+
 import numpy as np
 import torch
 
@@ -9,6 +11,11 @@ TOL = {"f32": 1e-4, "bf16": 2e-2}   # max|y - y_ref| / rms(y_ref)
 KEYS = ("x", "B", "C", "dt", "A", "lam", "theta")
 
 
+# (test id, what, measured error, bar) of every checked comparison in this process; conftest.py
+# prints the ones closest to their bar at the end of the run
+RECORD = []
+
+
 def norm_err(got, ref) -> float:
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
@@ -16,6 +23,15 @@ def norm_err(got, ref) -> float:
         return 0.0
     rms = np.sqrt(np.mean(ref * ref))
     return float(np.max(np.abs(got - ref)) / max(rms, 1e-30))
+
+
+def assert_err(got, ref, tol, what="") -> float:
+    """Asserts norm_err(got, ref) <= tol and records the measured error against its bar."""
+    e = norm_err(got, ref)
+    test = os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0]
+    RECORD.append((test, str(what), e, float(tol)))
+    assert e <= tol, (what, e, tol)
+    return e
 
 
 def slice_inputs(inp: dict, b: int, h: int) -> dict:

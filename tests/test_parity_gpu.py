@@ -13,7 +13,7 @@ import torch
 import oracle
 import selective_state_space_134_b300 as m3
 from selective_state_space_134_b300.synth import WORKLOADS, decode_pool, decode_state, prefill_inputs, to_f64
-from helpers import KEYS, TOL, norm_err, oracle_full, oracle_slices
+from helpers import KEYS, TOL, assert_err, norm_err, oracle_full, oracle_slices
 
 pytestmark = pytest.mark.gpu
 
@@ -72,8 +72,8 @@ def test_scan_small_matches_oracle(case, with_state):
     y, so = gpu_scan(inp, state_in=st)
     yr, hr, Br, xr = oracle_full(inp, st)
     tol = TOL[w.dtype]
-    assert norm_err(to_f64(y), yr) <= tol
-    assert norm_err(to_f64(so.h), hr) <= tol
+    assert_err(to_f64(y), yr, tol, "y")
+    assert_err(to_f64(so.h), hr, tol, "h")
     np.testing.assert_array_equal(to_f64(so.B_prev), Br)     # carry is a plain copy
     np.testing.assert_array_equal(to_f64(so.x_prev), xr)
 
@@ -89,10 +89,8 @@ def test_scan_full_size_sampled(wname):
     stack = {k: torch.cat([inp[k][b:b + 1, :, h:h + 1] for b, h in pairs], dim=0) for k in KEYS}
     yr, hr, _, _ = oracle.scan(*(to_f64(stack[k]) for k in KEYS), nthreads=len(pairs))
     for i, (b, h) in enumerate(pairs):
-        ey = norm_err(to_f64(y[b:b + 1, :, h:h + 1]), yr[i:i + 1])
-        eh = norm_err(to_f64(so.h[b:b + 1, h:h + 1]), hr[i:i + 1])
-        assert ey <= TOL[w.dtype], (b, h, ey)
-        assert eh <= TOL[w.dtype], (b, h, eh)
+        assert_err(to_f64(y[b:b + 1, :, h:h + 1]), yr[i:i + 1], TOL[w.dtype], f"y (b, h) = {(b, h)}")
+        assert_err(to_f64(so.h[b:b + 1, h:h + 1]), hr[i:i + 1], TOL[w.dtype], f"h (b, h) = {(b, h)}")
     assert torch.isfinite(y.float()).all()
 
 
@@ -117,8 +115,8 @@ def test_prefill_random_shapes_match_oracle(N, R, H, b, L, with_state):
     st = random_state(b, H, w.P, N, R, inp["x"].dtype, seed=L) if with_state else None
     y, so = gpu_scan(inp, state_in=st)
     yr, hr, Br, xr = oracle_full(inp, st)
-    assert norm_err(to_f64(y), yr) <= TOL[w.dtype]
-    assert norm_err(to_f64(so.h), hr) <= TOL[w.dtype]
+    assert_err(to_f64(y), yr, TOL[w.dtype], "y")
+    assert_err(to_f64(so.h), hr, TOL[w.dtype], "h")
     np.testing.assert_array_equal(to_f64(so.B_prev), Br)
     np.testing.assert_array_equal(to_f64(so.x_prev), xr)
 
@@ -133,8 +131,8 @@ def test_segmented_prefill_with_state_pass_pieces(with_state):
     st = random_state(w.batch, w.nheads, w.P, w.N, w.R, inp["x"].dtype) if with_state else None
     y, so = gpu_scan(inp, state_in=st)
     yr, hr, Br, xr = oracle_full(inp, st)
-    assert norm_err(to_f64(y), yr) <= TOL[w.dtype]
-    assert norm_err(to_f64(so.h), hr) <= TOL[w.dtype]
+    assert_err(to_f64(y), yr, TOL[w.dtype], "y")
+    assert_err(to_f64(so.h), hr, TOL[w.dtype], "h")
     np.testing.assert_array_equal(to_f64(so.B_prev), Br)
     np.testing.assert_array_equal(to_f64(so.x_prev), xr)
 
@@ -150,8 +148,8 @@ def test_decode_full_size_matches_oracle(wname):
         y = m3.decode_step(*(tok[k] for k in KEYS), state=state)
         assert m3.device_status() == m3.M3_OK
         yr, ref_h, ref_B, ref_x = oracle.decode_step(*(to_f64(tok[k]) for k in KEYS), ref_h, ref_B, ref_x)
-        assert norm_err(to_f64(y), yr) <= TOL[w.dtype], step
-        assert norm_err(to_f64(state.h), ref_h) <= 1e-5, step      # fp32 state, exact-input update
+        assert_err(to_f64(y), yr, TOL[w.dtype], f"y {step}")
+        assert_err(to_f64(state.h), ref_h, 1e-5, f"h step {step}")      # fp32 state, exact-input update
         np.testing.assert_array_equal(to_f64(state.B_prev), ref_B)
         np.testing.assert_array_equal(to_f64(state.x_prev), ref_x)
 
@@ -169,8 +167,8 @@ def test_decode_tensor_core_ranks_match_oracle(R, N, H):
         y = m3.decode_step(*(tok[k] for k in KEYS), state=state)
         assert m3.device_status() == m3.M3_OK
         yr, ref_h, ref_B, ref_x = oracle.decode_step(*(to_f64(tok[k]) for k in KEYS), ref_h, ref_B, ref_x)
-        assert norm_err(to_f64(y), yr) <= 1e-4, step     # hi + lo split of h: far inside the bf16 bar
-        assert norm_err(to_f64(state.h), ref_h) <= 1e-5, step
+        assert_err(to_f64(y), yr, 1e-4, f"y step {step}")     # hi + lo split of h: far inside the bf16 bar
+        assert_err(to_f64(state.h), ref_h, 1e-5, f"h {step}")
         np.testing.assert_array_equal(to_f64(state.B_prev), ref_B)
         np.testing.assert_array_equal(to_f64(state.x_prev), ref_x)
 
@@ -196,8 +194,8 @@ def test_decode_pooled_matches_oracle(N, R, H):
         one = {k: to_f64(tok[k][b:b + 1]) for k in KEYS}
         yr, hr, Br, xr = oracle.decode_step(*(one[k] for k in KEYS), to_f64(ps["h"][sl:sl + 1]),
                                             to_f64(ps["B_prev"][sl:sl + 1]), to_f64(ps["x_prev"][sl:sl + 1]))
-        assert norm_err(to_f64(y[b:b + 1]), yr) <= 1e-4, b
-        assert norm_err(to_f64(pool.h[sl:sl + 1]), hr) <= 1e-5, b
+        assert_err(to_f64(y[b:b + 1]), yr, 1e-4, f"y {b}")
+        assert_err(to_f64(pool.h[sl:sl + 1]), hr, 1e-5, f"h {b}")
         np.testing.assert_array_equal(to_f64(pool.B_prev[sl:sl + 1]), Br)
         np.testing.assert_array_equal(to_f64(pool.x_prev[sl:sl + 1]), xr)
     for sl in set(range(S)) - set(slots):                          # slots no row names: bitwise unchanged
@@ -243,8 +241,8 @@ def test_prefill_grouped_bc_matches_oracle(wname, H, G, L):
     st = random_state(w.batch, H, w.P, w.N, w.R, inp["x"].dtype, seed=G)
     y, so = gpu_scan(inp, state_in=st)
     yr, hr, Br, xr = oracle_full(full, st)
-    assert norm_err(to_f64(y), yr) <= TOL[w.dtype]
-    assert norm_err(to_f64(so.h), hr) <= TOL[w.dtype]
+    assert_err(to_f64(y), yr, TOL[w.dtype], "y")
+    assert_err(to_f64(so.h), hr, TOL[w.dtype], "h")
     np.testing.assert_array_equal(to_f64(so.B_prev), Br)       # per-head carry of the group's B
     np.testing.assert_array_equal(to_f64(so.x_prev), xr)
 
@@ -262,10 +260,46 @@ def test_decode_grouped_bc_matches_oracle(N, R, H, G):
         y = m3.decode_step(*(tok[k] for k in KEYS), state=state)
         assert m3.device_status() == m3.M3_OK
         yr, ref_h, ref_B, ref_x = oracle.decode_step(*(to_f64(full[k]) for k in KEYS), ref_h, ref_B, ref_x)
-        assert norm_err(to_f64(y), yr) <= 1e-4, step
-        assert norm_err(to_f64(state.h), ref_h) <= 1e-5, step
+        assert_err(to_f64(y), yr, 1e-4, f"y {step}")
+        assert_err(to_f64(state.h), ref_h, 1e-5, f"h {step}")
         np.testing.assert_array_equal(to_f64(state.B_prev), ref_B)
         np.testing.assert_array_equal(to_f64(state.x_prev), ref_x)
+
+
+@pytest.mark.parametrize("dtype,P,N,R,b,H", [
+    ("f32", 64, 64, 1, 5, 67), ("f32", 64, 64, 4, 5, 67), ("f32", 64, 128, 4, 3, 41), ("f32", 64, 64, 2, 2, 9),
+    ("f32", 64, 128, 8, 2, 7), ("f32", 32, 64, 4, 4, 37), ("f32", 128, 32, 2, 3, 19), ("f32", 64, 48, 1, 2, 11),
+    ("bf16", 128, 64, 1, 5, 33), ("bf16", 128, 128, 4, 2, 21), ("bf16", 32, 64, 2, 4, 37), ("bf16", 32, 32, 8, 3, 9),
+    ("bf16", 64, 96, 4, 2, 19)])
+def test_decode_streaming_kernel_matches_oracle(dtype, P, N, R, b, H):
+    # fp32 inputs with P in {32, 64, 128}, and bf16 inputs outside the tensor-core shapes, go to the
+    # streaming FMA kernel; its arithmetic is fp32 on exactly the stored inputs, so y and h match the
+    # fp64 oracle to fp32 rounding over several steps
+    w = WORKLOADS["decode_n64_r4"].with_(batch=b, nheads=H, P=P, N=N, R=R, dtype=dtype)
+    st = decode_state(w, "cuda")
+    state = m3.State(st["h"].clone(), st["B_prev"].clone(), st["x_prev"].clone())
+    ref_h, ref_B, ref_x = to_f64(st["h"]), to_f64(st["B_prev"]), to_f64(st["x_prev"])
+    for step, tok in enumerate(decode_pool(w, "cuda", pool=3)):
+        y = m3.decode_step(*(tok[k] for k in KEYS), state=state)
+        assert m3.decode_last_variant() == m3.DECODE_STREAM
+        assert m3.device_status() == m3.M3_OK
+        yr, ref_h, ref_B, ref_x = oracle.decode_step(*(to_f64(tok[k]) for k in KEYS), ref_h, ref_B, ref_x)
+        assert_err(to_f64(y), yr, 1e-5, f"y {step}")
+        assert_err(to_f64(state.h), ref_h, 1e-5, f"h {step}")
+        np.testing.assert_array_equal(to_f64(state.B_prev), ref_B)
+        np.testing.assert_array_equal(to_f64(state.x_prev), ref_x)
+
+
+def test_decode_variants_are_selected_by_shape():
+    # the bench's bf16 P = 64 workloads take the tensor-core kernel; P = 16 the generic one
+    for over, want in ((dict(), m3.DECODE_TENSOR), (dict(P=16, dtype="f32"), m3.DECODE_GENERIC),
+                       (dict(dtype="f32"), m3.DECODE_STREAM)):
+        w = WORKLOADS["decode_n64_r4"].with_(batch=2, nheads=4, **over)
+        st = decode_state(w, "cuda")
+        state = m3.State(st["h"], st["B_prev"], st["x_prev"])
+        tok = decode_pool(w, "cuda", pool=1)[0]
+        m3.decode_step(*(tok[k] for k in KEYS), state=state)
+        assert m3.decode_last_variant() == want, over
 
 
 def test_decode_f32_tight():
@@ -276,8 +310,8 @@ def test_decode_f32_tight():
     y = m3.decode_step(*(tok[k] for k in KEYS), state=state)
     yr, hr, _, _ = oracle.decode_step(*(to_f64(tok[k]) for k in KEYS), to_f64(st["h"]), to_f64(st["B_prev"]),
                                       to_f64(st["x_prev"]))
-    assert norm_err(to_f64(y), yr) <= 1e-5
-    assert norm_err(to_f64(state.h), hr) <= 1e-5
+    assert_err(to_f64(y), yr, 1e-5, "y")
+    assert_err(to_f64(state.h), hr, 1e-5, "h")
 
 
 # ---------------------------------------------------------------- GPU-side invariants
@@ -287,7 +321,7 @@ def test_chunk_length_does_not_change_the_result():
     inp = prefill_inputs(w, "cuda")
     ys = [gpu_scan(inp, chunk=q)[0] for q in (0, 1, 7, 32, 64)]
     for y in ys[1:]:
-        assert norm_err(to_f64(y), to_f64(ys[0])) <= 1e-5
+        assert_err(to_f64(y), to_f64(ys[0]), 1e-5, "y")
 
 
 def test_split_prefill_and_decode_resume_equal_full_prefill():
@@ -300,16 +334,16 @@ def test_split_prefill_and_decode_resume_equal_full_prefill():
     y1, s1 = gpu_scan(first)
     y2, s2 = gpu_scan(rest, state_in=s1)
     tol = TOL[w.dtype]
-    assert norm_err(to_f64(torch.cat([y1, y2], 1)), to_f64(y_full)) <= tol
-    assert norm_err(to_f64(s2.h), to_f64(s_full.h)) <= tol
+    assert_err(to_f64(torch.cat([y1, y2], 1)), to_f64(y_full), tol, "y")
+    assert_err(to_f64(s2.h), to_f64(s_full.h), tol, "h")
     # prefill L - k tokens, then k decode steps
     k = 5
     head = {kk: v[:, :-k].contiguous() for kk, v in inp.items()}
     _, st = gpu_scan(head)
     for t in range(w.seqlen - k, w.seqlen):
         yt = m3.decode_step(*(inp[kk][:, t].contiguous() for kk in KEYS), state=st)
-        assert norm_err(to_f64(yt), to_f64(y_full[:, t])) <= tol
-    assert norm_err(to_f64(st.h), to_f64(s_full.h)) <= tol
+        assert_err(to_f64(yt), to_f64(y_full[:, t]), tol, "y")
+    assert_err(to_f64(st.h), to_f64(s_full.h), tol, "h")
 
 
 def test_in_place_state_update_equals_out_of_place():
@@ -329,8 +363,8 @@ def test_in_place_segmented_long_sequence():
     st = random_state(1, 1, w.P, w.N, w.R, inp["x"].dtype, seed=4)
     ref = oracle_full(inp, st)
     y, _ = gpu_scan(inp, state_in=st, inplace=True)
-    assert norm_err(to_f64(y), ref[0]) <= TOL[w.dtype]
-    assert norm_err(to_f64(st.h), ref[1]) <= TOL[w.dtype]
+    assert_err(to_f64(y), ref[0], TOL[w.dtype], "y")
+    assert_err(to_f64(st.h), ref[1], TOL[w.dtype], "h")
 
 
 def test_empty_sequence_and_empty_batch():
@@ -391,6 +425,6 @@ def test_staged_host_prefill_matches_device_prefill(slices, groups):
     torch.cuda.synchronize()
     assert m3.device_status() == m3.M3_OK
     tol = TOL[w.dtype]
-    assert norm_err(y_host.double().numpy(), to_f64(y_ref)) <= tol
-    assert norm_err(h_host.double().numpy(), to_f64(s_ref.h)) <= tol
+    assert_err(y_host.double().numpy(), to_f64(y_ref), tol, "y")
+    assert_err(h_host.double().numpy(), to_f64(s_ref.h), tol, "h")
     assert torch.equal(st.B_prev, s_ref.B_prev) and torch.equal(st.x_prev, s_ref.x_prev)

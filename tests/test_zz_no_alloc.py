@@ -16,8 +16,8 @@ import torch
 
 import selective_state_space_134_b300 as m3
 from selective_state_space_134_b300 import mamba3 as api
-from selective_state_space_134_b300.synth import WORKLOADS, prefill_inputs, to_f64
-from helpers import KEYS, TOL, norm_err
+from selective_state_space_134_b300.synth import WORKLOADS, prefill_inputs
+from helpers import KEYS
 
 pytestmark = pytest.mark.gpu
 
@@ -45,12 +45,14 @@ def test_noalloc_matches_workspace_entry_point_twice_in_a_row():
         need = m3.scan_fwd_workspace(m3.dims(w.batch, w.seqlen, w.nheads, w.P, w.N, w.R, torch.bfloat16))
         assert 0 < need <= LIMIT
     calls = [(w1, prefill_inputs(w1, "cuda")), (w2, prefill_inputs(w2, "cuda"))]
-    for w, inp in calls:          # two different problems back to back: leftovers must not matter
+    # Two different problems back to back: leftovers in the shared scratch must not matter.  Both
+    # entry points run the same plan and the same deterministic kernels (no atomics, fixed
+    # reduction orders); only the scratch address differs, so the results must be bit-identical.
+    for w, inp in calls:
         y_ref, s_ref = _run(m3.scan_fwd, inp, w)
         y, s = _run(api.scan_fwd_noalloc, inp, w)
-        tol = TOL[w.dtype]
-        assert norm_err(to_f64(y), to_f64(y_ref)) <= tol
-        assert norm_err(to_f64(s.h), to_f64(s_ref.h)) <= tol
+        assert torch.equal(y, y_ref)
+        assert torch.equal(s.h, s_ref.h)
         assert torch.equal(s.B_prev, s_ref.B_prev) and torch.equal(s.x_prev, s_ref.x_prev)
 
 
