@@ -189,9 +189,11 @@ def max_over_ranks(v: float, ws: int) -> float:
 
 
 # ------------------------------------------------------------------ our arm
-def time_prefill(m3, w, steps, warmup, trace_kernel=None, groups=0):
+def time_prefill(m3, w, steps, warmup, trace_kernel=None, groups=0, y_dtype=torch.float32, bc=False, chunk=0):
     """Device time of `steps` scan_fwd calls (inputs resident). Returns dict.  groups > 0: B and C
-    shared by groups of nheads / groups heads (the first head's values of each group)."""
+    shared by groups of nheads / groups heads (the first head's values of each group); y_dtype:
+    element type of y; bc: with BC normalisation and bias (synthetic gains and biases); chunk: tokens
+    per chunk (0: the library's tile)."""
     from selective_state_space_134_b300.synth import prefill_inputs
     inp = prefill_inputs(w, "cuda")
     if groups:
@@ -200,14 +202,19 @@ def time_prefill(m3, w, steps, warmup, trace_kernel=None, groups=0):
             inp[k] = inp[k].index_select(2, idx).contiguous()
     dtype = inp["x"].dtype
     st = m3.State.zeros(w.batch, w.nheads, w.P, w.N, w.R, dtype)
-    y = torch.empty(inp["x"].shape, dtype=torch.float32, device="cuda")
-    ws_bytes = m3.scan_fwd_workspace(m3.dims(w.batch, w.seqlen, w.nheads, w.P, w.N, w.R, dtype,
+    y = torch.empty(inp["x"].shape, dtype=y_dtype, device="cuda")
+    ws_bytes = m3.scan_fwd_workspace(m3.dims(w.batch, w.seqlen, w.nheads, w.P, w.N, w.R, dtype, chunk=chunk,
                                              ngroups=groups if groups != w.nheads else 0))
     work = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device="cuda")
     args = [inp[k] for k in KEYS]
+    bcn = None
+    if bc:
+        from selective_state_space_134_b300.synth import bc_params
+        p = bc_params(w, "cuda")
+        bcn = m3.BcNorm(p["B_weight"], p["B_bias"], p["C_weight"], p["C_bias"], p["eps"])
 
     def step():
-        m3.scan_fwd(*args, state_out=st, y=y, workspace=work)
+        m3.scan_fwd(*args, state_out=st, y=y, workspace=work, bc=bcn, chunk=chunk)
 
     for _ in range(warmup):
         step()

@@ -29,11 +29,12 @@
  *     is the M3_NOALLOC_SCRATCH_BYTES scratch array behind
  *     mamba3_scan_fwd_noalloc, which the module holds on every device it is
  *     loaded on.
- *   - Element type of the per-token inputs is dims->dtype (fp32 or bf16).
- *     The outputs y and the state h are always fp32: rounding y to bf16 would
- *     by itself cost up to half a bf16 ulp of the largest |y|, about 1-2 % of
- *     rms(y), which is the whole error budget of a bf16-input run.  The carry
- *     (B_prev, x_prev) has the input dtype.
+ *   - Element type of the per-token inputs is dims->dtype (fp32 or bf16);
+ *     the output y has dims->ydtype (fp32 unless chosen otherwise: rounding y
+ *     to bf16 would by itself cost up to half a bf16 ulp of the largest |y|,
+ *     about 1-2 % of rms(y), which is the whole error budget of a bf16-input
+ *     run; fp16 costs an eighth of that).  The state h is always fp32.  The
+ *     carry (B_prev, x_prev) has the input dtype.
  *   - dt, A, lambda are already activated (dt >= 0, A <= 0, 0 <= lambda <= 1
  *     for a stable recurrence; other values are computed as given); theta is
  *     in radians.
@@ -69,7 +70,7 @@ typedef enum {
     M3_ERR_INDEX = 6          /* a pooled decode read a slot index outside [0, pool_size) */
 } m3_status;
 
-typedef enum { M3_F32 = 0, M3_BF16 = 1 } m3_dtype;
+typedef enum { M3_F32 = 0, M3_BF16 = 1, M3_F16 = 2 } m3_dtype;
 
 /* Problem sizes.  P = head dim, N = real state size (N/2 complex pairs),
  * R = MIMO rank.  chunk = tokens per chunk of the prefill kernels, 0 = the
@@ -81,7 +82,14 @@ typedef enum { M3_F32 = 0, M3_BF16 = 1 } m3_dtype;
  * a change of the recurrence, and are not from the Mamba-3 pages.  They are
  * supported on the tensor-core paths only (bf16 inputs, P = 64, N in
  * {64, 128}, 16-byte-aligned pointers); elsewhere M3_ERR_UNSUPPORTED.  The
- * state's carry stays per head. */
+ * state's carry stays per head.
+ * ydtype: element type of the output y (an m3_dtype; 0 = M3_F32).  The
+ * arithmetic is the same for all three; y is rounded once (to nearest even)
+ * from fp32.  M3_F16 keeps y at the input element size with an 11-bit
+ * significand (rounding costs at most 2^-11 |y|); its range ends at 65504,
+ * beyond which a value becomes infinite.  M3_BF16 has the input's format;
+ * its 8-bit significand alone can cost up to 2^-9 |y|.  Inputs must be
+ * M3_F32 or M3_BF16. */
 typedef struct {
     int batch;
     int seqlen;      /* L; ignored by mamba3_decode_step */
@@ -92,6 +100,7 @@ typedef struct {
     int chunk;
     int dtype;       /* m3_dtype */
     int ngroups;     /* G, 0 = H */
+    int ydtype;      /* m3_dtype of y, 0 = fp32 */
 } m3_dims;
 
 /* Recurrent state of every (batch, head): the checkpoint between calls.
@@ -120,7 +129,7 @@ m3_status mamba3_scan_fwd_workspace(const m3_dims *dims, size_t *bytes);
  *   dt, A, lambda [batch][L][H]     theta [batch][L][H][N/2]
  *   state_in: initial state and carry, or NULL for h0 = 0 and no carry.
  * Outputs:
- *   y      [batch][L][H][R][P] fp32, y_t = C_t^T h_t;
+ *   y      [batch][L][H][R][P] of dims->ydtype, y_t = C_t^T h_t;
  *   state_out: final state h_L (fp32) and carry (B_{L-1}, x_{L-1}); NULL = not
  *     written.  state_out may equal state_in (in-place update); otherwise the
  *     two must not overlap.
@@ -132,6 +141,29 @@ m3_status mamba3_scan_fwd(const m3_dims *dims, const void *x, const void *B, con
                           const void *dt, const void *A, const void *lambda, const void *theta,
                           const m3_state *state_in, void *y, const m3_state *state_out,
                           void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * BC normalisation and bias (linkstar.cloud/article/869, section
+ * "架构上的其他改动": BC归一化 -- B and C are RMS-normalised like a QK-norm --
+ * and BC偏置 -- a learnable, data-independent bias is added to B and C).  The
+ * page gives no formula; the reading taken: every row of B (and of C) -- the N
+ * entries of one (token, head, rank) -- becomes
+ *     v'[n] = v[n] / sqrt(mean_m v[m]^2 + eps) * weight[h][n] + bias[h][r][n]
+ * before the recurrence (and before the rotation of its RoPE form).  The carry
+ * keeps the raw B of the last token; the call that consumes it normalises it.
+ *   B_weight, C_weight [H][N] fp32 device arrays, or NULL for a gain of 1;
+ *   B_bias, C_bias  [H][R][N] fp32 device arrays, or NULL for no bias;
+ *   eps >= 0 (a row of zeros with eps = 0 gives a non-finite result).
+ * Pointers must be 4-byte aligned.  With grouped B / C the gain and bias are
+ * still per head (the heads of a group share the raw B, not the normalised one).
+ */
+typedef struct {
+    const float *B_weight;
+    const float *B_bias;
+    const float *C_weight;
+    const float *C_bias;
+    float eps;
+} m3_bc_norm;
 
 /* The seven per-token input tensors of a prefill (layouts as in mamba3_scan_fwd). */
 typedef struct {
@@ -205,6 +237,19 @@ m3_status mamba3_scan_fwd_noalloc(const m3_dims *dims, const void *x, const void
                                   void *stream);
 
 /*
+ * mamba3_scan_fwd with BC normalisation and bias (see m3_bc_norm) applied to
+ * B and C in front of the recurrence, fused into the prefill kernels.  bc =
+ * NULL is mamba3_scan_fwd.  The workspace query is mamba3_scan_fwd_workspace.
+ * Errors as mamba3_scan_fwd, plus M3_ERR_INVALID_ARG for a misaligned bc
+ * pointer or eps < 0 (or NaN).
+ */
+m3_status mamba3_scan_fwd_bc(const m3_dims *dims, const void *x, const void *B, const void *C,
+                             const void *dt, const void *A, const void *lambda, const void *theta,
+                             const m3_bc_norm *bc, const m3_state *state_in, void *y,
+                             const m3_state *state_out, void *workspace, size_t workspace_bytes,
+                             void *stream);
+
+/*
  * One-token recurrent step for every (b, h), updating `state` in place
  * (linkstar.cloud article, section "第一刀": the recursion used at inference).
  *
@@ -212,12 +257,25 @@ m3_status mamba3_scan_fwd_noalloc(const m3_dims *dims, const void *x, const void
  *   dt, A, lambda [batch][H]; theta [batch][H][N/2].
  * state: h (fp32) and carry; on return h is the state after this token and
  *   the carry is (B, x) of this token.  All three pointers are required.
- * Output: y [batch][H][R][P] fp32.
+ * Output: y [batch][H][R][P] of dims->ydtype.
  * dims->seqlen and dims->chunk are ignored.
  */
 m3_status mamba3_decode_step(const m3_dims *dims, const void *x, const void *B, const void *C,
                              const void *dt, const void *A, const void *lambda, const void *theta,
                              const m3_state *state, void *y, void *stream);
+
+/*
+ * mamba3_decode_step with BC normalisation and bias (see m3_bc_norm) applied to
+ * this token's B and C and to the carried B_prev; the carry written back is
+ * this token's raw B.  bc = NULL is mamba3_decode_step.  Runs on the decode
+ * kernels with per-thread FMA arithmetic (M3_DECODE_STREAM or
+ * M3_DECODE_GENERIC).  Grouped B / C is not supported here
+ * (M3_ERR_UNSUPPORTED).  Errors otherwise as mamba3_decode_step and
+ * mamba3_scan_fwd_bc.
+ */
+m3_status mamba3_decode_step_bc(const m3_dims *dims, const void *x, const void *B, const void *C,
+                                const void *dt, const void *A, const void *lambda, const void *theta,
+                                const m3_bc_norm *bc, const m3_state *state, void *y, void *stream);
 
 /*
  * One decode step for a batch whose states live in a caller-owned state pool
@@ -280,7 +338,8 @@ typedef enum {
     M3_KERNEL_SEGMENT_PASS = 1,     /* prefill pass 2: state passing across segments */
     M3_KERNEL_PREFILL_OUTPUT = 2,   /* prefill pass 3: outputs, final state, carry */
     M3_KERNEL_DECODE = 3,           /* decode step */
-    M3_KERNEL_COUNT = 4
+    M3_KERNEL_BACKWARD = 4,         /* backward pass of the prefill */
+    M3_KERNEL_COUNT = 5
 } m3_kernel;
 
 /*

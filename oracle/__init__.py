@@ -38,6 +38,11 @@ def _load():
         d = ctypes.POINTER(ctypes.c_double)
         lib.oracle_scan.argtypes = [ctypes.c_int] * 6 + [d] * 7 + [d] * 3 + [d] * 4 + [ctypes.c_int]
         lib.oracle_scan.restype = ctypes.c_int
+        lib.oracle_bc_prep.argtypes = [ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int, d, d, d,
+                                       ctypes.c_double, d]
+        lib.oracle_bc_prep.restype = ctypes.c_int
+        lib.oracle_scan_bwd.argtypes = [ctypes.c_int] * 6 + [d] * 7 + [d] * 3 + [d] * 4 + [d] * 10
+        lib.oracle_scan_bwd.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -101,3 +106,81 @@ def decode_step(x, B, C, dt, A, lam, theta, h, Bprev, xprev):
     y, h1, Bo, xo = scan(expand(x), expand(B), expand(C), expand(dt), expand(A), expand(lam),
                          expand(theta), h0=h, Bprev=Bprev, xprev=xprev)
     return y[:, 0], h1, Bo, xo
+
+
+def bc_prep(v, weight=None, bias=None, eps=1e-6):
+    """BC normalisation and bias of B or C (see oracle_bc_prep in oracle.c): every row of N entries
+    (one token, head and rank) becomes v / sqrt(mean(v^2) + eps) * weight[h] + bias[h, r].
+
+    v [..., H, R, N]; weight [H, N] or None (1); bias [H, R, N] or None (0).  Returns float64.
+    """
+    v = _f64(v)
+    H, R, N = v.shape[-3:]
+    weight, bias = _f64(weight), _f64(bias)
+    if weight is not None:
+        assert weight.shape == (H, N)
+    if bias is not None:
+        assert bias.shape == (H, R, N)
+    out = np.empty_like(v)
+    rows = v.size // N
+    if rows and _load().oracle_bc_prep(rows, H, R, N, _ptr(v), _ptr(weight), _ptr(bias), float(eps),
+                                       _ptr(out)) != 0:
+        raise RuntimeError("oracle_bc_prep failed")
+    return out
+
+
+def scan_bc(x, B, C, dt, A, lam, theta, bc, h0=None, Bprev=None, xprev=None, nthreads: int = 1):
+    """The recurrence with BC normalisation and bias in front of it.
+
+    ``bc`` = dict(B_weight, B_bias, C_weight, C_bias, eps) (None entries: 1 / 0).  B and C of every
+    token, and the carry's B_prev when one is passed, go through bc_prep before the recurrence; the
+    carry returned holds the raw (unnormalised) B of the last token, as the inputs gave it.
+    """
+    eps = bc.get("eps", 1e-6)
+    Bn = bc_prep(B, bc.get("B_weight"), bc.get("B_bias"), eps)
+    Cn = bc_prep(C, bc.get("C_weight"), bc.get("C_bias"), eps)
+    Bpn = bc_prep(Bprev, bc.get("B_weight"), bc.get("B_bias"), eps) if Bprev is not None else None
+    y, h, _, xo = scan(x, Bn, Cn, dt, A, lam, theta, h0=h0, Bprev=Bpn, xprev=xprev, nthreads=nthreads)
+    L = _f64(x).shape[1]
+    if L > 0:
+        Bo = _f64(B)[:, -1].copy()
+    else:
+        Bo = _f64(Bprev).copy() if Bprev is not None else np.zeros_like(_f64(B)[:, 0])
+    return y, h, Bo, xo
+
+
+def decode_step_bc(x, B, C, dt, A, lam, theta, h, Bprev, xprev, bc):
+    """One token per (b, h) with BC normalisation and bias (scan_bc with L = 1)."""
+    expand = lambda a: _f64(a)[:, None]
+    y, h1, Bo, xo = scan_bc(expand(x), expand(B), expand(C), expand(dt), expand(A), expand(lam),
+                            expand(theta), bc, h0=h, Bprev=Bprev, xprev=xprev)
+    return y[:, 0], h1, Bo, xo
+
+
+GRAD_KEYS = ("x", "B", "C", "dt", "A", "lam", "theta")
+
+
+def scan_bwd(x, B, C, dt, A, lam, theta, dy, h0=None, Bprev=None, xprev=None, dh_out=None, dBprev_out=None,
+             dxprev_out=None):
+    """Reverse mode of ``scan`` (oracle_scan_bwd in oracle.c): the gradient of the scalar
+    sum(dy * y) + sum(dh_out * h_out) + sum(dBprev_out * Bprev_out) + sum(dxprev_out * xprev_out)
+    with respect to every input.  Returns a dict with keys x, B, C, dt, A, lam, theta, h0, Bprev,
+    xprev (float64, the inputs' shapes; h0 / Bprev / xprev are returned even when the inputs were
+    None, i.e. zero)."""
+    x, B, C, dt, A, lam, theta, dy = (_f64(v) for v in (x, B, C, dt, A, lam, theta, dy))
+    h0, Bprev, xprev = _f64(h0), _f64(Bprev), _f64(xprev)
+    dh_out, dBprev_out, dxprev_out = _f64(dh_out), _f64(dBprev_out), _f64(dxprev_out)
+    b, L, H, R, P = x.shape
+    N = B.shape[-1]
+    assert dy.shape == x.shape and L >= 1
+    out = {k: np.zeros_like(v) for k, v in zip(GRAD_KEYS, (x, B, C, dt, A, lam, theta))}
+    out["h0"] = np.zeros((b, H, N, P))
+    out["Bprev"] = np.zeros((b, H, R, N))
+    out["xprev"] = np.zeros((b, H, R, P))
+    rc = _load().oracle_scan_bwd(b, L, H, P, N, R, _ptr(x), _ptr(B), _ptr(C), _ptr(dt), _ptr(A), _ptr(lam),
+                                 _ptr(theta), _ptr(h0), _ptr(Bprev), _ptr(xprev), _ptr(dy), _ptr(dh_out),
+                                 _ptr(dBprev_out), _ptr(dxprev_out),
+                                 *(_ptr(out[k]) for k in GRAD_KEYS + ("h0", "Bprev", "xprev")))
+    if rc != 0:
+        raise RuntimeError("oracle_scan_bwd failed")
+    return out

@@ -99,6 +99,7 @@ m3_status check_dims(const m3_dims *d, bool prefill) {
     if (d->dstate < 2 || d->dstate > 256 || (d->dstate % 2) != 0) return M3_ERR_UNSUPPORTED;
     if (d->rank < 1 || d->rank > 8) return M3_ERR_UNSUPPORTED;
     if (d->ngroups < 0 || (d->ngroups > 0 && d->nheads % d->ngroups != 0)) return M3_ERR_INVALID_ARG;
+    if (d->ydtype != M3_F32 && d->ydtype != M3_BF16 && d->ydtype != M3_F16) return M3_ERR_UNSUPPORTED;
     return M3_OK;
 }
 
@@ -141,21 +142,37 @@ m3_status mamba3_scan_fwd_workspace(const m3_dims *dims, size_t *bytes) {
     return M3_OK;
 }
 
-m3_status mamba3_scan_fwd(const m3_dims *dims, const void *x, const void *B, const void *C,
-                          const void *dt, const void *A, const void *lambda, const void *theta,
-                          const m3_state *state_in, void *y, const m3_state *state_out,
-                          void *workspace, size_t workspace_bytes, void *stream) {
+}  // extern "C"
+
+namespace {
+
+// Validates an m3_bc_norm (null = none) into `out`.
+m3_status bc_args(const m3_bc_norm *bc, BcNorm *out) {
+    *out = BcNorm{};
+    if (!bc) return M3_OK;
+    for (const float *p : {bc->B_weight, bc->B_bias, bc->C_weight, bc->C_bias})
+        if (p && (reinterpret_cast<uintptr_t>(p) & 3u)) return M3_ERR_INVALID_ARG;
+    if (!(bc->eps >= 0.f)) return M3_ERR_INVALID_ARG;   // also NaN
+    *out = BcNorm{bc->B_weight, bc->B_bias, bc->C_weight, bc->C_bias, bc->eps, 1};
+    return M3_OK;
+}
+
+m3_status scan_impl(const m3_dims *dims, const void *x, const void *B, const void *C, const void *dt, const void *A,
+                    const void *lambda, const void *theta, const m3_bc_norm *bcn, const m3_state *state_in, void *y,
+                    const m3_state *state_out, void *workspace, size_t workspace_bytes, void *stream) {
     m3_status st = check_dims(dims, true);
     if (st != M3_OK) return st;
     const m3_dims &d = *dims;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    BcNorm bc;
+    if ((st = bc_args(bcn, &bc)) != M3_OK) return st;
     if (d.batch == 0) return M3_OK;   // nothing to read or write; pointers are not inspected
     const bool work = d.seqlen > 0;
     const size_t es = elem_size(d.dtype);
     if (work) {
         for (const void *p : {x, B, C, dt, A, lambda, theta})
             if (!ptr_ok(p, es)) return M3_ERR_INVALID_ARG;
-        if (!ptr_ok(y, 4)) return M3_ERR_INVALID_ARG;
+        if (!ptr_ok(y, elem_size(d.ydtype))) return M3_ERR_INVALID_ARG;
     }
     for (const m3_state *st : {state_in, state_out}) {
         if (!st) continue;
@@ -202,7 +219,8 @@ m3_status mamba3_scan_fwd(const m3_dims *dims, const void *x, const void *B, con
         return M3_ERR_WORKSPACE;
 
     ScanArgs a{};
-    a.dtype = d.dtype; a.batch = d.batch; a.L = d.seqlen; a.H = d.nheads; a.G = groups_of(d);
+    a.dtype = d.dtype; a.ydtype = d.ydtype; a.batch = d.batch; a.L = d.seqlen; a.H = d.nheads; a.G = groups_of(d);
+    a.bc = bc;
     a.P = d.headdim; a.N = d.dstate; a.R = d.rank;
     a.x = x; a.B = B; a.C = C; a.dt = dt; a.A = A; a.lam = lambda; a.theta = theta;
     a.h0 = state_in ? state_in->h : nullptr;
@@ -221,6 +239,56 @@ m3_status mamba3_scan_fwd(const m3_dims *dims, const void *x, const void *B, con
     }
     cudaError_t e = use_tc ? tc_scan(a, pl, s) : simt_scan(a, pl, s);
     return e == cudaSuccess ? M3_OK : M3_ERR_CUDA;
+}
+
+m3_status decode_impl(const m3_dims *dims, const void *x, const void *B, const void *C, const void *dt, const void *A,
+                      const void *lambda, const void *theta, const m3_bc_norm *bcn, const m3_state *state, void *y,
+                      void *stream) {
+    m3_status st = check_dims(dims, false);
+    if (st != M3_OK) return st;
+    const m3_dims &d = *dims;
+    BcNorm bc;
+    if ((st = bc_args(bcn, &bc)) != M3_OK) return st;
+    if (d.batch == 0) return M3_OK;   // nothing to read or write; pointers are not inspected
+    if (!state) return M3_ERR_INVALID_ARG;
+    const size_t es = elem_size(d.dtype);
+    for (const void *p : {x, B, C, dt, A, lambda, theta, (const void *)state->B_prev,
+                          (const void *)state->x_prev})
+        if (!ptr_ok(p, es)) return M3_ERR_INVALID_ARG;
+    if (!ptr_ok(y, elem_size(d.ydtype))) return M3_ERR_INVALID_ARG;
+    if (!ptr_ok(state->h, 16)) return M3_ERR_INVALID_ARG;
+    const int G = groups_of(d);
+    if (G != d.nheads) {
+        if (bc.on) return M3_ERR_UNSUPPORTED;   // grouped B / C: tensor-core kernel only, which has no BC step
+        const void *ptrs[] = {x, B, C, theta, state->h, state->B_prev, state->x_prev};
+        if (!decode_tc_ok(d.dtype, d.headdim, d.dstate, d.rank, (long long)d.batch * d.nheads, ptrs, 7))
+            return M3_ERR_UNSUPPORTED;
+    }
+    cudaError_t e = decode_step(d.dtype, d.ydtype, d.batch, d.nheads, G, d.headdim, d.dstate, d.rank, x, B, C, dt,
+                                A, lambda, theta, state->h, state->B_prev, state->x_prev, y,
+                                static_cast<cudaStream_t>(stream), &bc);
+    return e == cudaSuccess ? M3_OK : M3_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+m3_status mamba3_scan_fwd(const m3_dims *dims, const void *x, const void *B, const void *C,
+                          const void *dt, const void *A, const void *lambda, const void *theta,
+                          const m3_state *state_in, void *y, const m3_state *state_out,
+                          void *workspace, size_t workspace_bytes, void *stream) {
+    return scan_impl(dims, x, B, C, dt, A, lambda, theta, nullptr, state_in, y, state_out, workspace,
+                     workspace_bytes, stream);
+}
+
+m3_status mamba3_scan_fwd_bc(const m3_dims *dims, const void *x, const void *B, const void *C,
+                             const void *dt, const void *A, const void *lambda, const void *theta,
+                             const m3_bc_norm *bc, const m3_state *state_in, void *y,
+                             const m3_state *state_out, void *workspace, size_t workspace_bytes,
+                             void *stream) {
+    return scan_impl(dims, x, B, C, dt, A, lambda, theta, bc, state_in, y, state_out, workspace,
+                     workspace_bytes, stream);
 }
 
 // Token range [l0, l1) of slice i when L tokens are cut into ns slices.
@@ -274,7 +342,7 @@ m3_status mamba3_scan_fwd_staged(const m3_dims *dims, const m3_token_inputs *hos
     const size_t nb = (size_t)d.batch;
     // bytes per token (all heads) of every tensor
     const size_t G = (size_t)groups_of(d);
-    const size_t tx = H * R * P * es, tB = G * R * N * es, ts = H * es, tth = H * (N / 2) * es, ty = H * R * P * 4;
+    const size_t tx = H * R * P * es, tB = G * R * N * es, ts = H * es, tth = H * (N / 2) * es, ty = H * R * P * elem_size(d.ydtype);
     const cudaStream_t s = static_cast<cudaStream_t>(stream), cs = static_cast<cudaStream_t>(copy_stream);
     // the previous call's copies out read buffers this call rewrites: start after them
     {
@@ -338,27 +406,13 @@ m3_status mamba3_scan_fwd_staged(const m3_dims *dims, const m3_token_inputs *hos
 m3_status mamba3_decode_step(const m3_dims *dims, const void *x, const void *B, const void *C,
                              const void *dt, const void *A, const void *lambda, const void *theta,
                              const m3_state *state, void *y, void *stream) {
-    m3_status st = check_dims(dims, false);
-    if (st != M3_OK) return st;
-    const m3_dims &d = *dims;
-    if (d.batch == 0) return M3_OK;   // nothing to read or write; pointers are not inspected
-    if (!state) return M3_ERR_INVALID_ARG;
-    const size_t es = elem_size(d.dtype);
-    for (const void *p : {x, B, C, dt, A, lambda, theta, (const void *)state->B_prev,
-                          (const void *)state->x_prev})
-        if (!ptr_ok(p, es)) return M3_ERR_INVALID_ARG;
-    if (!ptr_ok(y, 4)) return M3_ERR_INVALID_ARG;
-    if (!ptr_ok(state->h, 16)) return M3_ERR_INVALID_ARG;
-    const int G = groups_of(d);
-    if (G != d.nheads) {
-        const void *ptrs[] = {x, B, C, theta, state->h, state->B_prev, state->x_prev};
-        if (!decode_tc_ok(d.dtype, d.headdim, d.dstate, d.rank, (long long)d.batch * d.nheads, ptrs, 7))
-            return M3_ERR_UNSUPPORTED;
-    }
-    cudaError_t e = decode_step(d.dtype, d.batch, d.nheads, G, d.headdim, d.dstate, d.rank, x, B, C, dt,
-                                A, lambda, theta, state->h, state->B_prev, state->x_prev, y,
-                                static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? M3_OK : M3_ERR_CUDA;
+    return decode_impl(dims, x, B, C, dt, A, lambda, theta, nullptr, state, y, stream);
+}
+
+m3_status mamba3_decode_step_bc(const m3_dims *dims, const void *x, const void *B, const void *C,
+                                const void *dt, const void *A, const void *lambda, const void *theta,
+                                const m3_bc_norm *bc, const m3_state *state, void *y, void *stream) {
+    return decode_impl(dims, x, B, C, dt, A, lambda, theta, bc, state, y, stream);
 }
 
 m3_status mamba3_decode_step_pooled(const m3_dims *dims, const int *slot, const void *x, const void *B,
@@ -373,12 +427,12 @@ m3_status mamba3_decode_step_pooled(const m3_dims *dims, const int *slot, const 
     const size_t es = elem_size(d.dtype);
     for (const void *p : {x, B, C, dt, A, lambda, theta, (const void *)pool->B_prev, (const void *)pool->x_prev})
         if (!ptr_ok(p, es)) return M3_ERR_INVALID_ARG;
-    if (!ptr_ok(y, 4)) return M3_ERR_INVALID_ARG;
+    if (!ptr_ok(y, elem_size(d.ydtype))) return M3_ERR_INVALID_ARG;
     if (!ptr_ok(pool->h, 16)) return M3_ERR_INVALID_ARG;
     const void *ptrs[] = {x, B, C, theta, pool->h, pool->B_prev, pool->x_prev};
     const long long heads = (long long)(d.batch > pool_size ? d.batch : pool_size) * d.nheads;
     if (!decode_tc_ok(d.dtype, d.headdim, d.dstate, d.rank, heads, ptrs, 7)) return M3_ERR_UNSUPPORTED;
-    cudaError_t e = decode_step_pooled(d.batch, d.nheads, groups_of(d), d.headdim, d.dstate, d.rank, slot,
+    cudaError_t e = decode_step_pooled(d.ydtype, d.batch, d.nheads, groups_of(d), d.headdim, d.dstate, d.rank, slot,
                                        pool_size, x, B, C, dt, A, lambda, theta, pool->h, pool->B_prev,
                                        pool->x_prev, y, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? M3_OK : M3_ERR_CUDA;

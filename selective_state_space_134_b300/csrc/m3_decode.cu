@@ -40,7 +40,7 @@ __global__ void __launch_bounds__(kThreads)
 decode_kernel(int H, int P, int N, int R, const T *__restrict__ x, const T *__restrict__ Bm,
               const T *__restrict__ Cm, const T *__restrict__ dtp, const T *__restrict__ Ap,
               const T *__restrict__ lp, const T *__restrict__ thp, float *__restrict__ hs,
-              T *__restrict__ Bprev, T *__restrict__ xprev, float *__restrict__ y) {
+              T *__restrict__ Bprev, T *__restrict__ xprev, void *__restrict__ y, int yd, BcNorm bc) {
     extern __shared__ float sm[];
     const int K = N / 2, RN = R * N, RP = R * P;
     float *sB = sm, *sC = sB + RN, *sBp = sC + RN, *sx = sBp + RN, *sxp = sx + RP;
@@ -67,6 +67,22 @@ decode_kernel(int H, int P, int N, int R, const T *__restrict__ x, const T *__re
         ss[k] = s;
     }
     __syncthreads();
+    if (bc.on) {
+        // BC normalisation and bias of the staged rows, in place: B, C and the carried B_prev
+        // (one warp per row: inverse RMS over the N entries, then gain and bias)
+        const int lane = tid & 31, h = (int)(bh % H);
+        for (int q = tid >> 5; q < 3 * R; q += kThreads / 32) {
+            float *row = (q < R ? sB : (q < 2 * R ? sC : sBp)) + (q % R) * N;
+            const float *w = q >= R && q < 2 * R ? bc.wC : bc.wB, *bias = q >= R && q < 2 * R ? bc.bC : bc.bB;
+            float ssq = 0.f;
+            for (int n = lane; n < N; n += 32) ssq = fmaf(row[n], row[n], ssq);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) ssq += __shfl_xor_sync(0xffffffffu, ssq, o);
+            const float inv = 1.f / sqrtf(ssq / (float)N + bc.eps);
+            for (int n = lane; n < N; n += 32) row[n] = bc_apply(row[n], inv, w, bias, h, q % R, R, N, n);
+        }
+        __syncthreads();
+    }
     // new carry = this token's (B, x); every read of the old carry is above
     for (int i = tid; i < RN; i += kThreads) Bprev[bh * RN + i] = Bm[bh * RN + i];
     for (int i = tid; i < RP; i += kThreads) xprev[bh * RP + i] = x[bh * RP + i];
@@ -141,7 +157,7 @@ decode_kernel(int H, int P, int N, int R, const T *__restrict__ x, const T *__re
     for (int i = tid; i < RP; i += kThreads) {
         float v = 0.f;
         for (int g = 0; g < KG; ++g) v += red[g * RP + i];
-        y[bh * RP + i] = v;
+        store_y(y, bh * RP + i, v, yd);
     }
 }
 
@@ -163,7 +179,7 @@ constexpr uint64_t kStreamWaitNs = 2000000000ull;   // 2 s per mbarrier wait; fa
 
 struct StreamLayout {
     uint32_t st, B, C, Bp, x, xp, th, stage;   // byte offsets inside a stage, stage size
-    uint32_t red, bar, flag, total;            // offsets after the stages, total bytes
+    uint32_t red, bar, flag, inv, total;       // offsets after the stages, total bytes
     __host__ __device__ StreamLayout(int N, int P, int R, int e, int nst) {
         auto up = [](uint32_t v) { return (v + 127u) & ~127u; };
         const uint32_t bn = (uint32_t)(R * N * e), xn = (uint32_t)(R * P * e);
@@ -178,7 +194,8 @@ struct StreamLayout {
         red = stage * nst;                                     // y partial sums [NPG][R][P]
         bar = up(red + (uint32_t)(kStreamThreads * 4 * R * 4));
         flag = bar + 8u * nst;
-        total = flag + 16;
+        inv = flag + 16;                                       // BC norm: inverse RMS of 3 R rows
+        total = inv + 3u * 8u * 4u;
     }
 };
 
@@ -212,10 +229,10 @@ __device__ __forceinline__ void sincos_reduced(float a, float *s, float *c) {
 
 template <typename T, int R>
 __global__ void __launch_bounds__(kStreamThreads, 2)
-decode_stream_kernel(int nbh, int P, int N, int nst, const T *__restrict__ x, const T *__restrict__ Bm,
+decode_stream_kernel(int nbh, int H, int P, int N, int nst, BcNorm bc, const T *__restrict__ x, const T *__restrict__ Bm,
                      const T *__restrict__ Cm, const T *__restrict__ dtp, const T *__restrict__ Ap,
                      const T *__restrict__ lp, const T *__restrict__ thp, float *__restrict__ hs,
-                     T *__restrict__ Bprev, T *__restrict__ xprev, float *__restrict__ y, unsigned *status) {
+                     T *__restrict__ Bprev, T *__restrict__ xprev, void *__restrict__ y, int yd, unsigned *status) {
     using namespace tc;
     extern __shared__ __align__(128) unsigned char smem_s[];
     unsigned char *sm = smem_s;
@@ -283,6 +300,25 @@ decode_stream_kernel(int nbh, int P, int N, int nst, const T *__restrict__ x, co
         const T *sBp = reinterpret_cast<const T *>(sg + Lo.Bp), *sx = reinterpret_cast<const T *>(sg + Lo.x);
         const T *sxp = reinterpret_cast<const T *>(sg + Lo.xp), *sth = reinterpret_cast<const T *>(sg + Lo.th);
         float *st = reinterpret_cast<float *>(sg + Lo.st);
+        float *binv = reinterpret_cast<float *>(sm + Lo.inv);   // [3][R]: B, C, B_prev rows
+        const int hh = (int)(bh % H);
+        if (bc.on) {
+            // inverse RMS of the staged B, C and B_prev rows (one warp per row); the staged rows
+            // stay raw (B is stored back as the carry) and are normalised as they are read
+            const int lane = tid & 31;
+            for (int q = tid >> 5; q < 3 * R; q += kStreamThreads / 32) {
+                const T *row = (q < R ? sB : (q < 2 * R ? sC : sBp)) + (q % R) * N;
+                float ssq = 0.f;
+                for (int n = lane; n < N; n += 32) {
+                    const float v = to_f(row[n]);
+                    ssq = fmaf(v, v, ssq);
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) ssq += __shfl_xor_sync(0xffffffffu, ssq, o);
+                if (lane == 0) binv[q] = 1.f / sqrtf(ssq / (float)N + bc.eps);
+            }
+            __syncthreads();
+        }
 
         const float rho = expf(d * av), left = (1.f - l) * d, right = l * d;
         float xr[R][4], xq[R][4];
@@ -311,6 +347,12 @@ decode_stream_kernel(int nbh, int P, int N, int nst, const T *__restrict__ x, co
                 float b0, b1, q0, q1;
                 pair_f(sB + r * N + 2 * k, b0, b1);
                 pair_f(sBp + r * N + 2 * k, q0, q1);
+                if (bc.on) {
+                    b0 = bc_apply(b0, binv[r], bc.wB, bc.bB, hh, r, R, N, 2 * k);
+                    b1 = bc_apply(b1, binv[r], bc.wB, bc.bB, hh, r, R, N, 2 * k + 1);
+                    q0 = bc_apply(q0, binv[2 * R + r], bc.wB, bc.bB, hh, r, R, N, 2 * k);
+                    q1 = bc_apply(q1, binv[2 * R + r], bc.wB, bc.bB, hh, r, R, N, 2 * k + 1);
+                }
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     u0[c] = fmaf(q0, xq[r][c], u0[c]);
@@ -331,6 +373,10 @@ decode_stream_kernel(int nbh, int P, int N, int nst, const T *__restrict__ x, co
             for (int r = 0; r < R; ++r) {
                 float c0, c1;
                 pair_f(sC + r * N + 2 * k, c0, c1);
+                if (bc.on) {
+                    c0 = bc_apply(c0, binv[R + r], bc.wC, bc.bC, hh, r, R, N, 2 * k);
+                    c1 = bc_apply(c1, binv[R + r], bc.wC, bc.bC, hh, r, R, N, 2 * k + 1);
+                }
 #pragma unroll
                 for (int c = 0; c < 4; ++c) yacc[r][c] = fmaf(c0, a0[c], fmaf(c1, a1[c], yacc[r][c]));
             }
@@ -355,7 +401,7 @@ decode_stream_kernel(int nbh, int P, int N, int nst, const T *__restrict__ x, co
         for (int i = tid; i < R * P; i += kStreamThreads) {
             float v = 0.f;
             for (int q = 0; q < NPG; ++q) v += red[q * R * P + i];
-            y[bh * R * P + i] = v;
+            store_y(y, bh * R * P + i, v, yd);
         }
     }
     if (tid == 0) {
@@ -370,7 +416,7 @@ decode_stream_kernel(int nbh, int P, int N, int nst, const T *__restrict__ x, co
 template <typename T>
 cudaError_t launch_decode(int batch, int H, int P, int N, int R, const void *x, const void *B,
                           const void *C, const void *dt, const void *A, const void *lam,
-                          const void *theta, float *h, void *Bprev, void *xprev, void *y,
+                          const void *theta, float *h, void *Bprev, void *xprev, void *y, int yd, const BcNorm &bc,
                           cudaStream_t s) {
     const int NCG = P / 4, KG = kThreads / NCG, K = N / 2;
     const size_t smem = sizeof(float) * (3 * (size_t)R * N + 2 * (size_t)R * P + 2 * (size_t)K +
@@ -385,7 +431,7 @@ cudaError_t launch_decode(int batch, int H, int P, int N, int R, const void *x, 
         if (e != cudaSuccess) return e;                                                           \
         kern<<<grid, kThreads, smem, s>>>(H, P, N, R, (const T *)x, (const T *)B, (const T *)C,  \
                                           (const T *)dt, (const T *)A, (const T *)lam,            \
-                                          (const T *)theta, h, (T *)Bprev, (T *)xprev, (float *)y);   \
+                                          (const T *)theta, h, (T *)Bprev, (T *)xprev, y, yd, bc);   \
     } while (0)
     trace_mark(M3_KERNEL_DECODE, s, 0);
     if (pairs_per_thread <= 4)
@@ -400,9 +446,9 @@ cudaError_t launch_decode(int batch, int H, int P, int N, int R, const void *x, 
 
 
 template <typename T, int R>
-cudaError_t launch_stream(int nbh, int P, int N, const void *x, const void *B, const void *C, const void *dt,
+cudaError_t launch_stream(int nbh, int H, int P, int N, const void *x, const void *B, const void *C, const void *dt,
                           const void *A, const void *lam, const void *theta, float *h, void *Bprev, void *xprev,
-                          void *y, cudaStream_t s) {
+                          void *y, int yd, const BcNorm &bc, cudaStream_t s) {
     const int e = (int)sizeof(T);
     // two CTAs per SM with as many stages as fit (2..6), else one CTA per SM
     int per_sm = 2, nst = 6;
@@ -421,9 +467,9 @@ cudaError_t launch_stream(int nbh, int P, int N, const void *x, const void *B, c
     if (err != cudaSuccess) return err;
     const int grid = nbh < per_sm * sm_count() ? nbh : per_sm * sm_count();
     trace_mark(M3_KERNEL_DECODE, s, 0);
-    kern<<<grid, kStreamThreads, Lo.total, s>>>(nbh, P, N, nst, (const T *)x, (const T *)B, (const T *)C,
+    kern<<<grid, kStreamThreads, Lo.total, s>>>(nbh, H, P, N, nst, bc, (const T *)x, (const T *)B, (const T *)C,
                                                 (const T *)dt, (const T *)A, (const T *)lam, (const T *)theta, h,
-                                                (T *)Bprev, (T *)xprev, (float *)y, status);
+                                                (T *)Bprev, (T *)xprev, y, yd, status);
     trace_mark(M3_KERNEL_DECODE, s, 1);
     count_launch();
     return cudaGetLastError();
@@ -441,14 +487,14 @@ bool stream_ok(int e, int P, int N, int R, const void *const *ptrs, int nptr) {
 }
 
 template <typename T>
-cudaError_t stream_dispatch(int nbh, int P, int N, int R, const void *x, const void *B, const void *C,
+cudaError_t stream_dispatch(int nbh, int H, int P, int N, int R, const void *x, const void *B, const void *C,
                             const void *dt, const void *A, const void *lam, const void *theta, float *h,
-                            void *Bprev, void *xprev, void *y, cudaStream_t s) {
+                            void *Bprev, void *xprev, void *y, int yd, const BcNorm &bc, cudaStream_t s) {
     switch (R) {
-        case 1: return launch_stream<T, 1>(nbh, P, N, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, s);
-        case 2: return launch_stream<T, 2>(nbh, P, N, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, s);
-        case 4: return launch_stream<T, 4>(nbh, P, N, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, s);
-        default: return launch_stream<T, 8>(nbh, P, N, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, s);
+        case 1: return launch_stream<T, 1>(nbh, H, P, N, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, yd, bc, s);
+        case 2: return launch_stream<T, 2>(nbh, H, P, N, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, yd, bc, s);
+        case 4: return launch_stream<T, 4>(nbh, H, P, N, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, yd, bc, s);
+        default: return launch_stream<T, 8>(nbh, H, P, N, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, yd, bc, s);
     }
 }
 
@@ -521,7 +567,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap hmap, const __grid_constan
                   const __nv_bfloat16 *__restrict__ Bm, const __nv_bfloat16 *__restrict__ Cm,
                   const __nv_bfloat16 *__restrict__ dtp, const __nv_bfloat16 *__restrict__ Ap,
                   const __nv_bfloat16 *__restrict__ lp, const __nv_bfloat16 *__restrict__ thp,
-                  __nv_bfloat16 *__restrict__ Bprev, __nv_bfloat16 *__restrict__ xprev, float *__restrict__ y,
+                  __nv_bfloat16 *__restrict__ Bprev, __nv_bfloat16 *__restrict__ xprev, void *__restrict__ y, int yd,
                   unsigned *status) {
     using namespace tc;
     constexpr int P = kMmaP, K = N / 2, NW = HPU == 2 ? N : N / 2, NKS = NW / 16;
@@ -650,7 +696,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap hmap, const __grid_constan
         if (POOL && tid == 0 && sh0 < 0 && slot[bh0 / H] >= pool) atomicOr(status, kStatusBadIndex);
         float yacc[4] = {0.f, 0.f, 0.f, 0.f};
         // y[r][p] for r = 2t, 2t + 1 and p = p0 + g, p0 + g + 8
-        float *yo = y + (size_t)(bh0 + hh) * R * P + 2 * t * P + p0 + g;
+        const size_t yo = (size_t)(bh0 + hh) * R * P + 2 * t * P + p0 + g;
         if (sh0 >= 0) {
             const unsigned char *sB = sg + Lo.B, *sBp = sg + Lo.Bp, *sC = sg + Lo.C;
             const unsigned short *sx = reinterpret_cast<const unsigned short *>(sg + Lo.x) + hh * R * P;
@@ -722,11 +768,11 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap hmap, const __grid_constan
                 mma_m16n8k16(yacc, alo, b0, b1);
             }
             if (HPU == 2 && rlane) {
-                yo[0] = yacc[0];
-                yo[8] = yacc[2];
+                store_y(y, yo, yacc[0], yd);
+                store_y(y, yo + 8, yacc[2], yd);
                 if (R > 1) {
-                    yo[P] = yacc[1];
-                    yo[P + 8] = yacc[3];
+                    store_y(y, yo + P, yacc[1], yd);
+                    store_y(y, yo + P + 8, yacc[3], yd);
                 }
             }
             if (HPU == 1 && grp == 0) red[pt * 32 + lane] = make_float4(yacc[0], yacc[1], yacc[2], yacc[3]);
@@ -755,11 +801,11 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap hmap, const __grid_constan
         }
         if (sh0 >= 0 && HPU == 1 && grp == 1 && rlane) {
             const float4 o = red[pt * 32 + lane];
-            yo[0] = yacc[0] + o.x;
-            yo[8] = yacc[2] + o.z;
+            store_y(y, yo, yacc[0] + o.x, yd);
+            store_y(y, yo + 8, yacc[2] + o.z, yd);
             if (R > 1) {
-                yo[P] = yacc[1] + o.y;
-                yo[P + 8] = yacc[3] + o.w;
+                store_y(y, yo + P, yacc[1] + o.y, yd);
+                store_y(y, yo + P + 8, yacc[3] + o.w, yd);
             }
         }
     }
@@ -804,7 +850,7 @@ bool map_state(CUtensorMap *m, float *h, long long rows, int box_rows) {
 template <int R, int N, int HPU, bool kSwz>
 cudaError_t launch_mma_t(int nbh, int H, int G, const int *slot, int pool, const void *x, const void *B,
                          const void *C, const void *dt, const void *A, const void *lam, const void *theta, float *h,
-                         void *Bprev, void *xprev, void *y, cudaStream_t s) {
+                         void *Bprev, void *xprev, void *y, int yd, cudaStream_t s) {
     const long long pool_heads = slot ? (long long)pool * H : (long long)nbh;
     // the state and carry maps depend only on (h, B_prev, shape); a decode loop reuses one state
     struct MapCache {
@@ -855,7 +901,7 @@ cudaError_t launch_mma_t(int nbh, int H, int G, const int *slot, int pool, const
     kern<<<grid, kMmaThreads, Lo.total, s>>>(cache.hmap, bmap, cmap, cache.bpmap, nunit, nst, slot, pool, H, G,
                                             (const bf *)x, (const bf *)B, (const bf *)C, (const bf *)dt,
                                             (const bf *)A, (const bf *)lam, (const bf *)theta, (bf *)Bprev,
-                                            (bf *)xprev, (float *)y, status);
+                                            (bf *)xprev, y, yd, status);
     trace_mark(M3_KERNEL_DECODE, s, 1);
     count_launch();
     return cudaGetLastError();
@@ -864,13 +910,13 @@ cudaError_t launch_mma_t(int nbh, int H, int G, const int *slot, int pool, const
 template <int R, int N, int HPU>
 cudaError_t launch_mma(int nbh, int H, int G, const int *slot, int pool, const void *x, const void *B, const void *C,
                        const void *dt, const void *A, const void *lam, const void *theta, float *h, void *Bprev,
-                       void *xprev, void *y, cudaStream_t s) {
+                       void *xprev, void *y, int yd, cudaStream_t s) {
     if constexpr ((HPU * R) % 8 == 0) {
         if (G == H)
             return launch_mma_t<R, N, HPU, true>(nbh, H, G, slot, pool, x, B, C, dt, A, lam, theta, h, Bprev, xprev,
-                                                 y, s);
+                                                 y, yd, s);
     }
-    return launch_mma_t<R, N, HPU, false>(nbh, H, G, slot, pool, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, s);
+    return launch_mma_t<R, N, HPU, false>(nbh, H, G, slot, pool, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, yd, s);
 }
 
 // The tensor-core variant takes bf16 inputs with P = 64, N in {64, 128}, R in {1, 2, 4, 8},
@@ -886,11 +932,11 @@ bool mma_ok(int dtype, int P, int N, int R, long long nbh) {
 // when H is even, so that the two heads share a batch row and thus a pool slot).
 cudaError_t mma_dispatch(int nbh, int H, int G, const int *slot, int pool, int N, int R, const void *x,
                          const void *B, const void *C, const void *dt, const void *A, const void *lam,
-                         const void *theta, float *h, void *Bprev, void *xprev, void *y, cudaStream_t s) {
+                         const void *theta, float *h, void *Bprev, void *xprev, void *y, int yd, cudaStream_t s) {
     const bool pair = N == 64 && (slot || G != H ? H % 2 == 0 : nbh % 2 == 0);
 #define M3_MMA(RR, NN, HH)                                                                                         \
     if (R == RR && N == NN && (HH == 2) == pair)                                                                 \
-    return launch_mma<RR, NN, HH>(nbh, H, G, slot, pool, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, s)
+    return launch_mma<RR, NN, HH>(nbh, H, G, slot, pool, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, yd, s)
     M3_MMA(1, 64, 2);
     M3_MMA(2, 64, 2);
     M3_MMA(4, 64, 2);
@@ -911,47 +957,49 @@ cudaError_t mma_dispatch(int nbh, int H, int G, const int *slot, int pool, int N
 
 std::atomic<int> g_last_decode_variant{-1};
 
-cudaError_t decode_step(int dtype, int batch, int H, int G, int P, int N, int R, const void *x,
+cudaError_t decode_step(int dtype, int yd, int batch, int H, int G, int P, int N, int R, const void *x,
                         const void *B, const void *C, const void *dt, const void *A,
                         const void *lam, const void *theta, float *h, void *Bprev, void *xprev,
-                        void *y, cudaStream_t s) {
+                        void *y, cudaStream_t s, const BcNorm *bcp) {
     const int e = dtype == M3_F32 ? 4 : 2;
     const void *ptrs[] = {x, B, C, theta, h, Bprev, xprev};
     const int nbh = batch * H;
-    if (G != H) {   // grouped B / C: tensor-core kernel only (the caller checked decode_tc_ok)
+    const BcNorm bc = bcp ? *bcp : BcNorm{};
+    if (G != H) {   // grouped B / C: tensor-core kernel only (the caller checked decode_tc_ok, and bc is off)
         if (nbh == 0) return cudaSuccess;
         g_last_decode_variant.store(M3_DECODE_TENSOR, std::memory_order_relaxed);
-        return mma_dispatch(nbh, H, G, nullptr, batch, N, R, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, s);
+        return mma_dispatch(nbh, H, G, nullptr, batch, N, R, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, yd, s);
     }
     if (nbh > 0 && stream_ok(e, P, N, R, ptrs, 7)) {
-        if (mma_ok(dtype, P, N, R, nbh)) {
+        if (!bc.on && mma_ok(dtype, P, N, R, nbh)) {
             g_last_decode_variant.store(M3_DECODE_TENSOR, std::memory_order_relaxed);
-            return mma_dispatch(nbh, H, H, nullptr, batch, N, R, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, s);
+            return mma_dispatch(nbh, H, H, nullptr, batch, N, R, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, yd, s);
         }
         g_last_decode_variant.store(M3_DECODE_STREAM, std::memory_order_relaxed);
         if (dtype == M3_F32)
-            return stream_dispatch<float>(nbh, P, N, R, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, s);
-        return stream_dispatch<__nv_bfloat16>(nbh, P, N, R, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, s);
+            return stream_dispatch<float>(nbh, H, P, N, R, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, yd, bc, s);
+        return stream_dispatch<__nv_bfloat16>(nbh, H, P, N, R, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, yd, bc,
+                                              s);
     }
     g_last_decode_variant.store(M3_DECODE_GENERIC, std::memory_order_relaxed);
     if (dtype == M3_F32)
-        return launch_decode<float>(batch, H, P, N, R, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, s);
+        return launch_decode<float>(batch, H, P, N, R, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, yd, bc, s);
     return launch_decode<__nv_bfloat16>(batch, H, P, N, R, x, B, C, dt, A, lam, theta, h, Bprev,
-                                        xprev, y, s);
+                                        xprev, y, yd, bc, s);
 }
 
 bool decode_tc_ok(int dtype, int P, int N, int R, long long heads, const void *const *ptrs, int nptr) {
     return mma_ok(dtype, P, N, R, heads) && stream_ok(2, P, N, R, ptrs, nptr);
 }
 
-cudaError_t decode_step_pooled(int batch, int H, int G, int P, int N, int R, const int *slot, int pool,
+cudaError_t decode_step_pooled(int yd, int batch, int H, int G, int P, int N, int R, const int *slot, int pool,
                                const void *x, const void *B, const void *C, const void *dt, const void *A,
                                const void *lam, const void *theta, float *h, void *Bprev, void *xprev, void *y,
                                cudaStream_t s) {
     (void)P;
     if (batch == 0) return cudaSuccess;
     g_last_decode_variant.store(M3_DECODE_TENSOR, std::memory_order_relaxed);
-    return mma_dispatch(batch * H, H, G, slot, pool, N, R, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, s);
+    return mma_dispatch(batch * H, H, G, slot, pool, N, R, x, B, C, dt, A, lam, theta, h, Bprev, xprev, y, yd, s);
 }
 
 }  // namespace m3

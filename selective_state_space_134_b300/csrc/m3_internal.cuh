@@ -3,6 +3,7 @@
 
 #include <atomic>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -17,6 +18,13 @@ template <typename T> __device__ __forceinline__ T from_f(float v);
 template <> __device__ __forceinline__ float from_f<float>(float v) { return v; }
 template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) {
     return __float2bfloat16_rn(v);
+}
+
+// One element of y, rounded once (to nearest even) from fp32 to the output type `yd` (m3_dtype).
+__device__ __forceinline__ void store_y(void *y, size_t i, float v, int yd) {
+    if (yd == M3_F32) static_cast<float *>(y)[i] = v;
+    else if (yd == M3_BF16) static_cast<__nv_bfloat16 *>(y)[i] = __float2bfloat16_rn(v);
+    else static_cast<__half *>(y)[i] = __float2half_rn(v);
 }
 
 // Device status word bits (read and cleared by mamba3_device_status).
@@ -69,8 +77,24 @@ struct ScanPlan {
 };
 enum { kPathSimt = 0, kPathTc = 1 };
 
+// BC normalisation and bias (m3_bc_norm); on = 0: B and C enter the recurrence as given.
+struct BcNorm {
+    const float *wB, *bB, *wC, *bC;   // [H][N] gains (null = 1), [H][R][N] biases (null = 0)
+    float eps;
+    int on;
+};
+
+// The normalised value of entry n of a row whose inverse RMS is `inv` (head h, rank r).
+__device__ __forceinline__ float bc_apply(float v, float inv, const float *w, const float *bias, int h, int r,
+                                          int R, int N, int n) {
+    const float g = w ? __ldg(w + (size_t)h * N + n) : 1.f;
+    const float c = bias ? __ldg(bias + ((size_t)h * R + r) * N + n) : 0.f;
+    return fmaf(v * inv, g, c);
+}
+
 struct ScanArgs {
-    int dtype, batch, L, H, P, N, R;
+    int dtype, ydtype, batch, L, H, P, N, R;
+    BcNorm bc;
     int G;                      // B / C groups (G = H: one per head)
     const void *x, *B, *C, *dt, *A, *lam, *theta;
     const float *h0;            // may be null (zero state)
@@ -81,6 +105,21 @@ struct ScanArgs {
     float *ws_state;            // [b*H][nseg][N][P]  (nseg > 1)
     float *ws_tot;              // [b*H][nseg-1][1 + N/2]
 };
+
+// Backward pass (mamba3_scan_bwd): forward inputs, incoming and outgoing gradients (fp32).
+struct BwdArgs {
+    int dtype, batch, L, H, P, N, R;
+    const void *x, *B, *C, *dt, *A, *lam, *theta;
+    const float *h0;
+    const void *Bprev, *xprev;
+    const float *dy, *dh_out, *dBprev_out, *dxprev_out;
+    float *dx, *dB, *dC, *ddt, *dA, *dlam, *dtheta, *dh0, *dBprev, *dxprev;
+    float *ws;                  // [b*H][L/Q + 1][N][P] state checkpoints
+};
+int bwd_chunk(int R);                                                   // tokens per chunk
+size_t bwd_smem_bytes(int N, int P, int R);
+size_t bwd_workspace_bytes(int batch, int H, int L, int N, int P, int R);
+cudaError_t scan_bwd(const BwdArgs &a, cudaStream_t s);
 
 // Workspace layout sizes (bytes) for a plan.
 size_t scan_workspace_bytes(int batch, int H, int N, int P, int nseg);
@@ -98,13 +137,14 @@ cudaError_t tc_scan(const ScanArgs &a, const ScanPlan &plan, cudaStream_t s);
 cudaError_t segment_pass(const ScanArgs &a, const ScanPlan &plan, cudaStream_t s);
 
 // Decode step.
-cudaError_t decode_step(int dtype, int batch, int H, int G, int P, int N, int R, const void *x,
+// bc: BC normalisation (null or bc->on == 0: none; then the tensor-core kernel may serve the call)
+cudaError_t decode_step(int dtype, int ydtype, int batch, int H, int G, int P, int N, int R, const void *x,
                         const void *B, const void *C, const void *dt, const void *A,
                         const void *lam, const void *theta, float *h, void *Bprev, void *xprev,
-                        void *y, cudaStream_t s);
+                        void *y, cudaStream_t s, const BcNorm *bc = nullptr);
 // The tensor-core decode's shapes (pooled and grouped decode run only there), and the pooled launch.
 bool decode_tc_ok(int dtype, int P, int N, int R, long long heads, const void *const *ptrs, int nptr);
-cudaError_t decode_step_pooled(int batch, int H, int G, int P, int N, int R, const int *slot, int pool,
+cudaError_t decode_step_pooled(int ydtype, int batch, int H, int G, int P, int N, int R, const int *slot, int pool,
                                const void *x, const void *B, const void *C, const void *dt, const void *A,
                                const void *lam, const void *theta, float *h, void *Bprev, void *xprev, void *y,
                                cudaStream_t s);

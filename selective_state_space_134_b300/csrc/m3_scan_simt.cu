@@ -26,7 +26,7 @@ constexpr int kThreads = 256;
 // that threads reading consecutive rows hit different banks.
 struct SimtSmem {
     int N, P, Q, R, K, QR, NS;
-    size_t oH, oB, oC, oX, oG, ocA, og, ow, odt, ocs, osn, oacc, total;
+    size_t oH, oB, oC, oX, oG, ocA, og, ow, odt, ocs, osn, oacc, oiB, oiC, total;
     __host__ __device__ SimtSmem(int Q_, int R_, int N_, int P_, bool out) {
         Q = Q_; R = R_; N = N_; P = P_; K = N / 2; QR = Q * R; NS = N + 1;
         size_t o = 0;
@@ -42,6 +42,8 @@ struct SimtSmem {
         ocs = o; o += (size_t)Q * K;
         osn = o; o += (size_t)Q * K;
         oacc = o; o += 1 + K;        // segment totals (pass 1)
+        oiB = o; o += QR;            // BC norm: inverse RMS of the chunk's B rows (carry rows first)
+        oiC = o; o += QR;            // ... and of its C rows
         total = o;
     }
 };
@@ -70,7 +72,7 @@ simt_segment_kernel(ScanArgs a, int Q, int seglen, int nseg, int nlaunch) {
     const SimtSmem L(Q, a.R, a.N, a.P, OUT);
     float *Hs = sm + L.oH, *Bb = sm + L.oB, *Cb = sm + L.oC, *Xs = sm + L.oX, *G = sm + L.oG;
     float *cA = sm + L.ocA, *gv = sm + L.og, *wv = sm + L.ow, *dts = sm + L.odt;
-    float *cs = sm + L.ocs, *sn = sm + L.osn, *acc = sm + L.oacc;
+    float *cs = sm + L.ocs, *sn = sm + L.osn, *acc = sm + L.oacc, *iB = sm + L.oiB, *iC = sm + L.oiC;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int N = a.N, P = a.P, R = a.R, K = N / 2, H = a.H, Lq = a.L, NS = L.NS;
@@ -90,13 +92,30 @@ simt_segment_kernel(ScanArgs a, int Q, int seglen, int nseg, int nlaunch) {
     } else if (nseg == 1) {
         const float left0 = (1.f - to_f(lp[tok(0)])) * to_f(dtp[tok(0)]);
         const T *bq = (const T *)a.Bprev, *xq = (const T *)a.xprev;
+        if (a.bc.on && bq && xq) {
+            // inverse RMS of the carried B rows (BC normalisation; one warp per row)
+            for (int r = warp; r < R; r += kThreads / 32) {
+                float ssq = 0.f;
+                for (int n = lane; n < N; n += 32) {
+                    const float v = to_f(bq[((size_t)bh * R + r) * N + n]);
+                    ssq = fmaf(v, v, ssq);
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) ssq += __shfl_xor_sync(0xffffffffu, ssq, o);
+                if (lane == 0) iB[r] = 1.f / sqrtf(ssq / (float)N + a.bc.eps);
+            }
+            __syncthreads();
+        }
         for (int i = tid; i < N * P; i += kThreads) {
             const int n = i / P, p = i % P;
             float v = a.h0 ? a.h0[(size_t)bh * N * P + i] : 0.f;
             if (bq && xq) {
                 float u = 0.f;
-                for (int r = 0; r < R; ++r)
-                    u += to_f(bq[((size_t)bh * R + r) * N + n]) * to_f(xq[((size_t)bh * R + r) * P + p]);
+                for (int r = 0; r < R; ++r) {
+                    float bv = to_f(bq[((size_t)bh * R + r) * N + n]);
+                    if (a.bc.on) bv = bc_apply(bv, iB[r], a.bc.wB, a.bc.bB, h, r, R, N, n);
+                    u += bv * to_f(xq[((size_t)bh * R + r) * P + p]);
+                }
                 v += left0 * u;
             }
             Hs[i] = v;
@@ -126,6 +145,22 @@ simt_segment_kernel(ScanArgs a, int Q, int seglen, int nseg, int nlaunch) {
         }
         __syncthreads();
         if (warp == 0) warp_cumsum(cA, Qc, lane);
+        if (a.bc.on) {
+            // BC normalisation: inverse RMS of every B (and C) row of the chunk (one warp per row)
+            for (int row = warp; row < QRc * (OUT ? 2 : 1); row += kThreads / 32) {
+                const bool isC = row >= QRc;
+                const int rr = isC ? row - QRc : row, ti = rr / R, r = rr % R;
+                const T *src = (isC ? Cm : Bm) + (tok(s0 + ti) * R + r) * N;
+                float ssq = 0.f;
+                for (int n = lane; n < N; n += 32) {
+                    const float v = to_f(src[n]);
+                    ssq = fmaf(v, v, ssq);
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) ssq += __shfl_xor_sync(0xffffffffu, ssq, o);
+                if (lane == 0) (isC ? iC : iB)[rr] = 1.f / sqrtf(ssq / (float)N + a.bc.eps);
+            }
+        }
         // ---- chunk-local angles, their cos / sin
         for (int k = tid; k < K; k += kThreads) {
             float phi = 0.f;
@@ -144,11 +179,19 @@ simt_segment_kernel(ScanArgs a, int Q, int seglen, int nseg, int nlaunch) {
             const int row = i / K, k = i % K, ti = row / R, r = row % R;
             const float c = cs[ti * K + k], s = sn[ti * K + k];
             const size_t base = (tok(s0 + ti) * R + r) * N + 2 * k;
-            const float b0 = to_f(Bm[base]), b1 = to_f(Bm[base + 1]);
+            float b0 = to_f(Bm[base]), b1 = to_f(Bm[base + 1]);
+            if (a.bc.on) {
+                b0 = bc_apply(b0, iB[row], a.bc.wB, a.bc.bB, h, r, R, N, 2 * k);
+                b1 = bc_apply(b1, iB[row], a.bc.wB, a.bc.bB, h, r, R, N, 2 * k + 1);
+            }
             Bb[row * NS + 2 * k] = c * b0 + s * b1;
             Bb[row * NS + 2 * k + 1] = -s * b0 + c * b1;
             if (OUT) {
-                const float c0 = to_f(Cm[base]), c1 = to_f(Cm[base + 1]);
+                float c0 = to_f(Cm[base]), c1 = to_f(Cm[base + 1]);
+                if (a.bc.on) {
+                    c0 = bc_apply(c0, iC[row], a.bc.wC, a.bc.bC, h, r, R, N, 2 * k);
+                    c1 = bc_apply(c1, iC[row], a.bc.wC, a.bc.bC, h, r, R, N, 2 * k + 1);
+                }
                 Cb[row * NS + 2 * k] = c * c0 + s * c1;
                 Cb[row * NS + 2 * k + 1] = -s * c0 + c * c1;
             }
@@ -173,7 +216,6 @@ simt_segment_kernel(ScanArgs a, int Q, int seglen, int nseg, int nlaunch) {
             }
             __syncthreads();
             // ---- y = G X + exp(cA_t) C~ H
-            float *yp = (float *)a.y;
             for (int i = tid; i < QRc * P; i += kThreads) {
                 const int rt = i / P, p = i % P, ti = rt / R, r = rt % R;
                 float v = 0.f;
@@ -183,7 +225,7 @@ simt_segment_kernel(ScanArgs a, int Q, int seglen, int nseg, int nlaunch) {
                 const float *cr = Cb + rt * NS;
                 for (int n = 0; n < N; ++n) u += cr[n] * Hs[n * P + p];
                 v += expf(cA[ti]) * u;
-                yp[(tok(s0 + ti) * R + r) * P + p] = v;
+                store_y(a.y, (tok(s0 + ti) * R + r) * P + p, v, a.ydtype);
             }
             __syncthreads();   // every read of H above precedes the update below
         }
@@ -258,8 +300,17 @@ __global__ void segment_pass_kernel(ScanArgs a, int nseg) {
         float u0 = 0.f, u1 = 0.f;
         for (int r = 0; r < R; ++r) {
             const float xv = to_f(xq[((size_t)bh * R + r) * P + p]);
-            u0 += to_f(bq[((size_t)bh * R + r) * N + 2 * k]) * xv;
-            u1 += to_f(bq[((size_t)bh * R + r) * N + 2 * k + 1]) * xv;
+            const T *row = bq + ((size_t)bh * R + r) * N;
+            float q0 = to_f(row[2 * k]), q1 = to_f(row[2 * k + 1]);
+            if (a.bc.on) {   // BC normalisation of the carried B row (this thread sums it itself)
+                float ssq = 0.f;
+                for (int n = 0; n < N; ++n) ssq = fmaf(to_f(row[n]), to_f(row[n]), ssq);
+                const float inv = 1.f / sqrtf(ssq / (float)N + a.bc.eps);
+                q0 = bc_apply(q0, inv, a.bc.wB, a.bc.bB, bh % a.H, r, R, N, 2 * k);
+                q1 = bc_apply(q1, inv, a.bc.wB, a.bc.bB, bh % a.H, r, R, N, 2 * k + 1);
+            }
+            u0 += q0 * xv;
+            u1 += q1 * xv;
         }
         h0v += left0 * u0;
         h1v += left0 * u1;

@@ -1,0 +1,1111 @@
+// Kernel and launch templates of the tensor-core prefill, included by the translation units that
+// instantiate them (one per state size N and BC variant, so that they compile in parallel).
+#pragma once
+// Chunked prefill of the Mamba-3 recurrence on the sm_100-family tensor cores
+// (tcgen05 MMA with TMEM accumulators, operands brought in by TMA), as a
+// warp-specialised pipeline.
+//
+// One CTA walks the chunks of one segment of one (b, h) sequence in order.
+// Per chunk of Q tokens (QR = Q R rows (t, r); linkstar.cloud/article/869,
+// sections "第一刀" (parallel form), "RoPE技巧" and "第三刀" (MIMO)):
+//   prologue  chunk-local cumsums cA_t (warp shuffle scan) and phi_t; B and C
+//             turned by R(-phi_t) in place into fp16 tiles; X^_j = s_j x_j with
+//             s_j = exp(cA_e - cA_j) w_j; mask column factors
+//   MMA 1     S  = C~ B~^T        (QR x QR, K = N)    score
+//             Yi = C~ H           (QR x P,  K = N)    state -> output
+//             Sn = B~^T X^        (N x P,   K = QR)   the chunk's state contribution
+//   epilogue  P = S o M, M_tj = exp(cA_t - cA_j) w_j (j < t), lambda_t dt_t (j = t),
+//             into TMEM as fp16;  H <- R(phi_e) [exp(cA_e) H + Sn]
+//   MMA 2     Ya = P X            (QR x P,  K = QR, A operand read from TMEM)
+//   epilogue  y = Ya + exp(cA_t) Yi   (fp32)
+//
+// Roles: warp 0 issues the TMA loads (two raw slots), warp 1 allocates TMEM and
+// issues the MMAs, warps 2-9 run the prologue of chunk c+1 while warps 10-17
+// run the epilogues of chunk c; they hand chunks over through mbarriers.  The
+// fp32 state H stays in TMEM next to the accumulators.
+//
+// Precision.  Every MMA operand (B~, C~, X^, H, P and x) is fp16 (11-bit
+// significand, fp32 accumulation) scaled by a per-chunk power of two that
+// puts a bound of the tile just under 2^14, so the result does not depend on
+// the magnitude of the inputs (x itself converts exactly); the scales are
+// undone exactly in the fp32 epilogues.
+// The decay is always formed as exp2 of a difference of chunk-local
+// cumulative sums (exponent <= 0) and factored per 32-column block, so no
+// partial product overflows.
+#include "m3_internal.cuh"
+#include "m3_tc.cuh"
+
+#include <mutex>
+#include <type_traits>
+
+namespace m3 {
+namespace {
+
+using namespace tc;
+
+constexpr int kP = 64;
+constexpr int kWarps = 18;
+constexpr int kThreads = kWarps * 32;
+constexpr int kProW0 = 2, kProWarps = 8, kEpiW0 = 10, kEpiWarps = 8;
+constexpr int kProThreads = kProWarps * 32, kEpiThreads = kEpiWarps * 32;
+constexpr int kBarPro = 1, kBarEpi = 2;          // named barriers of the two groups
+constexpr uint64_t kWaitNs = 2000000000ull;      // 2 s per mbarrier wait; far above any legal wait
+constexpr float kLog2e = 1.4426950408889634f;
+
+// QRT: rows (t, r) per chunk; by default 128 for N = 64 and 64 for N = 128 (what shared memory
+// holds); 64 for N = 64 is the chunk rule Q = N / R of the pages
+template <int N, int R, int QRT = (N == 64 ? 128 : 64)>
+struct Cfg {
+    static constexpr int QR = QRT;                    // rows (t, r) per chunk
+    static constexpr int Q = QR / R;                  // tokens per chunk
+    static constexpr int K = N / 2;                   // complex pairs
+    static constexpr int NSLAB = N / 64;              // 64-column (128-byte) slabs of B and C
+    static constexpr int NSEG = kProWarps / NSLAB;    // token segments of the prologue
+    static constexpr int TPS = Q / NSEG;              // tokens per segment
+    static constexpr int TB = 32 / R;                 // tokens per 32-column block of the score
+    static constexpr uint32_t BT = QR * N * 2;        // B or C tile
+    static constexpr uint32_t XT = QR * kP * 2;       // X or X^ tile
+    static constexpr uint32_t TT = Q * K * 2;         // theta tile
+    static constexpr uint32_t HT = N * kP * 2;        // fp16 state tile
+    static_assert(Q % NSEG == 0 && TPS >= 1, "token segments must tile the chunk");
+    static_assert(K == 32 * NSLAB, "one lane per pair within a slab");
+    static_assert(Q <= kProThreads, "one prologue thread per token");
+};
+
+// Shared-memory map (byte offsets from a 1024-aligned base).
+// YB: bytes per element of y (4: fp32, 2: fp16 / bf16); BCN: BC normalisation and bias
+template <int N, int R, bool OUT, int YB = 4, bool BCN = false, int QRT = (N == 64 ? 128 : 64)>
+struct Smem {
+    using C = Cfg<N, R, QRT>;
+    // raw slot: B, C (turned into fp16 B~, C~ in place), X (bf16), theta
+    static constexpr uint32_t sB = 0;
+    static constexpr uint32_t sC = sB + C::BT;
+    static constexpr uint32_t sX = sC + (OUT ? C::BT : 0);
+    static constexpr uint32_t sT = sX + C::XT;
+    static constexpr uint32_t SLOT = ((sT + C::TT + 1023) / 1024) * 1024;
+    static constexpr uint32_t oXh = 2 * SLOT;                  // X^ [2] (fp16)
+    static constexpr uint32_t oXp = oXh + 2 * C::XT;           // X' [2] (fp16), OUT only
+    static constexpr uint32_t oH = oXp + (OUT ? 2 * C::XT : 0); // H (fp16), OUT only
+    // y staging, OUT only: fp32 y as 2 halves [QR][32]; 16-bit y as one [QR][64] tile
+    static constexpr uint32_t oYs = oH + (OUT ? C::HT : 0);
+    static constexpr uint32_t oVec = oYs + (OUT ? C::QR * kP * YB : 0);   // per-parity vectors
+    // per parity (floats): cA2[Q] g[Q] w[Q] vj[Q] dt[Q] cosE[K] sinE[K] sig[8]
+    static constexpr uint32_t VF = 5 * C::Q + 2 * C::K + 8;
+    static constexpr uint32_t oPart = oVec + 2 * 4 * VF;       // angle partials [8][K]
+    static constexpr uint32_t oMx = oPart + 4 * kProWarps * C::K;   // prologue maxima [8][4]
+    static constexpr uint32_t oMxH = oMx + 4 * kProWarps * 4;       // epilogue maxima [2][8]
+    static constexpr uint32_t oSigH = oMxH + 4 * 2 * kEpiWarps;     // H scale [2] and inverse [2]
+    static constexpr uint32_t oTot = oSigH + 16;                    // segment totals [1 + K]
+    static constexpr uint32_t oWtot = oTot + 4 * (1 + C::K);                    // per-warp dt A totals [4]
+    // BC normalisation (BCN only): row inverse RMS [B, C][QR] (room for [B, C][slab][QR]), gains [B, C][N],
+    // biases [B, C][R][N], static bounds of |B'|, |C'| [2]
+    static constexpr uint32_t oSS = ((oWtot + 16 + 15) / 16) * 16;   // float2 reads of gains and biases
+    static constexpr uint32_t oBW = oSS + (BCN ? 4 * 2 * C::NSLAB * C::QR : 0);
+    static constexpr uint32_t oBB = oBW + (BCN ? 4 * 2 * N : 0);
+    static constexpr uint32_t oBnd = oBB + (BCN ? 4 * 2 * R * N : 0);
+    static constexpr uint32_t oBar = ((oBnd + (BCN ? 8 : 0) + 7) / 8) * 8;
+    static_assert(oBW % 8 == 0 && oBB % 8 == 0, "8-byte aligned float2 gains and biases");
+    static constexpr int kNumBars = 16;
+    static constexpr uint32_t oTmem = oBar + 8 * kNumBars;
+    static constexpr uint32_t oFlag = oTmem + 4;
+    static constexpr uint32_t kBytes = oFlag + 4;
+    static constexpr uint32_t kAlloc = kBytes + 1024;          // slack for the 1024-byte alignment
+};
+
+// Byte offset of element (row, col) in a 128-byte-swizzled tile of 128-byte rows
+// (16-bit elements; sw128f: 32-bit elements).
+__device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t col) {
+    return row * 128u + ((((col >> 3) ^ row) & 7u) << 4) + ((col & 7u) << 1);
+}
+__device__ __forceinline__ uint32_t sw128f(uint32_t row, uint32_t col) {
+    return row * 128u + ((((col >> 2) ^ row) & 7u) << 4) + ((col & 3u) << 2);
+}
+
+// packed fp32 pairs (one instruction for two lanes of arithmetic)
+__device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
+__device__ __forceinline__ float2 f2u(uint32_t a, uint32_t b) { return make_float2(__uint_as_float(a), __uint_as_float(b)); }
+
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// 2^(13 - floor(log2 m)): maps m to [2^13, 2^14).  1 for m = 0 or non-finite m.
+__device__ __forceinline__ float pow2_scale(float m) {
+    if (!(m > 0.f) || !(m <= 3.0e38f)) return 1.f;
+    const int e = (int)((__float_as_uint(m) >> 23) & 0xFFu) - 127;
+    int s = 13 - e;
+    s = s < -126 ? -126 : (s > 127 ? 127 : s);
+    return __uint_as_float((uint32_t)(s + 127) << 23);
+}
+__device__ __forceinline__ float pow2_inv(float s) {   // exact inverse of a power of two
+    return __uint_as_float((uint32_t)(254 - (int)(__float_as_uint(s) >> 23)) << 23);
+}
+
+// fp16 pair (lo element in the low half), round to nearest even
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// fp16 x fp16 -> fp32, dense; a_mn / b_mn: 1 = MN-major operand.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int a_mn, int b_mn) {
+    return (1u << 4) | (static_cast<uint32_t>(a_mn) << 15) | (static_cast<uint32_t>(b_mn) << 16) |
+           (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void named_sync(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *m) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(m)) : "memory");
+}
+__device__ __forceinline__ float warp_max(float v) {   // v >= 0
+    return __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(v)));
+}
+
+struct TcMaps {
+    CUtensorMap B, C, X, T, Y;
+};
+
+enum Bar {
+    kRawFull = 0,      // [2] TMA -> prologue (transaction bytes)
+    kRawEmpty = 2,     // [2] MMAs done with a raw slot -> producer
+    kTilesFull = 4,    // [2] prologue -> MMA
+    kStateReady = 6,   // [2] epilogue wrote H (and read S, Sn) -> MMA
+    kMma1 = 8,         // [2] first MMAs done -> epilogue
+    kPReady = 10,      // [2] epilogue wrote P -> MMA
+    kMma2 = 12,        // [2] Ya done -> epilogue
+    kEpiDone = 14      // [2] epilogue done with a chunk -> prologue
+};
+
+// YT: element type of y (an m3_dtype; OUT only).  BCN: B and C go through the BC normalisation
+// and bias (a.bc) before the rotation.
+template <int N, int R, bool OUT, int YT = M3_F32, bool BCN = false, int QRT = (N == 64 ? 128 : 64)>
+__global__ void __launch_bounds__(kThreads, 1)
+tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, int nseg, int nlaunch, int ws_stride,
+                  int ws_step, unsigned *status) {
+    using Cf = Cfg<N, R, QRT>;
+    constexpr int YB = YT == M3_F32 ? 4 : 2;
+    using S = Smem<N, R, OUT, YB, BCN, QRT>;
+    constexpr int QR = Cf::QR, Q = Cf::Q, K = Cf::K, NSLAB = Cf::NSLAB, TPS = Cf::TPS, TB = Cf::TB;
+    constexpr uint32_t kTmemCols = OUT ? 512 : 128;
+    // TMEM columns: score, state contribution, Yi (two buffers), Ya, P (fp16 pairs), fp32 state
+    constexpr uint32_t cS = 0, cSn = OUT ? 128 : 0, cYi0 = 192, cYa = 320, cP = 384, cH = OUT ? 448 : 64;
+    constexpr bool kRowsM64 = (QR == 64);    // S / Yi / Ya use the M = 64 lane layout
+    constexpr bool kStateM64 = (N == 64);    // Sn uses the M = 64 lane layout
+
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + S::oBar);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + S::oTmem);
+    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(sm + S::oFlag);
+    float *part = reinterpret_cast<float *>(sm + S::oPart);
+    float *mx = reinterpret_cast<float *>(sm + S::oMx);
+    float *mxH = reinterpret_cast<float *>(sm + S::oMxH);
+    float *sigH = reinterpret_cast<float *>(sm + S::oSigH);   // [0..1] scale, [2..3] inverse
+    float *tot = reinterpret_cast<float *>(sm + S::oTot);
+    float *wtot = reinterpret_cast<float *>(sm + S::oWtot);
+    auto vec = [&](int p) { return reinterpret_cast<float *>(sm + S::oVec) + p * S::VF; };
+    // per-parity vector fields
+    auto v_cA = [&](int p) { return vec(p); };
+    auto v_g = [&](int p) { return vec(p) + Q; };
+    auto v_w = [&](int p) { return vec(p) + 2 * Q; };
+    auto v_vj = [&](int p) { return vec(p) + 3 * Q; };
+    auto v_dt = [&](int p) { return vec(p) + 4 * Q; };
+    auto v_cos = [&](int p) { return vec(p) + 5 * Q; };
+    auto v_sin = [&](int p) { return vec(p) + 5 * Q + K; };
+    // scales: sB, sC, sX, tauP / (sB sC), 1 / (sB sX), 1 / sC, 1 / (tauP sX')
+    auto v_sig = [&](int p) { return vec(p) + 5 * Q + 2 * K; };
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int H = a.H, L = a.L;
+    const int g = blockIdx.x % nlaunch, bh = blockIdx.x / nlaunch, b = bh / H, h = bh % H;
+    const int t_begin = g * seglen, t_end = min(L, t_begin + seglen);
+    const int nchunks = t_end > t_begin ? (t_end - t_begin + Q - 1) / Q : 0;
+    const __nv_bfloat16 *dtp = static_cast<const __nv_bfloat16 *>(a.dt);
+    const __nv_bfloat16 *Ap = static_cast<const __nv_bfloat16 *>(a.A);
+    const __nv_bfloat16 *lp = static_cast<const __nv_bfloat16 *>(a.lam);
+    auto tok = [&](int t) { return ((size_t)b * L + t) * H + h; };
+
+    // bounded wait; after any timeout every later wait returns at once
+    // (backoff: single-thread roles nap between polls so that they do not take
+    // issue slots from the warps doing arithmetic)
+    auto wait = [&](int i, uint32_t parity, bool backoff = false) {
+        uint64_t *m = bars + i;
+        const uint64_t t0 = global_ns();
+        for (uint32_t n = 0;; ++n) {
+            if (mbar_try_wait(m, parity)) return;
+            if (backoff) __nanosleep(64);
+            if ((n & 7u) == 7u) {
+                if (*abort_flag) return;
+                if (global_ns() - t0 > kWaitNs) break;
+            }
+        }
+        *abort_flag = 1;
+        atomicOr(status, kStatusTimeout);
+    };
+
+    // ---- set-up
+    if (tid == 0) {
+        for (int p = 0; p < 2; ++p) {
+            mbar_init(bars + kRawFull + p, 1);
+            mbar_init(bars + kRawEmpty + p, 1);
+            mbar_init(bars + kTilesFull + p, kProThreads);
+            mbar_init(bars + kStateReady + p, kEpiThreads);
+            mbar_init(bars + kMma1 + p, 1);
+            mbar_init(bars + kPReady + p, kEpiThreads);
+            mbar_init(bars + kMma2 + p, 1);
+            mbar_init(bars + kEpiDone + p, kEpiThreads);
+        }
+        mbar_init_fence();
+        *abort_flag = 0;
+        tma_prefetch_desc(&maps.B);
+        tma_prefetch_desc(&maps.X);
+        tma_prefetch_desc(&maps.T);
+        if (OUT) {
+            tma_prefetch_desc(&maps.C);
+            tma_prefetch_desc(&maps.Y);
+        }
+    }
+    for (int i = tid; i < 1 + K; i += kThreads) tot[i] = 0.f;
+    if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+    fence_before();
+    __syncthreads();
+    fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ================================================================ producer
+        if (lane == 0) {
+            for (int it = 0; it < nchunks; ++it) {
+                const int p = it & 1;
+                if (it >= 2) wait(kRawEmpty + p, ((it - 2) >> 1) & 1, true);
+                unsigned char *slot = sm + p * S::SLOT;
+                constexpr uint32_t bytes = Cf::BT * (OUT ? 2 : 1) + Cf::XT + Cf::TT;
+                mbar_expect_tx(bars + kRawFull + p, bytes);
+                const int row0 = b * L + t_begin + it * Q;
+                const int hg = h / (H / a.G);   // B / C group of this head
+#pragma unroll
+                for (int sl = 0; sl < NSLAB; ++sl) {
+                    tma_load_4d(slot + S::sB + sl * QR * 128, &maps.B, 64 * sl, 0, hg, row0, bars + kRawFull + p);
+                    if (OUT)
+                        tma_load_4d(slot + S::sC + sl * QR * 128, &maps.C, 64 * sl, 0, hg, row0, bars + kRawFull + p);
+                }
+                tma_load_4d(slot + S::sX, &maps.X, 0, 0, h, row0, bars + kRawFull + p);
+                tma_load_3d(slot + S::sT, &maps.T, 0, h, row0, bars + kRawFull + p);
+            }
+            if (*abort_flag) {
+                // let the copies already issued land before the CTA's shared memory goes away
+                for (int it = nchunks - 2 < 0 ? 0 : nchunks - 2; it < nchunks; ++it) {
+                    mbar_wait(bars + kRawFull + (it & 1), (it >> 1) & 1, kWaitNs);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ================================================================ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idS = idesc_f16(QR, QR, 0, 0);
+            constexpr uint32_t idYi = idesc_f16(QR, kP, 0, 1);
+            constexpr uint32_t idSn = idesc_f16(N, kP, 1, 1);
+            constexpr uint32_t idYa = idesc_f16(QR, kP, 0, 1);
+            for (int it = 0; it < nchunks; ++it) {
+                const int p = it & 1;
+                const uint32_t ph = (it >> 1) & 1;
+                wait(kTilesFull + p, ph, true);
+                wait(kStateReady + p, ph, true);
+                fence_after();
+                unsigned char *slot = sm + p * S::SLOT;
+                const uint32_t bA = smem_u32(slot + S::sB), xh = smem_u32(sm + S::oXh + p * Cf::XT);
+                if (OUT) {
+                    const uint32_t cA = smem_u32(slot + S::sC), hA = smem_u32(sm + S::oH);
+                    const uint32_t cYi = cYi0 + 64 * p;
+#pragma unroll
+                    for (int ks = 0; ks < N / 16; ++ks) {
+                        // K-major, 128-byte swizzle: slab ks / 4, 32 bytes per 16-column step inside it
+                        const uint32_t ko = (ks / 4) * (QR * 128) + (ks % 4) * 32;
+                        const uint64_t dC = make_desc(cA + ko, 16, 1024, kSwizzle128B);
+                        mma_ss(tmem + cS, dC, make_desc(bA + ko, 16, 1024, kSwizzle128B), idS, ks > 0);
+                        // state operand: MN-major (p), K = n rows in 8-row groups of 1024 bytes
+                        mma_ss(tmem + cYi, dC, make_desc(hA + ks * 2048, 0, 1024, kSwizzle128B), idYi, ks > 0);
+                    }
+                }
+#pragma unroll
+                for (int ks = 0; ks < QR / 16; ++ks) {
+                    // B~ read as the MN-major A operand (M = n in 64-wide slabs, K = rows j)
+                    mma_ss(tmem + cSn, make_desc(bA + ks * 2048, QR * 128, 1024, kSwizzle128B),
+                           make_desc(xh + ks * 2048, 0, 1024, kSwizzle128B), idSn, ks > 0);
+                }
+                mma_commit(bars + kMma1 + p);
+                mma_commit(bars + kRawEmpty + p);   // MMA 2 reads only TMEM and x'
+                if (OUT) {
+                    wait(kPReady + p, ph, true);
+                    fence_after();
+                    const uint32_t xb = smem_u32(sm + S::oXp + p * Cf::XT);
+#pragma unroll
+                    for (int ks = 0; ks < QR / 16; ++ks)
+                        mma_ts(tmem + cYa, tmem + cP + ks * 8, make_desc(xb + ks * 2048, 0, 1024, kSwizzle128B),
+                               idYa, ks > 0);
+                    mma_commit(bars + kMma2 + p);
+                }
+            }
+            if (*abort_flag && nchunks > 0) {
+                // let the last MMAs finish before TMEM is released
+                const int it = nchunks - 1;
+                mbar_wait(bars + (OUT ? kMma2 : kMma1) + (it & 1), (it >> 1) & 1, kWaitNs);
+            }
+        }
+        __syncwarp();
+    } else if (warp < kEpiW0) {
+        // ================================================================ prologue
+        const int ptid = tid - kProW0 * 32, pw = warp - kProW0;
+        const int slab = pw % NSLAB, seg = pw / NSLAB, k = 32 * slab + lane;
+        // per-token scalars of the next chunk, loaded one chunk ahead into registers
+        // (raw values: nothing waits on these loads until the chunk is processed)
+        __nv_bfloat16 r_dt, r_A, r_l, r_ln, r_dtn;
+        auto fetch = [&](int it) {
+            const __nv_bfloat16 z = __float2bfloat16_rn(0.f);
+            r_dt = r_A = r_l = r_ln = r_dtn = z;
+            const int t = t_begin + it * Q + ptid;
+            if (ptid < Q && it < nchunks && t < t_end) {
+                const size_t ti = tok(t);
+                r_dt = dtp[ti];
+                r_A = Ap[ti];
+                r_l = lp[ti];
+                if (t + 1 < L) {
+                    const size_t tn = tok(t + 1);
+                    r_ln = lp[tn];
+                    r_dtn = dtp[tn];
+                } else {
+                    r_ln = __float2bfloat16_rn(1.f);   // (1 - lambda) dt = 0 past the sequence end
+                }
+            }
+        };
+        fetch(0);
+        float acc_cA = 0.f;   // pass 1: total log2-decay of the segment (prologue thread 0)
+        float *bss = reinterpret_cast<float *>(sm + S::oSS);    // [B, C][QR] inverse RMS of the rows
+        const float *bw = reinterpret_cast<const float *>(sm + S::oBW);   // [B, C][N]
+        const float *bb = reinterpret_cast<const float *>(sm + S::oBB);   // [B, C][R][N]
+        const float *bnd = reinterpret_cast<const float *>(sm + S::oBnd); // [B, C]
+        if constexpr (BCN) {
+            // this head's gains and biases into shared memory, and the bounds |v'| <= sqrt(N) max|w| +
+            // max|bias| (|v| / rms(v) <= sqrt(N)) that replace the tile maxima of B and C
+            float *w = reinterpret_cast<float *>(sm + S::oBW), *bi = reinterpret_cast<float *>(sm + S::oBB);
+#pragma unroll
+            for (int tsr = 0; tsr < 2; ++tsr) {
+                const float *ws = tsr ? a.bc.wC : a.bc.wB, *bs = tsr ? a.bc.bC : a.bc.bB;
+                float mw = 0.f, mb = 0.f;
+                for (int n = ptid; n < N; n += kProThreads) {
+                    const float v = ws ? ws[(size_t)h * N + n] : 1.f;
+                    w[tsr * N + n] = v;
+                    mw = fmaxf(mw, fabsf(v));
+                }
+                for (int rn = ptid; rn < R * N; rn += kProThreads) {
+                    const float v = bs ? bs[(size_t)h * R * N + rn] : 0.f;
+                    bi[tsr * R * N + rn] = v;
+                    mb = fmaxf(mb, fabsf(v));
+                }
+                mw = warp_max(mw);
+                mb = warp_max(mb);
+                if (lane == 0) mx[pw * 4 + tsr] = sqrtf((float)N) * mw + mb;
+            }
+            named_sync(kBarPro, kProThreads);
+            if (ptid < 2) {
+                float m = 0.f;
+                for (int q = 0; q < kProWarps; ++q) m = fmaxf(m, mx[q * 4 + ptid]);
+                reinterpret_cast<float *>(sm + S::oBnd)[ptid] = m;
+            }
+            named_sync(kBarPro, kProThreads);
+        }
+        for (int it = 0; it < nchunks; ++it) {
+            const int p = it & 1;
+            const int s0 = t_begin + it * Q, Qc = min(Q, t_end - s0), e = Qc - 1;
+            unsigned char *slot = sm + p * S::SLOT;
+            float *cA2 = v_cA(p), *gv = v_g(p), *wv = v_w(p), *vj = v_vj(p), *dts = v_dt(p);
+            if (it >= 2) wait(kEpiDone + p, ((it - 2) >> 1) & 1);
+            // ---- P1: token scalars
+            const float c_dt = to_f(r_dt), c_a = c_dt * to_f(r_A) * kLog2e, c_g = to_f(r_l) * c_dt;
+            const float c_w = c_g + (1.f - to_f(r_ln)) * to_f(r_dtn);
+            // inclusive scan of dt A within each warp of tokens (shuffles); the warp totals
+            // are added after the barrier
+            float c_scan = c_a;
+            if (pw * 32 < Q) {
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float t = __shfl_up_sync(0xffffffffu, c_scan, o);
+                    if (lane >= o) c_scan += t;
+                }
+                if (lane == 31) wtot[pw] = c_scan;
+            }
+            if (ptid < Q) {
+                dts[ptid] = c_dt;
+                gv[ptid] = c_g;
+                wv[ptid] = c_w;
+            }
+            fetch(it + 1);
+            // one thread waits for the chunk's TMA; the named barrier (which costs the
+            // other warps no issue slots) releases the rest
+            if (ptid == 0) wait(kRawFull + p, (it >> 1) & 1);
+            named_sync(kBarPro, kProThreads);
+            // ---- P2: chunk-local cumsum of dt A, angle partial sums, bounds of |B|, |C|, |x|, w
+            if (ptid < Q) {
+                float off = 0.f;
+#pragma unroll
+                for (int q = 0; q < (Q + 31) / 32 - 1; ++q) off += (q < pw) ? wtot[q] : 0.f;
+                cA2[ptid] = c_scan + off;
+            }
+            const __nv_bfloat16 *rawT = reinterpret_cast<const __nv_bfloat16 *>(slot + S::sT);
+            float mW = ptid < Qc ? fabsf(c_w) : 0.f;
+            // this thread's tokens: dt (0 past the sequence end) and its pair's angle rate
+            float dd[TPS], th[TPS];
+#pragma unroll
+            for (int i = 0; i < TPS; ++i) {
+                const int t = seg * TPS + i;
+                dd[i] = dts[t];
+                th[i] = __bfloat162float(rawT[t * K + k]);
+            }
+            {
+                float ps = 0.f;
+#pragma unroll
+                for (int i = 0; i < TPS; ++i) ps = fmaf(dd[i], th[i], ps);
+                part[seg * K + k] = ps;
+            }
+            // bounds of |B|, |C|, |x| over the raw tiles: packed maxima of the bf16 magnitudes
+            // (their bit patterns order like the values)
+            auto tile_max = [&](const unsigned char *base, auto bytes_c) {
+                constexpr uint32_t bytes = decltype(bytes_c)::value;
+                static_assert(bytes % (16u * kProThreads) == 0, "whole 16-byte words per thread");
+                uint32_t m2 = 0;
+#pragma unroll
+                for (uint32_t o = 0; o < bytes; o += 16u * kProThreads) {
+                    const uint4 v = *reinterpret_cast<const uint4 *>(base + o + 16u * ptid);
+                    m2 = __vmaxu2(m2, v.x & 0x7FFF7FFFu);
+                    m2 = __vmaxu2(m2, v.y & 0x7FFF7FFFu);
+                    m2 = __vmaxu2(m2, v.z & 0x7FFF7FFFu);
+                    m2 = __vmaxu2(m2, v.w & 0x7FFF7FFFu);
+                }
+                return fmaxf(bf16_lo_f(m2), bf16_hi_f(m2));
+            };
+            using BTc = std::integral_constant<uint32_t, Cf::BT>;
+            using XTc = std::integral_constant<uint32_t, Cf::XT>;
+            float mB, mC;
+            if constexpr (BCN) {
+                // inverse RMS of the raw B (and C) rows: the 8 consecutive threads reading one 128-byte
+                // row of the first slab (64 entries) also read the same row of the other slab, add
+                // their squares with three shuffles, and one of them writes rsqrt(mean + eps)
+                auto row_ss = [&](const unsigned char *base, float *dst) {
+                    static_assert((QR * 128) % (16 * kProThreads) == 0, "whole rows per pass");
+#pragma unroll
+                    for (uint32_t o = 16u * ptid; o < QR * 128u; o += 16u * kProThreads) {
+                        float2 acc = f2(0.f);
+#pragma unroll
+                        for (int sl = 0; sl < NSLAB; ++sl) {
+                            const uint4 v = *reinterpret_cast<const uint4 *>(base + sl * (QR * 128) + o);
+                            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                            for (int z = 0; z < 4; ++z) {
+                                const float2 e2 = f2u(wv[z] << 16, wv[z] & 0xFFFF0000u);
+                                acc = __ffma2_rn(e2, e2, acc);
+                            }
+                        }
+                        float ssq = acc.x + acc.y;
+                        ssq += __shfl_xor_sync(0xffffffffu, ssq, 1);
+                        ssq += __shfl_xor_sync(0xffffffffu, ssq, 2);
+                        ssq += __shfl_xor_sync(0xffffffffu, ssq, 4);
+                        if ((ptid & 7) == 0) dst[o / 128u] = rsqrtf(fmaf(ssq, 1.f / N, a.bc.eps));
+                    }
+                };
+                row_ss(slot + S::sB, bss);
+                if (OUT) row_ss(slot + S::sC, bss + QR);
+                mB = bnd[0];
+                mC = OUT ? bnd[1] : 0.f;
+            } else {
+                mB = tile_max(slot + S::sB, BTc{});
+                mC = OUT ? tile_max(slot + S::sC, BTc{}) : 0.f;
+            }
+            float mX = tile_max(slot + S::sX, XTc{});
+            mB = warp_max(mB);
+            mC = warp_max(mC);
+            mX = warp_max(mX);
+            mW = warp_max(mW);
+            if (lane == 0) {
+                mx[pw * 4 + 0] = mB;
+                mx[pw * 4 + 1] = mC;
+                mx[pw * 4 + 2] = mX;
+                mx[pw * 4 + 3] = mW;
+            }
+            named_sync(kBarPro, kProThreads);
+            // ---- P3: scales, rotation of B and C in place (fp16), X^, mask column factors
+            float MB, MC, MX, MW;
+            {
+                const bool rd = lane < kProWarps;
+                MB = warp_max(rd ? mx[lane * 4 + 0] : 0.f);
+                MC = warp_max(rd ? mx[lane * 4 + 1] : 0.f);
+                MX = warp_max(rd ? mx[lane * 4 + 2] : 0.f);
+                MW = warp_max(rd ? mx[lane * 4 + 3] : 0.f);
+            }
+            // |B~| <= sqrt 2 max|B| (rotation of a pair);  |X^| <= max w max|x|;
+            // |P| <= N max|B~| max|C~| max(w, lambda dt)
+            // one scale for B~ and C~ (their rotations then share the scaled cos / sin)
+            const float sgB = pow2_scale(1.5f * fmaxf(MB, MC)), sgC = sgB, sgX = pow2_scale(MX * MW);
+            const float sgXp = pow2_scale(MX), tauP = pow2_scale((float)N * 2.25f * MB * MC * MW);
+            if (ptid == 0) {
+                float *sg = v_sig(p);
+                sg[0] = sgB;
+                sg[1] = sgC;
+                sg[2] = sgX;
+                sg[3] = tauP * pow2_inv(sgB) * pow2_inv(sgC);
+                sg[4] = pow2_inv(sgB) * pow2_inv(sgX);
+                sg[5] = pow2_inv(sgC);
+                sg[6] = pow2_inv(tauP) * pow2_inv(sgXp);
+                if (!OUT) acc_cA += cA2[e];
+            }
+            {
+                float phi = 0.f;
+#pragma unroll
+                for (int sg = 0; sg < Cf::NSEG - 1; ++sg) phi += (sg < seg) ? part[sg * K + k] : 0.f;
+                unsigned char *bs = slot + S::sB + slab * (QR * 128);
+                unsigned char *cs = slot + S::sC + slab * (QR * 128);
+                // angles of all the thread's tokens first (a short FMA chain), then
+                // independent rotations the scheduler can overlap
+                float ph[TPS];
+#pragma unroll
+                for (int i = 0; i < TPS; ++i) {
+                    phi = fmaf(dd[i], th[i], phi);
+                    ph[i] = phi;
+                }
+                const int ie = e - seg * TPS;   // the chunk's last token, if it is this thread's
+                // this thread's BC gains (entries 2k, 2k + 1 of B and of C)
+                float2 wkB = f2(1.f), wkC = f2(1.f);
+                if constexpr (BCN) {
+                    wkB = *reinterpret_cast<const float2 *>(bw + 2 * k);
+                    wkC = *reinterpret_cast<const float2 *>(bw + N + 2 * k);
+                }
+                // raw words are loaded kLA tokens ahead of their use (each load precedes, in
+                // program order, the in-place stores it could alias, so none waits on a store)
+                uint32_t rb[TPS * R], rc[TPS * R];
+                constexpr int kLA = TPS < 4 ? TPS : 4;
+                auto load_tok = [&](int i) {
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        const uint32_t off = sw128((seg * TPS + i) * R + r, 2 * lane);
+                        rb[i * R + r] = *reinterpret_cast<const uint32_t *>(bs + off);
+                        if (OUT) rc[i * R + r] = *reinterpret_cast<const uint32_t *>(cs + off);
+                    }
+                };
+#pragma unroll
+                for (int i = 0; i < kLA; ++i) load_tok(i);
+                // two tokens at a time on packed fp32.  sin / cos: Cody-Waite reduction by 2 pi
+                // (two-constant split) to [-pi, pi], n = round(x / 2 pi) by the 1.5 * 2^23
+                // addition (exact for |x / 2 pi| < 2^22, and on the FMA pipe rather than the
+                // conversion unit), then the hardware approximations there
+                static_assert(TPS % 2 == 0, "token pairs");
+#pragma unroll
+                for (int i = 0; i < TPS; i += 2) {
+                    if (i + kLA < TPS) load_tok(i + kLA);
+                    if (i + kLA + 1 < TPS) load_tok(i + kLA + 1);
+                    const float2 x2 = make_float2(ph[i], ph[i + 1]);
+                    const float2 n2 = __fadd2_rn(__ffma2_rn(x2, f2(0.15915494309189535f), f2(12582912.f)),
+                                                 f2(-12582912.f));
+                    float2 r2 = __ffma2_rn(n2, f2(-6.28318548202514648f), x2);
+                    r2 = __ffma2_rn(n2, f2(1.7484555314695172e-7f), r2);
+                    float c0, s0, c1, s1;
+                    __sincosf(r2.x, &s0, &c0);
+                    __sincosf(r2.y, &s1, &c1);
+                    if (i == ie || i + 1 == ie) {   // the chunk's last token: rotation of the state at the chunk end
+                        const bool first = i == ie;
+                        v_cos(p)[k] = first ? c0 : c1;
+                        v_sin(p)[k] = first ? s0 : s1;
+                        if (!OUT) tot[1 + k] += first ? ph[i] : ph[i + 1];
+                    }
+                    const float2 cb = __fmul2_rn(make_float2(c0, c1), f2(sgB));
+                    const float2 sb = __fmul2_rn(make_float2(s0, s1), f2(sgB));
+                    const float2 nsb = __fmul2_rn(make_float2(s0, s1), f2(-sgB));
+                    const int t = seg * TPS + i;
+                    const bool valid0 = t < Qc, valid1 = t + 1 < Qc;
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        const uint32_t off0 = sw128(t * R + r, 2 * lane), off1 = sw128((t + 1) * R + r, 2 * lane);
+                        const uint32_t vb0 = rb[i * R + r], vb1 = rb[(i + 1) * R + r];
+                        float2 b0 = f2u(vb0 << 16, vb1 << 16), b1 = f2u(vb0 & 0xFFFF0000u, vb1 & 0xFFFF0000u);
+                        // BC normalisation of the two tokens' rows: v * (w / rms) + bias, entries 2k, 2k + 1
+                        auto bc_norm = [&](int tsr, float2 &e0, float2 &e1) {
+                            const float *iv = bss + tsr * QR + t * R + r;
+                            const float2 inv = make_float2(iv[0], iv[R]);
+                            const float2 wk = tsr ? wkC : wkB;
+                            const float2 bk = *reinterpret_cast<const float2 *>(bb + (tsr * R + r) * N + 2 * k);
+                            e0 = __ffma2_rn(e0, __fmul2_rn(inv, f2(wk.x)), f2(bk.x));
+                            e1 = __ffma2_rn(e1, __fmul2_rn(inv, f2(wk.y)), f2(bk.y));
+                        };
+                        if constexpr (BCN) bc_norm(0, b0, b1);
+                        const float2 o0 = __ffma2_rn(cb, b0, __fmul2_rn(sb, b1));
+                        const float2 o1 = __ffma2_rn(cb, b1, __fmul2_rn(nsb, b0));
+                        *reinterpret_cast<uint32_t *>(bs + off0) = valid0 ? pack_f16x2(o0.x, o1.x) : 0u;
+                        *reinterpret_cast<uint32_t *>(bs + off1) = valid1 ? pack_f16x2(o0.y, o1.y) : 0u;
+                        if (OUT) {
+                            const uint32_t vc0 = rc[i * R + r], vc1 = rc[(i + 1) * R + r];
+                            float2 e0 = f2u(vc0 << 16, vc1 << 16), e1 = f2u(vc0 & 0xFFFF0000u, vc1 & 0xFFFF0000u);
+                            if constexpr (BCN) bc_norm(1, e0, e1);
+                            const float2 q0 = __ffma2_rn(cb, e0, __fmul2_rn(sb, e1));
+                            const float2 q1 = __ffma2_rn(cb, e1, __fmul2_rn(nsb, e0));
+                            *reinterpret_cast<uint32_t *>(cs + off0) = valid0 ? pack_f16x2(q0.x, q1.x) : 0u;
+                            *reinterpret_cast<uint32_t *>(cs + off1) = valid1 ? pack_f16x2(q0.y, q1.y) : 0u;
+                        }
+                    }
+                }
+            }
+            {
+                unsigned char *xh = sm + S::oXh + p * Cf::XT;
+                unsigned char *xp = sm + S::oXp + p * Cf::XT;
+                const float ce = cA2[e];
+                static_assert((QR * 8) % kProThreads == 0, "whole items per thread");
+                constexpr int kItems = QR * 8 / kProThreads;
+                uint4 xv[kItems];
+#pragma unroll
+                for (int i = 0; i < kItems; ++i) {
+                    const int item = ptid + i * kProThreads;
+                    xv[i] = *reinterpret_cast<const uint4 *>(slot + S::sX + sw128(item >> 3, 8 * (item & 7)));
+                }
+#pragma unroll
+                for (int i = 0; i < kItems; ++i) {
+                    const int item = ptid + i * kProThreads;
+                    const int row = item >> 3, c8 = item & 7, t = row / R;
+                    const uint32_t off = sw128(row, 8 * c8);
+                    uint4 o = make_uint4(0, 0, 0, 0), q = o;
+                    if (t < Qc) {
+                        const float sj = fast_exp2(ce - cA2[t]) * wv[t] * sgX;
+                        const uint4 v = xv[i];
+                        const float f[8] = {bf16_lo_f(v.x), bf16_hi_f(v.x), bf16_lo_f(v.y), bf16_hi_f(v.y),
+                                            bf16_lo_f(v.z), bf16_hi_f(v.z), bf16_lo_f(v.w), bf16_hi_f(v.w)};
+                        uint32_t ow[4], qw[4];
+#pragma unroll
+                        for (int z = 0; z < 4; ++z) {
+                            const float2 fz = make_float2(f[2 * z], f[2 * z + 1]);
+                            const float2 a = __fmul2_rn(f2(sj), fz);
+                            ow[z] = pack_f16x2(a.x, a.y);
+                            if (OUT) {   // x' = sX' x, exact in fp16
+                                const float2 b2 = __fmul2_rn(f2(sgXp), fz);
+                                qw[z] = pack_f16x2(b2.x, b2.y);
+                            }
+                        }
+                        o = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+                        if (OUT) q = make_uint4(qw[0], qw[1], qw[2], qw[3]);
+                    }
+                    *reinterpret_cast<uint4 *>(xh + off) = o;
+                    if (OUT) *reinterpret_cast<uint4 *>(xp + off) = q;   // rows past the end stay zero
+                }
+                if (ptid < Q) {
+                    const int bt = (ptid / TB) * TB;
+                    vj[ptid] = ptid < Qc ? fast_exp2(cA2[bt] - cA2[ptid]) * wv[ptid] : 0.f;
+                }
+            }
+            fence_proxy_async();
+            mbar_arrive(bars + kTilesFull + p);
+        }
+        if (!OUT) {
+            named_sync(kBarPro, kProThreads);
+            if (!*abort_flag) {
+                float *dst = a.ws_tot + ((size_t)bh * (ws_stride - 1) + g) * (1 + K);
+                if (ptid == 0) dst[0] = acc_cA / kLog2e;
+                for (int i = ptid; i < K; i += kProThreads) dst[1 + i] = tot[1 + i];
+            }
+        }
+    } else {
+        // ================================================================ epilogue
+        const int ew = warp - kEpiW0, eq = warp & 3, eh = ew >> 2;   // lane quadrant, column half
+        const uint32_t lane_base = static_cast<uint32_t>(eq * 32) << 16;
+        // state rows owned: row n of the N x P state, columns [32 eh, 32 eh + 32)
+        const bool st_owner = kStateM64 ? (lane < 16) : true;
+        const int st_row = kStateM64 ? eq * 16 + lane : eq * 32 + lane;
+        // score / output rows owned
+        const bool row_ok = kRowsM64 ? (lane < 16) : true;
+        const int row = kRowsM64 ? eq * 16 + lane : eq * 32 + lane;
+        const int ti = row / R;
+        // The fp32 state lives in TMEM columns [cH, cH + 64): row n in the lane of the Sn
+        // accumulator's row n, column p; this thread holds columns [32 eh, 32 eh + 32).
+        const uint32_t hcol = tmem + lane_base + cH + 32 * eh;
+        float hmax = 0.f;   // this thread's max |h| (state rows it owns)
+        {
+            const int n = st_row;
+            const float left0 = (OUT && nseg == 1) ? (1.f - to_f(lp[tok(0)])) * to_f(dtp[tok(0)]) : 0.f;
+            const __nv_bfloat16 *bq = static_cast<const __nv_bfloat16 *>(a.Bprev);
+            const __nv_bfloat16 *xq = static_cast<const __nv_bfloat16 *>(a.xprev);
+            // the carried B row entries n of every rank, BC-normalised when BCN
+            float bqn[R];
+#pragma unroll
+            for (int r = 0; r < R; ++r) bqn[r] = 0.f;
+            if (OUT && st_owner && nseg == 1 && bq && xq) {
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const __nv_bfloat16 *row = bq + ((size_t)bh * R + r) * N;
+                    bqn[r] = to_f(row[n]);
+                    if constexpr (BCN) {
+                        float ssq = 0.f;
+                        for (int m = 0; m < N; ++m) ssq = fmaf(to_f(row[m]), to_f(row[m]), ssq);
+                        bqn[r] = bc_apply(bqn[r], 1.f / sqrtf(ssq / (float)N + a.bc.eps), a.bc.wB, a.bc.bB, h, r,
+                                          R, N, n);
+                    }
+                }
+            }
+#pragma unroll
+            for (int h16 = 0; h16 < 32; h16 += 16) {
+                uint32_t w[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int pp = 32 * eh + h16 + j;
+                    float v = 0.f;
+                    if (OUT && st_owner) {
+                        if (nseg == 1) {
+                            v = a.h0 ? a.h0[((size_t)bh * N + n) * kP + pp] : 0.f;
+                            if (bq && xq) {
+                                float u = 0.f;
+#pragma unroll
+                                for (int r = 0; r < R; ++r) u += bqn[r] * to_f(xq[((size_t)bh * R + r) * kP + pp]);
+                                v += left0 * u;
+                            }
+                        } else {
+                            v = a.ws_state[(((size_t)bh * ws_stride + (size_t)g * ws_step) * N + n) * kP + pp];
+                        }
+                    }
+                    hmax = fmaxf(hmax, fabsf(v));
+                    w[j] = __float_as_uint(v);
+                }
+                tmem_st16(hcol + h16, w);
+            }
+        }
+        // fp16 copy of the state (scaled) for the C~ H MMA (MN-major, 128-byte swizzle, rows n)
+        auto publish_state = [&](int slot_parity, float m) {
+            if (!OUT) return;
+            m = warp_max(m);
+            if (lane == 0) mxH[slot_parity * kEpiWarps + ew] = m;
+            named_sync(kBarEpi, kEpiThreads);
+            float M = 0.f;
+#pragma unroll
+            for (int q = 0; q < kEpiWarps; ++q) M = fmaxf(M, mxH[slot_parity * kEpiWarps + q]);
+            const float sg = pow2_scale(M);
+            if (ew == 0 && lane == 0) {
+                sigH[slot_parity] = sg;
+                sigH[2 + slot_parity] = pow2_inv(sg);
+            }
+            uint32_t hv[32];
+            tmem_ld16_nw(hcol, hv);
+            tmem_ld16_nw(hcol + 16, hv + 16);
+            tmem_wait_ld(hv);
+            if (st_owner) {
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    uint32_t w4[4];
+#pragma unroll
+                    for (int e2 = 0; e2 < 4; ++e2) {
+                        const float2 v2 = __fmul2_rn(f2u(hv[8 * q4 + 2 * e2], hv[8 * q4 + 2 * e2 + 1]), f2(sg));
+                        w4[e2] = pack_f16x2(v2.x, v2.y);
+                    }
+                    *reinterpret_cast<uint4 *>(sm + S::oH + sw128(st_row, 32 * eh + 8 * q4)) =
+                        make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                }
+            }
+        };
+        publish_state(0, hmax);
+        fence_proxy_async();
+        fence_before();
+        mbar_arrive(bars + kStateReady + 0);
+
+        for (int it = 0; it < nchunks; ++it) {
+            const int p = it & 1;
+            const uint32_t ph = (it >> 1) & 1;
+            const int s0 = t_begin + it * Q, Qc = min(Q, t_end - s0), e = Qc - 1;
+            const float *cA2 = v_cA(p), *gv = v_g(p), *vj = v_vj(p), *sg = v_sig(p);
+            const bool last_chunk = it == nchunks - 1;
+            // one thread waits for the chunk's vectors and first MMAs; the named barrier
+            // releases the other epilogue warps without them polling
+            if (ew == 0 && lane == 0) {
+                wait(kTilesFull + p, ph);
+                wait(kMma1 + p, ph);
+            }
+            named_sync(kBarEpi, kEpiThreads);
+            fence_after();
+            // ---- masked score -> TMEM (fp16, scaled by tauP)
+            if (OUT) {
+                constexpr int COLS = QR / 2;    // score columns per thread
+                const int t = min(ti, Q - 1);
+                const float ca = cA2[t], invBC = sg[3];   // tauP / (sB sC)
+                const float gd = row_ok ? gv[t] * invBC : 0.f;
+                // token range of this warp's rows (warp-uniform): blocks past tmax are zero,
+                // blocks ending before tmin need no causal test
+                const int tmax = (kRowsM64 ? eq * 16 + 15 : eq * 32 + 31) / R;
+                const int tmin = (kRowsM64 ? eq * 16 : eq * 32) / R;
+#pragma unroll
+                for (int cc = 0; cc < COLS; cc += 32) {
+                    const int cb = eh * COLS + cc;   // first score column of this 32-column block
+                    const int btok = (cb / 32) * TB; // first token of the block
+                    uint32_t p16[16];
+                    if (btok > tmax) {
+#pragma unroll
+                        for (int q = 0; q < 16; ++q) p16[q] = 0u;
+                    } else {
+                        uint32_t sv[32];
+                        tmem_ld16_nw(tmem + lane_base + cS + cb, sv);
+                        tmem_ld16_nw(tmem + lane_base + cS + cb + 16, sv + 16);
+                        // exp2(cA_t - cA_btok) <= 1 wherever it is used (btok <= tj < t)
+                        const float u = (row_ok && btok < ti) ? fast_exp2(ca - cA2[btok]) * invBC : 0.f;
+                        float um[TB];
+#pragma unroll
+                        for (int q = 0; q < TB; q += 4) {
+                            const float4 v4 = *reinterpret_cast<const float4 *>(vj + btok + q);
+                            um[q] = u * v4.x;
+                            if (q + 1 < TB) um[q + 1] = u * v4.y;
+                            if (q + 2 < TB) um[q + 2] = u * v4.z;
+                            if (q + 3 < TB) um[q + 3] = u * v4.w;
+                        }
+                        tmem_wait_ld(sv);
+                        if (btok + TB <= tmin) {
+#pragma unroll
+                            for (int q = 0; q < 16; ++q) {
+                                const float2 v2 = __fmul2_rn(f2u(sv[2 * q], sv[2 * q + 1]),
+                                                             make_float2(um[(2 * q) / R], um[(2 * q + 1) / R]));
+                                p16[q] = pack_f16x2(v2.x, v2.y);
+                            }
+                        } else {
+#pragma unroll
+                            for (int q = 0; q < 16; ++q) {
+                                float mz[2];
+#pragma unroll
+                                for (int z = 0; z < 2; ++z) {
+                                    const int jq = (2 * q + z) / R;   // token offset in the block
+                                    const int tj = btok + jq;
+                                    mz[z] = (tj < ti) ? um[jq] : ((tj == ti) ? gd : 0.f);
+                                }
+                                const float2 v2 = __fmul2_rn(f2u(sv[2 * q], sv[2 * q + 1]), make_float2(mz[0], mz[1]));
+                                p16[q] = pack_f16x2(v2.x, v2.y);
+                            }
+                        }
+                    }
+                    tmem_st16(tmem + lane_base + cP + cb / 2, p16);
+                }
+                fence_before();
+                mbar_arrive(bars + kPReady + p);
+            }
+            // ---- state update: H <- R(phi_e) [exp(cA_e) H + Sn]
+            {
+                const float rho = fast_exp2(cA2[e]), invBX = sg[4];
+                const int n = st_row, kk = n >> 1;
+                const float c = st_owner ? v_cos(p)[kk] : 1.f, s = st_owner ? v_sin(p)[kk] : 0.f;
+                const bool odd = n & 1;
+                float *dst = nullptr;
+                if (last_chunk && st_owner && !*abort_flag) {
+                    if (!OUT) dst = a.ws_state + (((size_t)bh * ws_stride + g + 1) * N + n) * kP + 32 * eh;
+                    else if (g == nseg - 1 && a.h_out) dst = a.h_out + ((size_t)bh * N + n) * kP + 32 * eh;
+                }
+                float m = 0.f;
+#pragma unroll
+                for (int h16 = 0; h16 < 32; h16 += 16) {
+                    uint32_t sh[32];   // [0, 16): Sn, [16, 32): H
+                    tmem_ld16_nw(tmem + lane_base + cSn + 32 * eh + h16, sh);
+                    tmem_ld16_nw(hcol + h16, sh + 16);
+                    tmem_wait_ld(sh);
+                    uint32_t hv[16];
+                    const float sgn_s = odd ? s : -s;
+#pragma unroll
+                    for (int j = 0; j < 16; j += 2) {
+                        const float2 v = __ffma2_rn(f2(rho), f2u(sh[16 + j], sh[16 + j + 1]),
+                                                    __fmul2_rn(f2u(sh[j], sh[j + 1]), f2(invBX)));
+                        const float2 pv = make_float2(__shfl_xor_sync(0xffffffffu, v.x, 1),
+                                                      __shfl_xor_sync(0xffffffffu, v.y, 1));
+                        const float2 nv = __ffma2_rn(f2(sgn_s), pv, __fmul2_rn(f2(c), v));
+                        m = fmaxf(m, st_owner ? fmaxf(fabsf(nv.x), fabsf(nv.y)) : 0.f);
+                        hv[j] = __float_as_uint(nv.x);
+                        hv[j + 1] = __float_as_uint(nv.y);
+                    }
+                    tmem_st16(hcol + h16, hv);
+                    if (dst) {
+#pragma unroll
+                        for (int j = 0; j < 16; j += 4)
+                            *reinterpret_cast<float4 *>(dst + h16 + j) =
+                                make_float4(__uint_as_float(hv[j]), __uint_as_float(hv[j + 1]),
+                                            __uint_as_float(hv[j + 2]), __uint_as_float(hv[j + 3]));
+                    }
+                }
+                publish_state((it + 1) & 1, m);
+                fence_proxy_async();
+                fence_before();
+                mbar_arrive(bars + kStateReady + ((it + 1) & 1));
+            }
+            // ---- y = Ya + exp(cA_t) Yi
+            if (OUT) {
+                if (ew == 0 && lane == 0) {
+                    wait(kMma2 + p, ph);
+                    bulk_wait_read<0>();   // the previous chunk's y stores have left the staging tile
+                }
+                named_sync(kBarEpi, kEpiThreads);
+                fence_after();
+                const float sc = fast_exp2(cA2[min(ti, Q - 1)]) * sg[5] * sigH[2 + p], sa = sg[6];
+                // y rows go through a shared-memory tile (this thread: row `row`, columns
+                // [32 eh, 32 eh + 32)) and leave by TMA: rows past the sequence end are clipped by
+                // the map, and the global writes are whole lines
+#pragma unroll
+                for (int half16 = 0; half16 < 32; half16 += 16) {
+                    uint32_t yy[32];   // [0, 16): Ya, [16, 32): Yi
+                    tmem_ld16_nw(tmem + lane_base + cYa + 32 * eh + half16, yy);
+                    tmem_ld16_nw(tmem + lane_base + cYi0 + 64 * p + 32 * eh + half16, yy + 16);
+                    tmem_wait_ld(yy);
+                    const uint32_t *ya = yy, *yi = yy + 16;
+                    if (row_ok) {
+                        if constexpr (YB == 4) {
+                            // fp32: two halves [QR][32] of 128-byte rows
+                            unsigned char *ys = sm + S::oYs + eh * (QR * 128);
+#pragma unroll
+                            for (int j = 0; j < 16; j += 4) {
+                                const float2 u0 = __ffma2_rn(f2(sc), f2u(yi[j], yi[j + 1]),
+                                                             __fmul2_rn(f2(sa), f2u(ya[j], ya[j + 1])));
+                                const float2 u1 = __ffma2_rn(f2(sc), f2u(yi[j + 2], yi[j + 3]),
+                                                             __fmul2_rn(f2(sa), f2u(ya[j + 2], ya[j + 3])));
+                                *reinterpret_cast<float4 *>(ys + sw128f(row, half16 + j)) =
+                                    make_float4(u0.x, u0.y, u1.x, u1.y);
+                            }
+                        } else {
+                            // 16-bit: one [QR][64] tile of 128-byte rows, rounded once from fp32
+                            uint32_t w[8];
+#pragma unroll
+                            for (int j = 0; j < 16; j += 2) {
+                                const float2 u = __ffma2_rn(f2(sc), f2u(yi[j], yi[j + 1]),
+                                                            __fmul2_rn(f2(sa), f2u(ya[j], ya[j + 1])));
+                                w[j / 2] = YT == M3_F16 ? pack_f16x2(u.x, u.y) : pack_bf16x2(u.x, u.y);
+                            }
+                            const int c0 = 32 * eh + half16;
+                            *reinterpret_cast<uint4 *>(sm + S::oYs + sw128(row, c0)) = make_uint4(w[0], w[1], w[2], w[3]);
+                            *reinterpret_cast<uint4 *>(sm + S::oYs + sw128(row, c0 + 8)) =
+                                make_uint4(w[4], w[5], w[6], w[7]);
+                        }
+                    }
+                }
+                fence_proxy_async();
+                named_sync(kBarEpi, kEpiThreads);
+                if (ew == 0 && lane == 0) {
+                    if (!*abort_flag) {
+                        tma_store_5d(&maps.Y, sm + S::oYs, 0, 0, h, s0, b);
+                        if (YB == 4) tma_store_5d(&maps.Y, sm + S::oYs + QR * 128, 32, 0, h, s0, b);
+                    }
+                    bulk_commit();
+                }
+            }
+            fence_before();
+            mbar_arrive(bars + kEpiDone + p);
+        }
+        if (OUT && ew == 0 && lane == 0) bulk_wait<0>();
+        // ---- carry out (last segment)
+        if (OUT && g == nseg - 1 && a.Bprev_out && a.xprev_out && L > 0 && !*abort_flag) {
+            const int et = tid - kEpiW0 * 32;
+            const size_t tl = tok(L - 1);
+            const size_t tlg = ((size_t)b * L + L - 1) * a.G + h / (H / a.G);   // its B / C group row
+            const __nv_bfloat16 *Bm = static_cast<const __nv_bfloat16 *>(a.B);
+            const __nv_bfloat16 *xm = static_cast<const __nv_bfloat16 *>(a.x);
+            __nv_bfloat16 *bo = static_cast<__nv_bfloat16 *>(a.Bprev_out);
+            __nv_bfloat16 *xo = static_cast<__nv_bfloat16 *>(a.xprev_out);
+            for (int i = et; i < R * N; i += kEpiThreads) bo[(size_t)bh * R * N + i] = Bm[tlg * R * N + i];
+            for (int i = et; i < R * kP; i += kEpiThreads) xo[(size_t)bh * R * kP + i] = xm[tl * R * kP + i];
+        }
+    }
+    fence_before();
+    __syncthreads();
+    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+// ---------------------------------------------------------------- host side
+// 4-d map over a [b*L][H][R][inner] bf16 tensor, box = {64, R, 1, Q}, 128-byte swizzle
+bool map4(CUtensorMap *m, const void *base, int inner, int R, int H, long long rows, int Q) {
+    EncodeFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[4] = {(cuuint64_t)inner, (cuuint64_t)R, (cuuint64_t)H, (cuuint64_t)rows};
+    const cuuint64_t strides[3] = {(cuuint64_t)inner * 2, (cuuint64_t)inner * 2 * R, (cuuint64_t)inner * 2 * R * H};
+    const cuuint32_t box[4] = {64, (cuuint32_t)R, 1, (cuuint32_t)Q};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+// 3-d map over a [b*L][H][inner] bf16 tensor, box = {inner, 1, Q}
+bool map3(CUtensorMap *m, const void *base, int inner, int H, long long rows, int Q) {
+    EncodeFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)H, (cuuint64_t)rows};
+    const cuuint64_t strides[2] = {(cuuint64_t)inner * 2, (cuuint64_t)inner * 2 * H};
+    const cuuint32_t box[3] = {(cuuint32_t)inner, 1, (cuuint32_t)Q};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 5-d map over y [batch][L][H][R][64] of type yd: box = {32, R, 1, Q, 1} for fp32, {64, R, 1, Q, 1}
+// for 16-bit y (128-byte lines either way), 128-byte swizzle
+bool map_y(CUtensorMap *m, void *base, int yd, int R, int H, int L, int batch, int Q) {
+    EncodeFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t eb = yd == M3_F32 ? 4 : 2;
+    const cuuint64_t dims[5] = {64, (cuuint64_t)R, (cuuint64_t)H, (cuuint64_t)L, (cuuint64_t)batch};
+    const cuuint64_t strides[4] = {64 * eb, (cuuint64_t)R * 64 * eb, (cuuint64_t)H * R * 64 * eb,
+                                   (cuuint64_t)L * H * R * 64 * eb};
+    const cuuint32_t box[5] = {(cuuint32_t)(128 / eb), (cuuint32_t)R, 1, (cuuint32_t)Q, 1};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    const CUtensorMapDataType ty = yd == M3_F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : yd == M3_F16  ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                   : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    return enc(m, ty, 5, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int N, int R, bool OUT, int YT = M3_F32, bool BCN = false, int QRT = (N == 64 ? 128 : 64)>
+// ws_stride: workspace state slots per sequence; ws_step: slots per segment of this pass
+cudaError_t launch_pass(const TcMaps &maps, const ScanArgs &a, const ScanPlan &pl, int nlaunch, int ws_stride,
+                        int ws_step, cudaStream_t s) {
+    using Sm = Smem<N, R, OUT, YT == M3_F32 ? 4 : 2, BCN, QRT>;
+    static_assert(Sm::kAlloc <= 227 * 1024, "shared memory over the per-CTA limit");
+    auto kern = tc_segment_kernel<N, R, OUT, YT, BCN, QRT>;
+    cudaError_t e = allow_dynamic_smem<tc_segment_kernel<N, R, OUT, YT, BCN, QRT>>(Sm::kAlloc);
+    if (e != cudaSuccess) return e;
+    unsigned *status = device_status_word();
+    if (!status) return cudaErrorUnknown;
+    const long long grid = (long long)a.batch * a.H * nlaunch;
+    const int kid = OUT ? M3_KERNEL_PREFILL_OUTPUT : M3_KERNEL_PREFILL_STATE;
+    trace_mark(kid, s, 0);
+    kern<<<(unsigned)grid, kThreads, Sm::kAlloc, s>>>(maps, a, pl.seglen, pl.nseg, nlaunch, ws_stride, ws_step,
+                                                      status);
+    trace_mark(kid, s, 1);
+    count_launch();
+    return cudaGetLastError();
+}
+
+template <int N, int R, bool BCN, int QRT = (N == 64 ? 128 : 64)>
+cudaError_t run_tc(const ScanArgs &a, const ScanPlan &pl, cudaStream_t s) {
+    using Cf = Cfg<N, R, QRT>;
+    const long long rows = (long long)a.batch * a.L;
+    TcMaps maps;
+    if (!map4(&maps.B, a.B, N, R, a.G, rows, Cf::Q) || !map4(&maps.C, a.C, N, R, a.G, rows, Cf::Q) ||
+        !map4(&maps.X, a.x, kP, R, a.H, rows, Cf::Q) || !map3(&maps.T, a.theta, N / 2, a.H, rows, Cf::Q) ||
+        !map_y(&maps.Y, a.y, a.ydtype, R, a.H, a.L, a.batch, Cf::Q))
+        return cudaErrorInvalidValue;
+    cudaError_t e;
+    // The state pass works on pieces of seglen / nsub tokens (one CTA each) covering segments
+    // 0 .. nseg - 2; the segment pass chains the pieces' end states; the output pass starts
+    // segment g from the state at piece g * nsub.
+    const int npieces = pl.nseg > 1 ? (pl.nseg - 1) * pl.nsub + 1 : 1;
+    if (pl.nseg > 1) {
+        ScanPlan pp = pl;
+        pp.nseg = npieces;
+        pp.seglen = pl.seglen / pl.nsub;
+        if ((e = launch_pass<N, R, false, M3_F32, BCN, QRT>(maps, a, pp, npieces - 1, npieces, 1, s)) != cudaSuccess)
+            return e;
+        if ((e = segment_pass(a, pp, s)) != cudaSuccess) return e;
+    }
+    if (a.ydtype == M3_F16)
+        return launch_pass<N, R, true, M3_F16, BCN, QRT>(maps, a, pl, pl.nseg, npieces, pl.nsub, s);
+    if (a.ydtype == M3_BF16)
+        return launch_pass<N, R, true, M3_BF16, BCN, QRT>(maps, a, pl, pl.nseg, npieces, pl.nsub, s);
+    return launch_pass<N, R, true, M3_F32, BCN, QRT>(maps, a, pl, pl.nseg, npieces, pl.nsub, s);
+}
+
+}  // namespace
+}  // namespace m3

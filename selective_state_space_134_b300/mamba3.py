@@ -18,18 +18,43 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libmamba3.so")
 
 M3_OK, M3_ERR_INVALID_ARG, M3_ERR_UNSUPPORTED, M3_ERR_WORKSPACE, M3_ERR_CUDA, M3_ERR_TIMEOUT, M3_ERR_INDEX = range(7)
-M3_F32, M3_BF16 = 0, 1
-_DTYPE_CODE = {torch.float32: M3_F32, torch.bfloat16: M3_BF16}
+M3_F32, M3_BF16, M3_F16 = 0, 1, 2
+_DTYPE_CODE = {torch.float32: M3_F32, torch.bfloat16: M3_BF16, torch.float16: M3_F16}
 
 
 class m3_dims(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int), ("seqlen", ctypes.c_int), ("nheads", ctypes.c_int),
                 ("headdim", ctypes.c_int), ("dstate", ctypes.c_int), ("rank", ctypes.c_int),
-                ("chunk", ctypes.c_int), ("dtype", ctypes.c_int), ("ngroups", ctypes.c_int)]
+                ("chunk", ctypes.c_int), ("dtype", ctypes.c_int), ("ngroups", ctypes.c_int),
+                ("ydtype", ctypes.c_int)]
 
 
 class m3_state(ctypes.Structure):
     _fields_ = [("h", ctypes.c_void_p), ("B_prev", ctypes.c_void_p), ("x_prev", ctypes.c_void_p)]
+
+
+class m3_bc_norm(ctypes.Structure):
+    _fields_ = [("B_weight", ctypes.c_void_p), ("B_bias", ctypes.c_void_p), ("C_weight", ctypes.c_void_p),
+                ("C_bias", ctypes.c_void_p), ("eps", ctypes.c_float)]
+
+
+@dataclass
+class BcNorm:
+    """BC normalisation and bias: every (token, head, rank) row v of B (C) becomes
+    v / sqrt(mean(v^2) + eps) * weight[h] + bias[h, r].  weight [H, N], bias [H, R, N] fp32 device
+    tensors, or None (gain 1 / no bias)."""
+    B_weight: Optional[torch.Tensor] = None
+    B_bias: Optional[torch.Tensor] = None
+    C_weight: Optional[torch.Tensor] = None
+    C_bias: Optional[torch.Tensor] = None
+    eps: float = 1e-6
+
+    def c(self) -> m3_bc_norm:
+        for t in (self.B_weight, self.B_bias, self.C_weight, self.C_bias):
+            if t is not None and t.dtype != torch.float32:
+                raise ValueError("BC gains and biases are fp32")
+        return m3_bc_norm(_ptr(self.B_weight), _ptr(self.B_bias), _ptr(self.C_weight), _ptr(self.C_bias),
+                          float(self.eps))
 
 
 class m3_token_inputs(ctypes.Structure):
@@ -78,6 +103,11 @@ def lib() -> ctypes.CDLL:
         L.mamba3_scan_fwd_staged.argtypes = [dp, ip, ip, vp, vp, sp, sp, vp, vp, ctypes.c_size_t, ctypes.c_int,
                                              vp, vp]
         L.mamba3_scan_fwd_staged.restype = ctypes.c_int
+        bp = ctypes.POINTER(m3_bc_norm)
+        L.mamba3_scan_fwd_bc.argtypes = [dp] + [vp] * 7 + [bp, sp, vp, sp, vp, ctypes.c_size_t, vp]
+        L.mamba3_scan_fwd_bc.restype = ctypes.c_int
+        L.mamba3_decode_step_bc.argtypes = [dp] + [vp] * 7 + [bp, sp, vp, vp]
+        L.mamba3_decode_step_bc.restype = ctypes.c_int
         L.mamba3_decode_last_variant.argtypes = []
         L.mamba3_decode_last_variant.restype = ctypes.c_int
         L.mamba3_version.argtypes = []
@@ -130,10 +160,13 @@ class State:
                      torch.zeros(batch, nheads, R, P, dtype=dtype, device=device))
 
 
-def dims(batch, seqlen, nheads, P, N, R, dtype, chunk=0, ngroups=0) -> m3_dims:
-    """ngroups: B / C groups of heads (0 = one B and C per head)."""
-    code = _DTYPE_CODE.get(dtype, dtype) if isinstance(dtype, torch.dtype) else int(dtype)
-    return m3_dims(batch, seqlen, nheads, P, N, R, chunk, code, ngroups)
+def _code(dtype) -> int:
+    return _DTYPE_CODE[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+
+
+def dims(batch, seqlen, nheads, P, N, R, dtype, chunk=0, ngroups=0, ydtype=torch.float32) -> m3_dims:
+    """ngroups: B / C groups of heads (0 = one B and C per head); ydtype: element type of y."""
+    return m3_dims(batch, seqlen, nheads, P, N, R, chunk, _code(dtype), ngroups, _code(ydtype))
 
 
 def _groups(H: int, G: int) -> int:
@@ -149,48 +182,62 @@ def scan_fwd_workspace(d: m3_dims) -> int:
 
 def scan_fwd(x, B, C, dt, A, lam, theta, state_in: Optional[State] = None,
              state_out: Optional[State] = None, chunk: int = 0, y: Optional[torch.Tensor] = None,
-             workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+             workspace: Optional[torch.Tensor] = None, stream=None, y_dtype=torch.float32,
+             bc: Optional[BcNorm] = None) -> torch.Tensor:
     """Chunked prefill.  x [b,L,H,R,P]; B, C [b,L,H,R,N] (or [b,L,G,R,N]: G groups of heads);
     dt, A, lam [b,L,H]; theta [b,L,H,N/2].
 
-    Returns y [b,L,H,R,P] (fp32).  ``state_out`` (may be ``state_in``) receives the final
-    state and carry.  The workspace is allocated here through torch unless given.
+    Returns y [b,L,H,R,P] of ``y_dtype`` (fp32, fp16 or bf16; the dtype of ``y`` when given).
+    ``state_out`` (may be ``state_in``) receives the final state and carry.  The workspace is
+    allocated here through torch unless given.  ``bc``: BC normalisation and bias in front of the
+    recurrence (mamba3_scan_fwd_bc).
     """
     b, L, H, R, P = x.shape
     N = B.shape[-1]
-    d = dims(b, L, H, P, N, R, x.dtype, chunk, _groups(H, B.shape[2]))
+    if y is not None:
+        y_dtype = y.dtype
+    d = dims(b, L, H, P, N, R, x.dtype, chunk, _groups(H, B.shape[2]), y_dtype)
     if y is None:
-        y = torch.empty(x.shape, dtype=torch.float32, device=x.device)
+        y = torch.empty(x.shape, dtype=y_dtype, device=x.device)
     ws_bytes = scan_fwd_workspace(d)
     if workspace is None and ws_bytes > 0:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=x.device)
     st_in = state_in.c() if state_in is not None else None
     st_out = state_out.c() if state_out is not None else None
-    rc = lib().mamba3_scan_fwd(ctypes.byref(d), _ptr(x), _ptr(B), _ptr(C), _ptr(dt), _ptr(A), _ptr(lam),
-                               _ptr(theta), ctypes.byref(st_in) if st_in is not None else None, _ptr(y),
-                               ctypes.byref(st_out) if st_out is not None else None,
-                               _ptr(workspace), workspace.numel() if workspace is not None else 0,
-                               _stream_ptr(stream))
-    _check(rc, "mamba3_scan_fwd")
+    tail = (ctypes.byref(st_in) if st_in is not None else None, _ptr(y),
+            ctypes.byref(st_out) if st_out is not None else None,
+            _ptr(workspace), workspace.numel() if workspace is not None else 0, _stream_ptr(stream))
+    head = (ctypes.byref(d), _ptr(x), _ptr(B), _ptr(C), _ptr(dt), _ptr(A), _ptr(lam), _ptr(theta))
+    if bc is None:
+        _check(lib().mamba3_scan_fwd(*head, *tail), "mamba3_scan_fwd")
+    else:
+        bcs = bc.c()
+        _check(lib().mamba3_scan_fwd_bc(*head, ctypes.byref(bcs), *tail), "mamba3_scan_fwd_bc")
     return y
 
 
 def decode_step(x, B, C, dt, A, lam, theta, state: State, y: Optional[torch.Tensor] = None,
-                stream=None) -> torch.Tensor:
+                stream=None, y_dtype=torch.float32, bc: Optional[BcNorm] = None) -> torch.Tensor:
     """One token for every (b, h).  x [b,H,R,P]; B, C [b,H,R,N] (or [b,G,R,N]: G groups of heads);
     dt, A, lam [b,H]; theta [b,H,N/2].
 
-    Updates ``state`` in place and returns y [b,H,R,P] (fp32).
+    Updates ``state`` in place and returns y [b,H,R,P] of ``y_dtype`` (the dtype of ``y`` when given).
     """
     b, H, R, P = x.shape
     N = B.shape[-1]
-    d = dims(b, 1, H, P, N, R, x.dtype, 0, _groups(H, B.shape[1]))
+    if y is not None:
+        y_dtype = y.dtype
+    d = dims(b, 1, H, P, N, R, x.dtype, 0, _groups(H, B.shape[1]), y_dtype)
     if y is None:
-        y = torch.empty(x.shape, dtype=torch.float32, device=x.device)
+        y = torch.empty(x.shape, dtype=y_dtype, device=x.device)
     st = state.c()
-    rc = lib().mamba3_decode_step(ctypes.byref(d), _ptr(x), _ptr(B), _ptr(C), _ptr(dt), _ptr(A),
-                                  _ptr(lam), _ptr(theta), ctypes.byref(st), _ptr(y), _stream_ptr(stream))
-    _check(rc, "mamba3_decode_step")
+    head = (ctypes.byref(d), _ptr(x), _ptr(B), _ptr(C), _ptr(dt), _ptr(A), _ptr(lam), _ptr(theta))
+    if bc is None:
+        _check(lib().mamba3_decode_step(*head, ctypes.byref(st), _ptr(y), _stream_ptr(stream)), "mamba3_decode_step")
+    else:
+        bcs = bc.c()
+        _check(lib().mamba3_decode_step_bc(*head, ctypes.byref(bcs), ctypes.byref(st), _ptr(y), _stream_ptr(stream)),
+               "mamba3_decode_step_bc")
     return y
 
 
@@ -206,7 +253,7 @@ def decode_step_pooled(x, B, C, dt, A, lam, theta, slot: torch.Tensor, pool: Sta
     N = B.shape[-1]
     if slot.dtype != torch.int32:
         raise ValueError("slot must be int32")
-    d = dims(b, 1, H, P, N, R, x.dtype, 0, _groups(H, B.shape[1]))
+    d = dims(b, 1, H, P, N, R, x.dtype, 0, _groups(H, B.shape[1]), y.dtype if y is not None else torch.float32)
     if y is None:
         y = torch.zeros(x.shape, dtype=torch.float32, device=x.device)
     rc = lib().mamba3_decode_step_pooled(ctypes.byref(d), _ptr(slot), _ptr(x), _ptr(B), _ptr(C), _ptr(dt),
@@ -260,7 +307,7 @@ def scan_fwd_noalloc(x, B, C, dt, A, lam, theta, state_in: Optional[State] = Non
     fn.restype = ctypes.c_int
     b, L, H, R, P = x.shape
     N = B.shape[-1]
-    d = dims(b, L, H, P, N, R, x.dtype, chunk, _groups(H, B.shape[2]))
+    d = dims(b, L, H, P, N, R, x.dtype, chunk, _groups(H, B.shape[2]), y.dtype if y is not None else torch.float32)
     if y is None:
         y = torch.empty(x.shape, dtype=torch.float32, device=x.device)
     st_in = state_in.c() if state_in is not None else None
@@ -306,7 +353,7 @@ def scan_fwd_staged(host: dict, dev: dict, host_y: torch.Tensor, dev_y: torch.Te
     x = host["x"]
     b, L, H, R, P = x.shape
     N = host["B"].shape[-1]
-    d = dims(b, L, H, P, N, R, x.dtype, 0, _groups(H, host["B"].shape[2]))
+    d = dims(b, L, H, P, N, R, x.dtype, 0, _groups(H, host["B"].shape[2]), dev_y.dtype)
     need = scan_fwd_staged_workspace(d, slices)
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev_y.device)

@@ -121,3 +121,16 @@ def decode_pool(w: Workload, device="cpu", pool: int = DECODE_POOL) -> list:
 def to_f64(t: torch.Tensor):
     """Exact widening of stored values to float64 numpy (the oracle's input)."""
     return t.detach().to("cpu", torch.float64).numpy()
+
+
+def bc_params(w: Workload, device="cpu", seed: int = 0, eps: float = 1e-5) -> dict:
+    """Synthetic parameters of the BC normalisation and bias (no trained weights exist here): gains
+    U(0.5, 1.5) [H, N] and biases 0.5 N(0, 1) [H, R, N] for B and for C, fp32, and eps."""
+    out = {}
+    for i, k in enumerate(("B", "C")):
+        g = _gen(w.seed + 17 * seed, 500 + 2 * i, device)
+        out[f"{k}_weight"] = 0.5 + torch.rand((w.nheads, w.N), generator=g, device=device, dtype=torch.float32)
+        g = _gen(w.seed + 17 * seed, 501 + 2 * i, device)
+        out[f"{k}_bias"] = 0.5 * _normal((w.nheads, w.R, w.N), g, device)
+    out["eps"] = eps
+    return out

@@ -77,7 +77,8 @@ def test_workspace_query_validates():
                       (dict(rank=9), api.M3_ERR_UNSUPPORTED), (dict(rank=0), api.M3_ERR_UNSUPPORTED),
                       (dict(dtype=7), api.M3_ERR_UNSUPPORTED), (dict(batch=-1), api.M3_ERR_INVALID_ARG),
                       (dict(seqlen=-5), api.M3_ERR_INVALID_ARG), (dict(nheads=0), api.M3_ERR_INVALID_ARG),
-                      (dict(chunk=-1), api.M3_ERR_INVALID_ARG)]:
+                      (dict(chunk=-1), api.M3_ERR_INVALID_ARG), (dict(ydtype=3), api.M3_ERR_UNSUPPORTED),
+                      (dict(ydtype=-1), api.M3_ERR_UNSUPPORTED), (dict(dtype=api.M3_F16), api.M3_ERR_UNSUPPORTED)]:
         dd = m3.dims(4, 4096, 32, 64, 64, 1, torch.bfloat16)
         for k, v in bad.items():
             setattr(dd, k, v)
@@ -208,4 +209,27 @@ def test_staged_prefill_rejects_bad_arguments_before_any_copy():
     # several token ranges need a device state (with its carry) to hand on
     assert lib.mamba3_scan_fwd_staged(ctypes.byref(d), ctypes.byref(ins), ctypes.byref(ins), None, None, None,
                                       None, None, None, 0, 2, None, None) == api.M3_ERR_INVALID_ARG
+    assert m3.launch_count() == before
+
+
+def test_bc_norm_validation():
+    # eps < 0 or NaN, or a misaligned gain pointer: M3_ERR_INVALID_ARG before any launch; grouped
+    # decode with BC normalisation: M3_ERR_UNSUPPORTED
+    lib = m3.lib()
+    ptrs = Ptrs()
+    d = m3.dims(1, 64, 8, 64, 64, 1, torch.bfloat16)
+    args = [ptrs.get() for _ in range(8)]
+    before = m3.launch_count()
+    for eps, wptr in ((-1.0, None), (float("nan"), None), (1e-5, ptrs.get() + 2)):
+        bc = api.m3_bc_norm(wptr, None, None, None, eps)
+        rc = lib.mamba3_scan_fwd_bc(ctypes.byref(d), *args[:7], ctypes.byref(bc), None, args[7], None, None, 0, None)
+        assert rc == api.M3_ERR_INVALID_ARG, eps
+        st = api.m3_state(ptrs.get(), ptrs.get(), ptrs.get())
+        rc = lib.mamba3_decode_step_bc(ctypes.byref(d), *args[:7], ctypes.byref(bc), ctypes.byref(st), args[7], None)
+        assert rc == api.M3_ERR_INVALID_ARG, eps
+    bc = api.m3_bc_norm(None, None, None, None, 1e-5)
+    dg = m3.dims(1, 1, 8, 64, 64, 1, torch.bfloat16, ngroups=2)
+    st = api.m3_state(ptrs.get(), ptrs.get(), ptrs.get())
+    rc = lib.mamba3_decode_step_bc(ctypes.byref(dg), *args[:7], ctypes.byref(bc), ctypes.byref(st), args[7], None)
+    assert rc == api.M3_ERR_UNSUPPORTED
     assert m3.launch_count() == before

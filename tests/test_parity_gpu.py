@@ -428,3 +428,91 @@ def test_staged_host_prefill_matches_device_prefill(slices, groups):
     assert_err(y_host.double().numpy(), to_f64(y_ref), tol, "y")
     assert_err(h_host.double().numpy(), to_f64(s_ref.h), tol, "h")
     assert torch.equal(st.B_prev, s_ref.B_prev) and torch.equal(st.x_prev, s_ref.x_prev)
+
+
+# ---------------------------------------------------------------- output element type
+
+Y16 = (torch.float16, torch.bfloat16)
+
+
+@pytest.mark.parametrize("case", ["siso_n64_small", "mimo_r4_small", "long_small_segmented", "siso_n128_small",
+                                  "siso_n64_small_f32", "odd_shapes_bf16"])
+def test_prefill_16bit_y_is_the_fp32_result_rounded_once(case):
+    # the same arithmetic for every output type: y in fp16 / bf16 equals the fp32 y rounded to
+    # nearest even, bit for bit (tensor-core and SIMT paths)
+    wname, over = SMALL[case]
+    w = WORKLOADS[wname].with_(**over)
+    inp = prefill_inputs(w, "cuda")
+    st = random_state(w.batch, w.nheads, w.P, w.N, w.R, inp["x"].dtype, seed=3)
+    y32 = m3.scan_fwd(*(inp[k] for k in KEYS), state_in=st)
+    for yd in Y16:
+        y = m3.scan_fwd(*(inp[k] for k in KEYS), state_in=st, y_dtype=yd)
+        assert y.dtype == yd
+        assert torch.equal(y, y32.to(yd)), yd
+    assert m3.device_status() == m3.M3_OK
+
+
+@pytest.mark.parametrize("wname", ["siso_n64", "siso_n128", "mimo_r4"])
+def test_prefill_fp16_y_full_size_sampled_matches_oracle(wname):
+    # fp16 y keeps y at the input element size; rounding costs at most 2^-11 |y|, inside the bar
+    w = WORKLOADS[wname]
+    inp = prefill_inputs(w, "cuda")
+    so = m3.State.zeros(w.batch, w.nheads, w.P, w.N, w.R, inp["x"].dtype)
+    y = m3.scan_fwd(*(inp[k] for k in KEYS), state_out=so, y_dtype=torch.float16)
+    assert m3.device_status() == m3.M3_OK
+    pairs = [(0, 0), (w.batch // 2, w.nheads // 3), (w.batch - 1, w.nheads - 1)]
+    stack = {k: torch.cat([inp[k][b:b + 1, :, h:h + 1] for b, h in pairs], dim=0) for k in KEYS}
+    yr, hr, _, _ = oracle.scan(*(to_f64(stack[k]) for k in KEYS), nthreads=len(pairs))
+    for i, (b, h) in enumerate(pairs):
+        assert_err(to_f64(y[b:b + 1, :, h:h + 1]), yr[i:i + 1], TOL[w.dtype], f"y (b, h) = {(b, h)}")
+        assert_err(to_f64(so.h[b:b + 1, h:h + 1]), hr[i:i + 1], TOL[w.dtype], f"h (b, h) = {(b, h)}")
+    assert torch.isfinite(y.float()).all()
+
+
+@pytest.mark.parametrize("over", [dict(), dict(dtype="f32"), dict(P=16, dtype="f32")])
+def test_decode_16bit_y_is_the_fp32_result_rounded_once(over):
+    # tensor-core, streaming and generic decode kernels
+    w = WORKLOADS["decode_n64_r4"].with_(batch=3, nheads=6, **over)
+    st = decode_state(w, "cuda")
+    tok = decode_pool(w, "cuda", pool=1)[0]
+    s32 = m3.State(st["h"].clone(), st["B_prev"].clone(), st["x_prev"].clone())
+    y32 = m3.decode_step(*(tok[k] for k in KEYS), state=s32)
+    for yd in Y16:
+        s = m3.State(st["h"].clone(), st["B_prev"].clone(), st["x_prev"].clone())
+        y = m3.decode_step(*(tok[k] for k in KEYS), state=s, y_dtype=yd)
+        assert y.dtype == yd
+        assert torch.equal(y, y32.to(yd)), yd
+        assert torch.equal(s.h, s32.h)
+
+
+# ---------------------------------------------------------------- the chunk rule Q = N / R
+
+@pytest.mark.parametrize("R,H,b,L,with_state", [(1, 3, 2, 300, False), (2, 2, 1, 333, True), (4, 3, 1, 201, True),
+                                                (4, 2, 1, 3000, False), (1, 1, 1, 5000, True)])
+def test_chunk_rule_tile_matches_oracle(R, H, b, L, with_state):
+    # dims.chunk = N / R selects the 64-row tile for N = 64 (linkstar.cloud/article/869, section
+    # "训练怎么办"); long sequences with few heads are also cut into segments
+    w = WORKLOADS["mimo_r4"].with_(batch=b, nheads=H, seqlen=L, R=R)
+    inp = prefill_inputs(w, "cuda")
+    st = random_state(b, H, w.P, w.N, R, inp["x"].dtype, seed=R) if with_state else None
+    y, so = gpu_scan(inp, state_in=st, chunk=64 // R)
+    yr, hr, Br, xr = oracle_full(inp, st)
+    assert_err(to_f64(y), yr, TOL[w.dtype], "y")
+    assert_err(to_f64(so.h), hr, TOL[w.dtype], "h")
+    np.testing.assert_array_equal(to_f64(so.B_prev), Br)
+    # and it agrees with the default tile
+    y0, _ = gpu_scan(inp, state_in=st)
+    assert_err(to_f64(y), to_f64(y0), TOL[w.dtype], "y tiles")
+
+
+def test_chunk_rule_tile_with_bc_matches_oracle():
+    w = WORKLOADS["mimo_r4"].with_(batch=1, nheads=2, seqlen=2500)
+    inp = prefill_inputs(w, "cuda")
+    from selective_state_space_134_b300.synth import bc_params
+    p = bc_params(w, "cuda", seed=7)
+    bc = m3.BcNorm(p["B_weight"], p["B_bias"], p["C_weight"], p["C_bias"], p["eps"])
+    y = m3.scan_fwd(*(inp[k] for k in KEYS), chunk=16, bc=bc)
+    assert m3.device_status() == m3.M3_OK
+    bref = {k: (to_f64(v) if isinstance(v, torch.Tensor) else v) for k, v in p.items()}
+    yr, _, _, _ = oracle.scan_bc(*(to_f64(inp[k]) for k in KEYS), bref, nthreads=2)
+    assert_err(to_f64(y), yr, TOL[w.dtype], "y")
