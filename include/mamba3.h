@@ -207,6 +207,47 @@ m3_status mamba3_scan_fwd_staged(const m3_dims *dims, const m3_token_inputs *hos
                                  const m3_state *dev_state_out, float *host_h_out, void *workspace,
                                  size_t workspace_bytes, int slices, void *stream, void *copy_stream);
 
+/* Gradients flowing into the backward pass: fp32 device arrays of the forward outputs' layouts. */
+typedef struct {
+    const float *dy;            /* [batch][L][H][R][P], required */
+    const float *dh_out;        /* [batch][H][N][P], or NULL (zero) */
+    const float *dB_prev_out;   /* [batch][H][R][N], or NULL: gradient of the carry returned */
+    const float *dx_prev_out;   /* [batch][H][R][P], or NULL */
+} m3_grads_in;
+
+/* Gradients out: fp32 device arrays of the forward inputs' layouts (overwritten). */
+typedef struct {
+    float *dx, *dB, *dC;        /* [batch][L][H][R][P], [..][N], [..][N]; required */
+    float *ddt, *dA, *dlambda;  /* [batch][L][H]; required */
+    float *dtheta;              /* [batch][L][H][N/2]; required */
+    float *dh0;                 /* [batch][H][N][P], or NULL (not written) */
+    float *dB_prev, *dx_prev;   /* [batch][H][R][N], [batch][H][R][P], or NULL */
+} m3_grads_out;
+
+/*
+ * Workspace bytes mamba3_scan_bwd needs (the forward states at every chunk boundary:
+ * batch x H x (L / Q + 1) x N x P floats).  Errors as mamba3_scan_fwd_workspace.
+ */
+m3_status mamba3_scan_bwd_workspace(const m3_dims *dims, size_t *bytes);
+
+/*
+ * Backward pass of mamba3_scan_fwd (reverse mode, for training through the chunked
+ * form; linkstar.cloud/article/869, section "训练怎么办"): the gradient of
+ *   Loss = sum(dy * y) + sum(dh_out * h_out) + sum(dB_prev_out * B_prev_out)
+ *          + sum(dx_prev_out * x_prev_out)
+ * with respect to x, B, C, dt, A, lambda, theta and the initial state and carry,
+ * for the forward call with the same dims, inputs and state_in (NULL = zero state
+ * and no carry; the carry's gradients are then zero).  The forward states are
+ * recomputed here (chunk checkpoints in the workspace), so the forward outputs
+ * are not needed.  Arithmetic is fp32 on CUDA cores.
+ * Supported: every forward shape with N * P <= 8192 and one B and C per head
+ * (ngroups 0 or H); otherwise M3_ERR_UNSUPPORTED.  dims->ydtype is ignored.
+ * Errors as mamba3_scan_fwd (M3_ERR_INVALID_ARG for a missing required pointer).
+ */
+m3_status mamba3_scan_bwd(const m3_dims *dims, const m3_token_inputs *inputs, const m3_state *state_in,
+                          const m3_grads_in *grads_in, const m3_grads_out *grads_out, void *workspace,
+                          size_t workspace_bytes, void *stream);
+
 /* Size of the static scratch array behind mamba3_scan_fwd_noalloc (16 MiB). */
 #define M3_NOALLOC_SCRATCH_BYTES (16u << 20)
 

@@ -438,6 +438,74 @@ m3_status mamba3_decode_step_pooled(const m3_dims *dims, const int *slot, const 
     return e == cudaSuccess ? M3_OK : M3_ERR_CUDA;
 }
 
+m3_status mamba3_scan_bwd_workspace(const m3_dims *dims, size_t *bytes) {
+    if (!bytes) return M3_ERR_INVALID_ARG;
+    m3_status st = check_dims(dims, true);
+    if (st != M3_OK) return st;
+    const m3_dims &d = *dims;
+    if (groups_of(d) != d.nheads || (size_t)d.dstate * d.headdim > 8192 ||
+        bwd_smem_bytes(d.dstate, d.headdim, d.rank) > 227u * 1024u)
+        return M3_ERR_UNSUPPORTED;
+    *bytes = bwd_workspace_bytes(d.batch, d.nheads, d.seqlen, d.dstate, d.headdim, d.rank);
+    return M3_OK;
+}
+
+m3_status mamba3_scan_bwd(const m3_dims *dims, const m3_token_inputs *in, const m3_state *state_in,
+                          const m3_grads_in *gin, const m3_grads_out *gout, void *workspace, size_t workspace_bytes,
+                          void *stream) {
+    size_t need = 0;
+    m3_status st = mamba3_scan_bwd_workspace(dims, &need);
+    if (st != M3_OK) return st;
+    const m3_dims &d = *dims;
+    if (!in || !gin || !gout) return M3_ERR_INVALID_ARG;
+    if (d.batch == 0) return M3_OK;
+    const size_t es = elem_size(d.dtype);
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (state_in) {
+        if (state_in->h && !ptr_ok(state_in->h, 4)) return M3_ERR_INVALID_ARG;
+        if ((state_in->B_prev == nullptr) != (state_in->x_prev == nullptr)) return M3_ERR_INVALID_ARG;
+        if (state_in->B_prev && (!ptr_ok(state_in->B_prev, es) || !ptr_ok(state_in->x_prev, es)))
+            return M3_ERR_INVALID_ARG;
+    }
+    for (const float *p : {gin->dh_out, gin->dB_prev_out, gin->dx_prev_out})
+        if (p && !ptr_ok(p, 4)) return M3_ERR_INVALID_ARG;
+    for (float *p : {gout->dh0, gout->dB_prev, gout->dx_prev})
+        if (p && !ptr_ok(p, 4)) return M3_ERR_INVALID_ARG;
+    const size_t bh = (size_t)d.batch * d.nheads;
+    if (d.seqlen == 0) {
+        // nothing scanned: the state's and carry's gradients pass through
+        const struct { float *dst; const float *src; size_t n; } pass[3] = {
+            {gout->dh0, gin->dh_out, bh * d.dstate * d.headdim},
+            {gout->dB_prev, gin->dB_prev_out, bh * d.rank * d.dstate},
+            {gout->dx_prev, gin->dx_prev_out, bh * d.rank * d.headdim}};
+        for (const auto &q : pass) {
+            if (!q.dst) continue;
+            const cudaError_t e = q.src ? cudaMemcpyAsync(q.dst, q.src, q.n * 4, cudaMemcpyDeviceToDevice, s)
+                                        : cudaMemsetAsync(q.dst, 0, q.n * 4, s);
+            if (e != cudaSuccess) return M3_ERR_CUDA;
+        }
+        return M3_OK;
+    }
+    for (const void *p : {in->x, in->B, in->C, in->dt, in->A, in->lambda, in->theta})
+        if (!ptr_ok(p, es)) return M3_ERR_INVALID_ARG;
+    if (!ptr_ok(gin->dy, 4)) return M3_ERR_INVALID_ARG;
+    for (float *p : {gout->dx, gout->dB, gout->dC, gout->ddt, gout->dA, gout->dlambda, gout->dtheta})
+        if (!ptr_ok(p, 4)) return M3_ERR_INVALID_ARG;
+    if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return M3_ERR_WORKSPACE;
+    BwdArgs a{};
+    a.dtype = d.dtype; a.batch = d.batch; a.L = d.seqlen; a.H = d.nheads; a.P = d.headdim; a.N = d.dstate;
+    a.R = d.rank;
+    a.x = in->x; a.B = in->B; a.C = in->C; a.dt = in->dt; a.A = in->A; a.lam = in->lambda; a.theta = in->theta;
+    a.h0 = state_in ? state_in->h : nullptr;
+    a.Bprev = state_in ? state_in->B_prev : nullptr;
+    a.xprev = state_in ? state_in->x_prev : nullptr;
+    a.dy = gin->dy; a.dh_out = gin->dh_out; a.dBprev_out = gin->dB_prev_out; a.dxprev_out = gin->dx_prev_out;
+    a.dx = gout->dx; a.dB = gout->dB; a.dC = gout->dC; a.ddt = gout->ddt; a.dA = gout->dA; a.dlam = gout->dlambda;
+    a.dtheta = gout->dtheta; a.dh0 = gout->dh0; a.dBprev = gout->dB_prev; a.dxprev = gout->dx_prev;
+    a.ws = static_cast<float *>(workspace);
+    return scan_bwd(a, s) == cudaSuccess ? M3_OK : M3_ERR_CUDA;
+}
+
 m3_status mamba3_device_status(void *stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return M3_ERR_CUDA;
     unsigned *w = device_status_word();

@@ -61,6 +61,15 @@ class m3_token_inputs(ctypes.Structure):
     _fields_ = [(k, ctypes.c_void_p) for k in ("x", "B", "C", "dt", "A", "lam", "theta")]
 
 
+class m3_grads_in(ctypes.Structure):
+    _fields_ = [(k, ctypes.c_void_p) for k in ("dy", "dh_out", "dB_prev_out", "dx_prev_out")]
+
+
+class m3_grads_out(ctypes.Structure):
+    _fields_ = [(k, ctypes.c_void_p) for k in ("dx", "dB", "dC", "ddt", "dA", "dlambda", "dtheta", "dh0", "dB_prev",
+                                              "dx_prev")]
+
+
 class Mamba3Error(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
@@ -108,6 +117,11 @@ def lib() -> ctypes.CDLL:
         L.mamba3_scan_fwd_bc.restype = ctypes.c_int
         L.mamba3_decode_step_bc.argtypes = [dp] + [vp] * 7 + [bp, sp, vp, vp]
         L.mamba3_decode_step_bc.restype = ctypes.c_int
+        L.mamba3_scan_bwd_workspace.argtypes = [dp, ctypes.POINTER(ctypes.c_size_t)]
+        L.mamba3_scan_bwd_workspace.restype = ctypes.c_int
+        L.mamba3_scan_bwd.argtypes = [dp, ctypes.POINTER(m3_token_inputs), sp, ctypes.POINTER(m3_grads_in),
+                                      ctypes.POINTER(m3_grads_out), vp, ctypes.c_size_t, vp]
+        L.mamba3_scan_bwd.restype = ctypes.c_int
         L.mamba3_decode_last_variant.argtypes = []
         L.mamba3_decode_last_variant.restype = ctypes.c_int
         L.mamba3_version.argtypes = []
@@ -263,7 +277,43 @@ def decode_step_pooled(x, B, C, dt, A, lam, theta, slot: torch.Tensor, pool: Sta
     return y
 
 
-KERNEL_PREFILL_STATE, KERNEL_SEGMENT_PASS, KERNEL_PREFILL_OUTPUT, KERNEL_DECODE = range(4)
+KERNEL_PREFILL_STATE, KERNEL_SEGMENT_PASS, KERNEL_PREFILL_OUTPUT, KERNEL_DECODE, KERNEL_BACKWARD = range(5)
+
+
+def scan_bwd_workspace(d: m3_dims) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().mamba3_scan_bwd_workspace(ctypes.byref(d), ctypes.byref(n)), "mamba3_scan_bwd_workspace")
+    return int(n.value)
+
+
+def scan_bwd(x, B, C, dt, A, lam, theta, dy, state_in: Optional[State] = None, dh_out=None, dB_prev_out=None,
+             dx_prev_out=None, workspace: Optional[torch.Tensor] = None, grads: Optional[dict] = None,
+             stream=None) -> dict:
+    """mamba3_scan_bwd: gradients of sum(dy * y) (+ the final state's and carry's terms) with respect
+    to the prefill's inputs.  Returns a dict of fp32 tensors: x, B, C, dt, A, lam, theta, h0, Bprev,
+    xprev (allocated through torch unless ``grads`` holds them)."""
+    b, L, H, R, P = x.shape
+    N = B.shape[-1]
+    d = dims(b, L, H, P, N, R, x.dtype, 0, _groups(H, B.shape[2]))
+    need = scan_bwd_workspace(d)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    if grads is None:
+        f = lambda t: torch.empty(t.shape, dtype=torch.float32, device=x.device)
+        grads = {"x": f(x), "B": f(B), "C": f(C), "dt": f(dt), "A": f(A), "lam": f(lam), "theta": f(theta),
+                 "h0": torch.empty((b, H, N, P), dtype=torch.float32, device=x.device),
+                 "Bprev": torch.empty((b, H, R, N), dtype=torch.float32, device=x.device),
+                 "xprev": torch.empty((b, H, R, P), dtype=torch.float32, device=x.device)}
+    ins = m3_token_inputs(*(_ptr(t) for t in (x, B, C, dt, A, lam, theta)))
+    gin = m3_grads_in(_ptr(dy), _ptr(dh_out), _ptr(dB_prev_out), _ptr(dx_prev_out))
+    gout = m3_grads_out(*(_ptr(grads.get(k)) for k in ("x", "B", "C", "dt", "A", "lam", "theta", "h0", "Bprev",
+                                                        "xprev")))
+    st = state_in.c() if state_in is not None else None
+    rc = lib().mamba3_scan_bwd(ctypes.byref(d), ctypes.byref(ins), ctypes.byref(st) if st is not None else None,
+                               ctypes.byref(gin), ctypes.byref(gout), _ptr(workspace),
+                               workspace.numel() if workspace is not None else 0, _stream_ptr(stream))
+    _check(rc, "mamba3_scan_bwd")
+    return grads
 
 
 def trace_begin(kernel: int, max_launches: int):

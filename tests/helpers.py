@@ -16,18 +16,19 @@ KEYS = ("x", "B", "C", "dt", "A", "lam", "theta")
 RECORD = []
 
 
-def norm_err(got, ref) -> float:
+def norm_err(got, ref, floor=1e-30) -> float:
+    """max|got - ref| / rms(ref); the denominator is at least `floor` (for references that vanish)."""
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     if ref.size == 0:
         return 0.0
     rms = np.sqrt(np.mean(ref * ref))
-    return float(np.max(np.abs(got - ref)) / max(rms, 1e-30))
+    return float(np.max(np.abs(got - ref)) / max(rms, floor))
 
 
-def assert_err(got, ref, tol, what="") -> float:
-    """Asserts norm_err(got, ref) <= tol and records the measured error against its bar."""
-    e = norm_err(got, ref)
+def assert_err(got, ref, tol, what="", floor=1e-30) -> float:
+    """Asserts norm_err(got, ref, floor) <= tol and records the measured error against its bar."""
+    e = norm_err(got, ref, floor)
     test = os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0]
     RECORD.append((test, str(what), e, float(tol)))
     assert e <= tol, (what, e, tol)

@@ -233,3 +233,31 @@ def test_bc_norm_validation():
     rc = lib.mamba3_decode_step_bc(ctypes.byref(dg), *args[:7], ctypes.byref(bc), ctypes.byref(st), args[7], None)
     assert rc == api.M3_ERR_UNSUPPORTED
     assert m3.launch_count() == before
+
+
+def test_backward_validation():
+    lib = m3.lib()
+    ptrs = Ptrs()
+    n = ctypes.c_size_t(0)
+    d = m3.dims(2, 100, 4, 64, 64, 1, torch.bfloat16)
+    assert lib.mamba3_scan_bwd_workspace(ctypes.byref(d), ctypes.byref(n)) == 0 and n.value > 0
+    # one B and C per head only; N * P <= 8192
+    for bad in (m3.dims(2, 100, 4, 64, 64, 1, torch.bfloat16, ngroups=2), m3.dims(2, 100, 4, 128, 128, 1, torch.float32)):
+        assert lib.mamba3_scan_bwd_workspace(ctypes.byref(bad), ctypes.byref(n)) == api.M3_ERR_UNSUPPORTED
+    ins = api.m3_token_inputs(*(ptrs.get() for _ in range(7)))
+    gin = api.m3_grads_in(ptrs.get(), None, None, None)
+    gout = api.m3_grads_out(*(ptrs.get() for _ in range(7)), None, None, None)
+    before = m3.launch_count()
+    # missing workspace, missing dy, missing dx, NULL structs
+    assert lib.mamba3_scan_bwd(ctypes.byref(d), ctypes.byref(ins), None, ctypes.byref(gin), ctypes.byref(gout),
+                               None, 0, None) == api.M3_ERR_WORKSPACE
+    ws = ptrs.get(n.value)
+    gin0 = api.m3_grads_in(None, None, None, None)
+    assert lib.mamba3_scan_bwd(ctypes.byref(d), ctypes.byref(ins), None, ctypes.byref(gin0), ctypes.byref(gout),
+                               ws, n.value, None) == api.M3_ERR_INVALID_ARG
+    gout0 = api.m3_grads_out(None, *(ptrs.get() for _ in range(6)), None, None, None)
+    assert lib.mamba3_scan_bwd(ctypes.byref(d), ctypes.byref(ins), None, ctypes.byref(gin), ctypes.byref(gout0),
+                               ws, n.value, None) == api.M3_ERR_INVALID_ARG
+    assert lib.mamba3_scan_bwd(ctypes.byref(d), None, None, ctypes.byref(gin), ctypes.byref(gout),
+                               ws, n.value, None) == api.M3_ERR_INVALID_ARG
+    assert m3.launch_count() == before
