@@ -1,6 +1,7 @@
 """Benchmark of the Mamba-3 layer recurrence on B300: prefill and decode tokens/s.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--quick] [--decode-only]
+    python bench.py --workload NAME [--batch B] [--heads H] [--seqlen L] [--backward] [--steps K]
 
 A step is one mamba3_scan_fwd over the SISO bf16 prefill workload (batch 4,
 32 heads, L = 4096, P = 64, N = 64, R = 1): the prefill hot path end to end
@@ -363,33 +364,125 @@ def e2e_prefill(m3, w, inp, steps, warmup, slices=16):
             "slices": slices}
 
 
-def cpu_oracle_rate(w, inp, max_seconds=12.0):
-    """The fp64 CPU oracle on a bounded sample of the workload, all host cores; tokens/s.
+def _oracle_sample(w, nseq, max_tokens=None):
+    """CPU inputs for `nseq` (b, h) sequences of workload w (heads stacked as the batch axis) of at most
+    `max_tokens` tokens each, widened to float64 for the oracle (same distributions as the GPU runs)."""
+    from selective_state_space_134_b300.synth import prefill_inputs, to_f64
+    L = w.seqlen if max_tokens is None else min(w.seqlen, max_tokens)
+    inp = prefill_inputs(w.with_(batch=nseq, nheads=1, seqlen=max(L, 1)), "cpu")
+    return [to_f64(inp[k]) for k in KEYS], L
 
-    The sample is 2 x cores whole (b, h) sequences, scanned again and again until
-    about `max_seconds` of wall time have passed."""
+
+def oracle_rate(w, threads, seconds, max_tokens=None, nseq=None):
+    """Times the fp64 CPU oracle on a bounded sample of workload w: `nseq` whole (b, h) sequences
+    (default 2 x threads) of at most `max_tokens` tokens, scanned again and again for about `seconds`
+    of wall time on `threads` POSIX threads.  Returns tokens/s, a token counting all the workload's
+    heads (the GPU figures count the same way)."""
     import oracle
-    from selective_state_space_134_b300.synth import to_f64
-    cores = os.cpu_count() or 1
-    nseq = max(1, min(w.batch * w.nheads, 2 * cores))
-    pairs = [(i // w.nheads, i % w.nheads) for i in range(nseq)]
-    stack = {k: torch.cat([inp[k][b:b + 1, :, h:h + 1] for b, h in pairs], 0) for k in KEYS}
-    arrs = [to_f64(stack[k]) for k in KEYS]
-    threads = min(cores, nseq)
-    reps = 0
-    t = time.perf_counter()
+    nseq = nseq or max(1, min(w.batch * w.nheads, 2 * threads))
+    arrs, L = _oracle_sample(w, nseq, max_tokens)
+    reps, t = 0, time.perf_counter()
     while True:
         oracle.scan(*arrs, nthreads=threads)
         reps += 1
         sec = time.perf_counter() - t
-        if sec >= max_seconds:
+        if sec >= seconds:
             break
-    tok_heads = reps * nseq * w.seqlen
-    return {"value": tok_heads / w.nheads / sec, "unit": "tokens/s", "cores": threads,
-            "kind": "oracle",
-            "sample": f"{nseq} of {w.batch * w.nheads} (b,h) sequences x {w.seqlen} tokens of {w.name}, "
-                      f"scanned {reps} times ({sec:.1f} s); tokens/s counts a token as all {w.nheads} heads",
+    return {"value": reps * nseq * L / w.nheads / sec, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{nseq} of {w.batch * w.nheads} (b,h) sequences x {L} of {w.seqlen} tokens of {w.name}, "
+                      f"scanned {reps} times ({sec:.1f} s); a token counts all {w.nheads} heads",
             "seconds": round(sec, 2)}
+
+
+def oracle_decode_rate(w, threads, seconds):
+    """The oracle's decode step (the recurrence with L = 1) on a sample of 64 x threads (b, h) rows."""
+    import oracle
+    from selective_state_space_134_b300.synth import decode_pool, decode_state, to_f64
+    rows = min(w.batch * w.nheads, 64 * threads)
+    ws = w.with_(batch=rows, nheads=1)
+    st = decode_state(ws, "cpu")
+    tok = decode_pool(ws, "cpu", pool=1)[0]
+    args = [to_f64(tok[k]) for k in KEYS] + [to_f64(st["h"]), to_f64(st["B_prev"]), to_f64(st["x_prev"])]
+    reps, t = 0, time.perf_counter()
+    while True:
+        x, B, C, dt, A, lam, th, h, Bp, xp = args
+        oracle.scan(x[:, None], B[:, None], C[:, None], dt[:, None], A[:, None], lam[:, None], th[:, None],
+                    h0=h, Bprev=Bp, xprev=xp, nthreads=threads)
+        reps += 1
+        sec = time.perf_counter() - t
+        if sec >= seconds:
+            break
+    # decode tokens/s: one token per batch row, all heads
+    return {"value": reps * rows / w.nheads / sec, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{rows} of {w.batch * w.nheads} (b,h) rows, one step, {reps} times ({sec:.1f} s)",
+            "seconds": round(sec, 2)}
+
+
+def cpu_baseline_table(seconds=1.5):
+    """The oracle per workload, single-thread and on every host core (the long-context workload on
+    its first 4096 tokens of 2 x cores sequences)."""
+    from selective_state_space_134_b300.synth import WORKLOADS
+    cores = os.cpu_count() or 1
+    out = {}
+    for name in ("tiny_f32", "siso_n64", "siso_n128", "mimo_r4", "long_n128_r4"):
+        w = WORKLOADS[name]
+        cap = 4096 if name == "long_n128_r4" else None
+        one = oracle_rate(w, 1, seconds, cap, nseq=1)
+        allc = oracle_rate(w, cores, seconds, cap)
+        out[name] = {"single_thread": round(one["value"], 1), "all_cores": round(allc["value"], 1),
+                     "cores": cores, "sample_all_cores": allc["sample"]}
+    for name in ("decode_n64_r1", "decode_n64_r4", "decode_n128_r1", "decode_n128_r4"):
+        w = WORKLOADS[name]
+        one = oracle_decode_rate(w, 1, seconds / 2)
+        allc = oracle_decode_rate(w, cores, seconds / 2)
+        out[name] = {"single_thread": round(one["value"], 1), "all_cores": round(allc["value"], 1),
+                     "cores": cores, "sample_all_cores": allc["sample"]}
+    return out
+
+
+def time_backward(m3, w, steps, warmup):
+    """Device time of `steps` mamba3_scan_bwd calls on workload w (dy ~ N(0, 1), inputs resident)."""
+    from selective_state_space_134_b300.synth import prefill_inputs
+    inp = prefill_inputs(w, "cuda")
+    g = torch.Generator(device="cuda").manual_seed(5)
+    dy = torch.randn(inp["x"].shape, device="cuda", generator=g)
+    args = [inp[k] for k in KEYS]
+    d = m3.dims(w.batch, w.seqlen, w.nheads, w.P, w.N, w.R, inp["x"].dtype)
+    work = torch.empty(max(m3.scan_bwd_workspace(d), 1), dtype=torch.uint8, device="cuda")
+    grads = m3.scan_bwd(*args, dy, workspace=work)
+    for _ in range(warmup):
+        m3.scan_bwd(*args, dy, workspace=work, grads=grads)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        m3.scan_bwd(*args, dy, workspace=work, grads=grads)
+    e1.record()
+    torch.cuda.synchronize()
+    assert m3.device_status() == m3.M3_OK
+    return e0.elapsed_time(e1) / steps, work.numel()
+
+
+def backward_flops(w):
+    """fp32 flops of the backward kernel (its contractions; 2 per FMA).  Per chunk of QR rows (t, r):
+    S and Z (causal halves, QR^2 (N + P) / 2), dX's score term (QR^2 P / 2), dB~'s and dC~'s score terms
+    (QR^2 N), and five N x P x QR products (checkpoint update, B~ D~, dY H'^T, X D~^T, state gradient)."""
+    rows = 16 if w.N * w.P > 4096 else 32
+    Q = max(1, rows // w.R)
+    QR = Q * w.R
+    fma = QR * QR * (w.N + w.P) / 2 + QR * QR * w.P / 2 + QR * QR * w.N + 5 * QR * w.N * w.P
+    return 2.0 * fma / Q * w.token_heads
+
+
+def fp32_peak_tflops():
+    """fp32 CUDA-core peak: SMs x 128 lanes x 2 flops (FMA) x the maximum SM clock."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            mhz = float(json.load(f).get("sm_max_mhz", 2032.0))
+    except Exception:
+        mhz = 2032.0
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    return sms * 128 * 2 * mhz * 1e6 / 1e12
 
 
 def run_ours(args):
@@ -456,17 +549,46 @@ def run_ours(args):
             pre[name]["launches_per_step"] = r["launches"] / steps
             del r
             torch.cuda.empty_cache()
-        # grouped B / C: siso_n64 with one B and C per 8 heads
+        # variants of the headline shape (and of MIMO): grouped B / C (one B and C per 8 heads), fp16 y,
+        # BC normalisation and bias, and the chunk rule Q = N / R of the pages
         wp = WORKLOADS[HEADLINE]
-        r = time_prefill(m3, wp, 20, 1, m3.KERNEL_PREFILL_OUTPUT, groups=4)
-        pre["siso_n64_grouped_g4"] = prefill_line(m3, wp, r, 20, hbm_peak, peak_kind, groups=4)
-        pre["siso_n64_grouped_g4"]["launches_per_step"] = r["launches"] / 20
-        del r
-        torch.cuda.empty_cache()
+        variants = (("siso_n64_grouped_g4", HEADLINE, dict(groups=4)),
+                    ("siso_n64_y_f16", HEADLINE, dict(y_dtype=torch.float16)),
+                    ("siso_n64_bc", HEADLINE, dict(bc=True)),
+                    ("siso_n64_chunk_rule_q64", HEADLINE, dict(chunk=64)),
+                    ("mimo_r4_bc", "mimo_r4", dict(bc=True)),
+                    ("mimo_r4_chunk_rule_q16", "mimo_r4", dict(chunk=16)))
+        for key, name, kw in variants:
+            wp = WORKLOADS[name]
+            steps = 20 if name == HEADLINE else 5
+            r = time_prefill(m3, wp, steps, 1, m3.KERNEL_PREFILL_OUTPUT, **kw)
+            pre[key] = prefill_line(m3, wp, r, steps, hbm_peak, peak_kind, groups=kw.get("groups", 0),
+                                    y_bytes=kw.get("y_dtype", torch.float32).itemsize)
+            pre[key]["launches_per_step"] = r["launches"] / steps
+            del r
+            torch.cuda.empty_cache()
         extra["prefill"] = pre
+        # backward pass (training): siso_n64 and mimo_r4; the ALU roofline of its fp32 contractions
+        bwd = {}
+        for name, steps in ((HEADLINE, 3), ("mimo_r4", 1)):
+            wb = WORKLOADS[name]
+            ms_b, ws_b = time_backward(m3, wb, steps, 1)
+            fl = backward_flops(wb)
+            peak = fp32_peak_tflops()
+            bwd[name] = {"tokens_per_s": wb.batch * wb.seqlen / (ms_b * 1e-3), "ms_per_step": ms_b,
+                         "workspace_bytes": ws_b,
+                         "roofline": {"bound": "alu", "achieved": round(fl / (ms_b * 1e-3) / 1e12, 3),
+                                      "peak": round(peak, 1), "unit": "TFLOP/s",
+                                      "frac": round(fl / (ms_b * 1e-3) / 1e12 / peak, 4),
+                                      "flops": fl, "peak_source": "derived: SMs x 128 fp32 lanes x 2 x max clock"}}
+            torch.cuda.empty_cache()
+        extra["backward"] = {"metric": "backward tokens/s", "unit": "tokens/s", "workloads": bwd}
 
     e2e = e2e_prefill(m3, w, inp, max(2, min(args.steps, 10)), 1) if rank == 0 else None
-    cpu = cpu_oracle_rate(w, inp) if (rank == 0 and ws == 1 and not args.quick) else None
+    cpu = None
+    if rank == 0 and ws == 1 and not args.quick:
+        cpu = oracle_rate(w, os.cpu_count() or 1, 10.0)
+        cpu["per_workload"] = cpu_baseline_table()
 
     if rank == 0:
         line = {
@@ -492,32 +614,26 @@ def run_ours(args):
 
 # ------------------------------------------------------------------ reference arm (the CPU oracle)
 def run_reference(args):
+    """The reference arm: the fp64 CPU oracle on this host's cores, on the headline workload, timed
+    with the same sampling as the bench line's cpu_baseline; each step a bounded sample."""
     ws, rank, _ = dist_env()
     if rank != 0:
         return
-    import oracle
-    from selective_state_space_134_b300.synth import WORKLOADS, prefill_inputs, to_f64
+    from selective_state_space_134_b300.synth import WORKLOADS
     w = WORKLOADS[HEADLINE]
     cores = os.cpu_count() or 1
-    nseq = min(cores, w.batch * w.nheads)
-    inp = prefill_inputs(w.with_(batch=1, nheads=nseq), "cpu")
-    arrs = [to_f64(inp[k]) for k in KEYS]
-    for _ in range(args.warmup):
-        oracle.scan(*(a[:, :256] for a in arrs), nthreads=nseq)
-    t = time.perf_counter()
-    for _ in range(args.steps):
-        oracle.scan(*arrs, nthreads=nseq)
-    sec = (time.perf_counter() - t) / args.steps
-    value = nseq * w.seqlen / w.nheads / sec
-    sample = (f"per step {nseq} (b,h) sequences x {w.seqlen} tokens of {HEADLINE} (of {w.batch * w.nheads}); "
-              f"tokens/s counts a token as all {w.nheads} heads")
+    oracle_rate(w, cores, 0.5)                       # warm-up (input generation, library load)
+    per_step = max(1.0, min(10.0, 120.0 / max(args.steps, 1)))
+    r = oracle_rate(w, cores, per_step * args.steps)
+    value = r["value"]
+    sec = args.steps and r["seconds"] / args.steps
     print(json.dumps({
         "impl": "reference", "metric": "prefill tokens/s", "value": value, "unit": "tokens/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": f"{HEADLINE}: SISO bf16 prefill, batch {w.batch}, heads {w.nheads}, "
                                f"L={w.seqlen}, P={w.P}, N={w.N}, R={w.R}"},
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": nseq, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": r["sample"]},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }))
 
@@ -560,6 +676,28 @@ def run_decode_only(args):
                       "workloads": decode_results(m3, hbm_peak)}))
 
 
+def run_workload(args):
+    """One prefill (or backward) workload alone, optionally resized: a JSON line with its tokens/s
+    and roofline (used for profiling runs)."""
+    torch.cuda.set_device(0)
+    import selective_state_space_134_b300 as m3
+    from selective_state_space_134_b300.synth import WORKLOADS
+    m3.lib()
+    hbm_peak, _, peak_kind = peaks()
+    over = {k: v for k, v in (("batch", args.batch), ("nheads", args.heads), ("seqlen", args.seqlen)) if v}
+    w = WORKLOADS[args.workload].with_(**over)
+    if args.backward:
+        ms_b, _ = time_backward(m3, w, args.steps, args.warmup)
+        print(json.dumps({"metric": "backward tokens/s", "workload": w.name, "overrides": over,
+                          "tokens_per_s": w.batch * w.seqlen / (ms_b * 1e-3), "ms_per_step": ms_b}))
+        return
+    r = time_prefill(m3, w, args.steps, args.warmup, m3.KERNEL_PREFILL_OUTPUT)
+    line = prefill_line(m3, w, r, args.steps, hbm_peak, peak_kind)
+    line.update({"metric": "prefill tokens/s", "workload": w.name, "overrides": over,
+                 "launches_per_step": r["launches"] / args.steps})
+    print(json.dumps(line))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -569,10 +707,17 @@ def main():
     ap.add_argument("--quick", action="store_true", help="headline only (no decode / other workloads / oracle)")
     ap.add_argument("--decode-only", action="store_true",
                     help="one JSON line with the four decode workloads only (profiling runs)")
+    ap.add_argument("--workload", help="time this prefill workload alone (profiling runs)")
+    ap.add_argument("--batch", type=int, default=0, help="with --workload: batch override")
+    ap.add_argument("--heads", type=int, default=0, help="with --workload: head-count override")
+    ap.add_argument("--seqlen", type=int, default=0, help="with --workload: sequence-length override")
+    ap.add_argument("--backward", action="store_true", help="with --workload: time the backward pass")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.decode_only:
+    if args.workload:
+        run_workload(args)
+    elif args.decode_only:
         run_decode_only(args)
     elif args.impl == "reference":
         run_reference(args)

@@ -366,6 +366,16 @@ int mamba3_decode_last_variant(void);
  */
 m3_status mamba3_device_status(void *stream);
 
+/*
+ * Self-test of the device-side wait limit (failure detection without a fault):
+ * launches one kernel that waits, with the library's bounded mbarrier wait, on a
+ * barrier that nothing ever completes; after `limit_ns` nanoseconds (0 <
+ * limit_ns <= 1e8, else M3_ERR_INVALID_ARG) it gives up and sets the timeout bit
+ * of the device status word, so that the next mamba3_device_status() returns
+ * M3_ERR_TIMEOUT.  The context stays usable.  Not from the Mamba-3 pages.
+ */
+m3_status mamba3_selftest_wait_timeout(uint64_t limit_ns, void *stream);
+
 /* Human-readable name of a status code (static string). */
 const char *mamba3_status_string(int status);
 

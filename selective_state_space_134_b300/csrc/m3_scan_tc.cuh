@@ -280,9 +280,13 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
     if (warp == 0) {
         // ================================================================ producer
         if (lane == 0) {
+            int issued = 0;
             for (int it = 0; it < nchunks; ++it) {
                 const int p = it & 1;
                 if (it >= 2) wait(kRawEmpty + p, ((it - 2) >> 1) & 1, true);
+                // after a timeout nothing more is issued: a refill could land on a slot whose
+                // previous copy is still in flight
+                if (*abort_flag) break;
                 unsigned char *slot = sm + p * S::SLOT;
                 constexpr uint32_t bytes = Cf::BT * (OUT ? 2 : 1) + Cf::XT + Cf::TT;
                 mbar_expect_tx(bars + kRawFull + p, bytes);
@@ -296,12 +300,14 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                 }
                 tma_load_4d(slot + S::sX, &maps.X, 0, 0, h, row0, bars + kRawFull + p);
                 tma_load_3d(slot + S::sT, &maps.T, 0, h, row0, bars + kRawFull + p);
+                ++issued;
             }
             if (*abort_flag) {
-                // let the copies already issued land before the CTA's shared memory goes away
-                for (int it = nchunks - 2 < 0 ? 0 : nchunks - 2; it < nchunks; ++it) {
+                // let the copies issued land before the CTA's shared memory goes away: a slot is
+                // refilled only after its previous chunk was consumed, so at most the last two
+                // issued copies are outstanding, each the only one on its barrier phase
+                for (int it = issued - 2 < 0 ? 0 : issued - 2; it < issued; ++it)
                     mbar_wait(bars + kRawFull + (it & 1), (it >> 1) & 1, kWaitNs);
-                }
             }
         }
         __syncwarp();

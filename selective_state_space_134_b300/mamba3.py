@@ -122,6 +122,8 @@ def lib() -> ctypes.CDLL:
         L.mamba3_scan_bwd.argtypes = [dp, ctypes.POINTER(m3_token_inputs), sp, ctypes.POINTER(m3_grads_in),
                                       ctypes.POINTER(m3_grads_out), vp, ctypes.c_size_t, vp]
         L.mamba3_scan_bwd.restype = ctypes.c_int
+        L.mamba3_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
+        L.mamba3_selftest_wait_timeout.restype = ctypes.c_int
         L.mamba3_decode_last_variant.argtypes = []
         L.mamba3_decode_last_variant.restype = ctypes.c_int
         L.mamba3_version.argtypes = []

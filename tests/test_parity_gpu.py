@@ -516,3 +516,21 @@ def test_chunk_rule_tile_with_bc_matches_oracle():
     bref = {k: (to_f64(v) if isinstance(v, torch.Tensor) else v) for k, v in p.items()}
     yr, _, _, _ = oracle.scan_bc(*(to_f64(inp[k]) for k in KEYS), bref, nthreads=2)
     assert_err(to_f64(y), yr, TOL[w.dtype], "y")
+
+
+# ---------------------------------------------------------------- failure detection
+
+def test_bounded_wait_reports_timeout_and_the_context_stays_usable():
+    # a kernel waits on a barrier nothing completes; the bounded wait gives up after 1 ms and the
+    # timeout reaches the host through the device status word, once; then a prefill still runs right
+    from selective_state_space_134_b300 import mamba3 as api
+    assert m3.device_status() == m3.M3_OK
+    assert m3.lib().mamba3_selftest_wait_timeout(1_000_000, None) == api.M3_OK
+    assert m3.device_status() == api.M3_ERR_TIMEOUT
+    assert m3.device_status() == m3.M3_OK            # read and cleared
+    assert m3.lib().mamba3_selftest_wait_timeout(0, None) == api.M3_ERR_INVALID_ARG
+    w = WORKLOADS["siso_n64"].with_(batch=1, nheads=2, seqlen=150)
+    inp = prefill_inputs(w, "cuda")
+    y, so = gpu_scan(inp)
+    yr, hr, _, _ = oracle_full(inp)
+    assert_err(to_f64(y), yr, TOL[w.dtype], "y")
