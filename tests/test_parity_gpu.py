@@ -534,3 +534,40 @@ def test_bounded_wait_reports_timeout_and_the_context_stays_usable():
     y, so = gpu_scan(inp)
     yr, hr, _, _ = oracle_full(inp)
     assert_err(to_f64(y), yr, TOL[w.dtype], "y")
+
+
+# ---------------------------------------------------------------- more sequences than SMs (several waves of CTAs)
+
+@pytest.mark.parametrize("N,R,b,H,L,with_state,kw", [
+    (64, 4, 3, 60, 300, False, {}), (64, 4, 2, 90, 257, True, {}), (128, 1, 1, 200, 333, True, {}),
+    (64, 1, 4, 50, 650, False, dict(y_dtype=torch.float16)), (64, 2, 2, 100, 200, True, dict(chunk=32)),
+    (128, 4, 1, 170, 97, False, {})])
+def test_more_sequences_than_sms_match_oracle(N, R, b, H, L, with_state, kw):
+    # b x H > SMs: several waves of one-sequence CTAs, with a carry, fp16 y and the chunk rule
+    w = WORKLOADS["mimo_r4"].with_(batch=b, nheads=H, seqlen=L, N=N, R=R)
+    inp = prefill_inputs(w, "cuda")
+    st = random_state(b, H, w.P, N, R, inp["x"].dtype, seed=11) if with_state else None
+    so = m3.State.zeros(b, H, w.P, N, R, inp["x"].dtype)
+    y = m3.scan_fwd(*(inp[k] for k in KEYS), state_in=st, state_out=so, **kw)
+    assert m3.device_status() == m3.M3_OK
+    yr, hr, Br, xr = oracle_full(inp, st)
+    assert_err(to_f64(y), yr, TOL[w.dtype], "y")
+    assert_err(to_f64(so.h), hr, TOL[w.dtype], "h")
+    np.testing.assert_array_equal(to_f64(so.B_prev), Br)
+    np.testing.assert_array_equal(to_f64(so.x_prev), xr)
+    # twice in a row: the same result
+    y2 = m3.scan_fwd(*(inp[k] for k in KEYS), state_in=st, **kw)
+    assert torch.equal(y, y2)
+
+
+def test_more_sequences_than_sms_with_bc_match_oracle():
+    from selective_state_space_134_b300.synth import bc_params
+    w = WORKLOADS["mimo_r4"].with_(batch=2, nheads=96, seqlen=180)
+    inp = prefill_inputs(w, "cuda")
+    p = bc_params(w, "cuda", seed=5)
+    bc = m3.BcNorm(p["B_weight"], p["B_bias"], p["C_weight"], p["C_bias"], p["eps"])
+    y = m3.scan_fwd(*(inp[k] for k in KEYS), bc=bc)
+    assert m3.device_status() == m3.M3_OK
+    bref = {k: (to_f64(v) if isinstance(v, torch.Tensor) else v) for k, v in p.items()}
+    yr, _, _, _ = oracle.scan_bc(*(to_f64(inp[k]) for k in KEYS), bref, nthreads=8)
+    assert_err(to_f64(y), yr, TOL[w.dtype], "y")
