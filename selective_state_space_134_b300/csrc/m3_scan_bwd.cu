@@ -27,10 +27,11 @@
 namespace m3 {
 namespace {
 
-constexpr int kBwdThreads = 256;
+constexpr int kBwdThreads = 512;
 constexpr int kBwdWarps = kBwdThreads / 32;
 
-// Shared-memory carve-up (floats); row-major tiles padded by one column against bank conflicts.
+// Shared-memory carve-up (floats); row-major tiles padded by one column against bank conflicts
+// (the N x P tiles too: several contractions walk their rows n across the threads of a warp).
 struct BwdSmem {
     int Q, R, N, P, K, QR, NS, PS, QS;
     size_t oD, oDt, oH, oH2, oB, oC, oX, oY, oS, oZ, oT1, oT2, odM;
@@ -39,10 +40,10 @@ struct BwdSmem {
     __host__ __device__ BwdSmem(int Q_, int R_, int N_, int P_) {
         Q = Q_; R = R_; N = N_; P = P_; K = N / 2; QR = Q * R; NS = N + 1; PS = P + 1; QS = QR + 1;
         size_t o = 0;
-        oD = o;  o += (size_t)N * P;        // D (true frame); in pass 1 the running state
-        oDt = o; o += (size_t)N * P;        // D~ = R(-phi_e) D
-        oH = o;  o += (size_t)N * P;        // H'_c
-        oH2 = o; o += (size_t)N * P;        // H'_{c+1}
+        oD = o;  o += (size_t)N * PS;       // D (true frame); in pass 1 the running state
+        oDt = o; o += (size_t)N * PS;       // D~ = R(-phi_e) D
+        oH = o;  o += (size_t)N * PS;       // H'_c
+        oH2 = o; o += (size_t)N * PS;       // H'_{c+1}
         oB = o;  o += (size_t)QR * NS;      // B~
         oC = o;  o += (size_t)QR * NS;      // C~
         oX = o;  o += (size_t)QR * PS;      // x
@@ -69,7 +70,7 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kBwdThreads)
+__global__ void __launch_bounds__(kBwdThreads, 1)
 scan_bwd_kernel(BwdArgs a, int Q) {
     extern __shared__ float sm[];
     const BwdSmem Lo(Q, a.R, a.N, a.P);
@@ -128,15 +129,14 @@ scan_bwd_kernel(BwdArgs a, int Q) {
                 carry = __shfl_sync(0xffffffffu, v, 31);
             }
         }
-        for (int k = tid; k < K; k += kBwdThreads) {   // chunk-local angle per pair
+        for (int i = tid; i < Q * K; i += kBwdThreads) {   // chunk-local angle of token t, pair k
+            const int t = i / K, k = i % K;
             float phi = 0.f;
-            for (int t = 0; t < Q; ++t) {
-                phi = fmaf(vdt[t], thv[t * K + k], phi);
-                float s, c;
-                sincosf(phi, &s, &c);
-                cs[t * K + k] = c;
-                sn[t * K + k] = s;
-            }
+            for (int u = 0; u <= t; ++u) phi = fmaf(vdt[u], thv[u * K + k], phi);
+            float s, c;
+            sincosf(phi, &s, &c);
+            cs[i] = c;
+            sn[i] = s;
         }
         __syncthreads();
         const int e = Qc - 1;
@@ -186,7 +186,7 @@ scan_bwd_kernel(BwdArgs a, int Q) {
                     u += to_f(bq[((size_t)bh * R + r) * N + n]) * to_f(xq[((size_t)bh * R + r) * P + p]);
                 v += left0 * u;
             }
-            Dm[i] = v;
+            Dm[n * PS + p] = v;
             ckpt[i] = v;
         }
         __syncthreads();
@@ -197,7 +197,7 @@ scan_bwd_kernel(BwdArgs a, int Q) {
             float *dst = ckpt + (size_t)(c + 1) * N * P;
             for (int i = tid; i < K * P; i += kBwdThreads) {
                 const int k = i / P, p = i % P;
-                float v0 = de * Dm[(2 * k) * P + p], v1 = de * Dm[(2 * k + 1) * P + p];
+                float v0 = de * Dm[(2 * k) * PS + p], v1 = de * Dm[(2 * k + 1) * PS + p];
                 for (int row = 0; row < Qc * R; ++row) {
                     const float wx = sv[row / R] * Xs[row * PS + p];
                     v0 = fmaf(Bt[row * NS + 2 * k], wx, v0);
@@ -205,8 +205,8 @@ scan_bwd_kernel(BwdArgs a, int Q) {
                 }
                 const float cc = cs[e * K + k], ss = sn[e * K + k];
                 const float n0 = cc * v0 - ss * v1, n1 = ss * v0 + cc * v1;
-                Dm[(2 * k) * P + p] = n0;
-                Dm[(2 * k + 1) * P + p] = n1;
+                Dm[(2 * k) * PS + p] = n0;
+                Dm[(2 * k + 1) * PS + p] = n1;
                 dst[(2 * k) * P + p] = n0;
                 dst[(2 * k + 1) * P + p] = n1;
             }
@@ -215,14 +215,15 @@ scan_bwd_kernel(BwdArgs a, int Q) {
     }
 
     // ================================================================ pass 2: gradients
-    for (int i = tid; i < N * P; i += kBwdThreads) Dm[i] = a.dh_out ? a.dh_out[(size_t)bh * N * P + i] : 0.f;
+    for (int i = tid; i < N * P; i += kBwdThreads)
+        Dm[(i / P) * PS + i % P] = a.dh_out ? a.dh_out[(size_t)bh * N * P + i] : 0.f;
     __syncthreads();
     for (int c = nc - 1; c >= 0; --c) {
         const int s0 = c * Q, Qc = min(Q, L - s0), e = Qc - 1, QRc = Qc * R;
         load_chunk(s0, Qc, true);
         for (int i = tid; i < N * P; i += kBwdThreads) {
-            Hc[i] = ckpt[(size_t)c * N * P + i];
-            Hn[i] = ckpt[(size_t)(c + 1) * N * P + i];
+            Hc[(i / P) * PS + i % P] = ckpt[(size_t)c * N * P + i];
+            Hn[(i / P) * PS + i % P] = ckpt[(size_t)(c + 1) * N * P + i];
         }
         for (int i = tid; i < Q * R * P; i += kBwdThreads) {
             const int row = i / P, p = i % P, t = row / R, r = row % R;
@@ -238,16 +239,16 @@ scan_bwd_kernel(BwdArgs a, int Q) {
         for (int i = tid; i < K * P; i += kBwdThreads) {
             const int k = i / P, p = i % P;
             const float cc = cs[e * K + k], ss = sn[e * K + k];
-            const float d0 = Dm[(2 * k) * P + p], d1 = Dm[(2 * k + 1) * P + p];
-            Dt[(2 * k) * P + p] = cc * d0 + ss * d1;
-            Dt[(2 * k + 1) * P + p] = -ss * d0 + cc * d1;
+            const float d0 = Dm[(2 * k) * PS + p], d1 = Dm[(2 * k + 1) * PS + p];
+            Dt[(2 * k) * PS + p] = cc * d0 + ss * d1;
+            Dt[(2 * k + 1) * PS + p] = -ss * d0 + cc * d1;
         }
         for (int i = tid; i < Q * K; i += kBwdThreads) dph[i] = 0.f;
         __syncthreads();
         for (int k = warp; k < K; k += kBwdWarps) {
             float v = 0.f;
             for (int p = lane; p < P; p += 32)
-                v += Dm[(2 * k + 1) * P + p] * Hn[(2 * k) * P + p] - Dm[(2 * k) * P + p] * Hn[(2 * k + 1) * P + p];
+                v += Dm[(2 * k + 1) * PS + p] * Hn[(2 * k) * PS + p] - Dm[(2 * k) * PS + p] * Hn[(2 * k + 1) * PS + p];
             v = warp_sum(v);
             if (lane == 0) dph[e * K + k] += v;
         }
@@ -266,13 +267,13 @@ scan_bwd_kernel(BwdArgs a, int Q) {
         for (int i = tid; i < QRc * P; i += kBwdThreads) {
             const int row = i / P, p = i % P;
             float v = 0.f;
-            for (int n = 0; n < N; ++n) v = fmaf(Bt[row * NS + n], Dt[n * P + p], v);
+            for (int n = 0; n < N; ++n) v = fmaf(Bt[row * NS + n], Dt[n * PS + p], v);
             T1[row * PS + p] = v;
         }
         for (int i = tid; i < QRc * N; i += kBwdThreads) {
             const int row = i / N, n = i % N;
             float v = 0.f;
-            for (int p = 0; p < P; ++p) v = fmaf(Ys[row * PS + p], Hc[n * P + p], v);
+            for (int p = 0; p < P; ++p) v = fmaf(Ys[row * PS + p], Hc[n * PS + p], v);
             T2[row * NS + n] = v;
         }
         __syncthreads();
@@ -326,22 +327,26 @@ scan_bwd_kernel(BwdArgs a, int Q) {
         // <D~, H'_c> (the transport e^{cA_e} H'_c into the chunk end), per-warp partial sums
         {
             float v = 0.f;
-            for (int i = tid; i < N * P; i += kBwdThreads) v += Dt[i] * Hc[i];
+            for (int i = tid; i < N * P; i += kBwdThreads) {
+                const int q = (i / P) * PS + i % P;
+                v += Dt[q] * Hc[q];
+            }
             v = warp_sum(v);
             if (lane == 0) red[warp] = v;
         }
         __syncthreads();
-        if (tid == 0) {
-            // s_j = e^{cA_e - cA_j} w_j, and the transport
-            float tot = 0.f, dh = 0.f;
-            for (int q = 0; q < kBwdWarps; ++q) dh += red[q];
-            for (int j = 0; j < Qc; ++j) {
-                const float v = sv[j] * dsv[j];
-                tot += v;
-                dcA[j] -= v;
-                dwv[j] += expf(cA[e] - cA[j]) * dsv[j];
+        if (warp == 0) {
+            // s_j = e^{cA_e - cA_j} w_j, and the transport (one lane per token; Qc <= 32)
+            float dh = lane < kBwdWarps ? red[lane] : 0.f, v = 0.f;
+            if (lane < Qc) {
+                v = sv[lane] * dsv[lane];
+                dcA[lane] -= v;
+                dwv[lane] += expf(cA[e] - cA[lane]) * dsv[lane];
             }
-            dcA[e] += tot + expf(cA[e]) * dh;
+            dh = warp_sum(dh);
+            v = warp_sum(v);
+            __syncwarp();
+            if (lane == 0) dcA[e] += v + expf(cA[e]) * dh;
         }
         __syncthreads();
         // dX = (M o S)^T dY + diag(s) B~ D~  (the carry out adds to the sequence's last token)
@@ -365,8 +370,8 @@ scan_bwd_kernel(BwdArgs a, int Q) {
                 b1 = fmaf(m, Ct[rt * NS + 2 * k + 1], b1);
             }
             for (int p = 0; p < P; ++p) {
-                xd0 = fmaf(Xs[rj * PS + p], Dt[(2 * k) * P + p], xd0);
-                xd1 = fmaf(Xs[rj * PS + p], Dt[(2 * k + 1) * P + p], xd1);
+                xd0 = fmaf(Xs[rj * PS + p], Dt[(2 * k) * PS + p], xd0);
+                xd1 = fmaf(Xs[rj * PS + p], Dt[(2 * k + 1) * PS + p], xd1);
             }
             b0 = fmaf(sv[j], xd0, b0);
             b1 = fmaf(sv[j], xd1, b1);
@@ -424,33 +429,37 @@ scan_bwd_kernel(BwdArgs a, int Q) {
         __syncthreads();
         // parameter gradients of the chunk's tokens; the left-endpoint part of w_{u-1} belongs to
         // token u: for the chunk's first token it is added when the chunk before is processed
-        for (int u = tid; u < Qc; u += kBwdThreads) {
+        for (int i = tid; i < Qc * K; i += kBwdThreads) {
+            const int u = i / K, k = i % K;
+            a.dtheta[tok(s0 + u) * K + k] = vdt[u] * dph[i];
+        }
+        for (int u = warp; u < Qc; u += kBwdWarps) {   // one warp per token: sum_k theta_k d(dt theta)_k
             const size_t ti = tok(s0 + u);
-            const float d = vdt[u], av = vA[u], l = vl[u];
             float thsum = 0.f;
-            for (int k = 0; k < K; ++k) {
-                a.dtheta[ti * K + k] = d * dph[u * K + k];
-                thsum = fmaf(thv[u * K + k], dph[u * K + k], thsum);
+            for (int k = lane; k < K; k += 32) thsum = fmaf(thv[u * K + k], dph[u * K + k], thsum);
+            thsum = warp_sum(thsum);
+            if (lane == 0) {
+                const float d = vdt[u], av = vA[u], l = vl[u];
+                const float dwp = u > 0 ? dwv[u - 1] : 0.f;
+                const float ddt = av * dcA[u] + thsum + l * (dwv[u] + dgv[u]) + (1.f - l) * dwp;
+                const float dl = d * (dwv[u] + dgv[u]) - d * dwp;
+                if (u == Qc - 1 && s0 + Qc < L) {   // this token's w also feeds the next chunk's first token
+                    const size_t tn = tok(s0 + Qc);
+                    a.ddt[tn] += (1.f - vln[u]) * dwv[u];
+                    a.dlam[tn] -= vdtn[u] * dwv[u];
+                }
+                a.dA[ti] = d * dcA[u];
+                a.ddt[ti] = ddt;
+                a.dlam[ti] = dl;
             }
-            const float dwp = u > 0 ? dwv[u - 1] : 0.f;
-            float ddt = av * dcA[u] + thsum + l * (dwv[u] + dgv[u]) + (1.f - l) * dwp;
-            float dl = d * (dwv[u] + dgv[u]) - d * dwp;
-            if (u == Qc - 1 && s0 + Qc < L) {   // this token's w also feeds the next chunk's first token
-                const size_t tn = tok(s0 + Qc);
-                a.ddt[tn] += (1.f - vln[u]) * dwv[u];
-                a.dlam[tn] -= vdtn[u] * dwv[u];
-            }
-            a.dA[ti] = d * dcA[u];
-            a.ddt[ti] = ddt;
-            a.dlam[ti] = dl;
         }
         // D <- e^{cA_e} D~ + C~^T diag(e^{cA}) dY
         const float de = expf(cA[e]);
         for (int i = tid; i < N * P; i += kBwdThreads) {
             const int n = i / P, p = i % P;
-            float v = de * Dt[i];
+            float v = de * Dt[n * PS + p];
             for (int row = 0; row < QRc; ++row) v = fmaf(Ct[row * NS + n] * ev[row / R], Ys[row * PS + p], v);
-            Dm[i] = v;
+            Dm[n * PS + p] = v;
         }
         __syncthreads();
     }
@@ -458,7 +467,7 @@ scan_bwd_kernel(BwdArgs a, int Q) {
     // ================================================================ initial state and carry
     // H'_0 = h0 + left_0 B_{-1} x_{-1}^T: dh0 = D; d left_0 = <D, B_{-1} x_{-1}^T>
     if (a.dh0)
-        for (int i = tid; i < N * P; i += kBwdThreads) a.dh0[(size_t)bh * N * P + i] = Dm[i];
+        for (int i = tid; i < N * P; i += kBwdThreads) a.dh0[(size_t)bh * N * P + i] = Dm[(i / P) * PS + i % P];
     const T *bq = static_cast<const T *>(a.Bprev), *xq = static_cast<const T *>(a.xprev);
     if (bq && xq) {
         const float d0 = to_f(dtg[tok(0)]), l0 = to_f(lg[tok(0)]), left0 = (1.f - l0) * d0;
@@ -468,7 +477,7 @@ scan_bwd_kernel(BwdArgs a, int Q) {
             float u = 0.f;
             for (int r = 0; r < R; ++r)
                 u += to_f(bq[((size_t)bh * R + r) * N + n]) * to_f(xq[((size_t)bh * R + r) * P + p]);
-            dl = fmaf(Dm[i], u, dl);
+            dl = fmaf(Dm[n * PS + p], u, dl);
         }
         dl = warp_sum(dl);
         if (lane == 0) red[warp] = dl;
@@ -483,14 +492,14 @@ scan_bwd_kernel(BwdArgs a, int Q) {
             for (int i = tid; i < R * N; i += kBwdThreads) {
                 const int r = i / N, n = i % N;
                 float v = 0.f;
-                for (int p = 0; p < P; ++p) v = fmaf(Dm[n * P + p], to_f(xq[((size_t)bh * R + r) * P + p]), v);
+                for (int p = 0; p < P; ++p) v = fmaf(Dm[n * PS + p], to_f(xq[((size_t)bh * R + r) * P + p]), v);
                 a.dBprev[(size_t)bh * R * N + i] = left0 * v;
             }
         if (a.dxprev)
             for (int i = tid; i < R * P; i += kBwdThreads) {
                 const int r = i / P, p = i % P;
                 float v = 0.f;
-                for (int n = 0; n < N; ++n) v = fmaf(Dm[n * P + p], to_f(bq[((size_t)bh * R + r) * N + n]), v);
+                for (int n = 0; n < N; ++n) v = fmaf(Dm[n * PS + p], to_f(bq[((size_t)bh * R + r) * N + n]), v);
                 a.dxprev[(size_t)bh * R * P + i] = left0 * v;
             }
     } else {
