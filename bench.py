@@ -677,8 +677,8 @@ def run_decode_only(args):
 
 
 def run_workload(args):
-    """One prefill (or backward) workload alone, optionally resized: a JSON line with its tokens/s
-    and roofline (used for profiling runs)."""
+    """One prefill, backward or decode workload alone, optionally resized: a JSON line with its
+    tokens/s and roofline (used for profiling runs)."""
     torch.cuda.set_device(0)
     import selective_state_space_134_b300 as m3
     from selective_state_space_134_b300.synth import WORKLOADS
@@ -686,6 +686,17 @@ def run_workload(args):
     hbm_peak, _, peak_kind = peaks()
     over = {k: v for k, v in (("batch", args.batch), ("nheads", args.heads), ("seqlen", args.seqlen)) if v}
     w = WORKLOADS[args.workload].with_(**over)
+    if w.name.startswith("decode"):   # --steps decode calls (one token each), on a state pool with --pooled
+        timer = time_decode_pooled if args.pooled else time_decode
+        ms_call, k_ms = timer(m3, w, args.steps, args.warmup)
+        gbs = decode_bytes(w) / (k_ms * 1e-3) / 1e9
+        print(json.dumps({"metric": "decode tokens/s", "workload": w.name, "overrides": over,
+                          "pooled": bool(args.pooled), "tokens_per_s": w.batch / (ms_call * 1e-3),
+                          "us_per_call": round(ms_call * 1e3, 2), "calls": args.steps,
+                          "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak,
+                                       "unit": "GB/s", "frac": round(gbs / hbm_peak, 4),
+                                       "algorithmic_bytes": decode_bytes(w), "kernel_ms": k_ms}}))
+        return
     if args.backward:
         ms_b, _ = time_backward(m3, w, args.steps, args.warmup)
         print(json.dumps({"metric": "backward tokens/s", "workload": w.name, "overrides": over,
@@ -707,11 +718,12 @@ def main():
     ap.add_argument("--quick", action="store_true", help="headline only (no decode / other workloads / oracle)")
     ap.add_argument("--decode-only", action="store_true",
                     help="one JSON line with the four decode workloads only (profiling runs)")
-    ap.add_argument("--workload", help="time this prefill workload alone (profiling runs)")
+    ap.add_argument("--workload", help="time this prefill or decode workload alone (profiling runs)")
     ap.add_argument("--batch", type=int, default=0, help="with --workload: batch override")
     ap.add_argument("--heads", type=int, default=0, help="with --workload: head-count override")
     ap.add_argument("--seqlen", type=int, default=0, help="with --workload: sequence-length override")
     ap.add_argument("--backward", action="store_true", help="with --workload: time the backward pass")
+    ap.add_argument("--pooled", action="store_true", help="with a decode --workload: run it on a state pool")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

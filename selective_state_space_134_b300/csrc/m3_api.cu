@@ -443,10 +443,11 @@ m3_status mamba3_scan_bwd_workspace(const m3_dims *dims, size_t *bytes) {
     m3_status st = check_dims(dims, true);
     if (st != M3_OK) return st;
     const m3_dims &d = *dims;
+    const int esz = (int)elem_size(d.dtype);
     if (groups_of(d) != d.nheads || (size_t)d.dstate * d.headdim > 8192 ||
-        bwd_smem_bytes(d.dstate, d.headdim, d.rank) > 227u * 1024u)
+        bwd_smem_bytes(d.dstate, d.headdim, d.rank, esz) > 227u * 1024u)
         return M3_ERR_UNSUPPORTED;
-    *bytes = bwd_workspace_bytes(d.batch, d.nheads, d.seqlen, d.dstate, d.headdim, d.rank);
+    *bytes = bwd_workspace_bytes(d.batch, d.nheads, d.seqlen, d.dstate, d.headdim, d.rank, esz);
     return M3_OK;
 }
 

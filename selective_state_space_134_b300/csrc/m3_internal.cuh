@@ -116,9 +116,10 @@ struct BwdArgs {
     float *dx, *dB, *dC, *ddt, *dA, *dlam, *dtheta, *dh0, *dBprev, *dxprev;
     float *ws;                  // [b*H][L/Q + 1][N][P] state checkpoints
 };
-int bwd_chunk(int N, int P, int R);                                    // tokens per chunk
-size_t bwd_smem_bytes(int N, int P, int R);
-size_t bwd_workspace_bytes(int batch, int H, int L, int N, int P, int R);
+// esz: bytes per element of the token inputs
+int bwd_chunk(int N, int P, int R, int esz);                           // tokens per chunk
+size_t bwd_smem_bytes(int N, int P, int R, int esz);
+size_t bwd_workspace_bytes(int batch, int H, int L, int N, int P, int R, int esz);
 cudaError_t scan_bwd(const BwdArgs &a, cudaStream_t s);
 
 // Workspace layout sizes (bytes) for a plan.

@@ -22,6 +22,15 @@
 // w_j carries the next token's left-endpoint weight (1 - lambda_{j+1}) dt_{j+1}; the gradient of
 // that term reaches token j + 1's lambda and dt, which for the chunk's last token lies in the chunk
 // processed just before (a read-modify-write of its two gradients).
+//
+// Layout.  The contractions run as register tiles: a thread forms a 1 x 4 or 2 x 4 block of the
+// output from one broadcast scalar of the left operand and one float4 of the right one per step, so
+// every right operand is stored with the output's column index contiguous (B~ and its transpose, x
+// and its transpose, D~ and its transpose; the checkpoints are kept transposed, [P][N]).  Tiles are
+// zero-padded to whole float4 columns, and their rows padded by 4 floats against bank conflicts.
+// The raw rows of the next chunk (B, C, x, theta, dy, as stored) are copied into a staging area by
+// asynchronous 16-byte copies while the current chunk is processed, and its per-token scalars are
+// fetched into registers; the state checkpoint of a chunk is copied in while its inputs are turned.
 #include "m3_internal.cuh"
 
 namespace m3 {
@@ -30,34 +39,51 @@ namespace {
 constexpr int kBwdThreads = 512;
 constexpr int kBwdWarps = kBwdThreads / 32;
 
-// Shared-memory carve-up (floats); row-major tiles padded by one column against bank conflicts
-// (the N x P tiles too: several contractions walk their rows n across the threads of a warp).
+__host__ __device__ constexpr int rup4(int v) { return (v + 3) & ~3; }
+
+// Shared-memory carve-up (floats).  Tiles first (each a multiple of 4 floats, so every one starts on
+// a 16-byte boundary), then the per-token vectors.
 struct BwdSmem {
-    int Q, R, N, P, K, QR, NS, PS, QS;
-    size_t oD, oDt, oH, oH2, oB, oC, oX, oY, oS, oZ, oT1, oT2, odM;
+    int Q, R, N, P, K, QR, NP, PP, QRP, N4, P4, QR4, QS, QP1;
+    size_t rowB, rowX, rowT, rowY;   // bytes per token of the raw B (and C), x, theta, dy rows
+    size_t oD, oDtT, oH, oB, oC, oBT, oX, oXT, oY, oYe, oS, oZ, oT1, oT2, odM;
+    size_t oStB, oStC, oStX, oStT, oStY;   // staging (byte offsets from the start of the area)
     size_t odt, oA, olam, olamn, odtn, ocA, ow, og, os, oe, odcA, odw, odg, ods;
-    size_t ocs, osn, odph, oth, ored, total;
-    __host__ __device__ BwdSmem(int Q_, int R_, int N_, int P_) {
-        Q = Q_; R = R_; N = N_; P = P_; K = N / 2; QR = Q * R; NS = N + 1; PS = P + 1; QS = QR + 1;
+    size_t oStg, ocs, osn, odph, oth, ored, total;
+    __host__ __device__ BwdSmem(int Q_, int R_, int N_, int P_, int esz) {
+        Q = Q_; R = R_; N = N_; P = P_; K = N / 2; QR = Q * R;
+        NP = rup4(N); PP = rup4(P); QRP = rup4(QR);
+        N4 = NP + 4; P4 = PP + 4; QR4 = QRP + 4; QS = QRP + 4; QP1 = Q + 1;
+        rowB = (size_t)R * N * esz; rowX = (size_t)R * P * esz; rowT = (size_t)K * esz; rowY = (size_t)R * P * 4;
         size_t o = 0;
-        oD = o;  o += (size_t)N * PS;       // D (true frame); in pass 1 the running state
-        oDt = o; o += (size_t)N * PS;       // D~ = R(-phi_e) D
-        oH = o;  o += (size_t)N * PS;       // H'_c
-        oH2 = o; o += (size_t)N * PS;       // H'_{c+1}
-        oB = o;  o += (size_t)QR * NS;      // B~
-        oC = o;  o += (size_t)QR * NS;      // C~
-        oX = o;  o += (size_t)QR * PS;      // x
-        oY = o;  o += (size_t)QR * PS;      // dy
-        oS = o;  o += (size_t)QR * QS;      // S, then M o S
-        oZ = o;  o += (size_t)QR * QS;      // Z, then M o Z
-        oT1 = o; o += (size_t)QR * PS;      // B~ D~
-        oT2 = o; o += (size_t)QR * NS;      // dY H'^T
-        odM = o; o += (size_t)Q * Q;        // dM per token pair
+        oD = o;   o += (size_t)N * P4;      // D (true frame); during a chunk D~ = R(-phi_e) D   [N][P4]
+        oDtT = o; o += (size_t)PP * N4;     // D~^T                    [PP][N4]
+        oH = o;   o += (size_t)PP * N4;     // H'_c^T; in pass 1 the running state H'^T
+        oB = o;   o += (size_t)QR * N4;     // B~                      [QR][N4]
+        oC = o;   o += (size_t)QR * N4;     // C~
+        oBT = o;  o += (size_t)NP * QR4;    // B~^T                    [NP][QR4]
+        oX = o;   o += (size_t)QR * P4;     // x; in pass 1 X^ = s x   [QR][P4]
+        oXT = o;  o += (size_t)PP * QR4;    // x^T                     [PP][QR4]
+        oY = o;   o += (size_t)QR * P4;     // dy
+        oYe = o;  o += (size_t)QR * P4;     // e^{cA_t} dy
+        oS = o;   o += (size_t)QRP * QS;    // S, then M o S           [QRP][QS]
+        oZ = o;   o += (size_t)QRP * QS;    // Z, then M o Z
+        oT1 = o;  o += (size_t)QR * P4;     // B~ D~
+        oT2 = o;  o += (size_t)QR * N4;     // dY H'^T
+        // staging of the raw rows of one chunk (16-byte aligned parts)
+        {
+            size_t sb = 0;
+            auto part = [&](size_t bytes) { const size_t at = sb; sb += (bytes + 15) / 16 * 16; return at; };
+            oStB = part(Q * rowB); oStC = part(Q * rowB); oStX = part(Q * rowX); oStT = part(Q * rowT);
+            oStY = part(Q * rowY);
+            oStg = o; o += sb / 4;
+        }
+        odM = o;  o += (size_t)Q * Q;       // dM per token pair
         odt = o; o += Q; oA = o; o += Q; olam = o; o += Q; olamn = o; o += Q; odtn = o; o += Q;
         ocA = o; o += Q; ow = o; o += Q; og = o; o += Q; os = o; o += Q; oe = o; o += Q;
         odcA = o; o += Q; odw = o; o += Q; odg = o; o += Q; ods = o; o += Q;
         ocs = o; o += (size_t)Q * K; osn = o; o += (size_t)Q * K; odph = o; o += (size_t)Q * K;
-        oth = o; o += (size_t)Q * K;
+        oth = o; o += (size_t)K * QP1;     // theta of the chunk, [K][Q + 1]
         ored = o; o += kBwdWarps;           // per-warp partial sums
         total = o;
     }
@@ -69,19 +95,63 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((unsigned)__cvta_generic_to_shared(dst)), "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+__device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+__device__ __forceinline__ void st4(float *p, float4 v) { *reinterpret_cast<float4 *>(p) = v; }
+__device__ __forceinline__ void fma4(float a, float4 b, float4 &c) {
+    c.x = fmaf(a, b.x, c.x);
+    c.y = fmaf(a, b.y, c.y);
+    c.z = fmaf(a, b.z, c.z);
+    c.w = fmaf(a, b.w, c.w);
+}
+__device__ __forceinline__ float4 axpy4(float a, float4 x, float4 y) {   // a x + y
+    return make_float4(fmaf(a, x.x, y.x), fmaf(a, x.y, y.y), fmaf(a, x.z, y.z), fmaf(a, x.w, y.w));
+}
+
+// c0 += sum_k A0[k as] B[k bs .. + 3] for k in [k0, k1) (one output row, four columns)
+__device__ __forceinline__ void mm1(const float *A0, int as, const float *B, int bs, int k0, int k1, float4 &c0) {
+#pragma unroll 4
+    for (int k = k0; k < k1; ++k) fma4(A0[k * as], ld4(B + (size_t)k * bs), c0);
+}
+// c0, c1 += the same for two output rows sharing the right operand
+__device__ __forceinline__ void mm2(const float *A0, const float *A1, int as, const float *B, int bs, int k0, int k1,
+                                    float4 &c0, float4 &c1) {
+#pragma unroll 4
+    for (int k = k0; k < k1; ++k) {
+        const float4 b = ld4(B + (size_t)k * bs);
+        fma4(A0[k * as], b, c0);
+        fma4(A1[k * as], b, c1);
+    }
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kBwdThreads, 1)
-scan_bwd_kernel(BwdArgs a, int Q) {
-    extern __shared__ float sm[];
-    const BwdSmem Lo(Q, a.R, a.N, a.P);
-    const int N = a.N, P = a.P, R = a.R, K = N / 2, H = a.H, L = a.L, NS = Lo.NS, PS = Lo.PS, QS = Lo.QS;
-    float *Dm = sm + Lo.oD, *Dt = sm + Lo.oDt, *Hc = sm + Lo.oH, *Hn = sm + Lo.oH2;
-    float *Bt = sm + Lo.oB, *Ct = sm + Lo.oC, *Xs = sm + Lo.oX, *Ys = sm + Lo.oY;
+scan_bwd_kernel(BwdArgs a, int Q, int cp16) {   // cp16: the raw rows and checkpoints copy in 16-byte pieces
+    extern __shared__ __align__(16) float sm[];
+    const BwdSmem Lo(Q, a.R, a.N, a.P, (int)sizeof(T));
+    const int N = a.N, P = a.P, R = a.R, K = N / 2, H = a.H, L = a.L;
+    const int N4 = Lo.N4, P4 = Lo.P4, QR4 = Lo.QR4, QS = Lo.QS, NP = Lo.NP, PP = Lo.PP;
+    const int NC4 = NP / 4, PC4 = PP / 4;   // float4 columns of the N- and P-wide tiles
+    float *Dm = sm + Lo.oD, *DtT = sm + Lo.oDtT, *Hs = sm + Lo.oH;
+    float *Bt = sm + Lo.oB, *Ct = sm + Lo.oC, *BtT = sm + Lo.oBT, *Xs = sm + Lo.oX, *XsT = sm + Lo.oXT;
+    float *Ys = sm + Lo.oY, *Ye = sm + Lo.oYe;
     float *Sm = sm + Lo.oS, *Zm = sm + Lo.oZ, *T1 = sm + Lo.oT1, *T2 = sm + Lo.oT2, *dMt = sm + Lo.odM;
     float *vdt = sm + Lo.odt, *vA = sm + Lo.oA, *vl = sm + Lo.olam, *vln = sm + Lo.olamn, *vdtn = sm + Lo.odtn;
     float *cA = sm + Lo.ocA, *wv = sm + Lo.ow, *gv = sm + Lo.og, *sv = sm + Lo.os, *ev = sm + Lo.oe;
     float *dcA = sm + Lo.odcA, *dwv = sm + Lo.odw, *dgv = sm + Lo.odg, *dsv = sm + Lo.ods;
     float *cs = sm + Lo.ocs, *sn = sm + Lo.osn, *dph = sm + Lo.odph, *thv = sm + Lo.oth, *red = sm + Lo.ored;
+    unsigned char *stg = reinterpret_cast<unsigned char *>(sm + Lo.oStg);
+    const T *stB = reinterpret_cast<const T *>(stg + Lo.oStB), *stC = reinterpret_cast<const T *>(stg + Lo.oStC);
+    const T *stX = reinterpret_cast<const T *>(stg + Lo.oStX), *stT = reinterpret_cast<const T *>(stg + Lo.oStT);
+    const float *stY = reinterpret_cast<const float *>(stg + Lo.oStY);
+    const int QP1 = Lo.QP1;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int bh = blockIdx.x, b = bh / H, h = bh % H;
@@ -90,31 +160,87 @@ scan_bwd_kernel(BwdArgs a, int Q) {
     const T *dtg = static_cast<const T *>(a.dt), *Ag = static_cast<const T *>(a.A), *lg = static_cast<const T *>(a.lam);
     const T *thg = static_cast<const T *>(a.theta);
     auto tok = [&](int t) { return ((size_t)b * L + t) * H + h; };
-    float *ckpt = a.ws + (size_t)bh * (nc + 1) * N * P;   // H'_c, c = 0..nc
+    float *ckpt = a.ws + (size_t)bh * (nc + 1) * N * P;   // H'_c^T ([P][N]), c = 0..nc
 
-    // Loads the scalars, angles (cos / sin of the chunk-local phi) and rotated B (and C), x of the
-    // chunk at s0 into shared memory; Qc tokens.
-    auto load_chunk = [&](int s0, int Qc, bool withC) {
-        for (int i = tid; i < Q; i += kBwdThreads) {
-            float d = 0.f, av = 0.f, l = 0.f, ln = 1.f, dn = 0.f;
-            if (i < Qc) {
-                const size_t ti = tok(s0 + i);
-                d = to_f(dtg[ti]);
-                av = to_f(Ag[ti]);
-                l = to_f(lg[ti]);
-                if (s0 + i + 1 < L) {
-                    ln = to_f(lg[tok(s0 + i + 1)]);
-                    dn = to_f(dtg[tok(s0 + i + 1)]);
+    // every pad column and row starts (and stays) zero
+    for (size_t i = tid; i < Lo.total; i += kBwdThreads) sm[i] = 0.f;
+    __syncthreads();
+
+    // The raw rows of the Qn tokens at s0n (B; with C also C and dy) into the staging area: 16-byte
+    // asynchronous copies (one commit group), or plain copies where the rows do not split into them
+    auto stage = [&](int s0n, int Qn, bool withC) {
+        const size_t tok0 = ((size_t)b * L + s0n) * H + h;   // token rows are H rows apart
+        if (cp16) {
+            const int pB = (int)(Lo.rowB / 16), pX = (int)(Lo.rowX / 16), pT = (int)(Lo.rowT / 16);
+            const int pY = (int)(Lo.rowY / 16);
+            const int nB = Qn * pB, nC = withC ? nB : 0, nX = Qn * pX, nT = Qn * pT, nY = withC ? Qn * pY : 0;
+            for (int i = tid; i < nB + nC + nX + nT + nY; i += kBwdThreads) {
+                int j = i, pp;
+                size_t row, dst;
+                const char *base;
+                if (j < nB) {
+                    pp = pB; base = static_cast<const char *>(a.B); row = Lo.rowB; dst = Lo.oStB;
+                } else if ((j -= nB) < nC) {
+                    pp = pB; base = static_cast<const char *>(a.C); row = Lo.rowB; dst = Lo.oStC;
+                } else if ((j -= nC) < nX) {
+                    pp = pX; base = static_cast<const char *>(a.x); row = Lo.rowX; dst = Lo.oStX;
+                } else if ((j -= nX) < nT) {
+                    pp = pT; base = static_cast<const char *>(a.theta); row = Lo.rowT; dst = Lo.oStT;
+                } else {
+                    j -= nT; pp = pY; base = reinterpret_cast<const char *>(a.dy); row = Lo.rowY; dst = Lo.oStY;
                 }
+                const int t = j / pp, q = j % pp;
+                cp_async16(stg + dst + t * row + 16 * q, base + (tok0 + (size_t)t * H) * row + 16 * q);
             }
-            vdt[i] = d; vA[i] = av; vl[i] = l; vln[i] = ln; vdtn[i] = dn;
-            cA[i] = d * av;
+        } else {
+            T *sB = reinterpret_cast<T *>(stg + Lo.oStB), *sC = reinterpret_cast<T *>(stg + Lo.oStC);
+            T *sX = reinterpret_cast<T *>(stg + Lo.oStX), *sT = reinterpret_cast<T *>(stg + Lo.oStT);
+            float *sY = reinterpret_cast<float *>(stg + Lo.oStY);
+            for (int i = tid; i < Qn * R * N; i += kBwdThreads) {
+                const size_t g = (tok0 + (size_t)(i / (R * N)) * H) * R * N + i % (R * N);
+                sB[i] = Bg[g];
+                if (withC) sC[i] = Cg[g];
+            }
+            for (int i = tid; i < Qn * R * P; i += kBwdThreads) {
+                const size_t g = (tok0 + (size_t)(i / (R * P)) * H) * R * P + i % (R * P);
+                sX[i] = xg[g];
+                if (withC) sY[i] = a.dy[g];
+            }
+            for (int i = tid; i < Qn * K; i += kBwdThreads) sT[i] = thg[(tok0 + (size_t)(i / K) * H) * K + i % K];
         }
-        for (int i = tid; i < Q * K; i += kBwdThreads) {
-            const int t = i / K, k = i % K;
-            thv[i] = t < Qc ? to_f(thg[tok(s0 + t) * K + k]) : 0.f;
+        cp_async_commit();   // (an empty group on the plain path)
+    };
+    // per-token scalars of the Qn tokens at s0n, one token per thread (threads < Q), into registers
+    float r_dt = 0.f, r_A = 0.f, r_l = 0.f, r_ln = 1.f, r_dtn = 0.f;
+    auto fetch = [&](int s0n, int Qn) {
+        r_dt = r_A = r_l = r_dtn = 0.f;
+        r_ln = 1.f;
+        if (tid < Qn) {
+            const size_t ti = tok(s0n + tid);
+            r_dt = to_f(dtg[ti]);
+            r_A = to_f(Ag[ti]);
+            r_l = to_f(lg[ti]);
+            if (s0n + tid + 1 < L) {
+                r_ln = to_f(lg[tok(s0n + tid + 1)]);
+                r_dtn = to_f(dtg[tok(s0n + tid + 1)]);
+            }
+        }
+    };
+
+    // The chunk at s0 (Qc tokens, staged and fetched): its scalars, angles (cos / sin of the
+    // chunk-local phi), rotated B (with pass2 also C and the transposes) and x (pass 1: X^ = s x)
+    // into their tiles.  Entered with the staging copies complete (this thread's); its first
+    // barrier makes every thread's visible.
+    auto load_chunk = [&](int Qc, bool pass2) {
+        for (int i = tid; i < Q; i += kBwdThreads) {
+            vdt[i] = r_dt; vA[i] = r_A; vl[i] = r_l; vln[i] = r_ln; vdtn[i] = r_dtn;
+            cA[i] = r_dt * r_A;
         }
         __syncthreads();
+        for (int i = tid; i < Q * K; i += kBwdThreads) {
+            const int t = i / K, k = i % K;
+            thv[k * QP1 + t] = t < Qc ? to_f(stT[i]) : 0.f;
+        }
         if (warp == 0) {   // inclusive cumsum of dt A (chunk-local), 32 tokens at a time
             float carry = 0.f;
             for (int base = 0; base < Q; base += 32) {
@@ -129,16 +255,22 @@ scan_bwd_kernel(BwdArgs a, int Q) {
                 carry = __shfl_sync(0xffffffffu, v, 31);
             }
         }
-        for (int i = tid; i < Q * K; i += kBwdThreads) {   // chunk-local angle of token t, pair k
-            const int t = i / K, k = i % K;
-            float phi = 0.f;
-            for (int u = 0; u <= t; ++u) phi = fmaf(vdt[u], thv[u * K + k], phi);
-            float s, c;
-            sincosf(phi, &s, &c);
-            cs[i] = c;
-            sn[i] = s;
-        }
         __syncthreads();
+        // chunk-local angle of token t (a lane), pair k: an inclusive scan over the tokens (Q <= 32)
+        for (int k = warp; k < K; k += kBwdWarps) {
+            float phi = lane < Q ? vdt[lane] * thv[k * QP1 + lane] : 0.f;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float t = __shfl_up_sync(0xffffffffu, phi, o);
+                if (lane >= o) phi += t;
+            }
+            if (lane < Q) {
+                float s, c;
+                sincosf(phi, &s, &c);
+                cs[lane * K + k] = c;
+                sn[lane * K + k] = s;
+            }
+        }
         const int e = Qc - 1;
         for (int i = tid; i < Q; i += kBwdThreads) {
             const float w = vl[i] * vdt[i] + (1.f - vln[i]) * vdtn[i];
@@ -147,27 +279,39 @@ scan_bwd_kernel(BwdArgs a, int Q) {
             sv[i] = i < Qc ? expf(cA[e] - cA[i]) * w : 0.f;
             ev[i] = i < Qc ? expf(cA[i]) : 0.f;
         }
+        __syncthreads();
         for (int i = tid; i < Q * R * K; i += kBwdThreads) {
-            const int row = i / K, k = i % K, t = row / R, r = row % R;
+            const int row = i / K, k = i % K, t = row / R;
             float b0 = 0.f, b1 = 0.f, c0 = 0.f, c1 = 0.f;
             if (t < Qc) {
-                const size_t base = (tok(s0 + t) * R + r) * N + 2 * k;
-                b0 = to_f(Bg[base]);
-                b1 = to_f(Bg[base + 1]);
-                if (withC) {
-                    c0 = to_f(Cg[base]);
-                    c1 = to_f(Cg[base + 1]);
+                const int q = row * N + 2 * k;
+                b0 = to_f(stB[q]);
+                b1 = to_f(stB[q + 1]);
+                if (pass2) {
+                    c0 = to_f(stC[q]);
+                    c1 = to_f(stC[q + 1]);
                 }
             }
             const float c = cs[t * K + k], s = sn[t * K + k];
-            Bt[row * NS + 2 * k] = c * b0 + s * b1;       // R(-phi) applied to the pair
-            Bt[row * NS + 2 * k + 1] = -s * b0 + c * b1;
-            Ct[row * NS + 2 * k] = c * c0 + s * c1;
-            Ct[row * NS + 2 * k + 1] = -s * c0 + c * c1;
+            const float bt0 = c * b0 + s * b1, bt1 = -s * b0 + c * b1;   // R(-phi) applied to the pair
+            Bt[row * N4 + 2 * k] = bt0;
+            Bt[row * N4 + 2 * k + 1] = bt1;
+            if (pass2) {
+                BtT[(2 * k) * QR4 + row] = bt0;
+                BtT[(2 * k + 1) * QR4 + row] = bt1;
+                Ct[row * N4 + 2 * k] = c * c0 + s * c1;
+                Ct[row * N4 + 2 * k + 1] = -s * c0 + c * c1;
+            }
         }
         for (int i = tid; i < Q * R * P; i += kBwdThreads) {
-            const int row = i / P, p = i % P, t = row / R, r = row % R;
-            Xs[row * PS + p] = t < Qc ? to_f(xg[(tok(s0 + t) * R + r) * P + p]) : 0.f;
+            const int row = i / P, p = i % P, t = row / R;
+            float v = t < Qc ? to_f(stX[i]) : 0.f;
+            if (pass2) {
+                Xs[row * P4 + p] = v;
+                XsT[p * QR4 + row] = v;
+            } else {
+                Xs[row * P4 + p] = sv[t] * v;
+            }
         }
         __syncthreads();
     };
@@ -177,38 +321,57 @@ scan_bwd_kernel(BwdArgs a, int Q) {
         const float *h0 = a.h0 ? a.h0 + (size_t)bh * N * P : nullptr;
         const T *bq = static_cast<const T *>(a.Bprev), *xq = static_cast<const T *>(a.xprev);
         const float left0 = L > 0 ? (1.f - to_f(lg[tok(0)])) * to_f(dtg[tok(0)]) : 0.f;
-        for (int i = tid; i < N * P; i += kBwdThreads) {
-            const int n = i / P, p = i % P;
-            float v = h0 ? h0[i] : 0.f;
+        for (int i = tid; i < N * P; i += kBwdThreads) {   // i = p N + n: the transposed layout
+            const int p = i / N, n = i % N;
+            float v = h0 ? h0[(size_t)n * P + p] : 0.f;
             if (bq && xq) {
                 float u = 0.f;
                 for (int r = 0; r < R; ++r)
                     u += to_f(bq[((size_t)bh * R + r) * N + n]) * to_f(xq[((size_t)bh * R + r) * P + p]);
                 v += left0 * u;
             }
-            Dm[n * PS + p] = v;
+            Hs[p * N4 + n] = v;
             ckpt[i] = v;
         }
+        stage(0, min(Q, L), false);
+        fetch(0, min(Q, L));
         __syncthreads();
         for (int c = 0; c < nc; ++c) {
-            const int s0 = c * Q, Qc = min(Q, L - s0), e = Qc - 1;
-            load_chunk(s0, Qc, false);
+            const int s0 = c * Q, Qc = min(Q, L - s0), e = Qc - 1, QRc = Qc * R;
+            cp_async_wait<0>();
+            load_chunk(Qc, false);
+            if (c + 1 < nc) {   // the next chunk's rows come in while this one is folded into the state
+                stage(s0 + Q, min(Q, L - s0 - Q), false);
+                fetch(s0 + Q, min(Q, L - s0 - Q));
+            }
             const float de = expf(cA[e]);
             float *dst = ckpt + (size_t)(c + 1) * N * P;
-            for (int i = tid; i < K * P; i += kBwdThreads) {
-                const int k = i / P, p = i % P;
-                float v0 = de * Dm[(2 * k) * PS + p], v1 = de * Dm[(2 * k + 1) * PS + p];
-                for (int row = 0; row < Qc * R; ++row) {
-                    const float wx = sv[row / R] * Xs[row * PS + p];
-                    v0 = fmaf(Bt[row * NS + 2 * k], wx, v0);
-                    v1 = fmaf(Bt[row * NS + 2 * k + 1], wx, v1);
+            // H'^T <- R(phi_e) [e^{cA_e} H'^T + X^^T B~], rows p in pairs, four columns n (two pairs)
+            for (int i = tid; i < ((P + 1) / 2) * NC4; i += kBwdThreads) {
+                const int p = 2 * (i / NC4), n4 = i % NC4, p1 = min(p + 1, P - 1);
+                float4 u0 = make_float4(0.f, 0.f, 0.f, 0.f), u1 = u0;
+                mm2(Xs + p, Xs + p1, P4, Bt + 4 * n4, N4, 0, QRc, u0, u1);
+                const int k0 = 2 * n4, k1 = min(2 * n4 + 1, K - 1);
+                const float c0 = cs[e * K + k0], s0_ = sn[e * K + k0], c1 = cs[e * K + k1], s1 = sn[e * K + k1];
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const int pp = q ? p1 : p;
+                    if (q && p1 == p) continue;
+                    float *hrow = Hs + pp * N4 + 4 * n4;
+                    const float4 hv = ld4(hrow), u = q ? u1 : u0;
+                    const float4 v = axpy4(de, hv, u);
+                    const float4 nv = make_float4(c0 * v.x - s0_ * v.y, s0_ * v.x + c0 * v.y,
+                                                  c1 * v.z - s1 * v.w, s1 * v.z + c1 * v.w);
+                    st4(hrow, nv);
+                    const int n = 4 * n4;
+                    float *drow = dst + (size_t)pp * N + n;
+                    drow[0] = nv.x;
+                    drow[1] = nv.y;
+                    if (n + 2 < N) {
+                        drow[2] = nv.z;
+                        drow[3] = nv.w;
+                    }
                 }
-                const float cc = cs[e * K + k], ss = sn[e * K + k];
-                const float n0 = cc * v0 - ss * v1, n1 = ss * v0 + cc * v1;
-                Dm[(2 * k) * PS + p] = n0;
-                Dm[(2 * k + 1) * PS + p] = n1;
-                dst[(2 * k) * P + p] = n0;
-                dst[(2 * k + 1) * P + p] = n1;
             }
             __syncthreads();
         }
@@ -216,65 +379,99 @@ scan_bwd_kernel(BwdArgs a, int Q) {
 
     // ================================================================ pass 2: gradients
     for (int i = tid; i < N * P; i += kBwdThreads)
-        Dm[(i / P) * PS + i % P] = a.dh_out ? a.dh_out[(size_t)bh * N * P + i] : 0.f;
-    __syncthreads();
+        Dm[(i / P) * P4 + i % P] = a.dh_out ? a.dh_out[(size_t)bh * N * P + i] : 0.f;
+    stage((nc - 1) * Q, L - (nc - 1) * Q, true);
+    fetch((nc - 1) * Q, L - (nc - 1) * Q);
     for (int c = nc - 1; c >= 0; --c) {
         const int s0 = c * Q, Qc = min(Q, L - s0), e = Qc - 1, QRc = Qc * R;
-        load_chunk(s0, Qc, true);
-        for (int i = tid; i < N * P; i += kBwdThreads) {
-            Hc[(i / P) * PS + i % P] = ckpt[(size_t)c * N * P + i];
-            Hn[(i / P) * PS + i % P] = ckpt[(size_t)(c + 1) * N * P + i];
-        }
-        for (int i = tid; i < Q * R * P; i += kBwdThreads) {
-            const int row = i / P, p = i % P, t = row / R, r = row % R;
-            Ys[row * PS + p] = t < Qc ? a.dy[(tok(s0 + t) * R + r) * P + p] : 0.f;
-        }
         for (int i = tid; i < Q; i += kBwdThreads) {
             dcA[i] = 0.f;
             dwv[i] = 0.f;
             dgv[i] = 0.f;
             dsv[i] = 0.f;
         }
-        // D~ = R(-phi_e) D, and the angle gradient of the turn R(phi_e): <D, J H'_{c+1}> per pair
-        for (int i = tid; i < K * P; i += kBwdThreads) {
-            const int k = i / P, p = i % P;
-            const float cc = cs[e * K + k], ss = sn[e * K + k];
-            const float d0 = Dm[(2 * k) * PS + p], d1 = Dm[(2 * k + 1) * PS + p];
-            Dt[(2 * k) * PS + p] = cc * d0 + ss * d1;
-            Dt[(2 * k + 1) * PS + p] = -ss * d0 + cc * d1;
-        }
         for (int i = tid; i < Q * K; i += kBwdThreads) dph[i] = 0.f;
-        __syncthreads();
-        for (int k = warp; k < K; k += kBwdWarps) {
-            float v = 0.f;
-            for (int p = lane; p < P; p += 32)
-                v += Dm[(2 * k + 1) * PS + p] * Hn[(2 * k) * PS + p] - Dm[(2 * k) * PS + p] * Hn[(2 * k + 1) * PS + p];
-            v = warp_sum(v);
-            if (lane == 0) dph[e * K + k] += v;
+        // H'_c^T copied in while the chunk's inputs are turned (a second commit group)
+        const float *Hc = ckpt + (size_t)c * N * P;
+        if (cp16) {
+            const int pr = N / 4;
+            for (int i = tid; i < P * pr; i += kBwdThreads)
+                cp_async16(Hs + (i / pr) * N4 + 4 * (i % pr), Hc + (size_t)(i / pr) * N + 4 * (i % pr));
+        } else {
+            for (int i = tid; i < N * P; i += kBwdThreads) Hs[(i / N) * N4 + i % N] = Hc[i];
         }
-        // S = C~ B~^T and Z = dY X^T over the chunk's rows
-        for (int i = tid; i < QRc * QRc; i += kBwdThreads) {
-            const int rt = i / QRc, rj = i % QRc;
-            float s = 0.f, z = 0.f;
-            if (rj / R <= rt / R) {
-                for (int n = 0; n < N; ++n) s = fmaf(Ct[rt * NS + n], Bt[rj * NS + n], s);
-                for (int p = 0; p < P; ++p) z = fmaf(Ys[rt * PS + p], Xs[rj * PS + p], z);
-            }
-            Sm[rt * QS + rj] = s;
-            Zm[rt * QS + rj] = z;
-        }
-        // B~ D~ (rows x P) and dY H'^T (rows x N)
+        cp_async_commit();
+        cp_async_wait<1>();         // the staged rows (the group before)
+        load_chunk(Qc, true);       // its barriers also order the zeroing above
+        const float *Hn = ckpt + (size_t)(c + 1) * N * P;
         for (int i = tid; i < QRc * P; i += kBwdThreads) {
-            const int row = i / P, p = i % P;
-            float v = 0.f;
-            for (int n = 0; n < N; ++n) v = fmaf(Bt[row * NS + n], Dt[n * PS + p], v);
-            T1[row * PS + p] = v;
+            const int row = i / P, p = i % P, t = row / R;
+            const float v = stY[i];
+            Ys[row * P4 + p] = v;
+            Ye[row * P4 + p] = ev[t] * v;
         }
-        for (int i = tid; i < QRc * N; i += kBwdThreads) {
-            const int row = i / N, n = i % N;
+        for (int i = QRc * P + tid; i < Q * R * P; i += kBwdThreads) {   // rows past the sequence end
+            const int row = i / P, p = i % P;
+            Ys[row * P4 + p] = 0.f;
+            Ye[row * P4 + p] = 0.f;
+        }
+        // D~ = R(-phi_e) D in place (and its transpose), and the angle gradient of the turn R(phi_e):
+        // <D, J H'_{c+1}> per pair, over four columns p per thread
+        for (int i = tid; i < K * PC4; i += kBwdThreads) {
+            const int k = i / PC4, p4 = i % PC4, p = 4 * p4;
+            const float cc = cs[e * K + k], ss = sn[e * K + k];
+            const float4 d0 = ld4(Dm + (2 * k) * P4 + p), d1 = ld4(Dm + (2 * k + 1) * P4 + p);
+            const float4 t0 = make_float4(cc * d0.x + ss * d1.x, cc * d0.y + ss * d1.y, cc * d0.z + ss * d1.z,
+                                          cc * d0.w + ss * d1.w);
+            const float4 t1 = make_float4(-ss * d0.x + cc * d1.x, -ss * d0.y + cc * d1.y, -ss * d0.z + cc * d1.z,
+                                          -ss * d0.w + cc * d1.w);
+            st4(Dm + (2 * k) * P4 + p, t0);
+            st4(Dm + (2 * k + 1) * P4 + p, t1);
+            const float a0[4] = {t0.x, t0.y, t0.z, t0.w}, a1[4] = {t1.x, t1.y, t1.z, t1.w};
+            const float e0[4] = {d0.x, d0.y, d0.z, d0.w}, e1[4] = {d1.x, d1.y, d1.z, d1.w};
             float v = 0.f;
-            for (int p = 0; p < P; ++p) v = fmaf(Ys[row * PS + p], Hc[n * PS + p], v);
-            T2[row * NS + n] = v;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                *reinterpret_cast<float2 *>(DtT + (p + q) * N4 + 2 * k) = make_float2(a0[q], a1[q]);
+                if (p + q < P) {
+                    const float2 hn = *reinterpret_cast<const float2 *>(Hn + (size_t)(p + q) * N + 2 * k);
+                    v += e1[q] * hn.x - e0[q] * hn.y;
+                }
+            }
+            atomicAdd(&dph[e * K + k], v);
+        }
+        cp_async_wait<0>();         // H'_c^T
+        __syncthreads();
+        if (c > 0) {   // the chunk before: its rows come in while this one is processed
+            stage(s0 - Q, Q, true);
+            fetch(s0 - Q, Q);
+        }
+        // S = C~ B~^T, Z = dY X^T (1 x 4 tiles), B~ D~ (rows x P) and dY H'^T (rows x N) (2 x 4 tiles)
+        {
+            const int QC4 = (QRc + 3) / 4, R2 = (QRc + 1) / 2;
+            const int nS = QRc * QC4, nT1 = R2 * PC4, nT2 = R2 * NC4;
+            for (int i = tid; i < 2 * nS + nT1 + nT2; i += kBwdThreads) {
+                float4 c0 = make_float4(0.f, 0.f, 0.f, 0.f), c1 = c0;
+                if (i < 2 * nS) {
+                    const bool isZ = i >= nS;
+                    const int q = isZ ? i - nS : i, rt = q / QC4, j4 = q % QC4;
+                    if ((4 * j4) / R <= rt / R) {   // otherwise every column lies past the token
+                        if (isZ) mm1(Ys + rt * P4, 1, XsT + 4 * j4, QR4, 0, P, c0);
+                        else mm1(Ct + rt * N4, 1, BtT + 4 * j4, QR4, 0, N, c0);
+                    }
+                    st4((isZ ? Zm : Sm) + rt * QS + 4 * j4, c0);
+                } else if (i < 2 * nS + nT1) {
+                    const int q = i - 2 * nS, r0 = 2 * (q / PC4), p4 = q % PC4, r1 = min(r0 + 1, QRc - 1);
+                    mm2(Bt + r0 * N4, Bt + r1 * N4, 1, Dm + 4 * p4, P4, 0, N, c0, c1);
+                    st4(T1 + r0 * P4 + 4 * p4, c0);
+                    if (r1 != r0) st4(T1 + r1 * P4 + 4 * p4, c1);
+                } else {
+                    const int q = i - 2 * nS - nT1, r0 = 2 * (q / NC4), n4 = q % NC4, r1 = min(r0 + 1, QRc - 1);
+                    mm2(Ys + r0 * P4, Ys + r1 * P4, 1, Hs + 4 * n4, N4, 0, P, c0, c1);
+                    st4(T2 + r0 * N4 + 4 * n4, c0);
+                    if (r1 != r0) st4(T2 + r1 * N4 + 4 * n4, c1);
+                }
+            }
         }
         __syncthreads();
         // dM per token pair (sum over rank pairs), then M o S and M o Z in place
@@ -312,8 +509,8 @@ scan_bwd_kernel(BwdArgs a, int Q) {
             float yi = 0.f, dsum = 0.f;
             for (int r = 0; r < R; ++r) {
                 const int row = t * R + r;
-                for (int n = lane; n < N; n += 32) yi += Ct[row * NS + n] * T2[row * NS + n];
-                for (int p = lane; p < P; p += 32) dsum += Xs[row * PS + p] * T1[row * PS + p];
+                for (int n = lane; n < N; n += 32) yi += Ct[row * N4 + n] * T2[row * N4 + n];
+                for (int p = lane; p < P; p += 32) dsum += Xs[row * P4 + p] * T1[row * P4 + p];
             }
             yi = warp_sum(yi);
             dsum = warp_sum(dsum);
@@ -327,9 +524,10 @@ scan_bwd_kernel(BwdArgs a, int Q) {
         // <D~, H'_c> (the transport e^{cA_e} H'_c into the chunk end), per-warp partial sums
         {
             float v = 0.f;
-            for (int i = tid; i < N * P; i += kBwdThreads) {
-                const int q = (i / P) * PS + i % P;
-                v += Dt[q] * Hc[q];
+            for (int i = tid; i < P * NC4; i += kBwdThreads) {
+                const int q = (i / NC4) * N4 + 4 * (i % NC4);
+                const float4 d = ld4(DtT + q), hv = ld4(Hs + q);
+                v += d.x * hv.x + d.y * hv.y + d.z * hv.z + d.w * hv.w;
             }
             v = warp_sum(v);
             if (lane == 0) red[warp] = v;
@@ -349,58 +547,78 @@ scan_bwd_kernel(BwdArgs a, int Q) {
             if (lane == 0) dcA[e] += v + expf(cA[e]) * dh;
         }
         __syncthreads();
-        // dX = (M o S)^T dY + diag(s) B~ D~  (the carry out adds to the sequence's last token)
-        for (int i = tid; i < QRc * P; i += kBwdThreads) {
-            const int rj = i / P, p = i % P, j = rj / R, r = rj % R;
-            float v = sv[j] * T1[rj * PS + p];
-            for (int rt = rj - r; rt < QRc; ++rt) v = fmaf(Sm[rt * QS + rj], Ys[rt * PS + p], v);
-            if (s0 + j == L - 1 && a.dxprev_out) v += a.dxprev_out[((size_t)bh * R + r) * P + p];
-            a.dx[(tok(s0 + j) * R + r) * P + p] = v;
-        }
-        // dB~ = (M o Z)^T C~ + diag(s) X D~^T and dC~ = (M o Z) B~ + diag(e^{cA}) dY H'^T, pair by pair;
-        // they are un-rotated as they are formed, and the angle gradients gather
-        // dphi_{t,k} += dv0 v1 - dv1 v0 over the B~ and C~ rows of token t
-        for (int i = tid; i < QRc * K; i += kBwdThreads) {
-            const int rj = i / K, k = i % K, j = rj / R, r = rj % R;
-            // dB~ entries 2k, 2k + 1 of row rj
-            float b0 = 0.f, b1 = 0.f, xd0 = 0.f, xd1 = 0.f;
-            for (int rt = rj - r; rt < QRc; ++rt) {
-                const float m = Zm[rt * QS + rj];
-                b0 = fmaf(m, Ct[rt * NS + 2 * k], b0);
-                b1 = fmaf(m, Ct[rt * NS + 2 * k + 1], b1);
+        // dX = (M o S)^T dY + diag(s) B~ D~  (the carry out adds to the sequence's last token);
+        // dB~ = (M o Z)^T C~ + diag(s) X D~^T and dC~ = (M o Z) B~ + diag(e^{cA}) dY H'^T, un-rotated
+        // as they are formed, with the angle gradients dphi_{t,k} += dv0 v1 - dv1 v0 over the B~ and
+        // C~ rows of token t
+        {
+            const int R2 = (QRc + 1) / 2, nX = R2 * PC4, nB = R2 * NC4;
+            for (int i = tid; i < nX + 2 * nB; i += kBwdThreads) {
+                float4 c0 = make_float4(0.f, 0.f, 0.f, 0.f), c1 = c0;
+                if (i < nX) {
+                    const int r0 = 2 * (i / PC4), p4 = i % PC4, r1 = min(r0 + 1, QRc - 1), p = 4 * p4;
+                    // rows of earlier tokens hold M o S = 0: start at the first row of r0's token
+                    mm2(Sm + r0, Sm + r1, QS, Ys + p, P4, (r0 / R) * R, QRc, c0, c1);
+#pragma unroll
+                    for (int q = 0; q < 2; ++q) {
+                        const int rj = q ? r1 : r0;
+                        if (q && r1 == r0) continue;
+                        const int j = rj / R, r = rj % R;
+                        float4 v = axpy4(sv[j], ld4(T1 + rj * P4 + p), q ? c1 : c0);
+                        const float vv[4] = {v.x, v.y, v.z, v.w};
+                        const bool last = s0 + j == L - 1 && a.dxprev_out;
+                        float *dxr = a.dx + (tok(s0 + j) * R + r) * P;
+#pragma unroll
+                        for (int z = 0; z < 4; ++z)
+                            if (p + z < P)
+                                dxr[p + z] = vv[z] + (last ? a.dxprev_out[((size_t)bh * R + r) * P + p + z] : 0.f);
+                    }
+                } else {
+                    const bool isC = i >= nX + nB;
+                    const int q = isC ? i - nX - nB : i - nX;
+                    const int r0 = 2 * (q / NC4), n4 = q % NC4, r1 = min(r0 + 1, QRc - 1), n = 4 * n4;
+                    if (!isC) {
+                        mm2(Zm + r0, Zm + r1, QS, Ct + n, N4, (r0 / R) * R, QRc, c0, c1);
+                        float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
+                        mm2(Xs + r0 * P4, Xs + r1 * P4, 1, DtT + n, N4, 0, P, x0, x1);
+                        c0 = axpy4(sv[r0 / R], x0, c0);
+                        c1 = axpy4(sv[r1 / R], x1, c1);
+                    } else {
+                        // row r1's token ends the range of columns rj with M o Z != 0
+                        mm2(Zm + r0 * QS, Zm + r1 * QS, 1, Bt + n, N4, 0, min(QRc, (r1 / R + 1) * R), c0, c1);
+                        c0 = axpy4(ev[r0 / R], ld4(T2 + r0 * N4 + n), c0);
+                        c1 = axpy4(ev[r1 / R], ld4(T2 + r1 * N4 + n), c1);
+                    }
+                    const float *Vt = isC ? Ct : Bt;   // the rotated operand itself
+                    float *dst = isC ? a.dC : a.dB;
+#pragma unroll
+                    for (int qq = 0; qq < 2; ++qq) {
+                        const int row = qq ? r1 : r0;
+                        if (qq && r1 == r0) continue;
+                        const int j = row / R, r = row % R;
+                        const float4 g = qq ? c1 : c0, vt = ld4(Vt + row * N4 + n);
+                        const float gg[4] = {g.x, g.y, g.z, g.w}, tv[4] = {vt.x, vt.y, vt.z, vt.w};
+                        const size_t base = (tok(s0 + j) * R + r) * N;
+                        const bool last = !isC && s0 + j == L - 1 && a.dBprev_out;
+#pragma unroll
+                        for (int pr = 0; pr < 2; ++pr) {
+                            const int k = 2 * n4 + pr;
+                            if (k >= K) continue;
+                            const float g0 = gg[2 * pr], g1 = gg[2 * pr + 1];
+                            atomicAdd(&dph[j * K + k], g0 * tv[2 * pr + 1] - g1 * tv[2 * pr]);
+                            // un-rotate: dB = R(phi) dB~
+                            const float cc = cs[j * K + k], ss = sn[j * K + k];
+                            float o0 = cc * g0 - ss * g1, o1 = ss * g0 + cc * g1;
+                            if (last) {
+                                o0 += a.dBprev_out[((size_t)bh * R + r) * N + 2 * k];
+                                o1 += a.dBprev_out[((size_t)bh * R + r) * N + 2 * k + 1];
+                            }
+                            dst[base + 2 * k] = o0;
+                            dst[base + 2 * k + 1] = o1;
+                        }
+                    }
+                }
             }
-            for (int p = 0; p < P; ++p) {
-                xd0 = fmaf(Xs[rj * PS + p], Dt[(2 * k) * PS + p], xd0);
-                xd1 = fmaf(Xs[rj * PS + p], Dt[(2 * k + 1) * PS + p], xd1);
-            }
-            b0 = fmaf(sv[j], xd0, b0);
-            b1 = fmaf(sv[j], xd1, b1);
-            // dC~ entries 2k, 2k + 1 of row rj (as the row index t)
-            float c0 = 0.f, c1 = 0.f;
-            for (int rr = 0; rr < (j + 1) * R; ++rr) {
-                const float m = Zm[rj * QS + rr];
-                c0 = fmaf(m, Bt[rr * NS + 2 * k], c0);
-                c1 = fmaf(m, Bt[rr * NS + 2 * k + 1], c1);
-            }
-            c0 = fmaf(ev[j], T2[rj * NS + 2 * k], c0);
-            c1 = fmaf(ev[j], T2[rj * NS + 2 * k + 1], c1);
-            // angle gradient of the rotations R(-phi_j) of B~ and C~
-            const float bt0 = Bt[rj * NS + 2 * k], bt1 = Bt[rj * NS + 2 * k + 1];
-            const float ct0 = Ct[rj * NS + 2 * k], ct1 = Ct[rj * NS + 2 * k + 1];
-            atomicAdd(&dph[j * K + k], b0 * bt1 - b1 * bt0 + c0 * ct1 - c1 * ct0);
-            // un-rotate: dB = R(phi) dB~
-            const float cc = cs[j * K + k], ss = sn[j * K + k];
-            float db0 = cc * b0 - ss * b1, db1 = ss * b0 + cc * b1;
-            const float dc0 = cc * c0 - ss * c1, dc1 = ss * c0 + cc * c1;
-            if (s0 + j == L - 1 && a.dBprev_out) {
-                db0 += a.dBprev_out[((size_t)bh * R + r) * N + 2 * k];
-                db1 += a.dBprev_out[((size_t)bh * R + r) * N + 2 * k + 1];
-            }
-            const size_t base = (tok(s0 + j) * R + r) * N + 2 * k;
-            a.dB[base] = db0;
-            a.dB[base + 1] = db1;
-            a.dC[base] = dc0;
-            a.dC[base + 1] = dc1;
         }
         __syncthreads();
         // reverse cumulative sums: d(dt A)_u = sum_{t >= u} dcA_t, d(dt theta)_u = sum_{t >= u} dphi_t
@@ -436,7 +654,7 @@ scan_bwd_kernel(BwdArgs a, int Q) {
         for (int u = warp; u < Qc; u += kBwdWarps) {   // one warp per token: sum_k theta_k d(dt theta)_k
             const size_t ti = tok(s0 + u);
             float thsum = 0.f;
-            for (int k = lane; k < K; k += 32) thsum = fmaf(thv[u * K + k], dph[u * K + k], thsum);
+            for (int k = lane; k < K; k += 32) thsum = fmaf(thv[k * QP1 + u], dph[u * K + k], thsum);
             thsum = warp_sum(thsum);
             if (lane == 0) {
                 const float d = vdt[u], av = vA[u], l = vl[u];
@@ -453,13 +671,16 @@ scan_bwd_kernel(BwdArgs a, int Q) {
                 a.dlam[ti] = dl;
             }
         }
-        // D <- e^{cA_e} D~ + C~^T diag(e^{cA}) dY
-        const float de = expf(cA[e]);
-        for (int i = tid; i < N * P; i += kBwdThreads) {
-            const int n = i / P, p = i % P;
-            float v = de * Dt[n * PS + p];
-            for (int row = 0; row < QRc; ++row) v = fmaf(Ct[row * NS + n] * ev[row / R], Ys[row * PS + p], v);
-            Dm[n * PS + p] = v;
+        // D <- e^{cA_e} D~ + C~^T diag(e^{cA}) dY in place (rows n in pairs, four columns p)
+        {
+            const float de = expf(cA[e]);
+            for (int i = tid; i < (N / 2) * PC4; i += kBwdThreads) {
+                const int n0 = 2 * (i / PC4), p = 4 * (i % PC4);
+                float4 c0 = make_float4(0.f, 0.f, 0.f, 0.f), c1 = c0;
+                mm2(Ct + n0, Ct + n0 + 1, N4, Ye + p, P4, 0, QRc, c0, c1);
+                st4(Dm + n0 * P4 + p, axpy4(de, ld4(Dm + n0 * P4 + p), c0));
+                st4(Dm + (n0 + 1) * P4 + p, axpy4(de, ld4(Dm + (n0 + 1) * P4 + p), c1));
+            }
         }
         __syncthreads();
     }
@@ -467,7 +688,7 @@ scan_bwd_kernel(BwdArgs a, int Q) {
     // ================================================================ initial state and carry
     // H'_0 = h0 + left_0 B_{-1} x_{-1}^T: dh0 = D; d left_0 = <D, B_{-1} x_{-1}^T>
     if (a.dh0)
-        for (int i = tid; i < N * P; i += kBwdThreads) a.dh0[(size_t)bh * N * P + i] = Dm[(i / P) * PS + i % P];
+        for (int i = tid; i < N * P; i += kBwdThreads) a.dh0[(size_t)bh * N * P + i] = Dm[(i / P) * P4 + i % P];
     const T *bq = static_cast<const T *>(a.Bprev), *xq = static_cast<const T *>(a.xprev);
     if (bq && xq) {
         const float d0 = to_f(dtg[tok(0)]), l0 = to_f(lg[tok(0)]), left0 = (1.f - l0) * d0;
@@ -477,7 +698,7 @@ scan_bwd_kernel(BwdArgs a, int Q) {
             float u = 0.f;
             for (int r = 0; r < R; ++r)
                 u += to_f(bq[((size_t)bh * R + r) * N + n]) * to_f(xq[((size_t)bh * R + r) * P + p]);
-            dl = fmaf(Dm[n * PS + p], u, dl);
+            dl = fmaf(Dm[n * P4 + p], u, dl);
         }
         dl = warp_sum(dl);
         if (lane == 0) red[warp] = dl;
@@ -492,14 +713,14 @@ scan_bwd_kernel(BwdArgs a, int Q) {
             for (int i = tid; i < R * N; i += kBwdThreads) {
                 const int r = i / N, n = i % N;
                 float v = 0.f;
-                for (int p = 0; p < P; ++p) v = fmaf(Dm[n * PS + p], to_f(xq[((size_t)bh * R + r) * P + p]), v);
+                for (int p = 0; p < P; ++p) v = fmaf(Dm[n * P4 + p], to_f(xq[((size_t)bh * R + r) * P + p]), v);
                 a.dBprev[(size_t)bh * R * N + i] = left0 * v;
             }
         if (a.dxprev)
             for (int i = tid; i < R * P; i += kBwdThreads) {
                 const int r = i / P, p = i % P;
                 float v = 0.f;
-                for (int n = 0; n < N; ++n) v = fmaf(Dm[n * PS + p], to_f(bq[((size_t)bh * R + r) * N + n]), v);
+                for (int n = 0; n < N; ++n) v = fmaf(Dm[n * P4 + p], to_f(bq[((size_t)bh * R + r) * N + n]), v);
                 a.dxprev[(size_t)bh * R * P + i] = left0 * v;
             }
     } else {
@@ -512,34 +733,47 @@ scan_bwd_kernel(BwdArgs a, int Q) {
 
 }  // namespace
 
-// Tokens per chunk: 32 rows (t, r) per chunk, 16 when the four N x P state tiles are large (so that
-// the shared memory stays within one CTA's 227 KB).
-int bwd_chunk(int N, int P, int R) {
-    const int rows = N * P > 4096 ? 16 : 32;
-    return rows / R > 0 ? rows / R : 1;
+// Tokens per chunk: the most rows (t, r) per chunk, up to 32, whose tiles fit one CTA's 227 KB of
+// shared memory.
+int bwd_chunk(int N, int P, int R, int esz) {
+    int Q = 1;
+    for (int rows = 32; rows >= 1; rows /= 2) {
+        Q = rows / R > 0 ? rows / R : 1;
+        if (BwdSmem(Q, R, N, P, esz).total * sizeof(float) <= 227u * 1024u) break;
+    }
+    return Q;
 }
 
-size_t bwd_smem_bytes(int N, int P, int R) { return BwdSmem(bwd_chunk(N, P, R), R, N, P).total * sizeof(float); }
+size_t bwd_smem_bytes(int N, int P, int R, int esz) {
+    return BwdSmem(bwd_chunk(N, P, R, esz), R, N, P, esz).total * sizeof(float);
+}
 
-size_t bwd_workspace_bytes(int batch, int H, int L, int N, int P, int R) {
-    const int Q = bwd_chunk(N, P, R);
+size_t bwd_workspace_bytes(int batch, int H, int L, int N, int P, int R, int esz) {
+    const int Q = bwd_chunk(N, P, R, esz);
     const size_t nc = (size_t)(L + Q - 1) / Q;
     return (size_t)batch * H * (nc + 1) * N * P * sizeof(float);
 }
 
 cudaError_t scan_bwd(const BwdArgs &a, cudaStream_t s) {
-    const int Q = bwd_chunk(a.N, a.P, a.R);
-    const size_t smem = bwd_smem_bytes(a.N, a.P, a.R);
+    const int esz = a.dtype == M3_F32 ? 4 : 2;
+    const int Q = bwd_chunk(a.N, a.P, a.R, esz);
+    const size_t smem = bwd_smem_bytes(a.N, a.P, a.R, esz);
+    // 16-byte asynchronous copies: every raw row a whole number of 16-byte pieces, every base
+    // pointer on a 16-byte boundary (the workspace is), the checkpoint rows too
+    auto al16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    const int cp16 = ((size_t)a.R * a.N * esz) % 16 == 0 && ((size_t)a.R * a.P * esz) % 16 == 0 &&
+                     ((size_t)(a.N / 2) * esz) % 16 == 0 && ((size_t)a.R * a.P * 4) % 16 == 0 && a.N % 4 == 0 &&
+                     al16(a.B) && al16(a.C) && al16(a.x) && al16(a.theta) && al16(a.dy) && al16(a.ws);
     const unsigned grid = (unsigned)((long long)a.batch * a.H);
     if (grid == 0 || a.L == 0) return cudaSuccess;
     cudaError_t e;
     trace_mark(M3_KERNEL_BACKWARD, s, 0);
     if (a.dtype == M3_F32) {
         if ((e = allow_dynamic_smem<scan_bwd_kernel<float>>(smem)) != cudaSuccess) return e;
-        scan_bwd_kernel<float><<<grid, kBwdThreads, smem, s>>>(a, Q);
+        scan_bwd_kernel<float><<<grid, kBwdThreads, smem, s>>>(a, Q, cp16);
     } else {
         if ((e = allow_dynamic_smem<scan_bwd_kernel<__nv_bfloat16>>(smem)) != cudaSuccess) return e;
-        scan_bwd_kernel<__nv_bfloat16><<<grid, kBwdThreads, smem, s>>>(a, Q);
+        scan_bwd_kernel<__nv_bfloat16><<<grid, kBwdThreads, smem, s>>>(a, Q, cp16);
     }
     trace_mark(M3_KERNEL_BACKWARD, s, 1);
     count_launch();

@@ -178,7 +178,7 @@ enum Bar {
     kMma1 = 8,         // [2] first MMAs done -> epilogue
     kPReady = 10,      // [2] epilogue wrote P -> MMA
     kMma2 = 12,        // [2] Ya done -> epilogue
-    kEpiDone = 14      // [2] epilogue done with a chunk -> prologue
+    kEpiDone = 14      // [2] epilogue done with a chunk's vectors and x' -> prologue
 };
 
 // YT: element type of y (an m3_dtype; OUT only).  BCN: B and C go through the BC normalisation
@@ -948,6 +948,9 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                 named_sync(kBarEpi, kEpiThreads);
                 fence_after();
                 const float sc = fast_exp2(cA2[min(ti, Q - 1)]) * sg[5] * sigH[2 + p], sa = sg[6];
+                // the last read of this chunk's vectors (and MMA 2, the last reader of its x' tile, is
+                // done): the prologue may refill them while y is formed
+                mbar_arrive(bars + kEpiDone + p);
                 // y rows go through a shared-memory tile (this thread: row `row`, columns
                 // [32 eh, 32 eh + 32)) and leave by TMA: rows past the sequence end are clipped by
                 // the map, and the global writes are whole lines
@@ -997,8 +1000,7 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                     bulk_commit();
                 }
             }
-            fence_before();
-            mbar_arrive(bars + kEpiDone + p);
+            if (!OUT) mbar_arrive(bars + kEpiDone + p);
         }
         if (OUT && ew == 0 && lane == 0) bulk_wait<0>();
         // ---- carry out (last segment)
