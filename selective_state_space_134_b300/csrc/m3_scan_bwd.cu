@@ -115,29 +115,48 @@ __device__ __forceinline__ float4 axpy4(float a, float4 x, float4 y) {   // a x 
     return make_float4(fmaf(a, x.x, y.x), fmaf(a, x.y, y.y), fmaf(a, x.z, y.z), fmaf(a, x.w, y.w));
 }
 
-// c0 += sum_k A0[k as] B[k bs .. + 3] for k in [k0, k1) (one output row, four columns)
+// c0 += sum_k A0[k as] B[k bs .. + 3] for k in [k0, k1) (one output row, four columns); four steps
+// at a time, so that with constant strides every load takes an immediate offset
 __device__ __forceinline__ void mm1(const float *A0, int as, const float *B, int bs, int k0, int k1, float4 &c0) {
-#pragma unroll 4
-    for (int k = k0; k < k1; ++k) fma4(A0[k * as], ld4(B + (size_t)k * bs), c0);
+    int k = k0;
+    for (; k + 4 <= k1; k += 4) {
+        const float *a = A0 + k * as, *bp = B + k * bs;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) fma4(a[u * as], ld4(bp + u * bs), c0);
+    }
+    for (; k < k1; ++k) fma4(A0[k * as], ld4(B + k * bs), c0);
 }
 // c0, c1 += the same for two output rows sharing the right operand
 __device__ __forceinline__ void mm2(const float *A0, const float *A1, int as, const float *B, int bs, int k0, int k1,
                                     float4 &c0, float4 &c1) {
-#pragma unroll 4
-    for (int k = k0; k < k1; ++k) {
-        const float4 b = ld4(B + (size_t)k * bs);
+    int k = k0;
+    for (; k + 4 <= k1; k += 4) {
+        const float *a0 = A0 + k * as, *a1 = A1 + k * as, *bp = B + k * bs;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const float4 b = ld4(bp + u * bs);
+            fma4(a0[u * as], b, c0);
+            fma4(a1[u * as], b, c1);
+        }
+    }
+    for (; k < k1; ++k) {
+        const float4 b = ld4(B + k * bs);
         fma4(A0[k * as], b, c0);
         fma4(A1[k * as], b, c1);
     }
 }
 
-template <typename T>
+// NT, PT, QRT: the state size, head dim and rows per chunk when fixed at compile time (0: at run
+// time), so that the tile strides and most loop bounds are constants
+template <typename T, int NT, int PT, int QRT>
 __global__ void __launch_bounds__(kBwdThreads, 1)
 scan_bwd_kernel(BwdArgs a, int Q, int cp16) {   // cp16: the raw rows and checkpoints copy in 16-byte pieces
     extern __shared__ __align__(16) float sm[];
     const BwdSmem Lo(Q, a.R, a.N, a.P, (int)sizeof(T));
-    const int N = a.N, P = a.P, R = a.R, K = N / 2, H = a.H, L = a.L;
-    const int N4 = Lo.N4, P4 = Lo.P4, QR4 = Lo.QR4, QS = Lo.QS, NP = Lo.NP, PP = Lo.PP;
+    const int N = NT ? NT : a.N, P = PT ? PT : a.P, R = a.R, K = N / 2, H = a.H, L = a.L;
+    // the same values as Lo's, as constants where the shape is fixed
+    const int NP = NT ? rup4(NT) : Lo.NP, PP = PT ? rup4(PT) : Lo.PP;
+    const int N4 = NP + 4, P4 = PP + 4, QR4 = QRT ? rup4(QRT) + 4 : Lo.QR4, QS = QR4;
     const int NC4 = NP / 4, PC4 = PP / 4;   // float4 columns of the N- and P-wide tiles
     float *Dm = sm + Lo.oD, *DtT = sm + Lo.oDtT, *Hs = sm + Lo.oH;
     float *Bt = sm + Lo.oB, *Ct = sm + Lo.oC, *BtT = sm + Lo.oBT, *Xs = sm + Lo.oX, *XsT = sm + Lo.oXT;
@@ -754,6 +773,14 @@ size_t bwd_workspace_bytes(int batch, int H, int L, int N, int P, int R, int esz
     return (size_t)batch * H * (nc + 1) * N * P * sizeof(float);
 }
 
+template <auto Kern>
+cudaError_t launch_bwd(const BwdArgs &a, int Q, int cp16, size_t smem, unsigned grid, cudaStream_t s) {
+    const cudaError_t e = allow_dynamic_smem<Kern>(smem);
+    if (e != cudaSuccess) return e;
+    Kern<<<grid, kBwdThreads, smem, s>>>(a, Q, cp16);
+    return cudaSuccess;
+}
+
 cudaError_t scan_bwd(const BwdArgs &a, cudaStream_t s) {
     const int esz = a.dtype == M3_F32 ? 4 : 2;
     const int Q = bwd_chunk(a.N, a.P, a.R, esz);
@@ -768,13 +795,15 @@ cudaError_t scan_bwd(const BwdArgs &a, cudaStream_t s) {
     if (grid == 0 || a.L == 0) return cudaSuccess;
     cudaError_t e;
     trace_mark(M3_KERNEL_BACKWARD, s, 0);
-    if (a.dtype == M3_F32) {
-        if ((e = allow_dynamic_smem<scan_bwd_kernel<float>>(smem)) != cudaSuccess) return e;
-        scan_bwd_kernel<float><<<grid, kBwdThreads, smem, s>>>(a, Q, cp16);
-    } else {
-        if ((e = allow_dynamic_smem<scan_bwd_kernel<__nv_bfloat16>>(smem)) != cudaSuccess) return e;
-        scan_bwd_kernel<__nv_bfloat16><<<grid, kBwdThreads, smem, s>>>(a, Q, cp16);
-    }
+    // the shapes of the pages' models have their own constant-stride builds (bf16 inputs)
+    const int QR = Q * a.R;
+    if (a.dtype == M3_F32) e = launch_bwd<scan_bwd_kernel<float, 0, 0, 0>>(a, Q, cp16, smem, grid, s);
+    else if (a.N == 64 && a.P == 64 && QR == 32)
+        e = launch_bwd<scan_bwd_kernel<__nv_bfloat16, 64, 64, 32>>(a, Q, cp16, smem, grid, s);
+    else if (a.N == 128 && a.P == 64 && QR == 16)
+        e = launch_bwd<scan_bwd_kernel<__nv_bfloat16, 128, 64, 16>>(a, Q, cp16, smem, grid, s);
+    else e = launch_bwd<scan_bwd_kernel<__nv_bfloat16, 0, 0, 0>>(a, Q, cp16, smem, grid, s);
+    if (e != cudaSuccess) return e;
     trace_mark(M3_KERNEL_BACKWARD, s, 1);
     count_launch();
     return cudaGetLastError();

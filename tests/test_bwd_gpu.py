@@ -42,6 +42,8 @@ CASES = {
     "mimo_r4_bf16": ("mimo_r4", dict(batch=2, nheads=1, seqlen=67)),
     "mimo_r8_f32": ("mimo_r4", dict(batch=1, nheads=1, seqlen=21, R=8, dtype="f32")),
     "odd_f32": ("tiny_f32", dict(N=6, P=8, R=3, seqlen=37, nheads=2)),
+    "odd_bf16": ("tiny_f32", dict(N=6, P=8, R=3, seqlen=37, nheads=2, dtype="bf16")),
+    "mimo_r8_bf16": ("mimo_r4", dict(batch=1, nheads=2, seqlen=45, R=8)),
     "single_token": ("siso_n64", dict(batch=2, nheads=1, seqlen=1)),
 }
 
