@@ -82,7 +82,8 @@ struct BwdSmem {
         odt = o; o += Q; oA = o; o += Q; olam = o; o += Q; olamn = o; o += Q; odtn = o; o += Q;
         ocA = o; o += Q; ow = o; o += Q; og = o; o += Q; os = o; o += Q; oe = o; o += Q;
         odcA = o; o += Q; odw = o; o += Q; odg = o; o += Q; ods = o; o += Q;
-        ocs = o; o += (size_t)Q * K; osn = o; o += (size_t)Q * K; odph = o; o += (size_t)Q * K;
+        ocs = o; o += (size_t)K * QP1; osn = o; o += (size_t)K * QP1;   // cos / sin, [K][Q + 1]
+        odph = o; o += (size_t)Q * K;
         oth = o; o += (size_t)K * QP1;     // theta of the chunk, [K][Q + 1]
         ored = o; o += kBwdWarps;           // per-warp partial sums
         total = o;
@@ -286,8 +287,8 @@ scan_bwd_kernel(BwdArgs a, int Q, int cp16) {   // cp16: the raw rows and checkp
             if (lane < Q) {
                 float s, c;
                 sincosf(phi, &s, &c);
-                cs[lane * K + k] = c;
-                sn[lane * K + k] = s;
+                cs[k * QP1 + lane] = c;
+                sn[k * QP1 + lane] = s;
             }
         }
         const int e = Qc - 1;
@@ -311,7 +312,7 @@ scan_bwd_kernel(BwdArgs a, int Q, int cp16) {   // cp16: the raw rows and checkp
                     c1 = to_f(stC[q + 1]);
                 }
             }
-            const float c = cs[t * K + k], s = sn[t * K + k];
+            const float c = cs[k * QP1 + t], s = sn[k * QP1 + t];
             const float bt0 = c * b0 + s * b1, bt1 = -s * b0 + c * b1;   // R(-phi) applied to the pair
             Bt[row * N4 + 2 * k] = bt0;
             Bt[row * N4 + 2 * k + 1] = bt1;
@@ -371,7 +372,7 @@ scan_bwd_kernel(BwdArgs a, int Q, int cp16) {   // cp16: the raw rows and checkp
                 float4 u0 = make_float4(0.f, 0.f, 0.f, 0.f), u1 = u0;
                 mm2(Xs + p, Xs + p1, P4, Bt + 4 * n4, N4, 0, QRc, u0, u1);
                 const int k0 = 2 * n4, k1 = min(2 * n4 + 1, K - 1);
-                const float c0 = cs[e * K + k0], s0_ = sn[e * K + k0], c1 = cs[e * K + k1], s1 = sn[e * K + k1];
+                const float c0 = cs[k0 * QP1 + e], s0_ = sn[k0 * QP1 + e], c1 = cs[k1 * QP1 + e], s1 = sn[k1 * QP1 + e];
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
                     const int pp = q ? p1 : p;
@@ -436,9 +437,9 @@ scan_bwd_kernel(BwdArgs a, int Q, int cp16) {   // cp16: the raw rows and checkp
         }
         // D~ = R(-phi_e) D in place (and its transpose), and the angle gradient of the turn R(phi_e):
         // <D, J H'_{c+1}> per pair, over four columns p per thread
-        for (int i = tid; i < K * PC4; i += kBwdThreads) {
-            const int k = i / PC4, p4 = i % PC4, p = 4 * p4;
-            const float cc = cs[e * K + k], ss = sn[e * K + k];
+        for (int i = tid; i < K * PC4; i += kBwdThreads) {   // consecutive threads: consecutive pairs
+            const int k = i % K, p = 4 * (i / K);
+            const float cc = cs[k * QP1 + e], ss = sn[k * QP1 + e];
             const float4 d0 = ld4(Dm + (2 * k) * P4 + p), d1 = ld4(Dm + (2 * k + 1) * P4 + p);
             const float4 t0 = make_float4(cc * d0.x + ss * d1.x, cc * d0.y + ss * d1.y, cc * d0.z + ss * d1.z,
                                           cc * d0.w + ss * d1.w);
@@ -626,7 +627,7 @@ scan_bwd_kernel(BwdArgs a, int Q, int cp16) {   // cp16: the raw rows and checkp
                             const float g0 = gg[2 * pr], g1 = gg[2 * pr + 1];
                             atomicAdd(&dph[j * K + k], g0 * tv[2 * pr + 1] - g1 * tv[2 * pr]);
                             // un-rotate: dB = R(phi) dB~
-                            const float cc = cs[j * K + k], ss = sn[j * K + k];
+                            const float cc = cs[k * QP1 + j], ss = sn[k * QP1 + j];
                             float o0 = cc * g0 - ss * g1, o1 = ss * g0 + cc * g1;
                             if (last) {
                                 o0 += a.dBprev_out[((size_t)bh * R + r) * N + 2 * k];
