@@ -50,7 +50,9 @@ struct BwdSmem {
     size_t oStB, oStC, oStX, oStT, oStY;   // staging (byte offsets from the start of the area)
     size_t odt, oA, olam, olamn, odtn, ocA, ow, og, os, oe, odcA, odw, odg, ods;
     size_t oStg, ocs, osn, odph, oth, ored, total;
-    __host__ __device__ BwdSmem(int Q_, int R_, int N_, int P_, int esz) {
+    // hn2: a second state tile, so that H'_{c+1} (the checkpoint loaded for the chunk after) stays
+    // in shared memory for chunk c
+    __host__ __device__ BwdSmem(int Q_, int R_, int N_, int P_, int esz, bool hn2) {
         Q = Q_; R = R_; N = N_; P = P_; K = N / 2; QR = Q * R;
         NP = rup4(N); PP = rup4(P); QRP = rup4(QR);
         N4 = NP + 4; P4 = PP + 4; QR4 = QRP + 4; QS = QRP + 4; QP1 = Q + 1;
@@ -58,7 +60,7 @@ struct BwdSmem {
         size_t o = 0;
         oD = o;   o += (size_t)N * P4;      // D (true frame); during a chunk D~ = R(-phi_e) D   [N][P4]
         oDtT = o; o += (size_t)PP * N4;     // D~^T                    [PP][N4]
-        oH = o;   o += (size_t)PP * N4;     // H'_c^T; in pass 1 the running state H'^T
+        oH = o;   o += (size_t)PP * N4 * (hn2 ? 2 : 1);   // H'_c^T [2]; in pass 1 the running state H'^T
         oB = o;   o += (size_t)QR * N4;     // B~                      [QR][N4]
         oC = o;   o += (size_t)QR * N4;     // C~
         oBT = o;  o += (size_t)NP * QR4;    // B~^T                    [NP][QR4]
@@ -151,15 +153,16 @@ __device__ __forceinline__ void mm2(const float *A0, const float *A1, int as, co
 // time), so that the tile strides and most loop bounds are constants
 template <typename T, int NT, int PT, int QRT>
 __global__ void __launch_bounds__(kBwdThreads, 1)
-scan_bwd_kernel(BwdArgs a, int Q, int cp16) {   // cp16: the raw rows and checkpoints copy in 16-byte pieces
+scan_bwd_kernel(BwdArgs a, int Q, int cp16, int hn2) {   // cp16: the raw rows and checkpoints copy in 16-byte
+                                                        // pieces; hn2: two state tiles (BwdSmem)
     extern __shared__ __align__(16) float sm[];
-    const BwdSmem Lo(Q, a.R, a.N, a.P, (int)sizeof(T));
+    const BwdSmem Lo(Q, a.R, a.N, a.P, (int)sizeof(T), hn2 != 0);
     const int N = NT ? NT : a.N, P = PT ? PT : a.P, R = a.R, K = N / 2, H = a.H, L = a.L;
     // the same values as Lo's, as constants where the shape is fixed
     const int NP = NT ? rup4(NT) : Lo.NP, PP = PT ? rup4(PT) : Lo.PP;
     const int N4 = NP + 4, P4 = PP + 4, QR4 = QRT ? rup4(QRT) + 4 : Lo.QR4, QS = QR4;
     const int NC4 = NP / 4, PC4 = PP / 4;   // float4 columns of the N- and P-wide tiles
-    float *Dm = sm + Lo.oD, *DtT = sm + Lo.oDtT, *Hs = sm + Lo.oH;
+    float *Dm = sm + Lo.oD, *DtT = sm + Lo.oDtT, *Hs = sm + Lo.oH;   // Hs: pass 1's running state, buffer 0
     float *Bt = sm + Lo.oB, *Ct = sm + Lo.oC, *BtT = sm + Lo.oBT, *Xs = sm + Lo.oX, *XsT = sm + Lo.oXT;
     float *Ys = sm + Lo.oY, *Ye = sm + Lo.oYe;
     float *Sm = sm + Lo.oS, *Zm = sm + Lo.oZ, *T1 = sm + Lo.oT1, *T2 = sm + Lo.oT2, *dMt = sm + Lo.odM;
@@ -411,8 +414,12 @@ scan_bwd_kernel(BwdArgs a, int Q, int cp16) {   // cp16: the raw rows and checkp
             dsv[i] = 0.f;
         }
         for (int i = tid; i < Q * K; i += kBwdThreads) dph[i] = 0.f;
-        // H'_c^T copied in while the chunk's inputs are turned (a second commit group)
+        // H'_c^T copied in while the chunk's inputs are turned (a second commit group).  With two
+        // tiles, chunk c's goes to tile (c ^ nc) & 1: the other one holds H'_{c+1}, which for the
+        // last chunk is pass 1's final state, left in tile 0
         const float *Hc = ckpt + (size_t)c * N * P;
+        float *Hs = sm + Lo.oH + (hn2 ? (size_t)((c ^ nc) & 1) * Lo.PP * N4 : 0);
+        const float *Hn_s = sm + Lo.oH + (size_t)((c ^ nc ^ 1) & 1) * Lo.PP * N4;   // (hn2 only)
         if (cp16) {
             const int pr = N / 4;
             for (int i = tid; i < P * pr; i += kBwdThreads)
@@ -454,7 +461,8 @@ scan_bwd_kernel(BwdArgs a, int Q, int cp16) {   // cp16: the raw rows and checkp
             for (int q = 0; q < 4; ++q) {
                 *reinterpret_cast<float2 *>(DtT + (p + q) * N4 + 2 * k) = make_float2(a0[q], a1[q]);
                 if (p + q < P) {
-                    const float2 hn = *reinterpret_cast<const float2 *>(Hn + (size_t)(p + q) * N + 2 * k);
+                    const float2 hn = hn2 ? *reinterpret_cast<const float2 *>(Hn_s + (p + q) * N4 + 2 * k)
+                                          : *reinterpret_cast<const float2 *>(Hn + (size_t)(p + q) * N + 2 * k);
                     v += e1[q] * hn.x - e0[q] * hn.y;
                 }
             }
@@ -759,13 +767,13 @@ int bwd_chunk(int N, int P, int R, int esz) {
     int Q = 1;
     for (int rows = 32; rows >= 1; rows /= 2) {
         Q = rows / R > 0 ? rows / R : 1;
-        if (BwdSmem(Q, R, N, P, esz).total * sizeof(float) <= 227u * 1024u) break;
+        if (BwdSmem(Q, R, N, P, esz, false).total * sizeof(float) <= 227u * 1024u) break;
     }
     return Q;
 }
 
 size_t bwd_smem_bytes(int N, int P, int R, int esz) {
-    return BwdSmem(bwd_chunk(N, P, R, esz), R, N, P, esz).total * sizeof(float);
+    return BwdSmem(bwd_chunk(N, P, R, esz), R, N, P, esz, false).total * sizeof(float);
 }
 
 size_t bwd_workspace_bytes(int batch, int H, int L, int N, int P, int R, int esz) {
@@ -775,17 +783,20 @@ size_t bwd_workspace_bytes(int batch, int H, int L, int N, int P, int R, int esz
 }
 
 template <auto Kern>
-cudaError_t launch_bwd(const BwdArgs &a, int Q, int cp16, size_t smem, unsigned grid, cudaStream_t s) {
+cudaError_t launch_bwd(const BwdArgs &a, int Q, int cp16, int hn2, size_t smem, unsigned grid, cudaStream_t s) {
     const cudaError_t e = allow_dynamic_smem<Kern>(smem);
     if (e != cudaSuccess) return e;
-    Kern<<<grid, kBwdThreads, smem, s>>>(a, Q, cp16);
+    Kern<<<grid, kBwdThreads, smem, s>>>(a, Q, cp16, hn2);
     return cudaSuccess;
 }
 
 cudaError_t scan_bwd(const BwdArgs &a, cudaStream_t s) {
     const int esz = a.dtype == M3_F32 ? 4 : 2;
     const int Q = bwd_chunk(a.N, a.P, a.R, esz);
-    const size_t smem = bwd_smem_bytes(a.N, a.P, a.R, esz);
+    // a second state tile where it fits
+    const size_t smem2 = BwdSmem(Q, a.R, a.N, a.P, esz, true).total * sizeof(float);
+    const int hn2 = smem2 <= 227u * 1024u;
+    const size_t smem = hn2 ? smem2 : bwd_smem_bytes(a.N, a.P, a.R, esz);
     // 16-byte asynchronous copies: every raw row a whole number of 16-byte pieces, every base
     // pointer on a 16-byte boundary (the workspace is), the checkpoint rows too
     auto al16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
@@ -798,12 +809,12 @@ cudaError_t scan_bwd(const BwdArgs &a, cudaStream_t s) {
     trace_mark(M3_KERNEL_BACKWARD, s, 0);
     // the shapes of the pages' models have their own constant-stride builds (bf16 inputs)
     const int QR = Q * a.R;
-    if (a.dtype == M3_F32) e = launch_bwd<scan_bwd_kernel<float, 0, 0, 0>>(a, Q, cp16, smem, grid, s);
+    if (a.dtype == M3_F32) e = launch_bwd<scan_bwd_kernel<float, 0, 0, 0>>(a, Q, cp16, hn2, smem, grid, s);
     else if (a.N == 64 && a.P == 64 && QR == 32)
-        e = launch_bwd<scan_bwd_kernel<__nv_bfloat16, 64, 64, 32>>(a, Q, cp16, smem, grid, s);
+        e = launch_bwd<scan_bwd_kernel<__nv_bfloat16, 64, 64, 32>>(a, Q, cp16, hn2, smem, grid, s);
     else if (a.N == 128 && a.P == 64 && QR == 16)
-        e = launch_bwd<scan_bwd_kernel<__nv_bfloat16, 128, 64, 16>>(a, Q, cp16, smem, grid, s);
-    else e = launch_bwd<scan_bwd_kernel<__nv_bfloat16, 0, 0, 0>>(a, Q, cp16, smem, grid, s);
+        e = launch_bwd<scan_bwd_kernel<__nv_bfloat16, 128, 64, 16>>(a, Q, cp16, hn2, smem, grid, s);
+    else e = launch_bwd<scan_bwd_kernel<__nv_bfloat16, 0, 0, 0>>(a, Q, cp16, hn2, smem, grid, s);
     if (e != cudaSuccess) return e;
     trace_mark(M3_KERNEL_BACKWARD, s, 1);
     count_launch();

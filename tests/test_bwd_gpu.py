@@ -44,6 +44,8 @@ CASES = {
     "odd_f32": ("tiny_f32", dict(N=6, P=8, R=3, seqlen=37, nheads=2)),
     "odd_bf16": ("tiny_f32", dict(N=6, P=8, R=3, seqlen=37, nheads=2, dtype="bf16")),
     "mimo_r8_bf16": ("mimo_r4", dict(batch=1, nheads=2, seqlen=45, R=8)),
+    # fp32 N = 128: one state tile in shared memory (H'_{c+1} read back from the checkpoints)
+    "siso_n128_f32": ("siso_n128", dict(batch=1, nheads=1, seqlen=40, dtype="f32")),
     "single_token": ("siso_n64", dict(batch=2, nheads=1, seqlen=1)),
 }
 
