@@ -106,6 +106,15 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
+// sin and cos of x: reduced by 2 pi with a two-constant Cody-Waite split to [-pi, pi] (n = round(x / 2 pi)
+// by the 1.5 * 2^23 addition, exact for |x / 2 pi| < 2^22), then the hardware approximations
+__device__ __forceinline__ void sincos_red(float x, float *s, float *c) {
+    const float n = (fmaf(x, 0.15915494309189535f, 12582912.f) - 12582912.f);
+    float r = fmaf(n, -6.28318548202514648f, x);
+    r = fmaf(n, 1.7484555314695172e-7f, r);
+    __sincosf(r, s, c);
+}
+
 __device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
 __device__ __forceinline__ void st4(float *p, float4 v) { *reinterpret_cast<float4 *>(p) = v; }
 __device__ __forceinline__ void fma4(float a, float4 b, float4 &c) {
@@ -289,7 +298,7 @@ scan_bwd_kernel(BwdArgs a, int Q, int cp16, int hn2) {   // cp16: the raw rows a
             }
             if (lane < Q) {
                 float s, c;
-                sincosf(phi, &s, &c);
+                sincos_red(phi, &s, &c);
                 cs[k * QP1 + lane] = c;
                 sn[k * QP1 + lane] = s;
             }
@@ -515,7 +524,7 @@ scan_bwd_kernel(BwdArgs a, int Q, int cp16, int hn2) {   // cp16: the raw rows a
         __syncthreads();
         for (int i = tid; i < QRc * QRc; i += kBwdThreads) {
             const int rt = i / QRc, rj = i % QRc, t = rt / R, j = rj / R;
-            const float m = j < t ? expf(cA[t] - cA[j]) * wv[j] : (j == t ? gv[t] : 0.f);
+            const float m = j < t ? __expf(cA[t] - cA[j]) * wv[j] : (j == t ? gv[t] : 0.f);
             Sm[rt * QS + rj] *= m;
             Zm[rt * QS + rj] *= m;
         }
@@ -523,9 +532,9 @@ scan_bwd_kernel(BwdArgs a, int Q, int cp16, int hn2) {   // cp16: the raw rows a
         for (int t = warp; t < Qc; t += kBwdWarps) {
             float rowv = 0.f, colv = 0.f, dwj = 0.f;
             for (int j = lane; j < Qc; j += 32) {
-                if (j < t) rowv += dMt[t * Q + j] * expf(cA[t] - cA[j]) * wv[j];   // d cA_t
+                if (j < t) rowv += dMt[t * Q + j] * __expf(cA[t] - cA[j]) * wv[j];   // d cA_t
                 if (j > t) {
-                    const float f = expf(cA[j] - cA[t]);
+                    const float f = __expf(cA[j] - cA[t]);
                     colv += dMt[j * Q + t] * f * wv[t];                              // -d cA_t (as column)
                     dwj += dMt[j * Q + t] * f;                                       // d w_t
                 }
