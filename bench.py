@@ -262,14 +262,14 @@ def prefill_line(m3, w, res, steps, hbm_peak, peak_kind, groups=0, y_bytes=4):
 
 
 def traffic_for(kernel, workload):
-    """ncu DRAM bytes per launch recorded under profiles/ for the current kernel source, else None."""
+    """ncu DRAM bytes per launch recorded under profiles/ for the current sources of that kernel, else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
         from selective_state_space_134_b300.build import source_digest
         r = rec.get(f"{kernel}/{workload}")
-        if r and r.get("source_digest") == source_digest():
+        if r and r.get("source_digest") == source_digest(kernel):
             return r["dram_bytes_per_launch"]
     except Exception:
         pass

@@ -41,11 +41,23 @@ def _deps():
                                                                    os.path.abspath(__file__)]
 
 
-def source_digest() -> str:
-    """Short hash of the library sources (kernels, host code, public header)."""
+# the sources each kernel family is built from (its kernels, launch code and shared headers)
+KERNEL_SOURCES = {
+    "prefill_output": ("m3_scan_tc*.cu", "m3_scan_tc.cuh", "m3_tc.cuh", "m3_internal.cuh"),
+    "decode": ("m3_decode.cu", "m3_tc.cuh", "m3_internal.cuh"),
+}
+
+
+def source_digest(kernel: str = "") -> str:
+    """Short hash of the library sources (kernels, host code, public header), or of the sources one
+    kernel family is built from (a KERNEL_SOURCES key)."""
     import hashlib
     h = hashlib.sha256()
-    for p in sorted(sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + [os.path.join(ROOT, "include", "mamba3.h")]):
+    if kernel:
+        files = [p for pat in KERNEL_SOURCES[kernel] for p in glob.glob(os.path.join(CSRC, pat))]
+    else:
+        files = sources() + glob.glob(os.path.join(CSRC, "*.cuh"))
+    for p in sorted(set(files) | {os.path.join(ROOT, "include", "mamba3.h")}):
         h.update(os.path.basename(p).encode())
         with open(p, "rb") as f:
             h.update(f.read())

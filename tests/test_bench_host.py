@@ -63,7 +63,7 @@ def test_prefill_line_reports_the_whole_step():
 
 
 def test_traffic_lookup_requires_the_current_source_digest(tmp_path, monkeypatch):
-    rec = {"decode/decode_n64_r1": {"source_digest": source_digest(), "dram_bytes_per_launch": 123},
+    rec = {"decode/decode_n64_r1": {"source_digest": source_digest("decode"), "dram_bytes_per_launch": 123},
            "decode/decode_n64_r4": {"source_digest": "0" * 16, "dram_bytes_per_launch": 456}}
     prof = tmp_path / "profiles"
     prof.mkdir()
@@ -72,3 +72,9 @@ def test_traffic_lookup_requires_the_current_source_digest(tmp_path, monkeypatch
     assert bench.traffic_for("decode", "decode_n64_r1") == 123
     assert bench.traffic_for("decode", "decode_n64_r4") is None       # recorded for other sources
     assert bench.traffic_for("decode", "decode_n128_r1") is None      # never recorded
+
+
+def test_kernel_digests_cover_their_own_sources():
+    # a kernel's traffic record stays valid when only other kernels' sources change
+    assert source_digest("prefill_output") != source_digest("decode") != source_digest()
+    assert len(source_digest("prefill_output")) == 16
