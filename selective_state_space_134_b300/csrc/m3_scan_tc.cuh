@@ -723,9 +723,14 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
         // ================================================================ epilogue
         const int ew = warp - kEpiW0, eq = warp & 3, eh = ew >> 2;   // lane quadrant, column half
         const uint32_t lane_base = static_cast<uint32_t>(eq * 32) << 16;
-        // state rows owned: row n of the N x P state, columns [32 eh, 32 eh + 32)
+        // state rows loaded at the start: row n of the N x P state, columns [32 eh, 32 eh + 32)
         const bool st_owner = kStateM64 ? (lane < 16) : true;
         const int st_row = kStateM64 ? eq * 16 + lane : eq * 32 + lane;
+        // state rows updated per chunk: N = 64 (the M = 64 layout: 16 lanes per quadrant) uses the 16-lane
+        // TMEM shape, so that every thread holds 16 columns of a row: threads 16-31 take the same rows as
+        // 0-15, 16 columns further; N = 128 keeps one row per thread, 32 columns
+        const int up_row = kStateM64 ? eq * 16 + (lane & 15) : st_row;
+        const int up_col = kStateM64 ? 32 * eh + 16 * (lane >> 4) : 32 * eh;
         // score / output rows owned
         const bool row_ok = kRowsM64 ? (lane < 16) : true;
         const int row = kRowsM64 ? eq * 16 + lane : eq * 32 + lane;
@@ -796,22 +801,26 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                 sigH[slot_parity] = sg;
                 sigH[2 + slot_parity] = pow2_inv(sg);
             }
+            constexpr int kCols = kStateM64 ? 16 : 32;   // columns per thread
             uint32_t hv[32];
-            tmem_ld16_nw(hcol, hv);
-            tmem_ld16_nw(hcol + 16, hv + 16);
-            tmem_wait_ld(hv);
-            if (st_owner) {
+            if constexpr (kStateM64) {
+                tmem_ld16x2_nw(hcol, hv);
+                tmem_wait_ld16(hv);
+            } else {
+                tmem_ld16_nw(hcol, hv);
+                tmem_ld16_nw(hcol + 16, hv + 16);
+                tmem_wait_ld(hv);
+            }
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    uint32_t w4[4];
+            for (int q4 = 0; q4 < kCols / 8; ++q4) {
+                uint32_t w4[4];
 #pragma unroll
-                    for (int e2 = 0; e2 < 4; ++e2) {
-                        const float2 v2 = __fmul2_rn(f2u(hv[8 * q4 + 2 * e2], hv[8 * q4 + 2 * e2 + 1]), f2(sg));
-                        w4[e2] = pack_f16x2(v2.x, v2.y);
-                    }
-                    *reinterpret_cast<uint4 *>(sm + S::oH + sw128(st_row, 32 * eh + 8 * q4)) =
-                        make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                for (int e2 = 0; e2 < 4; ++e2) {
+                    const float2 v2 = __fmul2_rn(f2u(hv[8 * q4 + 2 * e2], hv[8 * q4 + 2 * e2 + 1]), f2(sg));
+                    w4[e2] = pack_f16x2(v2.x, v2.y);
                 }
+                *reinterpret_cast<uint4 *>(sm + S::oH + sw128(up_row, up_col + 8 * q4)) =
+                    make_uint4(w4[0], w4[1], w4[2], w4[3]);
             }
         };
         publish_state(0, hmax);
@@ -897,22 +906,17 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
             // ---- state update: H <- R(phi_e) [exp(cA_e) H + Sn]
             {
                 const float rho = fast_exp2(cA2[e]), invBX = sg[4];
-                const int n = st_row, kk = n >> 1;
-                const float c = st_owner ? v_cos(p)[kk] : 1.f, s = st_owner ? v_sin(p)[kk] : 0.f;
+                const int n = up_row, kk = n >> 1;
+                const float c = v_cos(p)[kk], s = v_sin(p)[kk];
                 const bool odd = n & 1;
                 float *dst = nullptr;
-                if (last_chunk && st_owner && !*abort_flag) {
-                    if (!OUT) dst = a.ws_state + (((size_t)bh * ws_stride + g + 1) * N + n) * kP + 32 * eh;
-                    else if (g == nseg - 1 && a.h_out) dst = a.h_out + ((size_t)bh * N + n) * kP + 32 * eh;
+                if (last_chunk && !*abort_flag) {
+                    if (!OUT) dst = a.ws_state + (((size_t)bh * ws_stride + g + 1) * N + n) * kP + up_col;
+                    else if (g == nseg - 1 && a.h_out) dst = a.h_out + ((size_t)bh * N + n) * kP + up_col;
                 }
                 float m = 0.f;
-#pragma unroll
-                for (int h16 = 0; h16 < 32; h16 += 16) {
-                    uint32_t sh[32];   // [0, 16): Sn, [16, 32): H
-                    tmem_ld16_nw(tmem + lane_base + cSn + 32 * eh + h16, sh);
-                    tmem_ld16_nw(hcol + h16, sh + 16);
-                    tmem_wait_ld(sh);
-                    uint32_t hv[16];
+                // 16 columns: sh [0, 16) Sn, [16, 32) H -> hv; the pair partner (row n ^ 1) is lane ^ 1
+                auto update16 = [&](const uint32_t *sh, uint32_t *hv, float *d) {
                     const float sgn_s = odd ? s : -s;
 #pragma unroll
                     for (int j = 0; j < 16; j += 2) {
@@ -921,17 +925,36 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                         const float2 pv = make_float2(__shfl_xor_sync(0xffffffffu, v.x, 1),
                                                       __shfl_xor_sync(0xffffffffu, v.y, 1));
                         const float2 nv = __ffma2_rn(f2(sgn_s), pv, __fmul2_rn(f2(c), v));
-                        m = fmaxf(m, st_owner ? fmaxf(fabsf(nv.x), fabsf(nv.y)) : 0.f);
+                        m = fmaxf(m, fmaxf(fabsf(nv.x), fabsf(nv.y)));
                         hv[j] = __float_as_uint(nv.x);
                         hv[j + 1] = __float_as_uint(nv.y);
                     }
-                    tmem_st16(hcol + h16, hv);
-                    if (dst) {
+                    if (d) {
 #pragma unroll
                         for (int j = 0; j < 16; j += 4)
-                            *reinterpret_cast<float4 *>(dst + h16 + j) =
+                            *reinterpret_cast<float4 *>(d + j) =
                                 make_float4(__uint_as_float(hv[j]), __uint_as_float(hv[j + 1]),
                                             __uint_as_float(hv[j + 2]), __uint_as_float(hv[j + 3]));
+                    }
+                };
+                if constexpr (kStateM64) {
+                    uint32_t sh[32];
+                    tmem_ld16x2_nw(tmem + lane_base + cSn + 32 * eh, sh);
+                    tmem_ld16x2_nw(hcol, sh + 16);
+                    tmem_wait_ld(sh);
+                    uint32_t hv[16];
+                    update16(sh, hv, dst);
+                    tmem_st16x2(hcol, hv);
+                } else {
+#pragma unroll
+                    for (int h16 = 0; h16 < 32; h16 += 16) {
+                        uint32_t sh[32];
+                        tmem_ld16_nw(tmem + lane_base + cSn + 32 * eh + h16, sh);
+                        tmem_ld16_nw(hcol + h16, sh + 16);
+                        tmem_wait_ld(sh);
+                        uint32_t hv[16];
+                        update16(sh, hv, dst ? dst + h16 : nullptr);
+                        tmem_st16(hcol + h16, *reinterpret_cast<const uint32_t(*)[16]>(hv));
                     }
                 }
                 publish_state((it + 1) & 1, m);
