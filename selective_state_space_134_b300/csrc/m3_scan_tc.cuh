@@ -731,9 +731,10 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
         // 0-15, 16 columns further; N = 128 keeps one row per thread, 32 columns
         const int up_row = kStateM64 ? eq * 16 + (lane & 15) : st_row;
         const int up_col = kStateM64 ? 32 * eh + 16 * (lane >> 4) : 32 * eh;
-        // score / output rows owned
-        const bool row_ok = kRowsM64 ? (lane < 16) : true;
-        const int row = kRowsM64 ? eq * 16 + lane : eq * 32 + lane;
+        // score / output rows owned: with QR = 64 (the M = 64 layout) the 16-lane TMEM shape, threads
+        // 16-31 taking the rows of threads 0-15 sixteen columns further (hf = 1)
+        const int row = kRowsM64 ? eq * 16 + (lane & 15) : eq * 32 + lane;
+        const int hf = kRowsM64 ? lane >> 4 : 0;
         const int ti = row / R;
         // The fp32 state lives in TMEM columns [cH, cH + 64): row n in the lane of the Sn
         // accumulator's row n, column p; this thread holds columns [32 eh, 32 eh + 32).
@@ -847,11 +848,52 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                 constexpr int COLS = QR / 2;    // score columns per thread
                 const int t = min(ti, Q - 1);
                 const float ca = cA2[t], invBC = sg[3];   // tauP / (sB sC)
-                const float gd = row_ok ? gv[t] * invBC : 0.f;
+                const float gd = gv[t] * invBC;
                 // token range of this warp's rows (warp-uniform): blocks past tmax are zero,
                 // blocks ending before tmin need no causal test
                 const int tmax = (kRowsM64 ? eq * 16 + 15 : eq * 32 + 31) / R;
                 const int tmin = (kRowsM64 ? eq * 16 : eq * 32) / R;
+                if constexpr (kRowsM64) {
+                    // one 32-column block per warp half (COLS = 32); this thread: 16 of its columns
+                    static_assert(COLS == 32, "QR = 64");
+                    constexpr int TH = TB / 2;            // tokens of 16 columns
+                    const int cb = eh * COLS, btok = eh * TB, tq0 = hf * TH;
+                    uint32_t p8[8];
+                    if (btok > tmax) {
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) p8[q] = 0u;
+                    } else {
+                        uint32_t sv[16];
+                        tmem_ld16x2_nw(tmem + lane_base + cS + cb, sv);
+                        const float u = (btok < ti) ? fast_exp2(ca - cA2[btok]) * invBC : 0.f;
+                        float um[TH];
+#pragma unroll
+                        for (int q = 0; q < TH; ++q) um[q] = u * vj[btok + tq0 + q];
+                        tmem_wait_ld16(sv);
+                        if (btok + TB <= tmin) {
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) {
+                                const float2 v2 = __fmul2_rn(f2u(sv[2 * q], sv[2 * q + 1]),
+                                                             make_float2(um[(2 * q) / R], um[(2 * q + 1) / R]));
+                                p8[q] = pack_f16x2(v2.x, v2.y);
+                            }
+                        } else {
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) {
+                                float mz[2];
+#pragma unroll
+                                for (int z = 0; z < 2; ++z) {
+                                    const int jq = (2 * q + z) / R;
+                                    const int tj = btok + tq0 + jq;
+                                    mz[z] = (tj < ti) ? um[jq] : ((tj == ti) ? gd : 0.f);
+                                }
+                                const float2 v2 = __fmul2_rn(f2u(sv[2 * q], sv[2 * q + 1]), make_float2(mz[0], mz[1]));
+                                p8[q] = pack_f16x2(v2.x, v2.y);
+                            }
+                        }
+                    }
+                    tmem_st8x2(tmem + lane_base + cP + cb / 2, p8);
+                } else {
 #pragma unroll
                 for (int cc = 0; cc < COLS; cc += 32) {
                     const int cb = eh * COLS + cc;   // first score column of this 32-column block
@@ -865,7 +907,7 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                         tmem_ld16_nw(tmem + lane_base + cS + cb, sv);
                         tmem_ld16_nw(tmem + lane_base + cS + cb + 16, sv + 16);
                         // exp2(cA_t - cA_btok) <= 1 wherever it is used (btok <= tj < t)
-                        const float u = (row_ok && btok < ti) ? fast_exp2(ca - cA2[btok]) * invBC : 0.f;
+                        const float u = (btok < ti) ? fast_exp2(ca - cA2[btok]) * invBC : 0.f;
                         float um[TB];
 #pragma unroll
                         for (int q = 0; q < TB; q += 4) {
@@ -899,6 +941,7 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                         }
                     }
                     tmem_st16(tmem + lane_base + cP + cb / 2, p16);
+                }
                 }
                 fence_before();
                 mbar_arrive(bars + kPReady + p);
@@ -975,16 +1018,21 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                 // done): the prologue may refill them while y is formed
                 mbar_arrive(bars + kEpiDone + p);
                 // y rows go through a shared-memory tile (this thread: row `row`, columns
-                // [32 eh, 32 eh + 32)) and leave by TMA: rows past the sequence end are clipped by
-                // the map, and the global writes are whole lines
+                // [32 eh, 32 eh + 32), or with QR = 64 the 16 of them at 16 hf) and leave by TMA: rows past
+                // the sequence end are clipped by the map, and the global writes are whole lines
 #pragma unroll
-                for (int half16 = 0; half16 < 32; half16 += 16) {
+                for (int half16 = 16 * hf; half16 < 32; half16 += (kRowsM64 ? 32 : 16)) {
                     uint32_t yy[32];   // [0, 16): Ya, [16, 32): Yi
-                    tmem_ld16_nw(tmem + lane_base + cYa + 32 * eh + half16, yy);
-                    tmem_ld16_nw(tmem + lane_base + cYi0 + 64 * p + 32 * eh + half16, yy + 16);
+                    if constexpr (kRowsM64) {
+                        tmem_ld16x2_nw(tmem + lane_base + cYa + 32 * eh, yy);
+                        tmem_ld16x2_nw(tmem + lane_base + cYi0 + 64 * p + 32 * eh, yy + 16);
+                    } else {
+                        tmem_ld16_nw(tmem + lane_base + cYa + 32 * eh + half16, yy);
+                        tmem_ld16_nw(tmem + lane_base + cYi0 + 64 * p + 32 * eh + half16, yy + 16);
+                    }
                     tmem_wait_ld(yy);
                     const uint32_t *ya = yy, *yi = yy + 16;
-                    if (row_ok) {
+                    {
                         if constexpr (YB == 4) {
                             // fp32: two halves [QR][32] of 128-byte rows
                             unsigned char *ys = sm + S::oYs + eh * (QR * 128);

@@ -132,6 +132,15 @@ __device__ __forceinline__ void tmem_st16x2(uint32_t taddr, const uint32_t *r) {
           "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
         : "memory");
 }
+// 8 columns of the 16-lane shape: threads 0-15 store lanes [0, 16) at columns [c, c + 8), threads
+// 16-31 the same lanes at [c + 8, c + 16); waits for completion
+__device__ __forceinline__ void tmem_st8x2(uint32_t taddr, const uint32_t *r) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.16x32bx2.x8.b32 [%0], 8, {%1,%2,%3,%4,%5,%6,%7,%8};\n"
+        "tcgen05.wait::st.sync.aligned;\n"
+        ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+        : "memory");
+}
 // waits for this thread's outstanding TMEM loads (16 registers tied to the wait)
 __device__ __forceinline__ void tmem_wait_ld16(uint32_t *r) {
     asm volatile("tcgen05.wait::ld.sync.aligned;\n"
