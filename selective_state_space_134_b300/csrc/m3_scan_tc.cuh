@@ -728,9 +728,12 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
         const int st_row = kStateM64 ? eq * 16 + lane : eq * 32 + lane;
         // state rows updated per chunk: N = 64 (the M = 64 layout: 16 lanes per quadrant) uses the 16-lane
         // TMEM shape, so that every thread holds 16 columns of a row: threads 16-31 take the same rows as
-        // 0-15, 16 columns further; N = 128 keeps one row per thread, 32 columns
-        const int up_row = kStateM64 ? eq * 16 + (lane & 15) : st_row;
-        const int up_col = kStateM64 ? 32 * eh + 16 * (lane >> 4) : 32 * eh;
+        // 0-15, 16 columns further; N = 128 keeps one row per thread, 32 columns.  The BC-normalised MIMO
+        // builds keep half the lanes idle instead (at their register cap the 16-lane form was slower)
+        constexpr bool kState16 = kStateM64 && !(BCN && R > 1);
+        const bool up_own = (kStateM64 && !kState16) ? lane < 16 : true;
+        const int up_row = kState16 ? eq * 16 + (lane & 15) : st_row;
+        const int up_col = kState16 ? 32 * eh + 16 * (lane >> 4) : 32 * eh;
         // score / output rows owned: with QR = 64 (the M = 64 layout) the 16-lane TMEM shape, threads
         // 16-31 taking the rows of threads 0-15 sixteen columns further (hf = 1)
         const int row = kRowsM64 ? eq * 16 + (lane & 15) : eq * 32 + lane;
@@ -802,9 +805,9 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                 sigH[slot_parity] = sg;
                 sigH[2 + slot_parity] = pow2_inv(sg);
             }
-            constexpr int kCols = kStateM64 ? 16 : 32;   // columns per thread
+            constexpr int kCols = kState16 ? 16 : 32;   // columns per thread
             uint32_t hv[32];
-            if constexpr (kStateM64) {
+            if constexpr (kState16) {
                 tmem_ld16x2_nw(hcol, hv);
                 tmem_wait_ld16(hv);
             } else {
@@ -814,6 +817,7 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
             }
 #pragma unroll
             for (int q4 = 0; q4 < kCols / 8; ++q4) {
+                if (!up_own) break;
                 uint32_t w4[4];
 #pragma unroll
                 for (int e2 = 0; e2 < 4; ++e2) {
@@ -950,10 +954,10 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
             {
                 const float rho = fast_exp2(cA2[e]), invBX = sg[4];
                 const int n = up_row, kk = n >> 1;
-                const float c = v_cos(p)[kk], s = v_sin(p)[kk];
+                const float c = up_own ? v_cos(p)[kk] : 1.f, s = up_own ? v_sin(p)[kk] : 0.f;
                 const bool odd = n & 1;
                 float *dst = nullptr;
-                if (last_chunk && !*abort_flag) {
+                if (last_chunk && up_own && !*abort_flag) {
                     if (!OUT) dst = a.ws_state + (((size_t)bh * ws_stride + g + 1) * N + n) * kP + up_col;
                     else if (g == nseg - 1 && a.h_out) dst = a.h_out + ((size_t)bh * N + n) * kP + up_col;
                 }
@@ -968,7 +972,7 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                         const float2 pv = make_float2(__shfl_xor_sync(0xffffffffu, v.x, 1),
                                                       __shfl_xor_sync(0xffffffffu, v.y, 1));
                         const float2 nv = __ffma2_rn(f2(sgn_s), pv, __fmul2_rn(f2(c), v));
-                        m = fmaxf(m, fmaxf(fabsf(nv.x), fabsf(nv.y)));
+                        m = fmaxf(m, up_own ? fmaxf(fabsf(nv.x), fabsf(nv.y)) : 0.f);
                         hv[j] = __float_as_uint(nv.x);
                         hv[j + 1] = __float_as_uint(nv.y);
                     }
@@ -980,7 +984,7 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                                             __uint_as_float(hv[j + 2]), __uint_as_float(hv[j + 3]));
                     }
                 };
-                if constexpr (kStateM64) {
+                if constexpr (kState16) {
                     uint32_t sh[32];
                     tmem_ld16x2_nw(tmem + lane_base + cSn + 32 * eh, sh);
                     tmem_ld16x2_nw(hcol, sh + 16);
