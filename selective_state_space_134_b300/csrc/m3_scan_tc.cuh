@@ -898,7 +898,7 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                     }
                     tmem_st8x2(tmem + lane_base + cP + cb / 2, p8);
                 } else {
-#pragma unroll
+#pragma unroll 1
                 for (int cc = 0; cc < COLS; cc += 32) {
                     const int cb = eh * COLS + cc;   // first score column of this 32-column block
                     const int btok = (cb / 32) * TB; // first token of the block
@@ -1024,7 +1024,7 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                 // y rows go through a shared-memory tile (this thread: row `row`, columns
                 // [32 eh, 32 eh + 32), or with QR = 64 the 16 of them at 16 hf) and leave by TMA: rows past
                 // the sequence end are clipped by the map, and the global writes are whole lines
-#pragma unroll
+#pragma unroll 1
                 for (int half16 = 16 * hf; half16 < 32; half16 += (kRowsM64 ? 32 : 16)) {
                     uint32_t yy[32];   // [0, 16): Ya, [16, 32): Yi
                     if constexpr (kRowsM64) {
