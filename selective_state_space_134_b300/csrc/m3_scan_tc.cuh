@@ -575,90 +575,172 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                 for (int sg = 0; sg < Cf::NSEG - 1; ++sg) phi += (sg < seg) ? part[sg * K + k] : 0.f;
                 unsigned char *bs = slot + S::sB + slab * (QR * 128);
                 unsigned char *cs = slot + S::sC + slab * (QR * 128);
-                // angles of all the thread's tokens first (a short FMA chain), then
-                // independent rotations the scheduler can overlap
-                float ph[TPS];
-#pragma unroll
-                for (int i = 0; i < TPS; ++i) {
-                    phi = fmaf(dd[i], th[i], phi);
-                    ph[i] = phi;
-                }
-                const int ie = e - seg * TPS;   // the chunk's last token, if it is this thread's
-                // this thread's BC gains (entries 2k, 2k + 1 of B and of C)
-                float2 wkB = f2(1.f), wkC = f2(1.f);
-                if constexpr (BCN) {
-                    wkB = *reinterpret_cast<const float2 *>(bw + 2 * k);
-                    wkC = *reinterpret_cast<const float2 *>(bw + N + 2 * k);
-                }
-                // raw words are loaded kLA tokens ahead of their use (each load precedes, in
-                // program order, the in-place stores it could alias, so none waits on a store)
-                uint32_t rb[TPS * R], rc[TPS * R];
-                constexpr int kLA = TPS < 4 ? TPS : 4;
-                auto load_tok = [&](int i) {
-#pragma unroll
-                    for (int r = 0; r < R; ++r) {
-                        const uint32_t off = sw128((seg * TPS + i) * R + r, 2 * lane);
-                        rb[i * R + r] = *reinterpret_cast<const uint32_t *>(bs + off);
-                        if (OUT) rc[i * R + r] = *reinterpret_cast<const uint32_t *>(cs + off);
+                if constexpr (R == 1 || N != 64) {
+                    // SISO (and N = 128): fully unrolled, the raw words loaded a few tokens ahead
+                    // angles of all the thread's tokens first (a short FMA chain), then
+                    // independent rotations the scheduler can overlap
+                    float ph[TPS];
+    #pragma unroll
+                    for (int i = 0; i < TPS; ++i) {
+                        phi = fmaf(dd[i], th[i], phi);
+                        ph[i] = phi;
                     }
-                };
-#pragma unroll
-                for (int i = 0; i < kLA; ++i) load_tok(i);
-                // two tokens at a time on packed fp32.  sin / cos: Cody-Waite reduction by 2 pi
-                // (two-constant split) to [-pi, pi], n = round(x / 2 pi) by the 1.5 * 2^23
-                // addition (exact for |x / 2 pi| < 2^22, and on the FMA pipe rather than the
-                // conversion unit), then the hardware approximations there
-                static_assert(TPS % 2 == 0, "token pairs");
-#pragma unroll
-                for (int i = 0; i < TPS; i += 2) {
-                    if (i + kLA < TPS) load_tok(i + kLA);
-                    if (i + kLA + 1 < TPS) load_tok(i + kLA + 1);
-                    const float2 x2 = make_float2(ph[i], ph[i + 1]);
-                    const float2 n2 = __fadd2_rn(__ffma2_rn(x2, f2(0.15915494309189535f), f2(12582912.f)),
-                                                 f2(-12582912.f));
-                    float2 r2 = __ffma2_rn(n2, f2(-6.28318548202514648f), x2);
-                    r2 = __ffma2_rn(n2, f2(1.7484555314695172e-7f), r2);
-                    float c0, s0, c1, s1;
-                    __sincosf(r2.x, &s0, &c0);
-                    __sincosf(r2.y, &s1, &c1);
-                    if (i == ie || i + 1 == ie) {   // the chunk's last token: rotation of the state at the chunk end
-                        const bool first = i == ie;
-                        v_cos(p)[k] = first ? c0 : c1;
-                        v_sin(p)[k] = first ? s0 : s1;
-                        if (!OUT) tot[1 + k] += first ? ph[i] : ph[i + 1];
+                    const int ie = e - seg * TPS;   // the chunk's last token, if it is this thread's
+                    // this thread's BC gains (entries 2k, 2k + 1 of B and of C)
+                    float2 wkB = f2(1.f), wkC = f2(1.f);
+                    if constexpr (BCN) {
+                        wkB = *reinterpret_cast<const float2 *>(bw + 2 * k);
+                        wkC = *reinterpret_cast<const float2 *>(bw + N + 2 * k);
                     }
-                    const float2 cb = __fmul2_rn(make_float2(c0, c1), f2(sgB));
-                    const float2 sb = __fmul2_rn(make_float2(s0, s1), f2(sgB));
-                    const float2 nsb = __fmul2_rn(make_float2(s0, s1), f2(-sgB));
-                    const int t = seg * TPS + i;
-                    const bool valid0 = t < Qc, valid1 = t + 1 < Qc;
-#pragma unroll
-                    for (int r = 0; r < R; ++r) {
-                        const uint32_t off0 = sw128(t * R + r, 2 * lane), off1 = sw128((t + 1) * R + r, 2 * lane);
-                        const uint32_t vb0 = rb[i * R + r], vb1 = rb[(i + 1) * R + r];
-                        float2 b0 = f2u(vb0 << 16, vb1 << 16), b1 = f2u(vb0 & 0xFFFF0000u, vb1 & 0xFFFF0000u);
-                        // BC normalisation of the two tokens' rows: v * (w / rms) + bias, entries 2k, 2k + 1
-                        auto bc_norm = [&](int tsr, float2 &e0, float2 &e1) {
-                            const float *iv = bss + tsr * QR + t * R + r;
-                            const float2 inv = make_float2(iv[0], iv[R]);
-                            const float2 wk = tsr ? wkC : wkB;
-                            const float2 bk = *reinterpret_cast<const float2 *>(bb + (tsr * R + r) * N + 2 * k);
-                            e0 = __ffma2_rn(e0, __fmul2_rn(inv, f2(wk.x)), f2(bk.x));
-                            e1 = __ffma2_rn(e1, __fmul2_rn(inv, f2(wk.y)), f2(bk.y));
-                        };
-                        if constexpr (BCN) bc_norm(0, b0, b1);
-                        const float2 o0 = __ffma2_rn(cb, b0, __fmul2_rn(sb, b1));
-                        const float2 o1 = __ffma2_rn(cb, b1, __fmul2_rn(nsb, b0));
-                        *reinterpret_cast<uint32_t *>(bs + off0) = valid0 ? pack_f16x2(o0.x, o1.x) : 0u;
-                        *reinterpret_cast<uint32_t *>(bs + off1) = valid1 ? pack_f16x2(o0.y, o1.y) : 0u;
-                        if (OUT) {
-                            const uint32_t vc0 = rc[i * R + r], vc1 = rc[(i + 1) * R + r];
-                            float2 e0 = f2u(vc0 << 16, vc1 << 16), e1 = f2u(vc0 & 0xFFFF0000u, vc1 & 0xFFFF0000u);
-                            if constexpr (BCN) bc_norm(1, e0, e1);
-                            const float2 q0 = __ffma2_rn(cb, e0, __fmul2_rn(sb, e1));
-                            const float2 q1 = __ffma2_rn(cb, e1, __fmul2_rn(nsb, e0));
-                            *reinterpret_cast<uint32_t *>(cs + off0) = valid0 ? pack_f16x2(q0.x, q1.x) : 0u;
-                            *reinterpret_cast<uint32_t *>(cs + off1) = valid1 ? pack_f16x2(q0.y, q1.y) : 0u;
+                    // raw words are loaded kLA tokens ahead of their use (each load precedes, in
+                    // program order, the in-place stores it could alias, so none waits on a store)
+                    uint32_t rb[TPS * R], rc[TPS * R];
+                    constexpr int kLA = TPS < 4 ? TPS : 4;
+                    auto load_tok = [&](int i) {
+    #pragma unroll
+                        for (int r = 0; r < R; ++r) {
+                            const uint32_t off = sw128((seg * TPS + i) * R + r, 2 * lane);
+                            rb[i * R + r] = *reinterpret_cast<const uint32_t *>(bs + off);
+                            if (OUT) rc[i * R + r] = *reinterpret_cast<const uint32_t *>(cs + off);
+                        }
+                    };
+    #pragma unroll
+                    for (int i = 0; i < kLA; ++i) load_tok(i);
+                    // two tokens at a time on packed fp32.  sin / cos: Cody-Waite reduction by 2 pi
+                    // (two-constant split) to [-pi, pi], n = round(x / 2 pi) by the 1.5 * 2^23
+                    // addition (exact for |x / 2 pi| < 2^22, and on the FMA pipe rather than the
+                    // conversion unit), then the hardware approximations there
+                    static_assert(TPS % 2 == 0, "token pairs");
+    #pragma unroll
+                    for (int i = 0; i < TPS; i += 2) {
+                        if (i + kLA < TPS) load_tok(i + kLA);
+                        if (i + kLA + 1 < TPS) load_tok(i + kLA + 1);
+                        const float2 x2 = make_float2(ph[i], ph[i + 1]);
+                        const float2 n2 = __fadd2_rn(__ffma2_rn(x2, f2(0.15915494309189535f), f2(12582912.f)),
+                                                     f2(-12582912.f));
+                        float2 r2 = __ffma2_rn(n2, f2(-6.28318548202514648f), x2);
+                        r2 = __ffma2_rn(n2, f2(1.7484555314695172e-7f), r2);
+                        float c0, s0, c1, s1;
+                        __sincosf(r2.x, &s0, &c0);
+                        __sincosf(r2.y, &s1, &c1);
+                        if (i == ie || i + 1 == ie) {   // the chunk's last token: rotation of the state at the chunk end
+                            const bool first = i == ie;
+                            v_cos(p)[k] = first ? c0 : c1;
+                            v_sin(p)[k] = first ? s0 : s1;
+                            if (!OUT) tot[1 + k] += first ? ph[i] : ph[i + 1];
+                        }
+                        const float2 cb = __fmul2_rn(make_float2(c0, c1), f2(sgB));
+                        const float2 sb = __fmul2_rn(make_float2(s0, s1), f2(sgB));
+                        const float2 nsb = __fmul2_rn(make_float2(s0, s1), f2(-sgB));
+                        const int t = seg * TPS + i;
+                        const bool valid0 = t < Qc, valid1 = t + 1 < Qc;
+    #pragma unroll
+                        for (int r = 0; r < R; ++r) {
+                            const uint32_t off0 = sw128(t * R + r, 2 * lane), off1 = sw128((t + 1) * R + r, 2 * lane);
+                            const uint32_t vb0 = rb[i * R + r], vb1 = rb[(i + 1) * R + r];
+                            float2 b0 = f2u(vb0 << 16, vb1 << 16), b1 = f2u(vb0 & 0xFFFF0000u, vb1 & 0xFFFF0000u);
+                            // BC normalisation of the two tokens' rows: v * (w / rms) + bias, entries 2k, 2k + 1
+                            auto bc_norm = [&](int tsr, float2 &e0, float2 &e1) {
+                                const float *iv = bss + tsr * QR + t * R + r;
+                                const float2 inv = make_float2(iv[0], iv[R]);
+                                const float2 wk = tsr ? wkC : wkB;
+                                const float2 bk = *reinterpret_cast<const float2 *>(bb + (tsr * R + r) * N + 2 * k);
+                                e0 = __ffma2_rn(e0, __fmul2_rn(inv, f2(wk.x)), f2(bk.x));
+                                e1 = __ffma2_rn(e1, __fmul2_rn(inv, f2(wk.y)), f2(bk.y));
+                            };
+                            if constexpr (BCN) bc_norm(0, b0, b1);
+                            const float2 o0 = __ffma2_rn(cb, b0, __fmul2_rn(sb, b1));
+                            const float2 o1 = __ffma2_rn(cb, b1, __fmul2_rn(nsb, b0));
+                            *reinterpret_cast<uint32_t *>(bs + off0) = valid0 ? pack_f16x2(o0.x, o1.x) : 0u;
+                            *reinterpret_cast<uint32_t *>(bs + off1) = valid1 ? pack_f16x2(o0.y, o1.y) : 0u;
+                            if (OUT) {
+                                const uint32_t vc0 = rc[i * R + r], vc1 = rc[(i + 1) * R + r];
+                                float2 e0 = f2u(vc0 << 16, vc1 << 16), e1 = f2u(vc0 & 0xFFFF0000u, vc1 & 0xFFFF0000u);
+                                if constexpr (BCN) bc_norm(1, e0, e1);
+                                const float2 q0 = __ffma2_rn(cb, e0, __fmul2_rn(sb, e1));
+                                const float2 q1 = __ffma2_rn(cb, e1, __fmul2_rn(nsb, e0));
+                                *reinterpret_cast<uint32_t *>(cs + off0) = valid0 ? pack_f16x2(q0.x, q1.x) : 0u;
+                                *reinterpret_cast<uint32_t *>(cs + off1) = valid1 ? pack_f16x2(q0.y, q1.y) : 0u;
+                            }
+                        }
+                    }
+                } else {
+                    // MIMO with N = 64: a few tokens per thread; one token pair per iteration of a rolled
+                    // loop keeps the code (and the instruction-cache footprint) small (+2 % there, -1 %
+                    // with N = 128)
+                    const int ie = e - seg * TPS;   // the chunk's last token, if it is this thread's
+                    // this thread's BC gains (entries 2k, 2k + 1 of B and of C)
+                    float2 wkB = f2(1.f), wkC = f2(1.f);
+                    if constexpr (BCN) {
+                        wkB = *reinterpret_cast<const float2 *>(bw + 2 * k);
+                        wkC = *reinterpret_cast<const float2 *>(bw + N + 2 * k);
+                    }
+                    // two tokens at a time on packed fp32, each pair's angles and raw words loaded in its
+                    // own iteration (the loop stays rolled: the kernel's code must fit the instruction
+                    // cache).  sin / cos: Cody-Waite reduction by 2 pi (two-constant split) to [-pi, pi],
+                    // n = round(x / 2 pi) by the 1.5 * 2^23 addition (exact for |x / 2 pi| < 2^22, and on
+                    // the FMA pipe rather than the conversion unit), then the hardware approximations there
+                    static_assert(TPS % 2 == 0, "token pairs");
+    #pragma unroll 2
+                    for (int i = 0; i < TPS; i += 2) {
+                        const int t = seg * TPS + i;
+                        const float ph0 = fmaf(dts[t], __bfloat162float(rawT[t * K + k]), phi);
+                        phi = fmaf(dts[t + 1], __bfloat162float(rawT[(t + 1) * K + k]), ph0);
+                        uint32_t rb[2 * R], rc[2 * R];
+    #pragma unroll
+                        for (int z = 0; z < 2; ++z)
+    #pragma unroll
+                            for (int r = 0; r < R; ++r) {
+                                const uint32_t off = sw128((t + z) * R + r, 2 * lane);
+                                rb[z * R + r] = *reinterpret_cast<const uint32_t *>(bs + off);
+                                if (OUT) rc[z * R + r] = *reinterpret_cast<const uint32_t *>(cs + off);
+                            }
+                        const float2 x2 = make_float2(ph0, phi);
+                        const float2 n2 = __fadd2_rn(__ffma2_rn(x2, f2(0.15915494309189535f), f2(12582912.f)),
+                                                     f2(-12582912.f));
+                        float2 r2 = __ffma2_rn(n2, f2(-6.28318548202514648f), x2);
+                        r2 = __ffma2_rn(n2, f2(1.7484555314695172e-7f), r2);
+                        float c0, s0, c1, s1;
+                        __sincosf(r2.x, &s0, &c0);
+                        __sincosf(r2.y, &s1, &c1);
+                        if (i == ie || i + 1 == ie) {   // the chunk's last token: rotation of the state at the chunk end
+                            const bool first = i == ie;
+                            v_cos(p)[k] = first ? c0 : c1;
+                            v_sin(p)[k] = first ? s0 : s1;
+                            if (!OUT) tot[1 + k] += first ? ph0 : phi;
+                        }
+                        const float2 cb = __fmul2_rn(make_float2(c0, c1), f2(sgB));
+                        const float2 sb = __fmul2_rn(make_float2(s0, s1), f2(sgB));
+                        const float2 nsb = __fmul2_rn(make_float2(s0, s1), f2(-sgB));
+                        const bool valid0 = t < Qc, valid1 = t + 1 < Qc;
+    #pragma unroll
+                        for (int r = 0; r < R; ++r) {
+                            const uint32_t off0 = sw128(t * R + r, 2 * lane), off1 = sw128((t + 1) * R + r, 2 * lane);
+                            const uint32_t vb0 = rb[r], vb1 = rb[R + r];
+                            float2 b0 = f2u(vb0 << 16, vb1 << 16), b1 = f2u(vb0 & 0xFFFF0000u, vb1 & 0xFFFF0000u);
+                            // BC normalisation of the two tokens' rows: v * (w / rms) + bias, entries 2k, 2k + 1
+                            auto bc_norm = [&](int tsr, float2 &e0, float2 &e1) {
+                                const float *iv = bss + tsr * QR + t * R + r;
+                                const float2 inv = make_float2(iv[0], iv[R]);
+                                const float2 wk = tsr ? wkC : wkB;
+                                const float2 bk = *reinterpret_cast<const float2 *>(bb + (tsr * R + r) * N + 2 * k);
+                                e0 = __ffma2_rn(e0, __fmul2_rn(inv, f2(wk.x)), f2(bk.x));
+                                e1 = __ffma2_rn(e1, __fmul2_rn(inv, f2(wk.y)), f2(bk.y));
+                            };
+                            if constexpr (BCN) bc_norm(0, b0, b1);
+                            const float2 o0 = __ffma2_rn(cb, b0, __fmul2_rn(sb, b1));
+                            const float2 o1 = __ffma2_rn(cb, b1, __fmul2_rn(nsb, b0));
+                            *reinterpret_cast<uint32_t *>(bs + off0) = valid0 ? pack_f16x2(o0.x, o1.x) : 0u;
+                            *reinterpret_cast<uint32_t *>(bs + off1) = valid1 ? pack_f16x2(o0.y, o1.y) : 0u;
+                            if (OUT) {
+                                const uint32_t vc0 = rc[r], vc1 = rc[R + r];
+                                float2 e0 = f2u(vc0 << 16, vc1 << 16), e1 = f2u(vc0 & 0xFFFF0000u, vc1 & 0xFFFF0000u);
+                                if constexpr (BCN) bc_norm(1, e0, e1);
+                                const float2 q0 = __ffma2_rn(cb, e0, __fmul2_rn(sb, e1));
+                                const float2 q1 = __ffma2_rn(cb, e1, __fmul2_rn(nsb, e0));
+                                *reinterpret_cast<uint32_t *>(cs + off0) = valid0 ? pack_f16x2(q0.x, q1.x) : 0u;
+                                *reinterpret_cast<uint32_t *>(cs + off1) = valid1 ? pack_f16x2(q0.y, q1.y) : 0u;
+                            }
                         }
                     }
                 }
