@@ -580,7 +580,7 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                     // angles of all the thread's tokens first (a short FMA chain), then
                     // independent rotations the scheduler can overlap
                     float ph[TPS];
-    #pragma unroll
+#pragma unroll
                     for (int i = 0; i < TPS; ++i) {
                         phi = fmaf(dd[i], th[i], phi);
                         ph[i] = phi;
@@ -597,21 +597,21 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                     uint32_t rb[TPS * R], rc[TPS * R];
                     constexpr int kLA = TPS < 4 ? TPS : 4;
                     auto load_tok = [&](int i) {
-    #pragma unroll
+#pragma unroll
                         for (int r = 0; r < R; ++r) {
                             const uint32_t off = sw128((seg * TPS + i) * R + r, 2 * lane);
                             rb[i * R + r] = *reinterpret_cast<const uint32_t *>(bs + off);
                             if (OUT) rc[i * R + r] = *reinterpret_cast<const uint32_t *>(cs + off);
                         }
                     };
-    #pragma unroll
+#pragma unroll
                     for (int i = 0; i < kLA; ++i) load_tok(i);
                     // two tokens at a time on packed fp32.  sin / cos: Cody-Waite reduction by 2 pi
                     // (two-constant split) to [-pi, pi], n = round(x / 2 pi) by the 1.5 * 2^23
                     // addition (exact for |x / 2 pi| < 2^22, and on the FMA pipe rather than the
                     // conversion unit), then the hardware approximations there
                     static_assert(TPS % 2 == 0, "token pairs");
-    #pragma unroll
+#pragma unroll
                     for (int i = 0; i < TPS; i += 2) {
                         if (i + kLA < TPS) load_tok(i + kLA);
                         if (i + kLA + 1 < TPS) load_tok(i + kLA + 1);
@@ -634,7 +634,7 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                         const float2 nsb = __fmul2_rn(make_float2(s0, s1), f2(-sgB));
                         const int t = seg * TPS + i;
                         const bool valid0 = t < Qc, valid1 = t + 1 < Qc;
-    #pragma unroll
+#pragma unroll
                         for (int r = 0; r < R; ++r) {
                             const uint32_t off0 = sw128(t * R + r, 2 * lane), off1 = sw128((t + 1) * R + r, 2 * lane);
                             const uint32_t vb0 = rb[i * R + r], vb1 = rb[(i + 1) * R + r];
@@ -681,15 +681,15 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                     // n = round(x / 2 pi) by the 1.5 * 2^23 addition (exact for |x / 2 pi| < 2^22, and on
                     // the FMA pipe rather than the conversion unit), then the hardware approximations there
                     static_assert(TPS % 2 == 0, "token pairs");
-    #pragma unroll 2
+#pragma unroll 2
                     for (int i = 0; i < TPS; i += 2) {
                         const int t = seg * TPS + i;
                         const float ph0 = fmaf(dts[t], __bfloat162float(rawT[t * K + k]), phi);
                         phi = fmaf(dts[t + 1], __bfloat162float(rawT[(t + 1) * K + k]), ph0);
                         uint32_t rb[2 * R], rc[2 * R];
-    #pragma unroll
+#pragma unroll
                         for (int z = 0; z < 2; ++z)
-    #pragma unroll
+#pragma unroll
                             for (int r = 0; r < R; ++r) {
                                 const uint32_t off = sw128((t + z) * R + r, 2 * lane);
                                 rb[z * R + r] = *reinterpret_cast<const uint32_t *>(bs + off);
@@ -713,7 +713,7 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                         const float2 sb = __fmul2_rn(make_float2(s0, s1), f2(sgB));
                         const float2 nsb = __fmul2_rn(make_float2(s0, s1), f2(-sgB));
                         const bool valid0 = t < Qc, valid1 = t + 1 < Qc;
-    #pragma unroll
+#pragma unroll
                         for (int r = 0; r < R; ++r) {
                             const uint32_t off0 = sw128(t * R + r, 2 * lane), off1 = sw128((t + 1) * R + r, 2 * lane);
                             const uint32_t vb0 = rb[r], vb1 = rb[R + r];
