@@ -128,9 +128,11 @@ __device__ __forceinline__ float4 axpy4(float a, float4 x, float4 y) {   // a x 
 }
 
 // c0 += sum_k A0[k as] B[k bs .. + 3] for k in [k0, k1) (one output row, four columns); four steps
-// at a time, so that with constant strides every load takes an immediate offset
+// at a time, so that with constant strides every load takes an immediate offset, in a loop kept
+// rolled (with constant bounds a full unroll of every call site crowds the instruction cache)
 __device__ __forceinline__ void mm1(const float *A0, int as, const float *B, int bs, int k0, int k1, float4 &c0) {
     int k = k0;
+#pragma unroll 1
     for (; k + 4 <= k1; k += 4) {
         const float *a = A0 + k * as, *bp = B + k * bs;
 #pragma unroll
@@ -142,6 +144,7 @@ __device__ __forceinline__ void mm1(const float *A0, int as, const float *B, int
 __device__ __forceinline__ void mm2(const float *A0, const float *A1, int as, const float *B, int bs, int k0, int k1,
                                     float4 &c0, float4 &c1) {
     int k = k0;
+#pragma unroll 1
     for (; k + 4 <= k1; k += 4) {
         const float *a0 = A0 + k * as, *a1 = A1 + k * as, *bp = B + k * bs;
 #pragma unroll
