@@ -73,6 +73,7 @@ struct ScanPlan {
     int seglen;   // tokens per segment (multiple of Q), last one may be shorter
     int nsub;     // state-pass pieces per segment (the pass that feeds the segment starts)
     int path;     // kPathSimt or kPathTc
+    int bal;      // > 0: the balanced output pass on this many CTAs (tensor-core path, one segment)
     size_t ws_bytes;
 };
 enum { kPathSimt = 0, kPathTc = 1 };

@@ -372,6 +372,7 @@ size_t scan_workspace_bytes(int batch, int H, int N, int P, int nseg) {
 }
 
 bool simt_plan(const m3_dims &d, int sms, ScanPlan *pl) {
+    pl->bal = 0;
     if (d.ngroups > 0 && d.ngroups != d.nheads) return false;   // grouped B / C: tensor-core path only
     const int R = d.rank, N = d.dstate, P = d.headdim;
     const size_t smem_cap = 200 * 1024;

@@ -67,6 +67,18 @@ bool tc_plan(const m3_dims &d, int sms, ScanPlan *pl) {
     pl->path = kPathTc;
     pl->ws_bytes = scan_workspace_bytes(d.batch, d.nheads, d.dstate, d.headdim,
                                         nseg > 1 ? (nseg - 1) * nsub + 1 : 1);
+    // More sequences than SMs in a last wave that would leave a tenth of the machine idle: the balanced
+    // output pass (one CTA per SM, equal shares of all sequences' chunks, a state slot and a flag per
+    // CTA).  Not with the chunk-rule tile (its own instantiation) or BC normalisation (falls back).
+    pl->bal = 0;
+    if (nseg == 1 && seqs > sms && Q * d.rank == (d.dstate == 64 ? 128 : 64)) {
+        const long long waves = (seqs + sms - 1) / sms;
+        if ((double)seqs / (double)(waves * sms) < 0.9) {
+            pl->bal = sms;
+            const size_t need = (size_t)sms * d.dstate * d.headdim * sizeof(float) + (size_t)sms * 8;
+            if (need > pl->ws_bytes) pl->ws_bytes = need;
+        }
+    }
     return true;
 }
 

@@ -35,6 +35,8 @@
 #include "m3_internal.cuh"
 #include "m3_tc.cuh"
 
+#include <atomic>
+#include <chrono>
 #include <mutex>
 #include <type_traits>
 
@@ -170,6 +172,16 @@ struct TcMaps {
     CUtensorMap B, C, X, T, Y;
 };
 
+// hand-off flags of the balanced plan (a CTA's end state of a sequence head, to the CTA holding its tail)
+__device__ __forceinline__ void flag_release(unsigned long long *f, unsigned long long v) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(f), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long flag_acquire(const unsigned long long *f) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(f) : "memory");
+    return v;
+}
+
 enum Bar {
     kRawFull = 0,      // [2] TMA -> prologue (transaction bytes)
     kRawEmpty = 2,     // [2] MMAs done with a raw slot -> producer
@@ -182,11 +194,17 @@ enum Bar {
 };
 
 // YT: element type of y (an m3_dtype; OUT only).  BCN: B and C go through the BC normalisation
-// and bias (a.bc) before the rotation.
-template <int N, int R, bool OUT, int YT = M3_F32, bool BCN = false, int QRT = (N == 64 ? 128 : 64)>
+// and bias (a.bc) before the rotation.  BAL: the balanced plan for more sequences than CTAs (OUT, one
+// segment): the sequences' chunk lists, laid end to end, are cut into nbal equal ranges, one per CTA
+// (a cooperative launch, so all of them run at once).  A range holds the tail of one sequence, whole
+// sequences and the head of another; the CTA runs the head first and hands its end state to the CTA
+// holding that sequence's tail (a state slot of the workspace and a flag set to `epoch`), then the
+// whole sequences, then its own tail, whose start state it takes from the CTA before.  With more
+// sequences than CTAs every range is at least one sequence long, so no hand-off waits on another.
+template <int N, int R, bool OUT, int YT = M3_F32, bool BCN = false, int QRT = (N == 64 ? 128 : 64), bool BAL = false>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, int nseg, int nlaunch, int ws_stride,
-                  int ws_step, unsigned *status) {
+                  int ws_step, unsigned *status, unsigned long long epoch, int nbal) {
     using Cf = Cfg<N, R, QRT>;
     constexpr int YB = YT == M3_F32 ? 4 : 2;
     using S = Smem<N, R, OUT, YB, BCN, QRT>;
@@ -222,13 +240,69 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int H = a.H, L = a.L;
-    const int g = blockIdx.x % nlaunch, bh = blockIdx.x / nlaunch, b = bh / H, h = bh % H;
+    // sequence of this CTA: its index scrambled by s -> m s mod (batch H), m = 41 or 43 (primes, so that one
+    // of them is coprime to the count and the map a permutation), spreading each wave over batches and heads
+    const int nseq_ = a.batch * a.H, smul = nseq_ % 41 ? 41 : (nseq_ % 43 ? 43 : 1);
+    const int g = blockIdx.x % nlaunch, bh = (int)(((long long)(blockIdx.x / nlaunch) * smul) % nseq_), b = bh / H, h = bh % H;
     const int t_begin = g * seglen, t_end = min(L, t_begin + seglen);
-    const int nchunks = t_end > t_begin ? (t_end - t_begin + Q - 1) / Q : 0;
+    int nchunks = t_end > t_begin ? (t_end - t_begin + Q - 1) / Q : 0;
+    static_assert(!BAL || (OUT && !BCN), "the balanced plan runs the output pass without BC normalisation");
+    // The chunks this CTA walks, in order, as pieces (sequence, chunks [cb, ce)).  Without BAL one piece:
+    // this CTA's segment of sequence bh.  With BAL: the range [c0, c1) of the concatenated chunk lists
+    // (ncs chunks per sequence), sequence sA from chunk a0 on to sequence sB up to chunk bE.
+    const int ncs = (L + Q - 1) / Q;
+    int sA = bh, a0 = t_begin / Q, sB = bh, bE = a0 + nchunks, npc = 1;
+    if constexpr (BAL) {
+        const long long T = (long long)a.batch * H * ncs;
+        const long long c0 = T * blockIdx.x / nbal, c1 = T * (blockIdx.x + 1) / nbal;
+        nchunks = (int)(c1 - c0);
+        if (nchunks > 0) {
+            sA = (int)(c0 / ncs);
+            a0 = (int)(c0 % ncs);
+            sB = (int)((c1 - 1) / ncs);
+            bE = (int)((c1 - 1) % ncs) + 1;
+            npc = sA == sB ? 1 : sB - sA + 1;
+        }
+    }
+    // piece p: sequence seq (batch qb, head qh), chunks [cb, ce); current chunk c.  The plain plan's one
+    // piece is the CTA's segment: only c varies, the rest are the CTA's constants (the accessors below)
+    struct PosB { int p, seq, qb, qh, cb, ce, c; };
+    struct PosP { int c; };
+    using Pos = std::conditional_t<BAL, PosB, PosP>;
+    auto piece_at = [&](int pi) -> Pos {
+        if constexpr (BAL) {
+            int sq = sA, cb = a0, ce = bE;
+            if (sA != sB) {
+                if (pi == 0) { sq = sB; cb = 0; ce = bE; }                       // head of the last sequence
+                else if (pi < npc - 1) { sq = sA + pi; cb = 0; ce = ncs; }       // whole sequences
+                else { sq = sA; cb = a0; ce = ncs; }                              // tail of the first
+            }
+            return Pos{pi, sq, sq / H, sq % H, cb, ce, cb};
+        } else {
+            return Pos{a0};
+        }
+    };
+    auto pos_next = [&](Pos u) {
+        ++u.c;
+        if constexpr (BAL) {
+            if (u.c >= u.ce && u.p + 1 < npc) u = piece_at(u.p + 1);
+        }
+        return u;
+    };
+    auto p_seq = [&](const Pos &u) { if constexpr (BAL) return u.seq; else return bh; };
+    auto p_qb = [&](const Pos &u) { if constexpr (BAL) return u.qb; else return b; };
+    auto p_qh = [&](const Pos &u) { if constexpr (BAL) return u.qh; else return h; };
+    auto p_cb = [&](const Pos &u) { if constexpr (BAL) return u.cb; else return a0; };
+    auto p_ce = [&](const Pos &u) { if constexpr (BAL) return u.ce; else return bE; };
+    const int t_stop = BAL ? L : t_end;   // y, and the chunk's tokens, end here
+    // state slots and flags of the hand-offs (BAL): slot i carries CTA i's head state to CTA i + 1
+    unsigned long long *hflags = BAL ? reinterpret_cast<unsigned long long *>(a.ws_state + (size_t)nbal * N * kP)
+                                     : nullptr;
     const __nv_bfloat16 *dtp = static_cast<const __nv_bfloat16 *>(a.dt);
     const __nv_bfloat16 *Ap = static_cast<const __nv_bfloat16 *>(a.A);
     const __nv_bfloat16 *lp = static_cast<const __nv_bfloat16 *>(a.lam);
     auto tok = [&](int t) { return ((size_t)b * L + t) * H + h; };
+    auto tokq = [&](const Pos &u, int t) { return ((size_t)p_qb(u) * L + t) * H + p_qh(u); };   // token t of u's sequence
 
     // bounded wait; after any timeout every later wait returns at once
     // (backoff: single-thread roles nap between polls so that they do not take
@@ -281,7 +355,8 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
         // ================================================================ producer
         if (lane == 0) {
             int issued = 0;
-            for (int it = 0; it < nchunks; ++it) {
+            Pos u = piece_at(0);
+            for (int it = 0; it < nchunks; ++it, u = pos_next(u)) {
                 const int p = it & 1;
                 if (it >= 2) wait(kRawEmpty + p, ((it - 2) >> 1) & 1, true);
                 // after a timeout nothing more is issued: a refill could land on a slot whose
@@ -290,16 +365,17 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                 unsigned char *slot = sm + p * S::SLOT;
                 constexpr uint32_t bytes = Cf::BT * (OUT ? 2 : 1) + Cf::XT + Cf::TT;
                 mbar_expect_tx(bars + kRawFull + p, bytes);
-                const int row0 = b * L + t_begin + it * Q;
-                const int hg = h / (H / a.G);   // B / C group of this head
+                const int qh = p_qh(u);
+                const int row0 = p_qb(u) * L + u.c * Q;
+                const int hg = qh / (H / a.G);   // B / C group of this head
 #pragma unroll
                 for (int sl = 0; sl < NSLAB; ++sl) {
                     tma_load_4d(slot + S::sB + sl * QR * 128, &maps.B, 64 * sl, 0, hg, row0, bars + kRawFull + p);
                     if (OUT)
                         tma_load_4d(slot + S::sC + sl * QR * 128, &maps.C, 64 * sl, 0, hg, row0, bars + kRawFull + p);
                 }
-                tma_load_4d(slot + S::sX, &maps.X, 0, 0, h, row0, bars + kRawFull + p);
-                tma_load_3d(slot + S::sT, &maps.T, 0, h, row0, bars + kRawFull + p);
+                tma_load_4d(slot + S::sX, &maps.X, 0, 0, qh, row0, bars + kRawFull + p);
+                tma_load_3d(slot + S::sT, &maps.T, 0, qh, row0, bars + kRawFull + p);
                 ++issued;
             }
             if (*abort_flag) {
@@ -372,17 +448,17 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
         // per-token scalars of the next chunk, loaded one chunk ahead into registers
         // (raw values: nothing waits on these loads until the chunk is processed)
         __nv_bfloat16 r_dt, r_A, r_l, r_ln, r_dtn;
-        auto fetch = [&](int it) {
+        auto fetch = [&](int it, const Pos &u) {
             const __nv_bfloat16 z = __float2bfloat16_rn(0.f);
             r_dt = r_A = r_l = r_ln = r_dtn = z;
-            const int t = t_begin + it * Q + ptid;
-            if (ptid < Q && it < nchunks && t < t_end) {
-                const size_t ti = tok(t);
+            const int t = u.c * Q + ptid;
+            if (ptid < Q && it < nchunks && t < t_stop) {
+                const size_t ti = tokq(u, t);
                 r_dt = dtp[ti];
                 r_A = Ap[ti];
                 r_l = lp[ti];
                 if (t + 1 < L) {
-                    const size_t tn = tok(t + 1);
+                    const size_t tn = ti + H;   // the next token of the sequence
                     r_ln = lp[tn];
                     r_dtn = dtp[tn];
                 } else {
@@ -390,7 +466,8 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                 }
             }
         };
-        fetch(0);
+        Pos pu = piece_at(0);   // this chunk
+        fetch(0, pu);
         float acc_cA = 0.f;   // pass 1: total log2-decay of the segment (prologue thread 0)
         float *bss = reinterpret_cast<float *>(sm + S::oSS);    // [B, C][QR] inverse RMS of the rows
         const float *bw = reinterpret_cast<const float *>(sm + S::oBW);   // [B, C][N]
@@ -426,9 +503,9 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
             }
             named_sync(kBarPro, kProThreads);
         }
-        for (int it = 0; it < nchunks; ++it) {
+        for (int it = 0; it < nchunks; ++it, pu = pos_next(pu)) {
             const int p = it & 1;
-            const int s0 = t_begin + it * Q, Qc = min(Q, t_end - s0), e = Qc - 1;
+            const int s0 = pu.c * Q, Qc = min(Q, t_stop - s0), e = Qc - 1;
             unsigned char *slot = sm + p * S::SLOT;
             float *cA2 = v_cA(p), *gv = v_g(p), *wv = v_w(p), *vj = v_vj(p), *dts = v_dt(p);
             if (it >= 2) wait(kEpiDone + p, ((it - 2) >> 1) & 1);
@@ -451,7 +528,7 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                 gv[ptid] = c_g;
                 wv[ptid] = c_w;
             }
-            fetch(it + 1);
+            fetch(it + 1, pos_next(pu));
             // one thread waits for the chunk's TMA; the named barrier (which costs the
             // other warps no issue slots) releases the rest
             if (ptid == 0) wait(kRawFull + p, (it >> 1) & 1);
@@ -824,26 +901,56 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
         // The fp32 state lives in TMEM columns [cH, cH + 64): row n in the lane of the Sn
         // accumulator's row n, column p; this thread holds columns [32 eh, 32 eh + 32).
         const uint32_t hcol = tmem + lane_base + cH + 32 * eh;
-        float hmax = 0.f;   // this thread's max |h| (state rows it owns)
-        {
-            const int n = st_row;
-            const float left0 = (OUT && nseg == 1) ? (1.f - to_f(lp[tok(0)])) * to_f(dtp[tok(0)]) : 0.f;
+        // bounded wait for the hand-off flag of the CTA before (balanced plan)
+        auto wait_flag = [&](const unsigned long long *f) {
+            const uint64_t t0 = global_ns();
+            for (uint32_t n = 0;; ++n) {
+                if (flag_acquire(f) == epoch) return;
+                __nanosleep(128);
+                if ((n & 15u) == 15u) {
+                    if (*abort_flag) return;
+                    if (global_ns() - t0 > kWaitNs) break;
+                }
+            }
+            *abort_flag = 1;
+            atomicOr(status, kStatusTimeout);
+        };
+        // The state entering piece u into TMEM (this thread's rows, columns [32 eh, 32 eh + 32)); returns
+        // the thread's max |h|.  A sequence's first chunk: h0 plus the carry's left-endpoint term; a later
+        // segment's: its workspace state; a balanced tail's: the state the CTA before handed over.
+        auto load_start = [&](const Pos &u) -> float {
+            const int sq = p_seq(u), n = st_row;
+            const float *src = nullptr;
+            bool from_h0;
+            if constexpr (BAL) {
+                from_h0 = u.c == 0;
+                if (!from_h0) {
+                    if (ew == 0 && lane == 0) wait_flag(hflags + blockIdx.x - 1);
+                    named_sync(kBarEpi, kEpiThreads);
+                    src = a.ws_state + (size_t)(blockIdx.x - 1) * N * kP;
+                }
+            } else {
+                from_h0 = nseg == 1;
+                if (!from_h0) src = a.ws_state + ((size_t)bh * ws_stride + (size_t)g * ws_step) * N * kP;
+            }
+            float hm = 0.f;
+            const float left0 = (OUT && from_h0) ? (1.f - to_f(lp[tokq(u, 0)])) * to_f(dtp[tokq(u, 0)]) : 0.f;
             const __nv_bfloat16 *bq = static_cast<const __nv_bfloat16 *>(a.Bprev);
             const __nv_bfloat16 *xq = static_cast<const __nv_bfloat16 *>(a.xprev);
             // the carried B row entries n of every rank, BC-normalised when BCN
             float bqn[R];
 #pragma unroll
             for (int r = 0; r < R; ++r) bqn[r] = 0.f;
-            if (OUT && st_owner && nseg == 1 && bq && xq) {
+            if (OUT && st_owner && from_h0 && bq && xq) {
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
-                    const __nv_bfloat16 *row = bq + ((size_t)bh * R + r) * N;
+                    const __nv_bfloat16 *row = bq + ((size_t)sq * R + r) * N;
                     bqn[r] = to_f(row[n]);
                     if constexpr (BCN) {
                         float ssq = 0.f;
                         for (int m = 0; m < N; ++m) ssq = fmaf(to_f(row[m]), to_f(row[m]), ssq);
-                        bqn[r] = bc_apply(bqn[r], 1.f / sqrtf(ssq / (float)N + a.bc.eps), a.bc.wB, a.bc.bB, h, r,
-                                          R, N, n);
+                        bqn[r] = bc_apply(bqn[r], 1.f / sqrtf(ssq / (float)N + a.bc.eps), a.bc.wB, a.bc.bB,
+                                          p_qh(u), r, R, N, n);
                     }
                 }
             }
@@ -855,24 +962,38 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                     const int pp = 32 * eh + h16 + j;
                     float v = 0.f;
                     if (OUT && st_owner) {
-                        if (nseg == 1) {
-                            v = a.h0 ? a.h0[((size_t)bh * N + n) * kP + pp] : 0.f;
+                        if (from_h0) {
+                            v = a.h0 ? a.h0[((size_t)sq * N + n) * kP + pp] : 0.f;
                             if (bq && xq) {
-                                float u = 0.f;
+                                float uu = 0.f;
 #pragma unroll
-                                for (int r = 0; r < R; ++r) u += bqn[r] * to_f(xq[((size_t)bh * R + r) * kP + pp]);
-                                v += left0 * u;
+                                for (int r = 0; r < R; ++r) uu += bqn[r] * to_f(xq[((size_t)sq * R + r) * kP + pp]);
+                                v += left0 * uu;
                             }
                         } else {
-                            v = a.ws_state[(((size_t)bh * ws_stride + (size_t)g * ws_step) * N + n) * kP + pp];
+                            v = __ldcg(src + (size_t)n * kP + pp);
                         }
                     }
-                    hmax = fmaxf(hmax, fabsf(v));
+                    hm = fmaxf(hm, fabsf(v));
                     w[j] = __float_as_uint(v);
                 }
                 tmem_st16(hcol + h16, w);
             }
-        }
+            return hm;
+        };
+        // the carry out of sequence sq (its last token's B and x), at the sequence's end
+        auto carry_out = [&](const Pos &u) {
+            if (!(OUT && a.Bprev_out && a.xprev_out && L > 0 && !*abort_flag)) return;
+            const int et = tid - kEpiW0 * 32, sq = p_seq(u);
+            const size_t tl = tokq(u, L - 1);
+            const size_t tlg = ((size_t)p_qb(u) * L + L - 1) * a.G + p_qh(u) / (H / a.G);   // its B / C group row
+            const __nv_bfloat16 *Bm = static_cast<const __nv_bfloat16 *>(a.B);
+            const __nv_bfloat16 *xm = static_cast<const __nv_bfloat16 *>(a.x);
+            __nv_bfloat16 *bo = static_cast<__nv_bfloat16 *>(a.Bprev_out);
+            __nv_bfloat16 *xo = static_cast<__nv_bfloat16 *>(a.xprev_out);
+            for (int i = et; i < R * N; i += kEpiThreads) bo[(size_t)sq * R * N + i] = Bm[tlg * R * N + i];
+            for (int i = et; i < R * kP; i += kEpiThreads) xo[(size_t)sq * R * kP + i] = xm[tl * R * kP + i];
+        };
         // fp16 copy of the state (scaled) for the C~ H MMA (MN-major, 128-byte swizzle, rows n)
         auto publish_state = [&](int slot_parity, float m) {
             if (!OUT) return;
@@ -910,17 +1031,32 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                     make_uint4(w4[0], w4[1], w4[2], w4[3]);
             }
         };
-        publish_state(0, hmax);
-        fence_proxy_async();
-        fence_before();
-        mbar_arrive(bars + kStateReady + 0);
 
-        for (int it = 0; it < nchunks; ++it) {
+        if constexpr (!BAL) {
+            publish_state(0, load_start(piece_at(0)));
+            fence_proxy_async();
+            fence_before();
+            mbar_arrive(bars + kStateReady + 0);
+        }
+        Pos eu = piece_at(0);
+        for (int it = 0; it < nchunks; ++it, eu = pos_next(eu)) {
             const int p = it & 1;
             const uint32_t ph = (it >> 1) & 1;
-            const int s0 = t_begin + it * Q, Qc = min(Q, t_end - s0), e = Qc - 1;
+            const int s0 = eu.c * Q, Qc = min(Q, t_stop - s0), e = Qc - 1;
             const float *cA2 = v_cA(p), *gv = v_g(p), *vj = v_vj(p), *sg = v_sig(p);
             const bool last_chunk = it == nchunks - 1;
+            const bool piece_end = BAL && eu.c == p_ce(eu) - 1;   // (balanced plan) the last chunk of a piece
+            if constexpr (BAL) {
+                if (eu.c == p_cb(eu)) {
+                    // a piece starts here: its state into TMEM and its fp16 copy for the MMAs (one call
+                    // site of the load, for the instruction cache); later chunks get theirs from the update
+                    const float hm = load_start(eu);
+                    publish_state(p, hm);
+                    fence_proxy_async();
+                    fence_before();
+                    mbar_arrive(bars + kStateReady + p);
+                }
+            }
             // one thread waits for the chunk's vectors and first MMAs; the named barrier
             // releases the other epilogue warps without them polling
             if (ew == 0 && lane == 0) {
@@ -1039,7 +1175,12 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                 const float c = up_own ? v_cos(p)[kk] : 1.f, s = up_own ? v_sin(p)[kk] : 0.f;
                 const bool odd = n & 1;
                 float *dst = nullptr;
-                if (last_chunk && up_own && !*abort_flag) {
+                if constexpr (BAL) {
+                    if (piece_end && up_own && !*abort_flag) {
+                        if (p_ce(eu) < ncs) dst = a.ws_state + ((size_t)blockIdx.x * N + n) * kP + up_col;   // hand-off
+                        else if (a.h_out) dst = a.h_out + ((size_t)p_seq(eu) * N + n) * kP + up_col;
+                    }
+                } else if (last_chunk && up_own && !*abort_flag) {
                     if (!OUT) dst = a.ws_state + (((size_t)bh * ws_stride + g + 1) * N + n) * kP + up_col;
                     else if (g == nseg - 1 && a.h_out) dst = a.h_out + ((size_t)bh * N + n) * kP + up_col;
                 }
@@ -1086,10 +1227,24 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                         tmem_st16(hcol + h16, *reinterpret_cast<const uint32_t(*)[16]>(hv));
                     }
                 }
-                publish_state((it + 1) & 1, m);
-                fence_proxy_async();
-                fence_before();
-                mbar_arrive(bars + kStateReady + ((it + 1) & 1));
+                if constexpr (BAL) {
+                    if (piece_end) {
+                        if (p_ce(eu) < ncs) {
+                            // this CTA's head state is in its slot: release it to the CTA after
+                            __threadfence();
+                            named_sync(kBarEpi, kEpiThreads);
+                            if (ew == 0 && lane == 0) flag_release(hflags + blockIdx.x, epoch);
+                        } else {
+                            carry_out(eu);
+                        }
+                    }
+                }
+                if (!(piece_end && it + 1 < nchunks)) {   // (the next piece publishes its own start state)
+                    publish_state((it + 1) & 1, m);
+                    fence_proxy_async();
+                    fence_before();
+                    mbar_arrive(bars + kStateReady + ((it + 1) & 1));
+                }
             }
             // ---- y = Ya + exp(cA_t) Yi
             if (OUT) {
@@ -1151,8 +1306,8 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                 named_sync(kBarEpi, kEpiThreads);
                 if (ew == 0 && lane == 0) {
                     if (!*abort_flag) {
-                        tma_store_5d(&maps.Y, sm + S::oYs, 0, 0, h, s0, b);
-                        if (YB == 4) tma_store_5d(&maps.Y, sm + S::oYs + QR * 128, 32, 0, h, s0, b);
+                        tma_store_5d(&maps.Y, sm + S::oYs, 0, 0, p_qh(eu), s0, p_qb(eu));
+                        if (YB == 4) tma_store_5d(&maps.Y, sm + S::oYs + QR * 128, 32, 0, p_qh(eu), s0, p_qb(eu));
                     }
                     bulk_commit();
                 }
@@ -1160,18 +1315,8 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
             if (!OUT) mbar_arrive(bars + kEpiDone + p);
         }
         if (OUT && ew == 0 && lane == 0) bulk_wait<0>();
-        // ---- carry out (last segment)
-        if (OUT && g == nseg - 1 && a.Bprev_out && a.xprev_out && L > 0 && !*abort_flag) {
-            const int et = tid - kEpiW0 * 32;
-            const size_t tl = tok(L - 1);
-            const size_t tlg = ((size_t)b * L + L - 1) * a.G + h / (H / a.G);   // its B / C group row
-            const __nv_bfloat16 *Bm = static_cast<const __nv_bfloat16 *>(a.B);
-            const __nv_bfloat16 *xm = static_cast<const __nv_bfloat16 *>(a.x);
-            __nv_bfloat16 *bo = static_cast<__nv_bfloat16 *>(a.Bprev_out);
-            __nv_bfloat16 *xo = static_cast<__nv_bfloat16 *>(a.xprev_out);
-            for (int i = et; i < R * N; i += kEpiThreads) bo[(size_t)bh * R * N + i] = Bm[tlg * R * N + i];
-            for (int i = et; i < R * kP; i += kEpiThreads) xo[(size_t)bh * R * kP + i] = xm[tl * R * kP + i];
-        }
+        // ---- carry out (last segment; the balanced plan wrote it at each sequence's end)
+        if (!BAL && g == nseg - 1) carry_out(piece_at(0));
     }
     fence_before();
     __syncthreads();
@@ -1237,10 +1382,46 @@ cudaError_t launch_pass(const TcMaps &maps, const ScanArgs &a, const ScanPlan &p
     const int kid = OUT ? M3_KERNEL_PREFILL_OUTPUT : M3_KERNEL_PREFILL_STATE;
     trace_mark(kid, s, 0);
     kern<<<(unsigned)grid, kThreads, Sm::kAlloc, s>>>(maps, a, pl.seglen, pl.nseg, nlaunch, ws_stride, ws_step,
-                                                      status);
+                                                      status, 0ull, 0);
     trace_mark(kid, s, 1);
     count_launch();
     return cudaGetLastError();
+}
+
+// A fresh value of the hand-off flags per balanced launch (so that flags left in a reused workspace never
+// match); the start is taken from the clock so that another process's leftovers do not either.
+unsigned long long next_epoch() {
+    static std::atomic<unsigned long long> e{0};
+    unsigned long long v = e.fetch_add(1) + 1;
+    static const unsigned long long base =
+        (unsigned long long)std::chrono::steady_clock::now().time_since_epoch().count() * 0x9E3779B97F4A7C15ull;
+    return (base + v) | 1ull;   // never 0
+}
+
+// The balanced output pass (one segment): pl.bal CTAs, all resident at once (a cooperative launch, which
+// fails rather than runs them in turns); returns cudaErrorCooperativeLaunchTooLarge when they cannot be.
+template <int N, int R, int YT, int QRT>
+cudaError_t launch_bal(const TcMaps &maps, const ScanArgs &a, const ScanPlan &pl, cudaStream_t s) {
+    using Sm = Smem<N, R, true, YT == M3_F32 ? 4 : 2, false, QRT>;
+    auto kern = tc_segment_kernel<N, R, true, YT, false, QRT, true>;
+    cudaError_t e = allow_dynamic_smem<tc_segment_kernel<N, R, true, YT, false, QRT, true>>(Sm::kAlloc);
+    if (e != cudaSuccess) return e;
+    int dev = 0, per_sm = 0, coop = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
+    if (!coop || cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, Sm::kAlloc) != cudaSuccess ||
+        per_sm * sm_count() < pl.bal)
+        return cudaErrorCooperativeLaunchTooLarge;
+    unsigned *status = device_status_word();
+    if (!status) return cudaErrorUnknown;
+    int seglen = pl.seglen, nseg = 1, nlaunch = 1, ws_stride = 1, ws_step = 1, nbal = pl.bal;
+    unsigned long long epoch = next_epoch();
+    void *args[] = {(void *)&maps, (void *)&a, &seglen, &nseg, &nlaunch, &ws_stride, &ws_step, &status, &epoch, &nbal};
+    trace_mark(M3_KERNEL_PREFILL_OUTPUT, s, 0);
+    e = cudaLaunchCooperativeKernel((const void *)kern, dim3(pl.bal), dim3(kThreads), args, Sm::kAlloc, s);
+    trace_mark(M3_KERNEL_PREFILL_OUTPUT, s, 1);
+    if (e == cudaSuccess) count_launch();
+    return e;
 }
 
 template <int N, int R, bool BCN, int QRT = (N == 64 ? 128 : 64)>
@@ -1264,6 +1445,15 @@ cudaError_t run_tc(const ScanArgs &a, const ScanPlan &pl, cudaStream_t s) {
         if ((e = launch_pass<N, R, false, M3_F32, BCN, QRT>(maps, a, pp, npieces - 1, npieces, 1, s)) != cudaSuccess)
             return e;
         if ((e = segment_pass(a, pp, s)) != cudaSuccess) return e;
+    }
+    if constexpr (!BCN) {
+        if (pl.bal > 0 && pl.nseg == 1) {
+            cudaError_t eb = a.ydtype == M3_F16    ? launch_bal<N, R, M3_F16, QRT>(maps, a, pl, s)
+                             : a.ydtype == M3_BF16 ? launch_bal<N, R, M3_BF16, QRT>(maps, a, pl, s)
+                                                   : launch_bal<N, R, M3_F32, QRT>(maps, a, pl, s);
+            if (eb != cudaErrorCooperativeLaunchTooLarge) return eb;
+            cudaGetLastError();   // not resident at once here: the plain plan below
+        }
     }
     if (a.ydtype == M3_F16)
         return launch_pass<N, R, true, M3_F16, BCN, QRT>(maps, a, pl, pl.nseg, npieces, pl.nsub, s);
