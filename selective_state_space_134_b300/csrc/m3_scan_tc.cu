@@ -18,6 +18,9 @@ namespace {
 // tokens per chunk of the default tile (128 rows (t, r) for N = 64, 64 for N = 128)
 int tc_chunk(int N, int R) { return (N == 64 ? 128 : 64) / R; }
 
+// tokens per chunk of the state pass: 128 rows for both N (it has room for them with N = 128)
+int tc_state_chunk(int N, int R, int Q) { return N == 128 ? 128 / R : Q; }
+
 // The chunk rule of the pages, Q = N / R tokens (N rows per chunk): a tile of its own for N = 64,
 // R <= 4 (N = 128 would need 128-row tiles of B, C and theta that do not fit shared memory).
 bool tc_rule_chunk(int N, int R, int chunk) { return N == 64 && R <= 4 && chunk == N / R; }
@@ -48,17 +51,20 @@ bool tc_plan(const m3_dims &d, int sms, ScanPlan *pl) {
         nseg = (int)(want < max_seg ? want : max_seg);
         if (nseg < 1) nseg = 1;
     }
+    // segments and the state pass's pieces are whole chunks of the pass that walks them: a segment
+    // of the output pass's chunks, a piece of the state pass's
+    const int Qs = nseg > 1 ? tc_state_chunk(d.dstate, d.rank, Q) : Q;
     int seglen = L > 0 ? (L + nseg - 1) / nseg : Q;
-    seglen = ((seglen + Q - 1) / Q) * Q;
+    seglen = ((seglen + Qs - 1) / Qs) * Qs;
     nseg = L > 0 ? (L + seglen - 1) / seglen : 1;
     // the state pass covers segments 0 .. nseg - 2: split them into as many whole pieces of
-    // at least 8 chunks as one wave of CTAs holds
+    // at least 8 output-pass chunks as one wave of CTAs holds
     int nsub = 1;
     if (nseg > 1) {
         const long long cap = sms / (seqs * (nseg - 1));
-        const int chunks = seglen / Q;
+        const int chunks = seglen / Q, schunks = seglen / Qs;
         for (int c = 2; c <= cap && chunks / c >= 8; ++c)
-            if (chunks % c == 0) nsub = c;
+            if (schunks % c == 0) nsub = c;
     }
     pl->Q = Q;
     pl->nseg = nseg;

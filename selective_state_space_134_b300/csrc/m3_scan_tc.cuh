@@ -1442,8 +1442,22 @@ cudaError_t run_tc(const ScanArgs &a, const ScanPlan &pl, cudaStream_t s) {
         ScanPlan pp = pl;
         pp.nseg = npieces;
         pp.seglen = pl.seglen / pl.nsub;
-        if ((e = launch_pass<N, R, false, M3_F32, BCN, QRT>(maps, a, pp, npieces - 1, npieces, 1, s)) != cudaSuccess)
-            return e;
+        // The state pass holds no score, output or state-copy tiles, so with N = 128 its chunk takes twice
+        // the rows of the output pass's (the per-chunk state update then serves twice the tokens).  A CTA
+        // starts at a whole chunk (its first is t_begin / Q), so the pieces must be whole chunks of it; the
+        // planner cuts them so, and a plan that is not gets the output pass's chunk here.
+        constexpr int QRS = (N == 128 && QRT == 64) ? 128 : QRT;
+        using Cs = Cfg<N, R, QRS>;
+        if (QRS != QRT && pp.seglen % Cs::Q == 0) {
+            TcMaps smaps = maps;
+            if (!map4(&smaps.B, a.B, N, R, a.G, rows, Cs::Q) || !map4(&smaps.X, a.x, kP, R, a.H, rows, Cs::Q) ||
+                !map3(&smaps.T, a.theta, N / 2, a.H, rows, Cs::Q))
+                return cudaErrorInvalidValue;
+            e = launch_pass<N, R, false, M3_F32, BCN, QRS>(smaps, a, pp, npieces - 1, npieces, 1, s);
+        } else {
+            e = launch_pass<N, R, false, M3_F32, BCN, QRT>(maps, a, pp, npieces - 1, npieces, 1, s);
+        }
+        if (e != cudaSuccess) return e;
         if ((e = segment_pass(a, pp, s)) != cudaSuccess) return e;
     }
     if constexpr (!BCN) {

@@ -357,6 +357,24 @@ def test_in_place_state_update_equals_out_of_place():
     assert torch.equal(s1.h, st.h) and torch.equal(s1.B_prev, st.B_prev) and torch.equal(s1.x_prev, st.x_prev)
 
 
+@pytest.mark.parametrize("R,L", [(1, 1728), (2, 864), (4, 432), (8, 216)])
+def test_state_pass_pieces_ending_inside_a_chunk(R, L):
+    # N = 128: the state pass runs chunks of 128 rows, twice the output pass's 64.  An even split of
+    # these lengths over the segments would give pieces of 7 output chunks, half a state-pass chunk
+    # past a whole number of them; a CTA starts at a whole chunk, so the plan must cut the segments at
+    # whole state-pass chunks (a piece starting inside one re-adds that chunk's first tokens and
+    # corrupts every later segment's start state).  h0 and the carry in, every output against the oracle
+    w = WORKLOADS["long_n128_r4"].with_(batch=1, nheads=3, seqlen=L, R=R)
+    inp = prefill_inputs(w, "cuda")
+    st = random_state(w.batch, w.nheads, w.P, w.N, w.R, inp["x"].dtype, seed=R)
+    y, so = gpu_scan(inp, state_in=st)
+    yr, hr, Br, xr = oracle_full(inp, st)
+    assert_err(to_f64(y), yr, TOL[w.dtype], "y")
+    assert_err(to_f64(so.h), hr, TOL[w.dtype], "h")
+    np.testing.assert_array_equal(to_f64(so.B_prev), Br)
+    np.testing.assert_array_equal(to_f64(so.x_prev), xr)
+
+
 def test_in_place_segmented_long_sequence():
     w = WORKLOADS["long_n128_r4"].with_(batch=1, nheads=1, seqlen=3000)
     inp = prefill_inputs(w, "cuda")
