@@ -325,7 +325,7 @@ def time_decode_pooled(m3, w, calls, warmup, pool_factor=2):
     return e0.elapsed_time(e1) / calls, tr_ms / max(n_tr, 1)
 
 
-def e2e_prefill(m3, w, inp, steps, warmup, slices=16):
+def e2e_prefill(m3, w, inp, steps, warmup, slices=8):
     """Same metric through host buffers, via the library's staged prefill: every step copies the
     inputs in from pinned host memory and y and the final state h back out, the copies of each
     token range overlapped with the kernels and copies of the others."""
@@ -584,7 +584,7 @@ def run_ours(args):
             torch.cuda.empty_cache()
         extra["backward"] = {"metric": "backward tokens/s", "unit": "tokens/s", "workloads": bwd}
 
-    e2e = e2e_prefill(m3, w, inp, max(2, min(args.steps, 10)), 1) if rank == 0 else None
+    e2e = e2e_prefill(m3, w, inp, max(2, min(args.steps, 10)), 3) if rank == 0 else None
     cpu = None
     if rank == 0 and ws == 1 and not args.quick:
         cpu = oracle_rate(w, os.cpu_count() or 1, 10.0)

@@ -180,10 +180,13 @@ m3_status mamba3_scan_fwd_staged_workspace(const m3_dims *dims, int slices, size
 /*
  * The prefill from and to host memory, with the host <-> device copies
  * overlapped: the sequences are cut into `slices` consecutive token ranges
- * (at most L); range i of every sequence is copied in and scanned on `stream`
+ * (at most L); range i of every sequence is copied in, then scanned on `stream`
  * (starting from range i-1's final state and carry), and its y is copied out
- * on `copy_stream` while range i+1 is copied in.  The host buffers should be
- * pinned (page-locked) for the copies to be asynchronous.
+ * on `copy_stream` while range i+1 is copied in.  The copies in run on a
+ * stream the library keeps for them (one per device, created on first use),
+ * queued ahead of the scans so that both directions of the host link stay
+ * busy.  The host buffers should be pinned (page-locked) for the copies to be
+ * asynchronous.
  *   host_in, host_y:   the inputs and y in host memory, full layouts;
  *   dev_in, dev_y:     device buffers of the same sizes (caller-owned staging;
  *                      range i occupies the block of batch * L_i tokens that
@@ -196,7 +199,8 @@ m3_status mamba3_scan_fwd_staged_workspace(const m3_dims *dims, int slices, size
  *                      also copied to this host buffer [batch][H][N][P] fp32;
  *   workspace:         at least mamba3_scan_fwd_staged_workspace(dims, slices).
  * Work on `stream` first waits for the copies already queued on `copy_stream`
- * (a previous call's outputs), so consecutive calls may share the buffers.
+ * (a previous call's outputs), and the copies in wait for the work already
+ * queued on `stream`, so consecutive calls may share the buffers.
  * Returns when everything is enqueued; `copy_stream` holds the last copies
  * (synchronise it before reading the host outputs).  Argument errors are
  * reported before anything is enqueued; a failing range reports M3_ERR_CUDA.

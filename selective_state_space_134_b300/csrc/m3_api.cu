@@ -67,6 +67,18 @@ int sm_count() {
     return g_sms[dev];
 }
 
+// The library's stream for the staged prefill's copies in, one per device (created on first use, kept for the
+// life of the process); nullptr on error.
+static cudaStream_t g_in_stream[kMaxDevices];
+cudaStream_t input_stream() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_in_stream[dev] && cudaStreamCreateWithFlags(&g_in_stream[dev], cudaStreamNonBlocking) != cudaSuccess)
+        g_in_stream[dev] = nullptr;
+    return g_in_stream[dev];
+}
+
 void *tensor_map_encoder() {
     static std::once_flag once;
     static void *fn = nullptr;
@@ -344,15 +356,17 @@ m3_status mamba3_scan_fwd_staged(const m3_dims *dims, const m3_token_inputs *hos
     const size_t G = (size_t)groups_of(d);
     const size_t tx = H * R * P * es, tB = G * R * N * es, ts = H * es, tth = H * (N / 2) * es, ty = H * R * P * elem_size(d.ydtype);
     const cudaStream_t s = static_cast<cudaStream_t>(stream), cs = static_cast<cudaStream_t>(copy_stream);
-    // the previous call's copies out read buffers this call rewrites: start after them
-    {
+    // `to` waits for the work queued on `from` so far
+    auto follow = [](cudaStream_t to, cudaStream_t from) {
         cudaEvent_t ev;
-        if (cudaEventCreateWithFlags(&ev, cudaEventDisableTiming) != cudaSuccess) return M3_ERR_CUDA;
-        cudaError_t e = cudaEventRecord(ev, cs);
-        if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ev, 0);
-        cudaEventDestroy(ev);
-        if (e != cudaSuccess) return M3_ERR_CUDA;
-    }
+        if (cudaEventCreateWithFlags(&ev, cudaEventDisableTiming) != cudaSuccess) return false;
+        cudaError_t e = cudaEventRecord(ev, from);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(to, ev, 0);
+        cudaEventDestroy(ev);   // released once the wait has been satisfied
+        return e == cudaSuccess;
+    };
+    // the previous call's copies out read buffers this call rewrites: start after them
+    if (!follow(s, cs)) return M3_ERR_CUDA;
     if (L == 0) {
         st = mamba3_scan_fwd(dims, dev_in->x, dev_in->B, dev_in->C, dev_in->dt, dev_in->A, dev_in->lambda,
                              dev_in->theta, dev_state_in, dev_y, dev_state_out, workspace, workspace_bytes, stream);
@@ -361,6 +375,11 @@ m3_status mamba3_scan_fwd_staged(const m3_dims *dims, const m3_token_inputs *hos
             st = M3_ERR_CUDA;
         return st;
     }
+    // The copies in run on the library's input stream, ahead of the kernels: range i + 1 comes in while
+    // range i is scanned and range i - 1 goes out, so both directions of the link stay busy.  They start
+    // after everything queued on `stream` so far (the previous call's kernels read the staging buffers).
+    const cudaStream_t is = input_stream();
+    if (!is || !follow(is, s)) return M3_ERR_CUDA;
     // Slice i holds tokens [l0, l1) of every sequence; its device copy is the contiguous
     // [batch][l1 - l0][...] block at offset batch * l0 * (bytes per token) of each device buffer.
     for (int i = 0; i < ns; ++i) {
@@ -377,9 +396,10 @@ m3_status mamba3_scan_fwd_staged(const m3_dims *dims, const m3_token_inputs *hos
             const char *src = static_cast<const char *>(in[k].h) + (size_t)l0 * in[k].tb;
             dp[k] = dst;
             if (cudaMemcpy2DAsync(dst, ls * in[k].tb, src, (size_t)L * in[k].tb, ls * in[k].tb, nb,
-                                  cudaMemcpyHostToDevice, s) != cudaSuccess)
+                                  cudaMemcpyHostToDevice, is) != cudaSuccess)
                 return M3_ERR_CUDA;
         }
+        if (!follow(s, is)) return M3_ERR_CUDA;
         m3_dims sd = d;
         sd.seqlen = (int)ls;
         char *ydev = static_cast<char *>(dev_y) + nb * (size_t)l0 * ty;
@@ -387,12 +407,7 @@ m3_status mamba3_scan_fwd_staged(const m3_dims *dims, const m3_token_inputs *hos
                              i == 0 ? dev_state_in : dev_state_out, ydev, dev_state_out, workspace, workspace_bytes,
                              stream);
         if (st != M3_OK) return st;
-        cudaEvent_t ev;
-        if (cudaEventCreateWithFlags(&ev, cudaEventDisableTiming) != cudaSuccess) return M3_ERR_CUDA;
-        cudaError_t e = cudaEventRecord(ev, s);
-        if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, ev, 0);
-        cudaEventDestroy(ev);   // released once the wait has been satisfied
-        if (e != cudaSuccess) return M3_ERR_CUDA;
+        if (!follow(cs, s)) return M3_ERR_CUDA;
         if (cudaMemcpy2DAsync(static_cast<char *>(host_y) + (size_t)l0 * ty, (size_t)L * ty, ydev, ls * ty, ls * ty, nb,
                               cudaMemcpyDeviceToHost, cs) != cudaSuccess)
             return M3_ERR_CUDA;

@@ -57,6 +57,7 @@ cudaError_t allow_dynamic_smem(size_t bytes) {
     return e;
 }
 void *tensor_map_encoder();          // the driver's cuTensorMapEncodeTiled (nullptr if unavailable)
+cudaStream_t input_stream();         // the staged prefill's stream for copies in (this device; nullptr on error)
 
 // ---------------------------------------------------------------- prefill plan
 // Prefill runs over segments of `seglen` tokens (a multiple of the chunk Q).
