@@ -1324,8 +1324,17 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
 }
 
 // ---------------------------------------------------------------- host side
+// L2 promotion of the loads through a map: how far past the requested bytes a fetch into L2 extends.
+// 256 bytes suits launches whose CTAs read neighbouring heads' rows of a token at the same time; a
+// launch whose CTAs do not (the balanced pass) promotes no further than one head's contiguous row.
+CUtensorMapL2promotion promo_for(int row_bytes) {
+    return row_bytes <= 64 ? CU_TENSOR_MAP_L2_PROMOTION_L2_64B
+                           : (row_bytes <= 128 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B : CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+}
+
 // 4-d map over a [b*L][H][R][inner] bf16 tensor, box = {64, R, 1, Q}, 128-byte swizzle
-bool map4(CUtensorMap *m, const void *base, int inner, int R, int H, long long rows, int Q) {
+bool map4(CUtensorMap *m, const void *base, int inner, int R, int H, long long rows, int Q,
+          CUtensorMapL2promotion prom = CU_TENSOR_MAP_L2_PROMOTION_L2_256B) {
     EncodeFn enc = encode_fn();
     if (!enc) return false;
     const cuuint64_t dims[4] = {(cuuint64_t)inner, (cuuint64_t)R, (cuuint64_t)H, (cuuint64_t)rows};
@@ -1333,11 +1342,12 @@ bool map4(CUtensorMap *m, const void *base, int inner, int R, int H, long long r
     const cuuint32_t box[4] = {64, (cuuint32_t)R, 1, (cuuint32_t)Q};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, prom,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 // 3-d map over a [b*L][H][inner] bf16 tensor, box = {inner, 1, Q}
-bool map3(CUtensorMap *m, const void *base, int inner, int H, long long rows, int Q) {
+bool map3(CUtensorMap *m, const void *base, int inner, int H, long long rows, int Q,
+          CUtensorMapL2promotion prom = CU_TENSOR_MAP_L2_PROMOTION_L2_256B) {
     EncodeFn enc = encode_fn();
     if (!enc) return false;
     const cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)H, (cuuint64_t)rows};
@@ -1345,7 +1355,7 @@ bool map3(CUtensorMap *m, const void *base, int inner, int H, long long rows, in
     const cuuint32_t box[3] = {(cuuint32_t)inner, 1, (cuuint32_t)Q};
     const cuuint32_t estr[3] = {1, 1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, prom,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -1462,9 +1472,17 @@ cudaError_t run_tc(const ScanArgs &a, const ScanPlan &pl, cudaStream_t s) {
     }
     if constexpr (!BCN) {
         if (pl.bal > 0 && pl.nseg == 1) {
-            cudaError_t eb = a.ydtype == M3_F16    ? launch_bal<N, R, M3_F16, QRT>(maps, a, pl, s)
-                             : a.ydtype == M3_BF16 ? launch_bal<N, R, M3_BF16, QRT>(maps, a, pl, s)
-                                                   : launch_bal<N, R, M3_F32, QRT>(maps, a, pl, s);
+            // rows of one (token, head): B and C R N, x R P, theta N / 2 elements (a 64-wide slab of each
+            // B and C row for N = 128, the neighbouring slab loaded next)
+            TcMaps bm = maps;
+            if (!map4(&bm.B, a.B, N, R, a.G, rows, Cf::Q, promo_for(R * 64 * 2)) ||
+                !map4(&bm.C, a.C, N, R, a.G, rows, Cf::Q, promo_for(R * 64 * 2)) ||
+                !map4(&bm.X, a.x, kP, R, a.H, rows, Cf::Q, promo_for(R * kP * 2)) ||
+                !map3(&bm.T, a.theta, N / 2, a.H, rows, Cf::Q, promo_for(N)))
+                return cudaErrorInvalidValue;
+            cudaError_t eb = a.ydtype == M3_F16    ? launch_bal<N, R, M3_F16, QRT>(bm, a, pl, s)
+                             : a.ydtype == M3_BF16 ? launch_bal<N, R, M3_BF16, QRT>(bm, a, pl, s)
+                                                   : launch_bal<N, R, M3_F32, QRT>(bm, a, pl, s);
             if (eb != cudaErrorCooperativeLaunchTooLarge) return eb;
             cudaGetLastError();   // not resident at once here: the plain plan below
         }
