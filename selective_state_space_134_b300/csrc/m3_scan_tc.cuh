@@ -445,6 +445,11 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
         // ================================================================ prologue
         const int ptid = tid - kProW0 * 32, pw = warp - kProW0;
         const int slab = pw % NSLAB, seg = pw / NSLAB, k = 32 * slab + lane;
+        // SISO with N = 64: each lane turns two adjacent pairs (2 kc, 2 kc + 1) of half of its warp's
+        // tokens (half hh), so that its shared-memory words are 8 bytes; otherwise one pair k per lane
+        constexpr bool kPair2 = N == 64 && R == 1 && !BCN;
+        constexpr int TH = TPS / 2;   // tokens per lane with two pairs
+        const int kc = lane & 15, hh = lane >> 4;
         // per-token scalars of the next chunk, loaded one chunk ahead into registers
         // (raw values: nothing waits on these loads until the chunk is processed)
         __nv_bfloat16 r_dt, r_A, r_l, r_ln, r_dtn;
@@ -544,13 +549,34 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
             float mW = ptid < Qc ? fabsf(c_w) : 0.f;
             // this thread's tokens: dt (0 past the sequence end) and its pair's angle rate
             float dd[TPS], th[TPS];
+            float dd2[TH];
+            float2 th2[TH], lo2 = f2(0.f);   // two pairs: rates; the first half's partial sums (hh = 1)
+            if constexpr (kPair2) {
 #pragma unroll
-            for (int i = 0; i < TPS; ++i) {
-                const int t = seg * TPS + i;
-                dd[i] = dts[t];
-                th[i] = __bfloat162float(rawT[t * K + k]);
-            }
-            {
+                for (int i = 0; i < TH; ++i) {
+                    const int t = seg * TPS + hh * TH + i;
+                    dd2[i] = dts[t];
+                    const uint32_t w = *reinterpret_cast<const uint32_t *>(rawT + t * K + 2 * kc);
+                    th2[i] = f2u(w << 16, w & 0xFFFF0000u);
+                }
+                float2 ps = f2(0.f);
+#pragma unroll
+                for (int i = 0; i < TH; ++i) ps = __ffma2_rn(f2(dd2[i]), th2[i], ps);
+                const float2 other = make_float2(__shfl_xor_sync(0xffffffffu, ps.x, 16),
+                                                 __shfl_xor_sync(0xffffffffu, ps.y, 16));
+                if (hh == 0) {
+                    part[seg * K + 2 * kc] = ps.x + other.x;
+                    part[seg * K + 2 * kc + 1] = ps.y + other.y;
+                } else {
+                    lo2 = other;
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < TPS; ++i) {
+                    const int t = seg * TPS + i;
+                    dd[i] = dts[t];
+                    th[i] = __bfloat162float(rawT[t * K + k]);
+                }
                 float ps = 0.f;
 #pragma unroll
                 for (int i = 0; i < TPS; ++i) ps = fmaf(dd[i], th[i], ps);
@@ -646,7 +672,75 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                 sg[6] = pow2_inv(tauP) * pow2_inv(sgXp);
                 if (!OUT) acc_cA += cA2[e];
             }
-            {
+            if constexpr (kPair2) {
+                // two pairs a lane: both pairs' angles as one packed pair, 8-byte words of B and C
+                float2 phi2 = lo2;
+#pragma unroll
+                for (int sg = 0; sg < Cf::NSEG - 1; ++sg)
+                    if (sg < seg) phi2 = __fadd2_rn(phi2, make_float2(part[sg * K + 2 * kc], part[sg * K + 2 * kc + 1]));
+                float2 ph2[TH];
+#pragma unroll
+                for (int i = 0; i < TH; ++i) {
+                    phi2 = __ffma2_rn(f2(dd2[i]), th2[i], phi2);
+                    ph2[i] = phi2;
+                }
+                const int t0 = seg * TPS + hh * TH;
+                const int ie = e - t0;   // the chunk's last token, if it is this lane's
+                unsigned char *bs = slot + S::sB, *cs = slot + S::sC;
+                uint2 rb2[TH], rc2[TH];
+                constexpr int kLA = TH < 4 ? TH : 4;
+                auto load_tok = [&](int i) {
+                    const uint32_t off = sw128(t0 + i, 4 * kc);
+                    rb2[i] = *reinterpret_cast<const uint2 *>(bs + off);
+                    if (OUT) rc2[i] = *reinterpret_cast<const uint2 *>(cs + off);
+                };
+#pragma unroll
+                for (int i = 0; i < kLA; ++i) load_tok(i);
+                // sin / cos as in the one-pair layout below (Cody-Waite by 2 pi, then the hardware
+                // approximations), the two lanes of each packed pair now the lane's two pairs
+#pragma unroll
+                for (int i = 0; i < TH; ++i) {
+                    if (i + kLA < TH) load_tok(i + kLA);
+                    const float2 x2 = ph2[i];
+                    const float2 n2 = __fadd2_rn(__ffma2_rn(x2, f2(0.15915494309189535f), f2(12582912.f)),
+                                                 f2(-12582912.f));
+                    float2 r2 = __ffma2_rn(n2, f2(-6.28318548202514648f), x2);
+                    r2 = __ffma2_rn(n2, f2(1.7484555314695172e-7f), r2);
+                    float c0, s0, c1, s1;
+                    __sincosf(r2.x, &s0, &c0);
+                    __sincosf(r2.y, &s1, &c1);
+                    if (i == ie) {   // the chunk's last token: rotation of the state at the chunk end
+                        v_cos(p)[2 * kc] = c0;
+                        v_cos(p)[2 * kc + 1] = c1;
+                        v_sin(p)[2 * kc] = s0;
+                        v_sin(p)[2 * kc + 1] = s1;
+                        if (!OUT) {
+                            tot[1 + 2 * kc] += x2.x;
+                            tot[1 + 2 * kc + 1] += x2.y;
+                        }
+                    }
+                    const float2 cb = __fmul2_rn(make_float2(c0, c1), f2(sgB));
+                    const float2 sb = __fmul2_rn(make_float2(s0, s1), f2(sgB));
+                    const float2 nsb = __fmul2_rn(make_float2(s0, s1), f2(-sgB));
+                    const bool valid = t0 + i < Qc;
+                    const uint32_t off = sw128(t0 + i, 4 * kc);
+                    // entries 2k (even) and 2k + 1 (odd) of the two pairs
+                    const uint2 vb = rb2[i];
+                    const float2 be = f2u(vb.x << 16, vb.y << 16), bo = f2u(vb.x & 0xFFFF0000u, vb.y & 0xFFFF0000u);
+                    const float2 oe = __ffma2_rn(cb, be, __fmul2_rn(sb, bo));
+                    const float2 oo = __ffma2_rn(cb, bo, __fmul2_rn(nsb, be));
+                    *reinterpret_cast<uint2 *>(bs + off) =
+                        valid ? make_uint2(pack_f16x2(oe.x, oo.x), pack_f16x2(oe.y, oo.y)) : make_uint2(0u, 0u);
+                    if (OUT) {
+                        const uint2 vc = rc2[i];
+                        const float2 ge = f2u(vc.x << 16, vc.y << 16), go = f2u(vc.x & 0xFFFF0000u, vc.y & 0xFFFF0000u);
+                        const float2 qe = __ffma2_rn(cb, ge, __fmul2_rn(sb, go));
+                        const float2 qo = __ffma2_rn(cb, go, __fmul2_rn(nsb, ge));
+                        *reinterpret_cast<uint2 *>(cs + off) =
+                            valid ? make_uint2(pack_f16x2(qe.x, qo.x), pack_f16x2(qe.y, qo.y)) : make_uint2(0u, 0u);
+                    }
+                }
+            } else {
                 float phi = 0.f;
 #pragma unroll
                 for (int sg = 0; sg < Cf::NSEG - 1; ++sg) phi += (sg < seg) ? part[sg * K + k] : 0.f;
