@@ -445,11 +445,12 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
         // ================================================================ prologue
         const int ptid = tid - kProW0 * 32, pw = warp - kProW0;
         const int slab = pw % NSLAB, seg = pw / NSLAB, k = 32 * slab + lane;
-        // SISO with N = 64: each lane turns two adjacent pairs (2 kc, 2 kc + 1) of half of its warp's
-        // tokens (half hh), so that its shared-memory words are 8 bytes; otherwise one pair k per lane
-        constexpr bool kPair2 = N == 64 && R == 1 && !BCN;
+        // Without BC normalisation (SISO, and any R with N = 128): each lane turns two adjacent pairs
+        // (kp = 32 slab + 2 kc and kp + 1) of half of its warp's tokens (half hh), so that its shared-
+        // memory words are 8 bytes; otherwise (and for MIMO with N = 64) one pair k per lane
+        constexpr bool kPair2 = !BCN && (R == 1 || N != 64);
         constexpr int TH = TPS / 2;   // tokens per lane with two pairs
-        const int kc = lane & 15, hh = lane >> 4;
+        const int kc = lane & 15, hh = lane >> 4, kp = 32 * slab + 2 * kc;
         // per-token scalars of the next chunk, loaded one chunk ahead into registers
         // (raw values: nothing waits on these loads until the chunk is processed)
         __nv_bfloat16 r_dt, r_A, r_l, r_ln, r_dtn;
@@ -556,7 +557,7 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                 for (int i = 0; i < TH; ++i) {
                     const int t = seg * TPS + hh * TH + i;
                     dd2[i] = dts[t];
-                    const uint32_t w = *reinterpret_cast<const uint32_t *>(rawT + t * K + 2 * kc);
+                    const uint32_t w = *reinterpret_cast<const uint32_t *>(rawT + t * K + kp);
                     th2[i] = f2u(w << 16, w & 0xFFFF0000u);
                 }
                 float2 ps = f2(0.f);
@@ -565,8 +566,8 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                 const float2 other = make_float2(__shfl_xor_sync(0xffffffffu, ps.x, 16),
                                                  __shfl_xor_sync(0xffffffffu, ps.y, 16));
                 if (hh == 0) {
-                    part[seg * K + 2 * kc] = ps.x + other.x;
-                    part[seg * K + 2 * kc + 1] = ps.y + other.y;
+                    part[seg * K + kp] = ps.x + other.x;
+                    part[seg * K + kp + 1] = ps.y + other.y;
                 } else {
                     lo2 = other;
                 }
@@ -677,7 +678,7 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                 float2 phi2 = lo2;
 #pragma unroll
                 for (int sg = 0; sg < Cf::NSEG - 1; ++sg)
-                    if (sg < seg) phi2 = __fadd2_rn(phi2, make_float2(part[sg * K + 2 * kc], part[sg * K + 2 * kc + 1]));
+                    if (sg < seg) phi2 = __fadd2_rn(phi2, make_float2(part[sg * K + kp], part[sg * K + kp + 1]));
                 float2 ph2[TH];
 #pragma unroll
                 for (int i = 0; i < TH; ++i) {
@@ -686,13 +687,16 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                 }
                 const int t0 = seg * TPS + hh * TH;
                 const int ie = e - t0;   // the chunk's last token, if it is this lane's
-                unsigned char *bs = slot + S::sB, *cs = slot + S::sC;
-                uint2 rb2[TH], rc2[TH];
+                unsigned char *bs = slot + S::sB + slab * (QR * 128), *cs = slot + S::sC + slab * (QR * 128);
+                uint2 rb2[TH * R], rc2[TH * R];
                 constexpr int kLA = TH < 4 ? TH : 4;
                 auto load_tok = [&](int i) {
-                    const uint32_t off = sw128(t0 + i, 4 * kc);
-                    rb2[i] = *reinterpret_cast<const uint2 *>(bs + off);
-                    if (OUT) rc2[i] = *reinterpret_cast<const uint2 *>(cs + off);
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        const uint32_t off = sw128((t0 + i) * R + r, 4 * kc);
+                        rb2[i * R + r] = *reinterpret_cast<const uint2 *>(bs + off);
+                        if (OUT) rc2[i * R + r] = *reinterpret_cast<const uint2 *>(cs + off);
+                    }
                 };
 #pragma unroll
                 for (int i = 0; i < kLA; ++i) load_tok(i);
@@ -710,34 +714,37 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                     __sincosf(r2.x, &s0, &c0);
                     __sincosf(r2.y, &s1, &c1);
                     if (i == ie) {   // the chunk's last token: rotation of the state at the chunk end
-                        v_cos(p)[2 * kc] = c0;
-                        v_cos(p)[2 * kc + 1] = c1;
-                        v_sin(p)[2 * kc] = s0;
-                        v_sin(p)[2 * kc + 1] = s1;
+                        v_cos(p)[kp] = c0;
+                        v_cos(p)[kp + 1] = c1;
+                        v_sin(p)[kp] = s0;
+                        v_sin(p)[kp + 1] = s1;
                         if (!OUT) {
-                            tot[1 + 2 * kc] += x2.x;
-                            tot[1 + 2 * kc + 1] += x2.y;
+                            tot[1 + kp] += x2.x;
+                            tot[1 + kp + 1] += x2.y;
                         }
                     }
                     const float2 cb = __fmul2_rn(make_float2(c0, c1), f2(sgB));
                     const float2 sb = __fmul2_rn(make_float2(s0, s1), f2(sgB));
                     const float2 nsb = __fmul2_rn(make_float2(s0, s1), f2(-sgB));
                     const bool valid = t0 + i < Qc;
-                    const uint32_t off = sw128(t0 + i, 4 * kc);
-                    // entries 2k (even) and 2k + 1 (odd) of the two pairs
-                    const uint2 vb = rb2[i];
-                    const float2 be = f2u(vb.x << 16, vb.y << 16), bo = f2u(vb.x & 0xFFFF0000u, vb.y & 0xFFFF0000u);
-                    const float2 oe = __ffma2_rn(cb, be, __fmul2_rn(sb, bo));
-                    const float2 oo = __ffma2_rn(cb, bo, __fmul2_rn(nsb, be));
-                    *reinterpret_cast<uint2 *>(bs + off) =
-                        valid ? make_uint2(pack_f16x2(oe.x, oo.x), pack_f16x2(oe.y, oo.y)) : make_uint2(0u, 0u);
-                    if (OUT) {
-                        const uint2 vc = rc2[i];
-                        const float2 ge = f2u(vc.x << 16, vc.y << 16), go = f2u(vc.x & 0xFFFF0000u, vc.y & 0xFFFF0000u);
-                        const float2 qe = __ffma2_rn(cb, ge, __fmul2_rn(sb, go));
-                        const float2 qo = __ffma2_rn(cb, go, __fmul2_rn(nsb, ge));
-                        *reinterpret_cast<uint2 *>(cs + off) =
-                            valid ? make_uint2(pack_f16x2(qe.x, qo.x), pack_f16x2(qe.y, qo.y)) : make_uint2(0u, 0u);
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        const uint32_t off = sw128((t0 + i) * R + r, 4 * kc);
+                        // entries 2k (even) and 2k + 1 (odd) of the two pairs
+                        const uint2 vb = rb2[i * R + r];
+                        const float2 be = f2u(vb.x << 16, vb.y << 16), bo = f2u(vb.x & 0xFFFF0000u, vb.y & 0xFFFF0000u);
+                        const float2 oe = __ffma2_rn(cb, be, __fmul2_rn(sb, bo));
+                        const float2 oo = __ffma2_rn(cb, bo, __fmul2_rn(nsb, be));
+                        *reinterpret_cast<uint2 *>(bs + off) =
+                            valid ? make_uint2(pack_f16x2(oe.x, oo.x), pack_f16x2(oe.y, oo.y)) : make_uint2(0u, 0u);
+                        if (OUT) {
+                            const uint2 vc = rc2[i * R + r];
+                            const float2 ge = f2u(vc.x << 16, vc.y << 16), go = f2u(vc.x & 0xFFFF0000u, vc.y & 0xFFFF0000u);
+                            const float2 qe = __ffma2_rn(cb, ge, __fmul2_rn(sb, go));
+                            const float2 qo = __ffma2_rn(cb, go, __fmul2_rn(nsb, ge));
+                            *reinterpret_cast<uint2 *>(cs + off) =
+                                valid ? make_uint2(pack_f16x2(qe.x, qo.x), pack_f16x2(qe.y, qo.y)) : make_uint2(0u, 0u);
+                        }
                     }
                 }
             } else {
