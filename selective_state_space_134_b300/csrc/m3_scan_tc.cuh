@@ -448,8 +448,9 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
         // Without BC normalisation (SISO, and any R with N = 128): each lane turns two adjacent pairs
         // (kp = 32 slab + 2 kc and kp + 1) of half of its warp's tokens (half hh), so that its shared-
         // memory words are 8 bytes; otherwise (and for MIMO with N = 64) one pair k per lane
-        constexpr bool kPair2 = !BCN && (R == 1 || N != 64);
+        constexpr bool kPair2 = !BCN;
         constexpr int TH = TPS / 2;   // tokens per lane with two pairs
+        static_assert(!kPair2 || TPS % 2 == 0, "two halves of whole tokens");
         const int kc = lane & 15, hh = lane >> 4, kp = 32 * slab + 2 * kc;
         // per-token scalars of the next chunk, loaded one chunk ahead into registers
         // (raw values: nothing waits on these loads until the chunk is processed)
