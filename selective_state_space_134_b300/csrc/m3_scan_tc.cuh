@@ -366,16 +366,16 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                 constexpr uint32_t bytes = Cf::BT * (OUT ? 2 : 1) + Cf::XT + Cf::TT;
                 mbar_expect_tx(bars + kRawFull + p, bytes);
                 const int qh = p_qh(u);
-                const int row0 = p_qb(u) * L + u.c * Q;
+                const int t0 = u.c * Q, b0 = p_qb(u);   // rows past the sequence end arrive as zeros
                 const int hg = qh / (H / a.G);   // B / C group of this head
 #pragma unroll
                 for (int sl = 0; sl < NSLAB; ++sl) {
-                    tma_load_4d(slot + S::sB + sl * QR * 128, &maps.B, 64 * sl, 0, hg, row0, bars + kRawFull + p);
+                    tma_load_5d(slot + S::sB + sl * QR * 128, &maps.B, 64 * sl, 0, hg, t0, b0, bars + kRawFull + p);
                     if (OUT)
-                        tma_load_4d(slot + S::sC + sl * QR * 128, &maps.C, 64 * sl, 0, hg, row0, bars + kRawFull + p);
+                        tma_load_5d(slot + S::sC + sl * QR * 128, &maps.C, 64 * sl, 0, hg, t0, b0, bars + kRawFull + p);
                 }
-                tma_load_4d(slot + S::sX, &maps.X, 0, 0, qh, row0, bars + kRawFull + p);
-                tma_load_3d(slot + S::sT, &maps.T, 0, qh, row0, bars + kRawFull + p);
+                tma_load_5d(slot + S::sX, &maps.X, 0, 0, qh, t0, b0, bars + kRawFull + p);
+                tma_load_4d(slot + S::sT, &maps.T, 0, qh, t0, b0, bars + kRawFull + p);
                 ++issued;
             }
             if (*abort_flag) {
@@ -449,6 +449,10 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
         // (kp = 32 slab + 2 kc and kp + 1) of half of its warp's tokens (half hh), so that its shared-
         // memory words are 8 bytes; otherwise (and for MIMO with N = 64) one pair k per lane
         constexpr bool kPair2 = !BCN;
+        // Rows past the sequence end come in as zeros (the input maps end there) and rotate to zeros, so
+        // the two-pair rotation needs no selects for them; the SISO build keeps them (without, the
+        // compiler's schedule spills at the register cap and runs 5 % slower)
+        constexpr bool kSelects = R == 1;
         constexpr int TH = TPS / 2;   // tokens per lane with two pairs
         static_assert(!kPair2 || TPS % 2 == 0, "two halves of whole tokens");
         const int kc = lane & 15, hh = lane >> 4, kp = 32 * slab + 2 * kc;
@@ -727,7 +731,7 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                     const float2 cb = __fmul2_rn(make_float2(c0, c1), f2(sgB));
                     const float2 sb = __fmul2_rn(make_float2(s0, s1), f2(sgB));
                     const float2 nsb = __fmul2_rn(make_float2(s0, s1), f2(-sgB));
-                    const bool valid = t0 + i < Qc;
+                    const bool valid = kSelects ? t0 + i < Qc : true;
 #pragma unroll
                     for (int r = 0; r < R; ++r) {
                         const uint32_t off = sw128((t0 + i) * R + r, 4 * kc);
@@ -1232,6 +1236,23 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                         tmem_ld16_nw(tmem + lane_base + cS + cb + 16, sv + 16);
                         // exp2(cA_t - cA_btok) <= 1 wherever it is used (btok <= tj < t)
                         const float u = (btok < ti) ? fast_exp2(ca - cA2[btok]) * invBC : 0.f;
+                        if (R == 1 && YB == 4 && btok + TB <= tmin) {
+                            // SISO block wholly before the row's token: (S o vj) u on packed pairs, no
+                            // per-column factors (fp32 y only: the 16-bit-y builds schedule it 6 % slower)
+                            float4 v4[TB / 4];
+#pragma unroll
+                            for (int q = 0; q < TB / 4; ++q) v4[q] = *reinterpret_cast<const float4 *>(vj + btok + 4 * q);
+                            tmem_wait_ld(sv);
+#pragma unroll
+                            for (int q = 0; q < 16; ++q) {
+                                const float4 w4 = v4[q / 2];
+                                const float2 w2 = (q & 1) ? make_float2(w4.z, w4.w) : make_float2(w4.x, w4.y);
+                                const float2 v2 = __fmul2_rn(__fmul2_rn(f2u(sv[2 * q], sv[2 * q + 1]), w2), f2(u));
+                                p16[q] = pack_f16x2(v2.x, v2.y);
+                            }
+                            tmem_st16(tmem + lane_base + cP + cb / 2, p16);
+                            continue;
+                        }
                         float um[TB];
 #pragma unroll
                         for (int q = 0; q < TB; q += 4) {
@@ -1434,29 +1455,32 @@ CUtensorMapL2promotion promo_for(int row_bytes) {
                            : (row_bytes <= 128 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B : CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
 }
 
-// 4-d map over a [b*L][H][R][inner] bf16 tensor, box = {64, R, 1, Q}, 128-byte swizzle
-bool map4(CUtensorMap *m, const void *base, int inner, int R, int H, long long rows, int Q,
+// 5-d map over a [batch][L][H][R][inner] bf16 tensor, box = {64, R, 1, Q, 1}, 128-byte swizzle.  Token
+// rows past a sequence's end are outside the map and arrive as zeros.
+bool map5(CUtensorMap *m, const void *base, int inner, int R, int H, int L, int batch, int Q,
           CUtensorMapL2promotion prom = CU_TENSOR_MAP_L2_PROMOTION_L2_256B) {
     EncodeFn enc = encode_fn();
     if (!enc) return false;
-    const cuuint64_t dims[4] = {(cuuint64_t)inner, (cuuint64_t)R, (cuuint64_t)H, (cuuint64_t)rows};
-    const cuuint64_t strides[3] = {(cuuint64_t)inner * 2, (cuuint64_t)inner * 2 * R, (cuuint64_t)inner * 2 * R * H};
-    const cuuint32_t box[4] = {64, (cuuint32_t)R, 1, (cuuint32_t)Q};
-    const cuuint32_t estr[4] = {1, 1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, estr,
+    const cuuint64_t dims[5] = {(cuuint64_t)inner, (cuuint64_t)R, (cuuint64_t)H, (cuuint64_t)L, (cuuint64_t)batch};
+    const cuuint64_t row = (cuuint64_t)inner * 2 * R * H;   // bytes per token
+    const cuuint64_t strides[4] = {(cuuint64_t)inner * 2, (cuuint64_t)inner * 2 * R, row, row * (cuuint64_t)L};
+    const cuuint32_t box[5] = {64, (cuuint32_t)R, 1, (cuuint32_t)Q, 1};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, prom,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
-// 3-d map over a [b*L][H][inner] bf16 tensor, box = {inner, 1, Q}
-bool map3(CUtensorMap *m, const void *base, int inner, int H, long long rows, int Q,
-          CUtensorMapL2promotion prom = CU_TENSOR_MAP_L2_PROMOTION_L2_256B) {
+// 4-d map over a [batch][L][H][inner] bf16 tensor, box = {inner, 1, Q, 1} (rows past the end arrive as zeros)
+bool map4t(CUtensorMap *m, const void *base, int inner, int H, int L, int batch, int Q,
+           CUtensorMapL2promotion prom = CU_TENSOR_MAP_L2_PROMOTION_L2_256B) {
     EncodeFn enc = encode_fn();
     if (!enc) return false;
-    const cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)H, (cuuint64_t)rows};
-    const cuuint64_t strides[2] = {(cuuint64_t)inner * 2, (cuuint64_t)inner * 2 * H};
-    const cuuint32_t box[3] = {(cuuint32_t)inner, 1, (cuuint32_t)Q};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+    const cuuint64_t dims[4] = {(cuuint64_t)inner, (cuuint64_t)H, (cuuint64_t)L, (cuuint64_t)batch};
+    const cuuint64_t row = (cuuint64_t)inner * 2 * H;
+    const cuuint64_t strides[3] = {(cuuint64_t)inner * 2, row, row * (cuuint64_t)L};
+    const cuuint32_t box[4] = {(cuuint32_t)inner, 1, (cuuint32_t)Q, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, prom,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -1539,10 +1563,10 @@ cudaError_t launch_bal(const TcMaps &maps, const ScanArgs &a, const ScanPlan &pl
 template <int N, int R, bool BCN, int QRT = (N == 64 ? 128 : 64)>
 cudaError_t run_tc(const ScanArgs &a, const ScanPlan &pl, cudaStream_t s) {
     using Cf = Cfg<N, R, QRT>;
-    const long long rows = (long long)a.batch * a.L;
+    const int L = a.L, nb = a.batch;
     TcMaps maps;
-    if (!map4(&maps.B, a.B, N, R, a.G, rows, Cf::Q) || !map4(&maps.C, a.C, N, R, a.G, rows, Cf::Q) ||
-        !map4(&maps.X, a.x, kP, R, a.H, rows, Cf::Q) || !map3(&maps.T, a.theta, N / 2, a.H, rows, Cf::Q) ||
+    if (!map5(&maps.B, a.B, N, R, a.G, L, nb, Cf::Q) || !map5(&maps.C, a.C, N, R, a.G, L, nb, Cf::Q) ||
+        !map5(&maps.X, a.x, kP, R, a.H, L, nb, Cf::Q) || !map4t(&maps.T, a.theta, N / 2, a.H, L, nb, Cf::Q) ||
         !map_y(&maps.Y, a.y, a.ydtype, R, a.H, a.L, a.batch, Cf::Q))
         return cudaErrorInvalidValue;
     cudaError_t e;
@@ -1562,8 +1586,8 @@ cudaError_t run_tc(const ScanArgs &a, const ScanPlan &pl, cudaStream_t s) {
         using Cs = Cfg<N, R, QRS>;
         if (QRS != QRT && pp.seglen % Cs::Q == 0) {
             TcMaps smaps = maps;
-            if (!map4(&smaps.B, a.B, N, R, a.G, rows, Cs::Q) || !map4(&smaps.X, a.x, kP, R, a.H, rows, Cs::Q) ||
-                !map3(&smaps.T, a.theta, N / 2, a.H, rows, Cs::Q))
+            if (!map5(&smaps.B, a.B, N, R, a.G, L, nb, Cs::Q) || !map5(&smaps.X, a.x, kP, R, a.H, L, nb, Cs::Q) ||
+                !map4t(&smaps.T, a.theta, N / 2, a.H, L, nb, Cs::Q))
                 return cudaErrorInvalidValue;
             e = launch_pass<N, R, false, M3_F32, BCN, QRS>(smaps, a, pp, npieces - 1, npieces, 1, s);
         } else {
@@ -1577,10 +1601,10 @@ cudaError_t run_tc(const ScanArgs &a, const ScanPlan &pl, cudaStream_t s) {
             // rows of one (token, head): B and C R N, x R P, theta N / 2 elements (a 64-wide slab of each
             // B and C row for N = 128, the neighbouring slab loaded next)
             TcMaps bm = maps;
-            if (!map4(&bm.B, a.B, N, R, a.G, rows, Cf::Q, promo_for(R * 64 * 2)) ||
-                !map4(&bm.C, a.C, N, R, a.G, rows, Cf::Q, promo_for(R * 64 * 2)) ||
-                !map4(&bm.X, a.x, kP, R, a.H, rows, Cf::Q, promo_for(R * kP * 2)) ||
-                !map3(&bm.T, a.theta, N / 2, a.H, rows, Cf::Q, promo_for(N)))
+            if (!map5(&bm.B, a.B, N, R, a.G, L, nb, Cf::Q, promo_for(R * 64 * 2)) ||
+                !map5(&bm.C, a.C, N, R, a.G, L, nb, Cf::Q, promo_for(R * 64 * 2)) ||
+                !map5(&bm.X, a.x, kP, R, a.H, L, nb, Cf::Q, promo_for(R * kP * 2)) ||
+                !map4t(&bm.T, a.theta, N / 2, a.H, L, nb, Cf::Q, promo_for(N)))
                 return cudaErrorInvalidValue;
             cudaError_t eb = a.ydtype == M3_F16    ? launch_bal<N, R, M3_F16, QRT>(bm, a, pl, s)
                              : a.ydtype == M3_BF16 ? launch_bal<N, R, M3_BF16, QRT>(bm, a, pl, s)

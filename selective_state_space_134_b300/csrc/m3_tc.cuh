@@ -217,6 +217,14 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, i
           "r"(smem_u32(mbar))
         : "memory");
 }
+__device__ __forceinline__ void tma_load_5d(void *dst, const CUtensorMap *map, int c0, int c1, int c2, int c3, int c4,
+                                            uint64_t *mbar) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5, %6}], [%7];"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
+          "r"(smem_u32(mbar))
+        : "memory");
+}
 // shared -> global tiled store, tracked by the issuing thread's bulk groups
 __device__ __forceinline__ void tma_store_5d(const CUtensorMap *map, const void *src, int c0, int c1, int c2, int c3,
                                              int c4) {
