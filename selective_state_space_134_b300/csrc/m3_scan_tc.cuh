@@ -450,9 +450,9 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
         // memory words are 8 bytes; otherwise (and for MIMO with N = 64) one pair k per lane
         constexpr bool kPair2 = !BCN;
         // Rows past the sequence end come in as zeros (the input maps end there) and rotate to zeros, so
-        // the two-pair rotation needs no selects for them; the SISO build keeps them (without, the
+        // the two-pair rotation needs no selects for them; the SISO N = 64 build keeps them (without, the
         // compiler's schedule spills at the register cap and runs 5 % slower)
-        constexpr bool kSelects = R == 1;
+        constexpr bool kSelects = R == 1 && N == 64;
         constexpr int TH = TPS / 2;   // tokens per lane with two pairs
         static_assert(!kPair2 || TPS % 2 == 0, "two halves of whole tokens");
         const int kc = lane & 15, hh = lane >> 4, kp = 32 * slab + 2 * kc;
@@ -946,7 +946,10 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                     const int row = item >> 3, c8 = item & 7, t = row / R;
                     const uint32_t off = sw128(row, 8 * c8);
                     uint4 o = make_uint4(0, 0, 0, 0), q = o;
-                    if (t < Qc) {
+                    // rows past the sequence end: x came in as zeros and w is 0 there, so both tiles get zeros
+                    // without a test (kept in the 16-bit-y SISO N = 64 build, whose schedule is 3 % faster with it)
+                    constexpr bool kXGuard = YB == 2 && N == 64 && R == 1;
+                    if (!kXGuard || t < Qc) {
                         const float sj = fast_exp2(ce - cA2[t]) * wv[t] * sgX;
                         const uint4 v = xv[i];
                         const float f[8] = {bf16_lo_f(v.x), bf16_hi_f(v.x), bf16_lo_f(v.y), bf16_hi_f(v.y),
@@ -966,7 +969,7 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                         if (OUT) q = make_uint4(qw[0], qw[1], qw[2], qw[3]);
                     }
                     *reinterpret_cast<uint4 *>(xh + off) = o;
-                    if (OUT) *reinterpret_cast<uint4 *>(xp + off) = q;   // rows past the end stay zero
+                    if (OUT) *reinterpret_cast<uint4 *>(xp + off) = q;
                 }
                 if (ptid < Q) {
                     const int bt = (ptid / TB) * TB;
