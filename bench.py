@@ -12,8 +12,10 @@ line carries the decode-step measurement (batch 256, 32 heads, one token per
 call over 1024 calls; also N = 64, R = 4 on a 512-slot state pool), the other
 prefill workloads (N = 128, MIMO R = 4, long context, and the headline shape
 with grouped B / C), the roofline of the dominant kernel (timed live through
-the library's event tracing; `traffic` from profiles/traffic.json while the
-library sources match its digest), the end-to-end figure through host
+the library's event tracing; the decode steps, which the library launches as
+programmatic dependents of one another, by CUDA events around all timed calls,
+so their rate is per call, gaps included; `traffic` from profiles/traffic.json
+while the library sources match its digest), the end-to-end figure through host
 buffers, the clocks seen, and the fp64 CPU oracle timed on this host's cores.
 --quick prints the headline alone; --decode-only prints the decode workloads
 alone.
@@ -286,16 +288,17 @@ def time_decode(m3, w, calls, warmup):
     for i in range(warmup):
         m3.decode_step(*argsets[i % len(pool)], state=state, y=ys[i % len(pool)])
     torch.cuda.synchronize()
-    m3.trace_begin(m3.KERNEL_DECODE, calls)
+    # no per-launch trace events here: consecutive steps are programmatic dependents of one another,
+    # and an event between two launches would serialise them; the kernel time is the per-call time
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
     for i in range(calls):
         m3.decode_step(*argsets[i % len(pool)], state=state, y=ys[i % len(pool)])
     e1.record()
     torch.cuda.synchronize()
-    n_tr, tr_ms = m3.trace_end()
     assert m3.device_status() == m3.M3_OK
-    return e0.elapsed_time(e1) / calls, tr_ms / max(n_tr, 1)
+    ms = e0.elapsed_time(e1) / calls
+    return ms, ms
 
 
 def time_decode_pooled(m3, w, calls, warmup, pool_factor=2):
@@ -313,16 +316,15 @@ def time_decode_pooled(m3, w, calls, warmup, pool_factor=2):
     for i in range(warmup):
         m3.decode_step_pooled(*argsets[i % len(toks)], slot=slot, pool=pool, y=ys[i % len(toks)])
     torch.cuda.synchronize()
-    m3.trace_begin(m3.KERNEL_DECODE, calls)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
     for i in range(calls):
         m3.decode_step_pooled(*argsets[i % len(toks)], slot=slot, pool=pool, y=ys[i % len(toks)])
     e1.record()
     torch.cuda.synchronize()
-    n_tr, tr_ms = m3.trace_end()
     assert m3.device_status() == m3.M3_OK
-    return e0.elapsed_time(e1) / calls, tr_ms / max(n_tr, 1)
+    ms = e0.elapsed_time(e1) / calls
+    return ms, ms
 
 
 def e2e_prefill(m3, w, inp, steps, warmup, slices=8):

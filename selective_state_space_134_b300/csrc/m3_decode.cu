@@ -635,6 +635,10 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap hmap, const __grid_constan
         bulk_load(sg + Lo.xp, xprev + (size_t)sh0 * R * P, xn, bar);
     };
 
+    // Programmatic dependent launch: the next step's grid may be scheduled now (its CTAs take SMs as
+    // these leave and set up while the last units drain); this grid touches no global memory before
+    // the grid it depends on has completed and its writes are visible
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (tid == 0) {
         tma_prefetch_desc(&hmap);
         if (SWZ) {
@@ -647,6 +651,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap hmap, const __grid_constan
         *abort_flag = 0;
     }
     __syncthreads();
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     int issued = 0;
     if (tid == 0)
         for (; issued < nst - 1 && issued < mine; ++issued) issue(issued);
@@ -897,14 +902,25 @@ cudaError_t launch_mma_t(int nbh, int H, int G, const int *slot, int pool, const
     const int nunit = nbh / HPU;
     const int grid = nunit < per_sm * sm_count() ? nunit : per_sm * sm_count();
     using bf = __nv_bfloat16;
+    // launched as a programmatic dependent of the kernel before it in the stream (consecutive decode
+    // steps overlap one's launch and set-up with the other's tail; see the kernel's entry)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kMmaThreads);
+    cfg.dynamicSmemBytes = Lo.total;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     trace_mark(M3_KERNEL_DECODE, s, 0);
-    kern<<<grid, kMmaThreads, Lo.total, s>>>(cache.hmap, bmap, cmap, cache.bpmap, nunit, nst, slot, pool, H, G,
-                                            (const bf *)x, (const bf *)B, (const bf *)C, (const bf *)dt,
-                                            (const bf *)A, (const bf *)lam, (const bf *)theta, (bf *)Bprev,
-                                            (bf *)xprev, y, yd, status);
+    err = cudaLaunchKernelEx(&cfg, kern, cache.hmap, bmap, cmap, cache.bpmap, nunit, nst, slot, pool, H, G,
+                             (const bf *)x, (const bf *)B, (const bf *)C, (const bf *)dt, (const bf *)A,
+                             (const bf *)lam, (const bf *)theta, (bf *)Bprev, (bf *)xprev, y, yd, status);
     trace_mark(M3_KERNEL_DECODE, s, 1);
     count_launch();
-    return cudaGetLastError();
+    return err != cudaSuccess ? err : cudaGetLastError();
 }
 
 template <int R, int N, int HPU>
