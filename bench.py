@@ -11,11 +11,13 @@ head), inputs resident in HBM and larger than L2 (no flush needed).  The same
 line carries the decode-step measurement (batch 256, 32 heads, one token per
 call over 1024 calls; also N = 64, R = 4 on a 512-slot state pool), the other
 prefill workloads (N = 128, MIMO R = 4, long context, and the headline shape
-with grouped B / C), the roofline of the dominant kernel (timed live through
-the library's event tracing; the decode steps, which the library launches as
-programmatic dependents of one another, by CUDA events around all timed calls,
-so their rate is per call, gaps included; `traffic` from profiles/traffic.json
-while the library sources match its digest), the end-to-end figure through host
+with grouped B / C), the roofline of the dominant kernel (timed live by CUDA
+events around all timed steps on the launch stream, so rates are per step,
+gaps included: the library launches its kernels as programmatic dependents of
+the kernel before them, and trace events between launches would serialise
+them; a step of several launches also reports the output pass's own time from
+a second, traced run; `traffic` from profiles/traffic.json while the library
+sources match its digest), the end-to-end figure through host
 buffers, the clocks seen, and the fp64 CPU oracle timed on this host's cores.
 --quick prints the headline alone; --decode-only prints the decode workloads
 alone.
@@ -222,8 +224,6 @@ def time_prefill(m3, w, steps, warmup, trace_kernel=None, groups=0, y_dtype=torc
     for _ in range(warmup):
         step()
     torch.cuda.synchronize()
-    if trace_kernel is not None:
-        m3.trace_begin(trace_kernel, steps)
     n0 = m3.launch_count()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
@@ -233,7 +233,16 @@ def time_prefill(m3, w, steps, warmup, trace_kernel=None, groups=0, y_dtype=torc
     torch.cuda.synchronize()
     launches = m3.launch_count() - n0
     ms = e0.elapsed_time(e1)
-    traced = m3.trace_end() if trace_kernel is not None else (0, 0.0)
+    traced = (0, 0.0)
+    if trace_kernel is not None and launches > steps:
+        # several launches a step: the traced kernel's own time from a second run of the same steps
+        # (trace events between launches would hold back the programmatic dependent launches of the
+        # timed run, so they stay out of it)
+        m3.trace_begin(trace_kernel, steps)
+        for _ in range(steps):
+            step()
+        torch.cuda.synchronize()
+        traced = m3.trace_end()
     assert m3.device_status() == m3.M3_OK
     return {"ms": ms, "launches": launches, "traced": traced, "inputs": inp, "ws": ws_bytes}
 
@@ -513,7 +522,8 @@ def run_ours(args):
         m3.scan_fwd(*a, state_out=st, y=y, workspace=work)
     barrier(ws)
     torch.cuda.synchronize()
-    m3.trace_begin(m3.KERNEL_PREFILL_OUTPUT, args.steps)
+    # one launch a step: the step's CUDA-event time is the kernel's (no per-launch trace events in the
+    # timed region; they would hold back the programmatic dependent launches)
     n0 = m3.launch_count()
     if sampler:
         sampler.mark("t0")
@@ -528,7 +538,7 @@ def run_ours(args):
     barrier(ws)
     launches = m3.launch_count() - n0
     ms = max_over_ranks(e0.elapsed_time(e1), ws)
-    traced = m3.trace_end()
+    traced = (0, 0.0)
     status = m3.device_status()
     clocks = sampler.stop() if sampler else None
     if status != m3.M3_OK:

@@ -323,6 +323,10 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
     };
 
     // ---- set-up
+    // Programmatic dependent launch: the next kernel in the stream may be scheduled from now on (its CTAs
+    // take SMs as these leave); nothing below touches global memory or TMEM before the grid this one
+    // depends on has completed and its writes are visible
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (tid == 0) {
         for (int p = 0; p < 2; ++p) {
             mbar_init(bars + kRawFull + p, 1);
@@ -345,6 +349,7 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
         }
     }
     for (int i = tid; i < 1 + K; i += kThreads) tot[i] = 0.f;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
     fence_before();
     __syncthreads();
@@ -1519,12 +1524,22 @@ cudaError_t launch_pass(const TcMaps &maps, const ScanArgs &a, const ScanPlan &p
     if (!status) return cudaErrorUnknown;
     const long long grid = (long long)a.batch * a.H * nlaunch;
     const int kid = OUT ? M3_KERNEL_PREFILL_OUTPUT : M3_KERNEL_PREFILL_STATE;
+    // a programmatic dependent of the kernel before it in the stream (see the kernel's set-up)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = Sm::kAlloc;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     trace_mark(kid, s, 0);
-    kern<<<(unsigned)grid, kThreads, Sm::kAlloc, s>>>(maps, a, pl.seglen, pl.nseg, nlaunch, ws_stride, ws_step,
-                                                      status, 0ull, 0);
+    e = cudaLaunchKernelEx(&cfg, kern, maps, a, pl.seglen, pl.nseg, nlaunch, ws_stride, ws_step, status, 0ull, 0);
     trace_mark(kid, s, 1);
     count_launch();
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 // A fresh value of the hand-off flags per balanced launch (so that flags left in a reused workspace never
