@@ -42,6 +42,10 @@
  *     default stream).  The return value reports argument validation and
  *     launch status; on an argument error nothing is launched or written.
  *     Device-side wait limits report through mamba3_device_status().
+ *     The tensor-core prefill (one-wave plans) and decode kernels are
+ *     launched as programmatic dependents of the kernel before them in the
+ *     stream: they may be scheduled while it finishes, and touch no global
+ *     memory until it has completed (ordering on the stream is unchanged).
  *   - batch = 0 is a successful call that touches nothing (pointers are not
  *     inspected).
  *   - Inputs must not overlap outputs, except that a state may be updated in
