@@ -346,6 +346,35 @@ def test_split_prefill_and_decode_resume_equal_full_prefill():
     assert_err(to_f64(st.h), to_f64(s_full.h), tol, "h")
 
 
+@pytest.mark.parametrize("wname,over", [("siso_n64", dict(batch=3, nheads=4)), ("mimo_r4", dict(batch=2, nheads=3)),
+                                        ("siso_n128", dict(batch=2, nheads=3))])
+def test_alternating_prefill_and_decode_on_one_stream_match_oracle(wname, over):
+    # prefill pieces and single decode steps alternate on one stream with no host synchronisation
+    # between the calls: each call reads the state the call before wrote (the kernels are launched
+    # as programmatic dependents and must wait for it), in both orders (prefill after decode and
+    # decode after prefill); every output and the final state against the oracle
+    pieces = [70, 3, 45, 1, 1, 60, 2]   # tokens per call: prefill for >= 3 (ragged chunks), else decode steps
+    w = WORKLOADS[wname].with_(seqlen=sum(pieces), **over)
+    inp = prefill_inputs(w, "cuda")
+    st = m3.State.zeros(w.batch, w.nheads, w.P, w.N, w.R, inp["x"].dtype)
+    ys, t = [], 0
+    for n in pieces:
+        if n >= 3:
+            part = {k: v[:, t:t + n].contiguous() for k, v in inp.items()}
+            ys.append(m3.scan_fwd(*(part[k] for k in KEYS), state_in=st, state_out=st))
+        else:
+            for i in range(n):
+                ys.append(m3.decode_step(*(inp[k][:, t + i].contiguous() for k in KEYS), state=st).unsqueeze(1))
+        t += n
+    assert m3.device_status() == m3.M3_OK
+    torch.cuda.synchronize()
+    yr, hr, bpr, xpr = oracle_full(inp)
+    tol = TOL[w.dtype]
+    assert_err(to_f64(torch.cat(ys, dim=1)), yr, tol, "y")
+    assert_err(to_f64(st.h), hr, tol, "h")
+    assert np.array_equal(to_f64(st.B_prev), bpr) and np.array_equal(to_f64(st.x_prev), xpr)
+
+
 def test_in_place_state_update_equals_out_of_place():
     w = WORKLOADS["siso_n64"].with_(batch=2, nheads=3, seqlen=130)
     inp = prefill_inputs(w, "cuda")
