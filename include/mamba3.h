@@ -406,7 +406,10 @@ typedef enum {
  * m3_kernel) is bracketed by two CUDA events recorded on the stream it is
  * launched on.  Events are created here on the current device (no device
  * memory is allocated).  A trace already running is discarded.  Returns
- * M3_ERR_INVALID_ARG for a bad kernel id or max_launches < 1.
+ * M3_ERR_INVALID_ARG for a bad kernel id or max_launches < 1.  The events
+ * sit between launches on the stream, so a traced launch does not overlap
+ * the kernel before it (see programmatic dependents above): time rates with
+ * events around a whole untraced run, and trace for one kernel's share.
  */
 m3_status mamba3_trace_begin(int kernel, int max_launches);
 

@@ -919,8 +919,9 @@ cudaError_t launch_mma_t(int nbh, int H, int G, const int *slot, int pool, const
                              (const bf *)x, (const bf *)B, (const bf *)C, (const bf *)dt, (const bf *)A,
                              (const bf *)lam, (const bf *)theta, (bf *)Bprev, (bf *)xprev, y, yd, status);
     trace_mark(M3_KERNEL_DECODE, s, 1);
+    if (err != cudaSuccess) return err;
     count_launch();
-    return err != cudaSuccess ? err : cudaGetLastError();
+    return cudaGetLastError();
 }
 
 template <int R, int N, int HPU>

@@ -450,9 +450,9 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
         // ================================================================ prologue
         const int ptid = tid - kProW0 * 32, pw = warp - kProW0;
         const int slab = pw % NSLAB, seg = pw / NSLAB, k = 32 * slab + lane;
-        // Without BC normalisation (SISO, and any R with N = 128): each lane turns two adjacent pairs
-        // (kp = 32 slab + 2 kc and kp + 1) of half of its warp's tokens (half hh), so that its shared-
-        // memory words are 8 bytes; otherwise (and for MIMO with N = 64) one pair k per lane
+        // Without BC normalisation each lane turns two adjacent pairs (kp = 32 slab + 2 kc and kp + 1) of
+        // half of its warp's tokens (half hh), so that its shared-memory words are 8 bytes; with it, one
+        // pair k per lane (the two-pair form measured slower there, its gains and biases held or reloaded)
         constexpr bool kPair2 = !BCN;
         // Rows past the sequence end come in as zeros (the input maps end there) and rotate to zeros, so
         // the two-pair rotation needs no selects for them; the SISO N = 64 build keeps them (without, the
@@ -764,7 +764,7 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                 unsigned char *bs = slot + S::sB + slab * (QR * 128);
                 unsigned char *cs = slot + S::sC + slab * (QR * 128);
                 if constexpr (R == 1 || N != 64) {
-                    // SISO (and N = 128): fully unrolled, the raw words loaded a few tokens ahead
+                    // (BC normalisation) SISO and N = 128: fully unrolled, the raw words loaded a few tokens ahead
                     // angles of all the thread's tokens first (a short FMA chain), then
                     // independent rotations the scheduler can overlap
                     float ph[TPS];
@@ -853,9 +853,8 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                         }
                     }
                 } else {
-                    // MIMO with N = 64: a few tokens per thread; one token pair per iteration of a rolled
-                    // loop keeps the code (and the instruction-cache footprint) small (+2 % there, -1 %
-                    // with N = 128)
+                    // (BC normalisation) MIMO with N = 64: a few tokens per thread; one token pair per
+                    // iteration of a rolled loop keeps the code (and the instruction-cache footprint) small
                     const int ie = e - seg * TPS;   // the chunk's last token, if it is this thread's
                     // this thread's BC gains (entries 2k, 2k + 1 of B and of C)
                     float2 wkB = f2(1.f), wkC = f2(1.f);
@@ -1538,8 +1537,9 @@ cudaError_t launch_pass(const TcMaps &maps, const ScanArgs &a, const ScanPlan &p
     trace_mark(kid, s, 0);
     e = cudaLaunchKernelEx(&cfg, kern, maps, a, pl.seglen, pl.nseg, nlaunch, ws_stride, ws_step, status, 0ull, 0);
     trace_mark(kid, s, 1);
+    if (e != cudaSuccess) return e;
     count_launch();
-    return e != cudaSuccess ? e : cudaGetLastError();
+    return cudaGetLastError();
 }
 
 // A fresh value of the hand-off flags per balanced launch (so that flags left in a reused workspace never
