@@ -375,6 +375,32 @@ def test_alternating_prefill_and_decode_on_one_stream_match_oracle(wname, over):
     assert np.array_equal(to_f64(st.B_prev), bpr) and np.array_equal(to_f64(st.x_prev), xpr)
 
 
+@pytest.mark.parametrize("wname,over", [("siso_n64", dict(nheads=2, seqlen=129)), ("siso_n128", dict(nheads=2, seqlen=65)),
+                                        ("mimo_r4", dict(nheads=2, seqlen=33)),
+                                        ("long_n128_r4", dict(nheads=2, seqlen=1041))])
+def test_last_chunk_sees_nothing_of_the_next_sequence(wname, over):
+    # Sequences whose last chunk holds one token (or a few); the batch row after the first one
+    # starts with B, C and x set to +inf.  The tensor-core prefill's input tiles end at each
+    # sequence's last token, so none of those values may reach the first row's last chunk: a value
+    # read past the end would turn into NaN (a zero weight times inf) in its scores, its state or its
+    # tile scales, where the oracle, which sees each sequence alone, has finite results.  The planted
+    # row's own outputs are not compared (they are not finite); the rows before and after it are
+    w = WORKLOADS[wname].with_(batch=3, **over)
+    inp = prefill_inputs(w, "cuda")
+    for k in ("B", "C", "x"):
+        v = inp[k].float()
+        v[1, :8] = float("inf")
+        inp[k] = v.to(inp[k].dtype)
+    y, so = gpu_scan(inp)
+    yr, hr, Br, xr = oracle_full(inp)
+    tol = TOL[w.dtype]
+    for b in (0, 2):
+        assert_err(to_f64(y[b:b + 1]), yr[b:b + 1], tol, f"y batch {b}")
+        assert_err(to_f64(so.h[b:b + 1]), hr[b:b + 1], tol, f"h batch {b}")
+    np.testing.assert_array_equal(to_f64(so.B_prev), Br)
+    np.testing.assert_array_equal(to_f64(so.x_prev), xr)
+
+
 def test_in_place_state_update_equals_out_of_place():
     w = WORKLOADS["siso_n64"].with_(batch=2, nheads=3, seqlen=130)
     inp = prefill_inputs(w, "cuda")
