@@ -633,6 +633,25 @@ def test_more_sequences_than_sms_match_oracle(N, R, b, H, L, with_state, kw):
     assert torch.equal(y, y2)
 
 
+@pytest.mark.parametrize("N,R,b,H,G,L", [(64, 4, 4, 40, 8, 300), (64, 1, 5, 36, 12, 333), (128, 4, 2, 80, 20, 150)])
+def test_more_sequences_than_sms_with_grouped_bc_match_oracle(N, R, b, H, G, L):
+    # more sequences than SMs (the balanced pass: equal chunk ranges over one CTA per SM, its own input
+    # maps) with B and C shared by groups of H / G heads, an initial state and a carry; against the
+    # oracle on the per-head expansion
+    w = WORKLOADS["mimo_r4"].with_(batch=b, nheads=H, seqlen=L, N=N, R=R)
+    inp = prefill_inputs(w, "cuda")
+    full = dict(inp)
+    for k in ("B", "C"):
+        inp[k], full[k] = _grouped(inp[k], H, G, 2)
+    st = random_state(b, H, w.P, N, R, inp["x"].dtype, seed=G)
+    y, so = gpu_scan(inp, state_in=st)
+    yr, hr, Br, xr = oracle_full(full, st)
+    assert_err(to_f64(y), yr, TOL[w.dtype], "y")
+    assert_err(to_f64(so.h), hr, TOL[w.dtype], "h")
+    np.testing.assert_array_equal(to_f64(so.B_prev), Br)
+    np.testing.assert_array_equal(to_f64(so.x_prev), xr)
+
+
 def test_more_sequences_than_sms_with_bc_match_oracle():
     from selective_state_space_134_b300.synth import bc_params
     w = WORKLOADS["mimo_r4"].with_(batch=2, nheads=96, seqlen=180)
