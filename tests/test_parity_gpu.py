@@ -503,6 +503,35 @@ def test_staged_host_prefill_matches_device_prefill(slices, groups):
     assert torch.equal(st.B_prev, s_ref.B_prev) and torch.equal(st.x_prev, s_ref.x_prev)
 
 
+@pytest.mark.parametrize("wname,over,slices", [("long_n128_r4", dict(batch=1, nheads=6, seqlen=1500), 3),
+                                               ("mimo_r4", dict(batch=2, nheads=5, seqlen=700), 4)])
+def test_staged_host_prefill_of_segmented_ranges_matches_oracle(wname, over, slices):
+    # the staged prefill from host memory where every token range is itself a segmented prefill (state
+    # pass, segment pass, output pass on few sequences), the state and carry handed from range to
+    # range on the device; y and the final state copied back, against the oracle
+    w = WORKLOADS[wname].with_(**over)
+    inp = prefill_inputs(w, "cuda")
+    st_in = random_state(w.batch, w.nheads, w.P, w.N, w.R, inp["x"].dtype, seed=slices)
+    host = {k: v.cpu().pin_memory() for k, v in inp.items()}
+    dev = {k: torch.empty_like(v) for k, v in inp.items()}
+    y = torch.empty(inp["x"].shape, dtype=torch.float32, device="cuda")
+    y_host = torch.zeros(y.shape, dtype=torch.float32).pin_memory()
+    st = m3.State.zeros(w.batch, w.nheads, w.P, w.N, w.R, inp["x"].dtype)
+    h_host = torch.zeros(st.h.shape, dtype=torch.float32).pin_memory()
+    side = torch.cuda.Stream()
+    m3.mamba3.scan_fwd_staged(host, dev, y_host, y, state_in=st_in, state_out=st, host_h=h_host, slices=slices,
+                              copy_stream=side)
+    side.synchronize()
+    torch.cuda.synchronize()
+    assert m3.device_status() == m3.M3_OK
+    yr, hr, Br, xr = oracle_full(inp, st_in)
+    tol = TOL[w.dtype]
+    assert_err(y_host.double().numpy(), yr, tol, "y")
+    assert_err(h_host.double().numpy(), hr, tol, "h")
+    np.testing.assert_array_equal(to_f64(st.B_prev), Br)
+    np.testing.assert_array_equal(to_f64(st.x_prev), xr)
+
+
 # ---------------------------------------------------------------- output element type
 
 Y16 = (torch.float16, torch.bfloat16)
