@@ -57,14 +57,24 @@ bool tc_plan(const m3_dims &d, int sms, ScanPlan *pl) {
     int seglen = L > 0 ? (L + nseg - 1) / nseg : Q;
     seglen = ((seglen + Qs - 1) / Qs) * Qs;
     nseg = L > 0 ? (L + seglen - 1) / seglen : 1;
-    // the state pass covers segments 0 .. nseg - 2: split them into as many whole pieces of
-    // at least 8 output-pass chunks as one wave of CTAs holds
+    // the state pass covers segments 0 .. nseg - 2, cut into nsub whole pieces (of at least 8 output-pass
+    // chunks) each: one CTA a piece, in as many waves as it takes.  Its time goes as waves / nsub (a
+    // wave lasts one piece), so nsub is the smallest count that minimises that: more, shorter pieces
+    // let the last wave fill the SMs (64 sequences: 16 pieces, 7 waves, 0.4375 of a segment a CTA
+    // slot against 0.5 for one wave of 2 pieces)
     int nsub = 1;
     if (nseg > 1) {
-        const long long cap = sms / (seqs * (nseg - 1));
+        const long long units = seqs * (nseg - 1);
         const int chunks = seglen / Q, schunks = seglen / Qs;
-        for (int c = 2; c <= cap && chunks / c >= 8; ++c)
-            if (schunks % c == 0) nsub = c;
+        double best = (double)((units + sms - 1) / sms);
+        for (int c = 2; c <= 64 && chunks / c >= 8; ++c) {
+            if (schunks % c) continue;
+            const double t = (double)((units * c + sms - 1) / sms) / c;
+            if (t < best - 1e-9) {
+                best = t;
+                nsub = c;
+            }
+        }
     }
     pl->Q = Q;
     pl->nseg = nseg;
