@@ -554,9 +554,11 @@ def run_ours(args):
         extra["decode"] = {"metric": "decode tokens/s", "unit": "tokens/s", "workloads": dec}
         # other prefill workloads
         pre = {}
-        for name, steps in (("siso_n128", 20), ("mimo_r4", 5), ("long_n128_r4", 2)):
+        # (at least 3 warm-up steps, and enough timed steps that host-side call overhead and the
+        # queue's start stay out of the rate: tens of milliseconds a workload)
+        for name, steps in (("siso_n128", 100), ("mimo_r4", 10), ("long_n128_r4", 3)):
             wp = WORKLOADS[name]
-            r = time_prefill(m3, wp, steps, 1, m3.KERNEL_PREFILL_OUTPUT)
+            r = time_prefill(m3, wp, steps, 3, m3.KERNEL_PREFILL_OUTPUT)
             pre[name] = prefill_line(m3, wp, r, steps, hbm_peak, peak_kind)
             pre[name]["launches_per_step"] = r["launches"] / steps
             del r
@@ -572,8 +574,8 @@ def run_ours(args):
                     ("mimo_r4_chunk_rule_q16", "mimo_r4", dict(chunk=16)))
         for key, name, kw in variants:
             wp = WORKLOADS[name]
-            steps = 20 if name == HEADLINE else 5
-            r = time_prefill(m3, wp, steps, 1, m3.KERNEL_PREFILL_OUTPUT, **kw)
+            steps = 100 if name == HEADLINE else 10
+            r = time_prefill(m3, wp, steps, 3, m3.KERNEL_PREFILL_OUTPUT, **kw)
             pre[key] = prefill_line(m3, wp, r, steps, hbm_peak, peak_kind, groups=kw.get("groups", 0),
                                     y_bytes=kw.get("y_dtype", torch.float32).itemsize)
             pre[key]["launches_per_step"] = r["launches"] / steps
@@ -582,9 +584,9 @@ def run_ours(args):
         extra["prefill"] = pre
         # backward pass (training): siso_n64 and mimo_r4; the ALU roofline of its fp32 contractions
         bwd = {}
-        for name, steps in ((HEADLINE, 3), ("mimo_r4", 1)):
+        for name, steps in ((HEADLINE, 5), ("mimo_r4", 2)):
             wb = WORKLOADS[name]
-            ms_b, ws_b = time_backward(m3, wb, steps, 1)
+            ms_b, ws_b = time_backward(m3, wb, steps, 3)
             fl = backward_flops(wb)
             peak = fp32_peak_tflops()
             bwd[name] = {"tokens_per_s": wb.batch * wb.seqlen / (ms_b * 1e-3), "ms_per_step": ms_b,
