@@ -262,7 +262,8 @@ def prefill_line(m3, w, res, steps, hbm_peak, peak_kind, groups=0, y_bytes=4):
         "ms_per_step": ms_step,
         "roofline": {"bound": "hbm", "kernel": "whole prefill step", "achieved": round(achieved, 1),
                      "peak": hbm_peak, "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
-                     "traffic": traffic_for("prefill_output", w.name + (f"_g{groups}" if groups else "")),
+                     "traffic": (traffic_for("prefill_output", w.name + (f"_g{groups}" if groups else ""))
+                                 if _full_size(w) else None),
                      "algorithmic_bytes": algo,
                      "extra_bytes_wide_y": int(w.token_heads * y_surplus_per_token_head(w, y_bytes)),
                      "y_bytes": y_bytes,
@@ -270,6 +271,13 @@ def prefill_line(m3, w, res, steps, hbm_peak, peak_kind, groups=0, y_bytes=4):
                                      "frac": round(achieved_k / hbm_peak, 4)},
                      "peak_source": peak_kind},
     }
+
+
+def _full_size(w) -> bool:
+    """The traffic records are of the named workloads at their own sizes: a resized run has none."""
+    from selective_state_space_134_b300.synth import WORKLOADS
+    ref = WORKLOADS.get(w.name)
+    return ref is not None and ref.token_heads == w.token_heads and ref.R == w.R and ref.N == w.N
 
 
 def traffic_for(kernel, workload):
