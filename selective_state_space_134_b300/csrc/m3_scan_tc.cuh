@@ -1145,12 +1145,12 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
             }
         };
 
-        if constexpr (!BAL) {
-            publish_state(0, load_start(piece_at(0)));
-            fence_proxy_async();
-            fence_before();
-            mbar_arrive(bars + kStateReady + 0);
-        }
+        // the first piece's start state; a later piece's is loaded where the piece before ends (below), so
+        // that the loop holds one copy of the load and of the fp16 publication (instruction cache)
+        publish_state(0, load_start(piece_at(0)));
+        fence_proxy_async();
+        fence_before();
+        mbar_arrive(bars + kStateReady + 0);
         Pos eu = piece_at(0);
         for (int it = 0; it < nchunks; ++it, eu = pos_next(eu)) {
             const int p = it & 1;
@@ -1159,17 +1159,6 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
             const float *cA2 = v_cA(p), *gv = v_g(p), *vj = v_vj(p), *sg = v_sig(p);
             const bool last_chunk = it == nchunks - 1;
             const bool piece_end = BAL && eu.c == p_ce(eu) - 1;   // (balanced plan) the last chunk of a piece
-            if constexpr (BAL) {
-                if (eu.c == p_cb(eu)) {
-                    // a piece starts here: its state into TMEM and its fp16 copy for the MMAs (one call
-                    // site of the load, for the instruction cache); later chunks get theirs from the update
-                    const float hm = load_start(eu);
-                    publish_state(p, hm);
-                    fence_proxy_async();
-                    fence_before();
-                    mbar_arrive(bars + kStateReady + p);
-                }
-            }
             // one thread waits for the chunk's vectors and first MMAs; the named barrier
             // releases the other epilogue warps without them polling
             if (ew == 0 && lane == 0) {
@@ -1369,12 +1358,15 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                         }
                     }
                 }
-                if (!(piece_end && it + 1 < nchunks)) {   // (the next piece publishes its own start state)
-                    publish_state((it + 1) & 1, m);
-                    fence_proxy_async();
-                    fence_before();
-                    mbar_arrive(bars + kStateReady + ((it + 1) & 1));
+                // the next chunk's state: the one just updated, or (balanced plan, a piece ended here) the
+                // next piece's start state
+                if constexpr (BAL) {
+                    if (piece_end && it + 1 < nchunks) m = load_start(pos_next(eu));
                 }
+                publish_state((it + 1) & 1, m);
+                fence_proxy_async();
+                fence_before();
+                mbar_arrive(bars + kStateReady + ((it + 1) & 1));
             }
             // ---- y = Ya + exp(cA_t) Yi
             if (OUT) {
