@@ -1152,7 +1152,21 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
         fence_before();
         mbar_arrive(bars + kStateReady + 0);
         Pos eu = piece_at(0);
-        for (int it = 0; it < nchunks; ++it, eu = pos_next(eu)) {
+        int it = 0;
+        // pieces (one without the balanced plan), then their chunks: a later piece's start state is loaded
+        // and published here, outside the chunk loop, whose code then holds none of it (instruction cache)
+        for (int pi = 0; pi < (BAL ? npc : 1); ++pi) {
+        if constexpr (BAL) {
+            if (pi > 0) {
+                eu = piece_at(pi);
+                const float hm = load_start(eu);
+                publish_state(it & 1, hm);
+                fence_proxy_async();
+                fence_before();
+                mbar_arrive(bars + kStateReady + (it & 1));
+            }
+        }
+        for (; it < nchunks && (!BAL || eu.c < p_ce(eu)); ++it, ++eu.c) {
             const int p = it & 1;
             const uint32_t ph = (it >> 1) & 1;
             const int s0 = eu.c * Q, Qc = min(Q, t_stop - s0), e = Qc - 1;
@@ -1358,15 +1372,12 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                         }
                     }
                 }
-                // the next chunk's state: the one just updated, or (balanced plan, a piece ended here) the
-                // next piece's start state
-                if constexpr (BAL) {
-                    if (piece_end && it + 1 < nchunks) m = load_start(pos_next(eu));
+                if (!(piece_end && it + 1 < nchunks)) {   // (a next piece publishes its own start state)
+                    publish_state((it + 1) & 1, m);
+                    fence_proxy_async();
+                    fence_before();
+                    mbar_arrive(bars + kStateReady + ((it + 1) & 1));
                 }
-                publish_state((it + 1) & 1, m);
-                fence_proxy_async();
-                fence_before();
-                mbar_arrive(bars + kStateReady + ((it + 1) & 1));
             }
             // ---- y = Ya + exp(cA_t) Yi
             if (OUT) {
@@ -1435,6 +1446,7 @@ tc_segment_kernel(const __grid_constant__ TcMaps maps, ScanArgs a, int seglen, i
                 }
             }
             if (!OUT) mbar_arrive(bars + kEpiDone + p);
+        }
         }
         if (OUT && ew == 0 && lane == 0) bulk_wait<0>();
         // ---- carry out (last segment; the balanced plan wrote it at each sequence's end)
