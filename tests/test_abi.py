@@ -261,3 +261,22 @@ def test_backward_validation():
     assert lib.mamba3_scan_bwd(ctypes.byref(d), None, None, ctypes.byref(gin), ctypes.byref(gout),
                                ws, n.value, None) == api.M3_ERR_INVALID_ARG
     assert m3.launch_count() == before
+
+
+def test_long_prefill_plan_cuts_the_state_pass_into_full_waves():
+    # The tensor-core plan of the long-context workload (64 sequences of 131072 tokens, N = 128, R = 4)
+    # on 148 SMs: two segments, the first cut into the smallest number of whole pieces that minimises
+    # waves / pieces (16 pieces: 1024 CTAs in 7 waves, 0.4375 of a segment per CTA slot, against 0.5
+    # for one wave of 2 pieces), so the workspace holds (2 - 1) * 16 + 1 = 17 state slots per sequence
+    # and the segment totals of 16 pieces.  (The workspace query covers the SIMT plan too; here it has
+    # 5 segments and needs less.)
+    if torch.cuda.is_available() and torch.cuda.get_device_properties(0).multi_processor_count != 148:
+        pytest.skip("the plan is pinned for 148 SMs")
+    lib = m3.lib()
+    n = ctypes.c_size_t(0)
+    d = m3.dims(1, 131072, 64, 64, 128, 4, torch.bfloat16)
+    assert lib.mamba3_scan_fwd_workspace(ctypes.byref(d), ctypes.byref(n)) == 0
+    bh, N, P, slots = 64, 128, 64, 17
+    state = bh * slots * N * P * 4
+    tot = bh * (slots - 1) * (1 + N // 2) * 4
+    assert n.value == ((state + 255) // 256) * 256 + tot
